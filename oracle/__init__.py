@@ -1,0 +1,226 @@
+"""CPU oracle for the NVFP4 routed-MoE expert forward (TEST INFRASTRUCTURE ONLY).
+
+A ctypes front end over ``ftmoe_oracle.c``, the plain fp64 C statement of the
+layer. Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline import this package; the CUDA library never does, and this package
+never imports the CUDA library.
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ftmoe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (portable C11, no target-specific flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC",
+                               "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class Bank(ctypes.Structure):
+    _fields_ = [("gu", ctypes.c_void_p), ("gu_scale", ctypes.c_void_p), ("gu_global", ctypes.c_void_p),
+                ("dn", ctypes.c_void_p), ("dn_scale", ctypes.c_void_p), ("dn_global", ctypes.c_void_p),
+                ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("Il", ctypes.c_int32), ("g", ctypes.c_int32)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+            L.orc_e2m1.restype = D; L.orc_e2m1.argtypes = [ctypes.c_uint]
+            L.orc_e4m3.restype = D; L.orc_e4m3.argtypes = [ctypes.c_uint]
+            L.orc_dequant_bf16.restype = ctypes.c_uint16
+            L.orc_dequant_bf16.argtypes = [ctypes.c_uint, ctypes.c_uint]
+            L.orc_bf16_to_double.restype = D; L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.orc_dequant_matrix.restype = None
+            L.orc_dequant_matrix.argtypes = [P, P, P, I, I, I, P]
+            L.orc_route.restype = I; L.orc_route.argtypes = [P, I, I, I, P, P]
+            L.orc_align.restype = I; L.orc_align.argtypes = [P, I, I, I, I, P, P, P, P]
+            L.orc_slice.restype = I; L.orc_slice.argtypes = [I] * 6 + [P] * 15
+            L.orc_expert_gate_up.restype = None
+            L.orc_expert_gate_up.argtypes = [ctypes.POINTER(Bank), I, P, P]
+            L.orc_swiglu.restype = None; L.orc_swiglu.argtypes = [P, I, P]
+            L.orc_expert_down.restype = None
+            L.orc_expert_down.argtypes = [ctypes.POINTER(Bank), I, P, P]
+            L.orc_moe_forward.restype = I
+            L.orc_moe_forward.argtypes = [ctypes.POINTER(Bank), ctypes.POINTER(Bank), P, I, P, P, I,
+                                          P, I, P, I]
+            _lib = L
+        return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return a.ctypes.data
+
+
+@contextlib.contextmanager
+def mutation(code: int):
+    """Plant one known mistake in the oracle for the duration of the block."""
+    v = ctypes.c_int.in_dll(lib(), "orc_mutation")
+    old = v.value
+    v.value = code
+    try:
+        yield
+    finally:
+        v.value = old
+
+
+MUTATIONS = {
+    "nibble_order": 1, "swap_gate_up": 2, "drop_global": 3, "scale_index": 4, "e2m1_sign": 5,
+    "no_renorm": 6, "tie_high": 7, "down_rows": 8, "drop_shared": 9, "drop_route_w": 10,
+    "e4m3_bias": 11, "up_slice": 12,
+}
+
+
+def e2m1(nibble: int) -> float:
+    return lib().orc_e2m1(nibble)
+
+
+def e4m3(byte: int) -> float:
+    return lib().orc_e4m3(byte)
+
+
+def dequant_bf16(nibble: int, scale_byte: int) -> int:
+    return lib().orc_dequant_bf16(nibble, scale_byte)
+
+
+def dequant_matrix(codes: np.ndarray, scales: np.ndarray, glob: np.ndarray, group: int) -> np.ndarray:
+    """Dense fp64 [rows, K] of one expert matrix (codes [rows, K/2])."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    glob = np.ascontiguousarray(glob, np.float32)
+    rows, K = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((rows, K), np.float64)
+    lib().orc_dequant_matrix(_p(codes), _p(scales), _p(glob), rows, K, group, _p(out))
+    return out
+
+
+def route(logits: np.ndarray, k: int):
+    """(ids int32 [T,k], w float64 [T,k]) -- softmax, top-k, renormalise."""
+    logits = np.ascontiguousarray(logits, np.float32)
+    T, E = logits.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    if lib().orc_route(_p(logits), T, E, k, _p(ids), _p(w)) != 0:
+        raise ValueError("bad routing arguments")
+    return ids, w
+
+
+def align(ids: np.ndarray, E: int, block: int):
+    """(sorted_slot, block_expert, expert_off, n_padded) for ids [T, k]."""
+    ids = np.ascontiguousarray(ids, np.int32)
+    T, k = ids.shape
+    cap = T * k + E * (block - 1)
+    sorted_slot = np.full(max(cap, 1), -1, np.int32)
+    block_expert = np.full(max(cap // block, 1), -1, np.int32)
+    expert_off = np.zeros(E + 1, np.int32)
+    n_padded = np.zeros(1, np.int32)
+    if lib().orc_align(_p(ids), T, k, E, block, _p(sorted_slot), _p(block_expert),
+                       _p(expert_off), _p(n_padded)) != 0:
+        raise ValueError("invalid expert id or arguments")
+    n = int(n_padded[0])
+    return sorted_slot[:n].copy(), block_expert[:n // block].copy(), expert_off, n
+
+
+def slice_bank(pieces: dict, group: int, tp_rank: int = 0, tp_size: int = 1) -> dict:
+    """Rank-local bank {gu, gu_scale, gu_global, dn, dn_scale, dn_global} from full pieces."""
+    c = {k: np.ascontiguousarray(v) for k, v in pieces.items()}
+    E, I, H2 = c["gate"].shape
+    H = H2 * 2
+    if I % tp_size:
+        raise ValueError("intermediate not divisible by tp_size")
+    Il = I // tp_size
+    out = {
+        "gu": np.zeros((E, 2 * Il, H // 2), np.uint8),
+        "gu_scale": np.zeros((E, 2 * Il, H // group), np.uint8),
+        "gu_global": np.zeros((E, 2 * Il), np.float32),
+        "dn": np.zeros((E, H, Il // 2), np.uint8),
+        "dn_scale": np.zeros((E, H, Il // group), np.uint8),
+        "dn_global": np.zeros((E, H), np.float32),
+    }
+    rc = lib().orc_slice(E, H, I, group, tp_rank, tp_size,
+                         *[_p(c[n]) for n in ("gate", "gate_scale", "gate_global", "up", "up_scale",
+                                              "up_global", "down", "down_scale", "down_global")],
+                         *[_p(out[n]) for n in ("gu", "gu_scale", "gu_global", "dn", "dn_scale",
+                                                "dn_global")])
+    if rc != 0:
+        raise ValueError("indivisible or invalid tp geometry")
+    return out
+
+
+def _bank(b: dict, group: int) -> Bank:
+    E, rows, H2 = b["gu"].shape
+    return Bank(_p(b["gu"]), _p(b["gu_scale"]), _p(b["gu_global"]), _p(b["dn"]), _p(b["dn_scale"]),
+                _p(b["dn_global"]), E, H2 * 2, rows // 2, group)
+
+
+def expert_gate_up(bank: dict, group: int, e: int, x_row: np.ndarray) -> np.ndarray:
+    x_row = np.ascontiguousarray(x_row, np.uint16)
+    G = np.zeros(bank["gu"].shape[1], np.float64)
+    lib().orc_expert_gate_up(ctypes.byref(_bank(bank, group)), e, _p(x_row), _p(G))
+    return G
+
+
+def swiglu(G: np.ndarray) -> np.ndarray:
+    G = np.ascontiguousarray(G, np.float64)
+    Il = G.shape[0] // 2
+    h = np.zeros(Il, np.float64)
+    lib().orc_swiglu(_p(G), Il, _p(h))
+    return h
+
+
+def expert_down(bank: dict, group: int, e: int, h: np.ndarray) -> np.ndarray:
+    h = np.ascontiguousarray(h, np.float64)
+    y = np.zeros(bank["dn"].shape[1], np.float64)
+    lib().orc_expert_down(ctypes.byref(_bank(bank, group)), e, _p(h), _p(y))
+    return y
+
+
+def moe_forward(routed: dict | None, shared: dict | None, group: int, x: np.ndarray,
+                ids: np.ndarray | None = None, w: np.ndarray | None = None,
+                tokens=None, nthreads: int = 1) -> np.ndarray:
+    """Rank-local partial [len(tokens), H] in fp64 (x: bf16 bits [T, H])."""
+    x = np.ascontiguousarray(x, np.uint16)
+    T, H = x.shape
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, np.int32)
+    out = np.zeros((len(tokens), H), np.float64)
+    rb = _bank(routed, group) if routed is not None else None
+    sb = _bank(shared, group) if shared is not None else None
+    if rb is not None:
+        ids = np.ascontiguousarray(ids, np.int32)
+        w = np.ascontiguousarray(w, np.float64)
+        k = ids.shape[1]
+        pids, pw = _p(ids), _p(w)
+    else:
+        k, pids, pw = 0, None, None
+    rc = lib().orc_moe_forward(ctypes.byref(rb) if rb is not None else None,
+                               ctypes.byref(sb) if sb is not None else None,
+                               _p(x), H, pids, pw, k, _p(tokens), len(tokens), _p(out), nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle forward failed")
+    return out
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
