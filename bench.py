@@ -1,0 +1,358 @@
+"""Benchmark of the NVFP4 routed-MoE expert forward (route + forward) on GB300.
+
+Default workload: the Qwen3.6-35B-A3B-shaped MoE layer in the decode regime (H=2048,
+E=256, top-8, I=512, shared expert 512, group 16), T=64 tokens, seed 0. One step
+runs 40 distinct layer copies (same bytes, distinct addresses, each with its own
+routing), so the touched weights of a step (~16 GB) are far larger than the 129 MB
+L2 and every layer streams its experts from HBM. One step is captured once in a
+CUDA graph and replayed.
+
+Metric: MoE-layer tokens/s = T * layers / step time. The JSON line also carries the
+roofline of the dominant kernel (algorithmic weight bytes / its average launch
+duration, from CUDA events recorded on the launch stream inside the graph), the
+oracle's CPU throughput, an end-to-end number with host buffers, and SM clocks.
+
+`--impl reference` times the CPU oracle (the reference arm of this build) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; decode weight-stream HBM GB/s & prefill TFLOPS vs roofline"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.lines, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """CPU oracle on a bounded sample of the workload (the reference arm)."""
+    import oracle
+    oracle.build()
+    if rank != 0:
+        return
+    shape = synth.SHAPES["qwen36"]
+    routed = synth.make_pieces(shape, 0)
+    shared = synth.make_pieces(shape, 0, shared=True)
+    rb, sb = oracle.slice_bank(routed, shape.group), oracle.slice_bank(shared, shape.group)
+    cores = oracle.default_threads()
+    T = args.T
+    tok = min(T, args.ref_tokens)
+    times = []
+    for step in range(args.warmup + args.steps):
+        logits = synth.make_logits(T, shape.num_experts, seed=step % args.layers)
+        x = synth.make_activations(T, shape.hidden, seed=step % args.layers)
+        t0 = time.perf_counter()
+        ids, w = oracle.route(logits, shape.top_k)
+        oracle.moe_forward(rb, sb, shape.group, x, ids, w, tokens=np.arange(tok), nthreads=cores)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    value = tok * len(times) / sum(times)
+    sample = f"{tok} of the {T} tokens of one layer per step, route + forward, {cores} threads"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(args):
+    return {"workload": f"qwen36-moe-decode-T{args.T}", "T": args.T, "layers": args.layers, "hidden": 2048,
+            "num_experts": 256, "top_k": 8, "intermediate": 512, "shared_intermediate": 512, "group": 16,
+            "tp": 1, "seed": 0, "routing": "N(0,1) logits",
+            "l2": f"inputs larger than L2: {args.layers} distinct layer copies per step"}
+
+
+def cpu_baseline(T, budget_s=10.0):
+    import oracle
+    oracle.build()
+    shape = synth.SHAPES["qwen36"]
+    routed = synth.make_pieces(shape, 0)
+    shared = synth.make_pieces(shape, 0, shared=True)
+    rb, sb = oracle.slice_bank(routed, shape.group), oracle.slice_bank(shared, shape.group)
+    cores = oracle.default_threads()
+    tokens, layers, t_total = 0, 0, 0.0
+    while t_total < budget_s and layers < 40:
+        logits = synth.make_logits(T, shape.num_experts, seed=layers)
+        x = synth.make_activations(T, shape.hidden, seed=layers)
+        t0 = time.perf_counter()
+        ids, w = oracle.route(logits, shape.top_k)
+        oracle.moe_forward(rb, sb, shape.group, x, ids, w, nthreads=cores)
+        t_total += time.perf_counter() - t0
+        tokens += T
+        layers += 1
+    return {"value": tokens / t_total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{layers} layers x {T} tokens (route + forward, fp64), {t_total:.1f} s"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import nvfp4_quantized_moe_gb300 as ft
+    from nvfp4_quantized_moe_gb300 import build as ftbuild
+
+    if rank == 0 or world == 1:
+        ftbuild.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        dist.barrier()
+        ftbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ft.load()
+    shape = synth.SHAPES["qwen36"]
+    cfg = ft.MoEConfig.of(shape)
+    T, L, H, E, k = args.T, args.layers, shape.hidden, shape.num_experts, shape.top_k
+    routed_np = synth.make_pieces(shape, 0)
+    shared_np = synth.make_pieces(shape, 0, shared=True)
+    routed_d = {n: torch.from_numpy(v).to(dev) for n, v in routed_np.items()}
+    shared_d = {n: torch.from_numpy(v).to(dev) for n, v in shared_np.items()}
+    layers = []
+    for l in range(L):
+        rb, sb = ft.alloc_banks(cfg, 0, dev), ft.alloc_banks(cfg, 1, dev)
+        ft.ft_moe_pack(cfg, 0, routed_d, rb)
+        ft.ft_moe_pack(cfg, 1, shared_d, sb)
+        layers.append((rb, sb))
+    del routed_d, shared_d
+    x_host = [synth.make_activations(T, H, seed=l) for l in range(L)]
+    lg_host = [synth.make_logits(T, E, seed=l) for l in range(L)]
+    x = torch.from_numpy(np.stack(x_host).view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(np.stack(lg_host)).to(dev)
+    ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
+    out = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(ft.ft_moe_workspace_size(cfg, T), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    n_stage = ft.FT_NSTAGES + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(L)]
+
+    def step(profile: bool):
+        for l in range(L):
+            ft.ft_moe_route(lg[l], k, ids[l], w[l])
+            if profile:
+                ft.ft_moe_set_stage_events(ev[l])
+            ft.ft_moe_forward(cfg, layers[l][0], layers[l][1], x[l], ids[l], w[l], out[l], ws)
+
+    with torch.cuda.stream(stream):
+        step(False)  # eager warm-up (also checks the status word below)
+    torch.cuda.synchronize(dev)
+    assert ft.ft_moe_read_status(ws) == 0
+    graphs = {}
+    for profile in (False, True):
+        g = torch.cuda.CUDAGraph()
+        n0 = ft.ft_moe_launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            step(profile)
+        graphs[profile] = (g, ft.ft_moe_launch_count() - n0)
+    g_plain, launches_per_step = graphs[False]
+
+    # touched experts per layer (algorithmic bytes)
+    ids_np = ids.cpu().numpy()
+    touched = [len(np.unique(ids_np[l])) for l in range(L)]
+    per_expert = 1781760
+    gu_bytes_per_expert = 1024 * 1024 + 1024 * 128 + 1024 * 4
+    layer_bytes = [(t + 1) * per_expert for t in touched]
+
+    for _ in range(args.warmup):
+        g_plain.replay()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(args.steps):
+                g_plain.replay()
+            stop.record(stream)
+        torch.cuda.synchronize(dev)
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    value = world * T * L * args.steps / (elapsed_ms / 1e3)
+
+    # per-stage durations from the profiled graph
+    g_prof = graphs[True][0]
+    reps = 5
+    stage_ms = np.zeros((reps, L, ft.FT_NSTAGES))
+    for r in range(reps):
+        g_prof.replay()
+        torch.cuda.synchronize(dev)
+        for l in range(L):
+            for s in range(ft.FT_NSTAGES):
+                stage_ms[r, l, s] = ev[l][s].elapsed_time(ev[l][s + 1])
+    stage_mean_us = {name: float(stage_ms[:, :, i].mean() * 1e3) for i, name in enumerate(ft.STAGES)}
+    dominant = max(stage_mean_us, key=stage_mean_us.get)
+    hbm, tfl, peak_kind = _peaks()
+    gu_alg = float(np.mean([t * gu_bytes_per_expert for t in touched]))
+    dn_alg = float(np.mean([t * (2048 * 256 + 2048 * 32 + 2048 * 4) for t in touched]))
+    alg = {"gate_up": gu_alg, "down": dn_alg, "shared_gate_up": float(gu_bytes_per_expert),
+           "shared_down": float(2048 * 256 + 2048 * 32 + 2048 * 4)}
+    dom_bytes = alg.get(dominant, 0.0)
+    dom_s = stage_mean_us[dominant] * 1e-6
+    achieved = dom_bytes / dom_s / 1e9 if dom_bytes else None
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm if achieved else None, "traffic": None,
+                "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "alg_bytes_per_launch": dom_bytes, "avg_launch_us": stage_mean_us[dominant]}
+    layer_us = ms_step * 1e3 / L
+    layer_gbs = float(np.mean(layer_bytes)) / (layer_us * 1e-6) / 1e9
+
+    # end to end: pinned host inputs in, bf16 outputs back, every step
+    x_pin = torch.from_numpy(np.stack(x_host).view(np.int16)).pin_memory()
+    lg_pin = torch.from_numpy(np.stack(lg_host)).pin_memory()
+    out_pin = torch.empty((L, T, H), dtype=torch.bfloat16).pin_memory()
+    x16 = x.view(torch.int16)
+    for _ in range(2):
+        with torch.cuda.stream(stream):
+            x16.copy_(x_pin, non_blocking=True)
+            lg.copy_(lg_pin, non_blocking=True)
+            g_plain.replay()
+            out_pin.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            x16.copy_(x_pin, non_blocking=True)
+            lg.copy_(lg_pin, non_blocking=True)
+            g_plain.replay()
+            out_pin.copy_(out, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    wall_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    e2e = {"value": world * T * L / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x_pin.numel() * 2 + lg_pin.numel() * 4),
+           "d2h_bytes_per_step": int(out_pin.numel() * 2), "ms_per_step": e2e_ms, "host_wall_ms_per_step": wall_ms}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(args),
+        "roofline": roofline, "layer": {"us": layer_us, "touched_experts_mean": float(np.mean(touched)),
+                                        "weight_bytes_mean": float(np.mean(layer_bytes)), "gbs": layer_gbs,
+                                        "frac_of_hbm": layer_gbs / hbm},
+        "stage_us": stage_mean_us, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(T)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--T", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=40)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,465 @@
+// extern "C" entry points of libftmoe: argument validation, workspace layout and
+// kernel orchestration. See include/ft_moe.h for the contract of every call.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "ft_moe.h"
+#include "ftmoe_internal.h"
+
+namespace ftmoe {
+
+static thread_local char g_err[512];
+static thread_local cudaEvent_t g_stage_events[FT_NSTAGES + 1];
+static thread_local bool g_stage_armed = false;
+static thread_local int64_t g_launches = 0;
+
+void count_launches(int n) { g_launches += n; }
+
+// Record the stage boundary event i, if timing is armed.
+static cudaError_t stage_mark(int i, cudaStream_t s)
+{
+    if (!g_stage_armed) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecordWithFlags(g_stage_events[i], s,
+                                    cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0);
+}
+
+static ft_status fail(ft_status code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static ft_status ok()
+{
+    g_err[0] = 0;
+    return FT_OK;
+}
+
+static ft_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(FT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int sm_count()
+{
+    static int cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------- geometry
+
+struct Geometry {
+    int H, I, E, k, g, Is, r, tp;
+    int Il, Isl;
+};
+
+static ft_status check_config(const ft_moe_config *cfg, Geometry &G)
+{
+    if (!cfg) return fail(FT_ERR_INVALID_ARG, "config is NULL");
+    G.H = cfg->hidden; G.I = cfg->intermediate; G.E = cfg->num_experts; G.k = cfg->top_k;
+    G.g = cfg->group; G.Is = cfg->shared_intermediate; G.r = cfg->tp_rank; G.tp = cfg->tp_size;
+    if (G.H <= 0 || G.I <= 0 || G.E <= 0 || G.k <= 0 || G.Is < 0 || G.tp <= 0 || G.r < 0 || G.r >= G.tp)
+        return fail(FT_ERR_INVALID_ARG, "config fields must be positive and 0 <= tp_rank < tp_size");
+    if (G.g != 16 && G.g != 32) return fail(FT_ERR_UNSUPPORTED, "group must be 16 or 32 (got %d)", G.g);
+    if (G.E > 1024 || G.k > 32 || G.k > G.E)
+        return fail(FT_ERR_UNSUPPORTED, "need top_k <= 32, top_k <= num_experts <= 1024");
+    if (G.H % G.g || G.H % 2)
+        return fail(FT_ERR_INDIVISIBLE, "hidden %d is not a multiple of the %d-element scale block", G.H, G.g);
+    if (G.I % G.tp)
+        return fail(FT_ERR_INDIVISIBLE, "intermediate %d does not split across %d tp ranks", G.I, G.tp);
+    G.Il = G.I / G.tp;
+    if (G.Il % G.g)
+        return fail(FT_ERR_INDIVISIBLE, "local intermediate %d is not a multiple of the %d-element scale block",
+                    G.Il, G.g);
+    if (G.Is % G.tp)
+        return fail(FT_ERR_INDIVISIBLE, "shared intermediate %d does not split across %d tp ranks", G.Is, G.tp);
+    G.Isl = G.Is / G.tp;
+    if (G.Isl % G.g)
+        return fail(FT_ERR_INDIVISIBLE, "local shared intermediate %d is not a multiple of the %d-element block",
+                    G.Isl, G.g);
+    if (G.H % 128) return fail(FT_ERR_UNSUPPORTED, "hidden must be a multiple of 128 (got %d)", G.H);
+    return FT_OK;
+}
+
+static void spec(ft_bank_spec &s, int dtype, int64_t a, int64_t b, int64_t c, int nd)
+{
+    s.ndim = nd;
+    s.dtype = dtype;
+    s.shape[0] = a; s.shape[1] = b; s.shape[2] = nd == 3 ? c : 0;
+    int64_t el = nd == 3 ? a * b * c : a * b;
+    s.bytes = el * (dtype == FT_DTYPE_F32 ? 4 : 1);
+}
+
+static void bank_specs(const Geometry &G, int shared, ft_bank_spec out[FT_NBANKS])
+{
+    const int64_t E = shared ? 1 : G.E, Il = shared ? G.Isl : G.Il;
+    spec(out[FT_GU], FT_DTYPE_U8, E, 2 * Il, G.H / 2, 3);
+    spec(out[FT_GU_SCALE], FT_DTYPE_E4M3, E, 2 * Il, G.H / G.g, 3);
+    spec(out[FT_GU_GLOBAL], FT_DTYPE_F32, E, 2 * Il, 0, 2);
+    spec(out[FT_DN], FT_DTYPE_U8, E, G.H, Il / 2, 3);
+    spec(out[FT_DN_SCALE], FT_DTYPE_E4M3, E, G.H, Il / G.g, 3);
+    spec(out[FT_DN_GLOBAL], FT_DTYPE_F32, E, G.H, 0, 2);
+}
+
+// Workspace regions of ft_moe_forward, each 256-byte aligned.
+struct WsLayout {
+    size_t status, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    int pmax;
+};
+
+static WsLayout ws_layout(const Geometry &G, int T)
+{
+    WsLayout L;
+    const int64_t n = (int64_t)T * G.k;
+    const int64_t pmax = n + (int64_t)(n < G.E ? n : G.E) * (kGemvBlock - 1);
+    const int64_t tpad = (T + kGemvBlock - 1) / kGemvBlock * kGemvBlock;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = round_up(o + bytes, 256); return at; };
+    L.status = take(256);
+    L.sorted = take(sizeof(int) * (size_t)pmax);
+    L.block_expert = take(sizeof(int) * (size_t)(pmax / kGemvBlock + 1));
+    L.expert_off = take(sizeof(int) * (size_t)(G.E + 1));
+    L.npad = take(sizeof(int));
+    L.scratch = take(align_scratch_bytes((int)n, G.E));
+    L.h = take(2 * (size_t)pmax * G.Il);
+    L.h_sh = take(G.Is ? 2 * (size_t)tpad * G.Isl : 0);
+    L.y = take(4 * (size_t)n * G.H);
+    L.y_sh = take(G.Is ? 4 * (size_t)T * G.H : 0);
+    L.total = o;
+    L.pmax = (int)pmax;
+    return L;
+}
+
+static bool banks_ok(const ft_moe_banks *b)
+{
+    if (!b) return false;
+    for (int i = 0; i < FT_NBANKS; ++i)
+        if (!b->p[i] || !aligned(b->p[i], 16)) return false;
+    return true;
+}
+
+}  // namespace ftmoe
+
+using namespace ftmoe;
+
+extern "C" {
+
+const char *ft_last_error(void) { return g_err; }
+
+ft_status ft_moe_set_stage_events(void *const *events)
+{
+    if (!events) {
+        g_stage_armed = false;
+        return ok();
+    }
+    for (int i = 0; i <= FT_NSTAGES; ++i) {
+        if (!events[i]) return fail(FT_ERR_INVALID_ARG, "stage event %d is NULL", i);
+        g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    g_stage_armed = true;
+    return ok();
+}
+
+int64_t ft_moe_launch_count(void) { return g_launches; }
+
+ft_status ft_moe_layout(const ft_moe_config *cfg, int32_t shared, ft_bank_spec out[FT_NBANKS])
+{
+    Geometry G;
+    ft_status st = check_config(cfg, G);
+    if (st) return st;
+    if (!out) return fail(FT_ERR_INVALID_ARG, "out is NULL");
+    if (shared != 0 && shared != 1) return fail(FT_ERR_INVALID_ARG, "shared must be 0 or 1");
+    if (shared && G.Is == 0) return fail(FT_ERR_UNSUPPORTED, "layer has no shared expert");
+    bank_specs(G, shared, out);
+    return ok();
+}
+
+ft_status ft_moe_workspace_size(const ft_moe_config *cfg, int32_t T, size_t *bytes)
+{
+    Geometry G;
+    ft_status st = check_config(cfg, G);
+    if (st) return st;
+    if (!bytes) return fail(FT_ERR_INVALID_ARG, "bytes is NULL");
+    if (T < 0 || T > (1 << 20)) return fail(FT_ERR_UNSUPPORTED, "T must be in [0, 2^20]");
+    *bytes = ws_layout(G, T).total;
+    return ok();
+}
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pieces *src, const ft_moe_banks *dst,
+                      void *stream)
+{
+    Geometry G;
+    ft_status st = check_config(cfg, G);
+    if (st) return st;
+    if (shared != 0 && shared != 1) return fail(FT_ERR_INVALID_ARG, "shared must be 0 or 1");
+    if (shared && G.Is == 0) return fail(FT_ERR_UNSUPPORTED, "layer has no shared expert");
+    if (!src || !src->gate || !src->gate_scale || !src->gate_global || !src->up || !src->up_scale ||
+        !src->up_global || !src->down || !src->down_scale || !src->down_global)
+        return fail(FT_ERR_INVALID_ARG, "a source piece is NULL");
+    if (!banks_ok(dst)) return fail(FT_ERR_INVALID_ARG, "destination banks must be non-NULL and 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t E = shared ? 1 : G.E, I = shared ? G.Is : G.I, Il = I / G.tp, r = G.r, H = G.H, g = G.g;
+    ft_bank_spec specs[FT_NBANKS];
+    bank_specs(G, shared, specs);
+    const size_t src_bytes[9] = {E * I * H / 2, E * I * H / g, E * I * 4, E * I * H / 2, E * I * H / g, E * I * 4,
+                                 E * H * I / 2, E * H * I / g, E * H * 4};
+    const void *srcs[9] = {src->gate, src->gate_scale, src->gate_global, src->up, src->up_scale,
+                           src->up_global, src->down, src->down_scale, src->down_global};
+    if (src->on_device) {
+        for (int i = 0; i < 9; ++i)
+            for (int j = 0; j < FT_NBANKS; ++j)
+                if (overlaps(srcs[i], src_bytes[i], dst->p[j], (size_t)specs[j].bytes))
+                    return fail(FT_ERR_INVALID_ARG, "pack destination overlaps its source");
+    }
+    struct Copy { const void *s; size_t sp; void *d; size_t dp; size_t w; size_t h; };
+    auto u8 = [](const void *p, size_t off) { return static_cast<const uint8_t *>(p) + off; };
+    auto w8 = [](void *p, size_t off) { return static_cast<uint8_t *>(p) + off; };
+    const Copy copies[9] = {
+        {u8(src->gate, r * Il * H / 2), I * H / 2, w8(dst->p[FT_GU], 0), 2 * Il * H / 2, Il * H / 2, E},
+        {u8(src->up, r * Il * H / 2), I * H / 2, w8(dst->p[FT_GU], Il * H / 2), 2 * Il * H / 2, Il * H / 2, E},
+        {u8(src->gate_scale, r * Il * H / g), I * H / g, w8(dst->p[FT_GU_SCALE], 0), 2 * Il * H / g, Il * H / g, E},
+        {u8(src->up_scale, r * Il * H / g), I * H / g, w8(dst->p[FT_GU_SCALE], Il * H / g), 2 * Il * H / g,
+         Il * H / g, E},
+        {u8(src->gate_global, r * Il * 4), I * 4, w8(dst->p[FT_GU_GLOBAL], 0), 2 * Il * 4, Il * 4, E},
+        {u8(src->up_global, r * Il * 4), I * 4, w8(dst->p[FT_GU_GLOBAL], Il * 4), 2 * Il * 4, Il * 4, E},
+        {u8(src->down, r * Il / 2), I / 2, w8(dst->p[FT_DN], 0), Il / 2, Il / 2, E * H},
+        {u8(src->down_scale, r * Il / g), I / g, w8(dst->p[FT_DN_SCALE], 0), Il / g, Il / g, E * H},
+        {u8(src->down_global, 0), E * H * 4, w8(dst->p[FT_DN_GLOBAL], 0), E * H * 4, E * H * 4, 1},
+    };
+    for (const Copy &c : copies) {
+        cudaError_t e;
+        if (src->on_device)
+            e = launch_pack_copy2d(static_cast<const uint8_t *>(c.s), c.sp, static_cast<uint8_t *>(c.d), c.dp, c.w,
+                                   c.h, s);
+        else
+            e = cudaMemcpy2DAsync(c.d, c.dp, c.s, c.sp, c.w, c.h, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ft_moe_pack copy");
+    }
+    return ok();
+}
+
+ft_status ft_moe_route(const float *logits, int32_t T, int32_t E, int32_t k, int32_t *topk_ids, float *topk_w,
+                       void *stream)
+{
+    if (T < 0 || E <= 0 || k <= 0) return fail(FT_ERR_INVALID_ARG, "need T >= 0, E > 0, k > 0");
+    if (E > 1024 || k > 32 || k > E) return fail(FT_ERR_UNSUPPORTED, "need k <= 32, k <= E <= 1024");
+    if (T == 0) return ok();
+    if (!logits || !topk_ids || !topk_w || !aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return fail(FT_ERR_INVALID_ARG, "route pointers must be non-NULL and 4-byte aligned");
+    cudaError_t e = launch_route(logits, T, E, k, topk_ids, topk_w, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    return ok();
+}
+
+ft_status ft_moe_align_workspace_size(int32_t T, int32_t k, int32_t E, size_t *bytes)
+{
+    if (!bytes || T < 0 || k <= 0 || E <= 0) return fail(FT_ERR_INVALID_ARG, "bad align arguments");
+    if (E > 1024 || T > (1 << 20) || k > 32) return fail(FT_ERR_UNSUPPORTED, "align limits exceeded");
+    *bytes = 256 + align_scratch_bytes(T * k, E);
+    return ok();
+}
+
+ft_status ft_moe_align(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E, int32_t block, int32_t *sorted_slot,
+                       int32_t *block_expert, int32_t *expert_off, int32_t *n_padded, void *workspace,
+                       size_t workspace_bytes, void *stream)
+{
+    if (T < 0 || k <= 0 || E <= 0 || block < 1 || block > 1024)
+        return fail(FT_ERR_INVALID_ARG, "need T >= 0, k > 0, E > 0, 1 <= block <= 1024");
+    if (E > 1024 || T > (1 << 20) || k > 32) return fail(FT_ERR_UNSUPPORTED, "align limits exceeded");
+    if (!sorted_slot || !block_expert || !expert_off || !n_padded || !workspace || (T > 0 && !topk_ids))
+        return fail(FT_ERR_INVALID_ARG, "align pointers must be non-NULL");
+    if (!aligned(workspace, 256)) return fail(FT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    size_t need = 256 + align_scratch_bytes(T * k, E);
+    if (workspace_bytes < need) return fail(FT_ERR_WORKSPACE, "align workspace needs %zu bytes", need);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int *status = static_cast<int *>(workspace);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+    if (e == cudaSuccess)
+        e = launch_align(topk_ids, T, k, E, block, sorted_slot, block_expert, expert_off, n_padded, status,
+                         static_cast<char *>(workspace) + 256, s);
+    if (e != cudaSuccess) return cuda_fail(e, "align launch");
+    return ok();
+}
+
+ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, const ft_moe_banks *shared,
+                         const void *x, int32_t T, const int32_t *topk_ids, const float *topk_w, void *out,
+                         int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Geometry G;
+    ft_status st = check_config(cfg, G);
+    if (st) return st;
+    if (T < 0 || T > (1 << 20)) return fail(FT_ERR_UNSUPPORTED, "T must be in [0, 2^20]");
+    if (out_dtype != FT_DTYPE_BF16 && out_dtype != FT_DTYPE_F32)
+        return fail(FT_ERR_INVALID_ARG, "out_dtype must be FT_DTYPE_BF16 or FT_DTYPE_F32");
+    if (!banks_ok(routed)) return fail(FT_ERR_INVALID_ARG, "routed banks must be non-NULL and 16-byte aligned");
+    if (G.Is > 0 && !banks_ok(shared))
+        return fail(FT_ERR_INVALID_ARG, "shared banks required (shared_intermediate > 0), 16-byte aligned");
+    if (G.Is == 0 && shared) return fail(FT_ERR_INVALID_ARG, "shared banks given but shared_intermediate is 0");
+    if (T == 0) return ok();
+    if (!x || !topk_ids || !topk_w || !out || !workspace)
+        return fail(FT_ERR_INVALID_ARG, "x, topk_ids, topk_w, out and workspace must be non-NULL");
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return fail(FT_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+    if (!aligned(workspace, 256)) return fail(FT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const WsLayout L = ws_layout(G, T);
+    if (workspace_bytes < L.total) return fail(FT_ERR_WORKSPACE, "workspace needs %zu bytes", L.total);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    int *status = reinterpret_cast<int *>(ws + L.status);
+    int *sorted = reinterpret_cast<int *>(ws + L.sorted);
+    int *bexp = reinterpret_cast<int *>(ws + L.block_expert);
+    int *eoff = reinterpret_cast<int *>(ws + L.expert_off);
+    int *npad = reinterpret_cast<int *>(ws + L.npad);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    uint16_t *h_sh = reinterpret_cast<uint16_t *>(ws + L.h_sh);
+    float *y = reinterpret_cast<float *>(ws + L.y);
+    float *y_sh = reinterpret_cast<float *>(ws + L.y_sh);
+    const int n_slots = T * G.k;
+
+    struct Disarm { ~Disarm() { g_stage_armed = false; } } disarm_on_return;
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    e = launch_align(topk_ids, T, G.k, G.E, kGemvBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s);
+    if (e != cudaSuccess) return cuda_fail(e, "align launch");
+
+    const int max_blocks = L.pmax / kGemvBlock;
+    const int tpad = (T + kGemvBlock - 1) / kGemvBlock;
+    auto down_ksplit = [](int K) { int ks = K / 256; return ks >= 8 ? 8 : ks >= 4 ? 4 : ks >= 2 ? 2 : 1; };
+
+    // gate_up + SwiGLU
+    GemvParams gp = {};
+    gp.codes = static_cast<const uint8_t *>(routed->p[FT_GU]);
+    gp.scales = static_cast<const uint8_t *>(routed->p[FT_GU_SCALE]);
+    gp.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
+    gp.e_codes = (int64_t)2 * G.Il * G.H / 2; gp.e_scales = (int64_t)2 * G.Il * G.H / G.g; gp.e_glob = 2 * G.Il;
+    gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il;
+    gp.act = static_cast<const uint16_t *>(x);
+    gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp;
+    gp.n_slots = n_slots; gp.top_k = G.k; gp.n_tiles = G.Il / 16; gp.num_experts = G.E;
+    gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
+    if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    e = launch_gemv_gated(gp, max_blocks * gp.n_tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
+
+    GemvParams sp = {};
+    if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    if (G.Is) {
+        sp = gp;
+        sp.codes = static_cast<const uint8_t *>(shared->p[FT_GU]);
+        sp.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
+        sp.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
+        sp.e_codes = (int64_t)G.Isl * G.H; sp.e_scales = (int64_t)2 * G.Isl * G.H / G.g; sp.e_glob = 2 * G.Isl;
+        sp.R = 2 * G.Isl; sp.up_off = G.Isl;
+        sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
+        sp.n_slots = T; sp.top_k = 1; sp.n_tiles = G.Isl / 16; sp.num_experts = 1;
+        sp.h_out = h_sh; sp.h_ld = G.Isl;
+        e = launch_gemv_gated(sp, tpad * sp.n_tiles, s);
+        if (e != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
+    }
+
+    // down + routing weight
+    if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    {
+        GemvParams dp = {};
+        const int ks = down_ksplit(G.Il), rows_per_cta = 16 * (8 / ks);
+        dp.codes = static_cast<const uint8_t *>(routed->p[FT_DN]);
+        dp.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
+        dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
+        dp.e_codes = (int64_t)G.H * G.Il / 2; dp.e_scales = (int64_t)G.H * G.Il / G.g; dp.e_glob = G.H;
+        dp.R = G.H; dp.K = G.Il; dp.group = G.g;
+        dp.act = h;
+        dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp;
+        dp.n_slots = n_slots; dp.top_k = G.k; dp.n_tiles = (G.H + rows_per_cta - 1) / rows_per_cta;
+        dp.num_experts = G.E; dp.y_out = y; dp.route_w = topk_w; dp.status = status;
+        e = launch_gemv_down(dp, ks, max_blocks * dp.n_tiles, s);
+        if (e != cudaSuccess) return cuda_fail(e, "down launch");
+    }
+    if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    if (G.Is) {
+        GemvParams dp = {};
+        const int ks = down_ksplit(G.Isl), rows_per_cta = 16 * (8 / ks);
+        dp.codes = static_cast<const uint8_t *>(shared->p[FT_DN]);
+        dp.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
+        dp.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
+        dp.e_codes = (int64_t)G.H * G.Isl / 2; dp.e_scales = (int64_t)G.H * G.Isl / G.g; dp.e_glob = G.H;
+        dp.R = G.H; dp.K = G.Isl; dp.group = G.g;
+        dp.act = h_sh;
+        dp.n_pos_static = T; dp.n_slots = T; dp.top_k = 1; dp.n_tiles = (G.H + rows_per_cta - 1) / rows_per_cta;
+        dp.num_experts = 1; dp.y_out = y_sh; dp.route_w = nullptr; dp.status = status;
+        e = launch_gemv_down(dp, ks, tpad * dp.n_tiles, s);
+        if (e != cudaSuccess) return cuda_fail(e, "shared down launch");
+    }
+    if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    return ok();
+}
+
+ft_status ft_moe_dequant(const ft_moe_config *cfg, int32_t shared, const ft_moe_banks *banks, int32_t which,
+                         int32_t expert, void *out_bf16, void *stream)
+{
+    Geometry G;
+    ft_status st = check_config(cfg, G);
+    if (st) return st;
+    if (shared != 0 && shared != 1) return fail(FT_ERR_INVALID_ARG, "shared must be 0 or 1");
+    if (shared && G.Is == 0) return fail(FT_ERR_UNSUPPORTED, "layer has no shared expert");
+    if (!banks_ok(banks) || !out_bf16 || !aligned(out_bf16, 16))
+        return fail(FT_ERR_INVALID_ARG, "banks and out must be non-NULL and 16-byte aligned");
+    const int E = shared ? 1 : G.E, Il = shared ? G.Isl : G.Il;
+    if (expert < 0 || expert >= E) return fail(FT_ERR_INVALID_ARG, "expert %d out of range", expert);
+    int rows, K, cidx, sidx;
+    if (which == FT_GU) { rows = 2 * Il; K = G.H; cidx = FT_GU; sidx = FT_GU_SCALE; }
+    else if (which == FT_DN) { rows = G.H; K = Il; cidx = FT_DN; sidx = FT_DN_SCALE; }
+    else return fail(FT_ERR_INVALID_ARG, "which must be FT_GU or FT_DN");
+    const uint8_t *codes = static_cast<const uint8_t *>(banks->p[cidx]) + (size_t)expert * rows * (K / 2);
+    const uint8_t *scales = static_cast<const uint8_t *>(banks->p[sidx]) + (size_t)expert * rows * (K / G.g);
+    cudaError_t e = launch_dequant(codes, scales, rows, K, G.g, static_cast<uint16_t *>(out_bf16),
+                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+    return ok();
+}
+
+ft_status ft_moe_read_status(const void *workspace, void *stream)
+{
+    if (!workspace) return fail(FT_ERR_INVALID_ARG, "workspace is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (v == FT_OK) return ok();
+    if (v == FT_ERR_INVALID_ROUTING) return fail(FT_ERR_INVALID_ROUTING, "invalid routing ids were skipped");
+    if (v == FT_ERR_TIMEOUT) return fail(FT_ERR_TIMEOUT, "a bounded device wait gave up");
+    return fail(FT_ERR_CUDA, "unexpected device status %d", v);
+}
+
+}  // extern "C"

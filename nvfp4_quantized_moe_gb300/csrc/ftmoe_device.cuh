@@ -1,0 +1,123 @@
+// Device-side building blocks shared by the libftmoe kernels (sm_103a).
+//
+// The NVFP4 weight element is W[n][k] = e2m1(code) * e4m3(scale[n][k/group]) *
+// global[n] (bank layout of the NVFP4 expert kernel, "[TP=2] Quantized MoE expert
+// parallelism ... NVFP4 port", section 4). The kernels feed the tensor cores with the
+// exact bf16 value code*scale and apply global[n] to the fp32 accumulator of row n,
+// which is the same sum (the global is constant along k).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ft_moe.h"
+
+namespace ftmoe {
+
+constexpr int kWarp = 32;
+
+// First error wins; later errors leave the first one in place.
+__device__ __forceinline__ void raise_status(int *status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- dequantisation
+
+// Four packed code bytes (eight e2m1 codes, element 2m in the low nibble of byte m)
+// -> four f16x2 registers holding the exact code values, lower element in the lower
+// half. cvt.rn.f16x2.e2m1x2 is exact: every e2m1 value is an f16 value.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t codes, uint32_t (&f)[4])
+{
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "mov.b32 {q0, q1, q2, q3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, q2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, q3;\n\t}"
+        : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+        : "r"(codes));
+}
+
+// f16x2 holding e2m1 code values -> bf16x2 holding code * 2^-112, exactly.
+// An f16 normal 2^(E-15)(1+M/1024) whose low three mantissa bits are zero (true for
+// every e2m1 value) re-read with its exponent field E in the low bits of a bf16
+// exponent and M>>3 as the bf16 mantissa is 2^(E-127)(1+M/1024) = value * 2^-112.
+// Zero maps to zero and the sign bit stays in place.
+__device__ __forceinline__ uint32_t f16x2_codes_to_bf16x2_scaled(uint32_t f)
+{
+    return ((f & 0x7FFF7FFFu) >> 3) | (f & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Two e4m3 scale bytes (low byte = first) -> two bf16x2 registers, each holding the
+// scale * 2^112 in both halves (exact: <= 4 significant bits, inside bf16 range).
+__device__ __forceinline__ void e4m3x2_to_bf16x2_scaled(uint32_t two_bytes, uint32_t &s0, uint32_t &s1)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(h2)
+        : "r"(two_bytes));
+    __half2 hh = *reinterpret_cast<__half2 *>(&h2);
+    float f0 = __low2float(hh) * 0x1p112f;
+    float f1 = __high2float(hh) * 0x1p112f;
+    __nv_bfloat16 b0 = __float2bfloat16_rn(f0), b1 = __float2bfloat16_rn(f1);
+    uint32_t u0 = *reinterpret_cast<uint16_t *>(&b0), u1 = *reinterpret_cast<uint16_t *>(&b1);
+    s0 = u0 | (u0 << 16);
+    s1 = u1 | (u1 << 16);
+}
+
+// Eight codes sharing one scale -> four bf16x2 registers of exact code*scale values.
+__device__ __forceinline__ void dequant8(uint32_t codes, uint32_t scale_bf16x2, uint32_t (&out)[4])
+{
+    uint32_t f[4];
+    e2m1x8_to_f16x2(codes, f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = bf16x2_mul(f16x2_codes_to_bf16x2_scaled(f[i]), scale_bf16x2);
+}
+
+// ---------------------------------------------------------------- warp MMA
+
+// D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 ldg_nc_v2(const void *p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+}  // namespace ftmoe

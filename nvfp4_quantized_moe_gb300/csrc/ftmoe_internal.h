@@ -1,0 +1,69 @@
+// Host-side declarations shared by the libftmoe translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ft_moe.h"
+
+namespace ftmoe {
+
+// Slots are grouped into blocks of this many rows for the warp-MMA (decode) path:
+// one block is the N=8 side of an m16n8k16 MMA.
+constexpr int kGemvBlock = 8;
+// Align: slot counts up to this size are sorted by one CTA; larger ones by three
+// grid-wide passes over chunks of kAlignChunk slots.
+constexpr int kAlignFusedMax = 8192;
+constexpr int kAlignChunk = 2048;
+
+// Everything one grouped warp-MMA launch needs. Rows of an expert matrix are the
+// MMA M side (16 per warp tile); up to eight activation rows (slots of one block)
+// are the N side; K is split across KSPLIT warps of the CTA.
+struct GemvParams {
+    const uint8_t *codes;    // [E][R][K/2]
+    const uint8_t *scales;   // [E][R][K/group]
+    const float *glob;       // [E][R]
+    int64_t e_codes, e_scales, e_glob;  // per-expert strides (elements)
+    int R, K, group;
+    int up_off;              // gated: row offset of the up half (I_l)
+    const uint16_t *act;     // bf16 rows of length K
+    const int *n_pos_dev;    // routed: device count of padded positions
+    int n_pos_static;        // shared: number of positions (tokens)
+    const int *sorted_slot;  // routed: position -> slot (>= n_slots: padding)
+    const int *block_expert; // routed: block -> expert
+    int n_slots;             // routed: T*k; shared: T
+    int top_k;               // routed: k (slot -> token); shared: 1
+    int n_tiles;             // CTA tiles per block
+    int num_experts;
+    uint16_t *h_out;         // gated: bf16 [positions][h_ld]
+    int h_ld;
+    float *y_out;            // down: f32 [n_slots][R]
+    const float *route_w;    // down, routed: [T*k]; nullptr = weight 1
+    int *status;
+};
+
+int sm_count();
+// Adds n to the calling thread's launch counter (ft_moe_launch_count).
+void count_launches(int n);
+
+cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t s);
+
+// Align into caller buffers; `scratch` holds kAlignChunk-sized chunk counts and
+// per-slot ranks (align_scratch_bytes).
+size_t align_scratch_bytes(int n_slots, int E);
+cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t *sorted_slot,
+                         int32_t *block_expert, int32_t *expert_off, int32_t *n_padded, int *status,
+                         void *scratch, cudaStream_t s);
+
+cudaError_t launch_gemv_gated(const GemvParams &p, int max_units, cudaStream_t s);
+cudaError_t launch_gemv_down(const GemvParams &p, int ksplit, int max_units, cudaStream_t s);
+cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, int H, void *out, int out_dtype,
+                           cudaStream_t s);
+
+cudaError_t launch_pack_copy2d(const uint8_t *src, size_t src_pitch, uint8_t *dst, size_t dst_pitch,
+                               size_t width, size_t height, cudaStream_t s);
+cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, int rows, int K, int group,
+                           uint16_t *out, cudaStream_t s);
+
+}  // namespace ftmoe

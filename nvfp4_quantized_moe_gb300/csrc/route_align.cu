@@ -1,0 +1,331 @@
+// Router (softmax / top-k / renormalise) and moe_align (expert-sorted, tile-padded
+// slot order) kernels.
+//
+// Routing follows norm_topk_prob with a replicated router ("Offloaded MoE ignores
+// tensor parallelism", follow-up comment): every rank selects the same experts.
+// moe_align is the sort/pad step the "feat(qwen3_5_moe): tensor-parallel weight
+// sharding" Notes name for the MoE paths.
+#include <cuda_runtime.h>
+#include <float.h>
+#include <math.h>
+
+#include "ftmoe_device.cuh"
+#include "ftmoe_internal.h"
+
+namespace ftmoe {
+
+// ---------------------------------------------------------------- router
+
+// One warp per token. Lane l holds logits l, l+32, ...; k rounds of a warp-wide
+// arg-max over the unselected experts (larger logit first, then the lower index).
+// Softmax is monotone, so this selects exactly the top-k probabilities. The kept
+// weights are exp(l_j - l_max) / sum over kept exp(l_i - l_max): the softmax
+// normaliser cancels in the renormalisation.
+template <int VPL>
+__global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int T, int E, int k,
+                                                    int32_t *__restrict__ ids, float *__restrict__ w)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float *row = logits + (size_t)t * E;
+    float v[VPL];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        int e = lane + 32 * i;
+        v[i] = (e < E) ? __ldg(row + e) : 0.0f;
+        if (e >= E) taken |= 1u << i;
+    }
+    float top = 0.0f, sum = 0.0f, my_w = 0.0f;
+    int my_id = 0;
+    for (int r = 0; r < k; ++r) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            if (!((taken >> i) & 1u)) {
+                int e = lane + 32 * i;
+                if (bi == 0x7FFFFFFF || v[i] > bv) { bv = v[i]; bi = e; }  // ascending e: ties keep the lower
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+            int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+            bool better = (oi != 0x7FFFFFFF) && (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi));
+            if (better) { bv = ov; bi = oi; }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (r == 0) top = bv;
+        float ex = expf(bv - top);
+        sum += ex;
+        if (lane == r) { my_id = bi; my_w = ex; }
+    }
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = my_id;
+        w[(size_t)t * k + lane] = my_w / sum;
+    }
+}
+
+cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t s)
+{
+    const int warps = 8;
+    dim3 grid((T + warps - 1) / warps), block(warps * 32);
+    int vpl = (E + 31) / 32;
+    if (vpl <= 1) route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+    else if (vpl <= 2) route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+    else if (vpl <= 4) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+    else if (vpl <= 8) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+    else if (vpl <= 16) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+    else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- align
+
+// Expert id of slot s, or -1 when it is out of range (flagged, then skipped).
+// A repeated id inside a token's row is flagged but still placed.
+__device__ __forceinline__ int checked_expert(const int32_t *ids, int s, int k, int E, int *status)
+{
+    int e = __ldg(ids + s);
+    if (e < 0 || e >= E) {
+        raise_status(status, FT_ERR_INVALID_ROUTING);
+        return -1;
+    }
+    int base = s - s % k;
+    for (int j = base; j < s; ++j)
+        if (__ldg(ids + j) == e) raise_status(status, FT_ERR_INVALID_ROUTING);
+    return e;
+}
+
+// Rank of each slot among the slots of the same expert inside a warp's contiguous
+// range [lo, hi), in slot order; per-warp expert counts accumulate in cnt[E].
+__device__ __forceinline__ void warp_rank_range(const int32_t *ids, int lo, int hi, int k, int E, int *cnt,
+                                                int *rank_out, int rank_base, int *status)
+{
+    const int lane = threadIdx.x & 31;
+    for (int s0 = lo; s0 < hi; s0 += 32) {
+        int s = s0 + lane;
+        int e = (s < hi) ? checked_expert(ids, s, k, E, status) : -1;
+        uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+        int rank = __popc(peers & lanemask_lt());
+        int leader = __ffs(peers) - 1;
+        int before = (e >= 0) ? cnt[e] : 0;
+        if (e >= 0) rank_out[s - rank_base] = before + rank;
+        __syncwarp();
+        if (e >= 0 && lane == leader) cnt[e] = before + __popc(peers);
+        __syncwarp();
+    }
+}
+
+// Exclusive scan of vals[0..n) in place (n <= blockDim.x <= 1024), returns the total.
+__device__ int block_exclusive_scan(int *vals, int n, int *warp_tot)
+{
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int v = (tid < n) ? vals[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int nw = (blockDim.x + 31) >> 5;
+        int x = (lane < nw) ? warp_tot[lane] : 0;
+        int xi = x;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xFFFFFFFFu, xi, off);
+            if (lane >= off) xi += o;
+        }
+        warp_tot[lane] = xi - x;  // exclusive warp offsets
+        if (lane == 31) warp_tot[32] = xi;
+    }
+    __syncthreads();
+    if (tid < n) vals[tid] = incl - v + warp_tot[wid];
+    int total = warp_tot[32];
+    __syncthreads();
+    return total;
+}
+
+// Fill padding positions with the sentinel and give every block its expert.
+__device__ void fill_blocks(const int *off, const int *count, int E, int B, int n_slots, int total,
+                            int32_t *sorted_slot, int32_t *block_expert)
+{
+    for (int b = threadIdx.x; b < total / B; b += blockDim.x) {
+        int pos = b * B;
+        int lo = 0, hi = E;  // largest e with off[e] <= pos and a non-empty run
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (off[mid] <= pos) lo = mid; else hi = mid;
+        }
+        while (lo + 1 < E && off[lo + 1] <= pos) ++lo;
+        block_expert[b] = lo;
+        int run_end_real = off[lo] + count[lo];
+        for (int q = pos; q < pos + B; ++q)
+            if (q >= run_end_real) sorted_slot[q] = n_slots;
+    }
+}
+
+// One CTA sorts up to kAlignFusedMax slots: 32 warps each rank a contiguous range,
+// then per-expert prefixes over warps, padded offsets, placement.
+__global__ void __launch_bounds__(1024) align_fused_kernel(const int32_t *__restrict__ ids, int n, int k, int E,
+                                                           int B, int32_t *sorted_slot, int32_t *block_expert,
+                                                           int32_t *expert_off, int32_t *n_padded, int *status)
+{
+    extern __shared__ int smem[];
+    int *cnt = smem;                    // [32][E]
+    int *rank = cnt + 32 * E;           // [n]
+    int *off = rank + n;                // [E+1]
+    int *count = off + E + 1;           // [E]
+    int *wt = count + E;                // [33]
+    const int tid = threadIdx.x, wid = tid >> 5;
+    for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    const int per = (n + 31) / 32;
+    int lo = min(n, wid * per), hi = min(n, lo + per);
+    warp_rank_range(ids, lo, hi, k, E, cnt + wid * E, rank, 0, status);
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            int c = cnt[w * E + e];
+            cnt[w * E + e] = run;
+            run += c;
+        }
+        count[e] = run;
+        off[e] = (run + B - 1) / B * B;
+    }
+    __syncthreads();
+    int total = 0;
+    // E may exceed blockDim only if E > 1024, which the host rejects.
+    total = block_exclusive_scan(off, E, wt);
+    if (tid == 0) off[E] = total;
+    __syncthreads();
+    for (int s = tid; s < n; s += blockDim.x) {
+        int e = __ldg(ids + s);
+        if (e < 0 || e >= E) continue;
+        int w = s / per;
+        sorted_slot[off[e] + cnt[w * E + e] + rank[s]] = s;
+    }
+    fill_blocks(off, count, E, B, n, total, sorted_slot, block_expert);
+    for (int e = tid; e <= E; e += blockDim.x) expert_off[e] = off[e];
+    if (tid == 0) *n_padded = total;
+}
+
+// Pass 1 of the large align: chunk c = slots [c*kAlignChunk, ...) handled by one
+// CTA of 8 warps; ranks within the chunk and per-chunk expert counts.
+__global__ void __launch_bounds__(256) align_count_kernel(const int32_t *__restrict__ ids, int n, int k, int E,
+                                                          int *chunk_cnt, int *rank, int *status)
+{
+    extern __shared__ int smem[];
+    int *cnt = smem;  // [8][E]
+    const int tid = threadIdx.x, wid = tid >> 5;
+    for (int i = tid; i < 8 * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    const int c0 = blockIdx.x * kAlignChunk;
+    const int per = kAlignChunk / 8;
+    int lo = min(n, c0 + wid * per), hi = min(n, lo + per);
+    warp_rank_range(ids, lo, hi, k, E, cnt + wid * E, rank, 0, status);
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            int c = cnt[w * E + e];
+            cnt[w * E + e] = run;
+            run += c;
+        }
+        chunk_cnt[(size_t)blockIdx.x * E + e] = run;
+    }
+    __syncthreads();
+    for (int s = lo + (tid & 31); s < hi; s += 32) {
+        int e = __ldg(ids + s);
+        if (e >= 0 && e < E) rank[s] += cnt[wid * E + e];
+    }
+}
+
+// Pass 2: per-expert prefix over chunks, padded offsets, sentinel/block fill.
+__global__ void __launch_bounds__(1024) align_scan_kernel(int *chunk_cnt, int n_chunks, int E, int B, int n,
+                                                          int32_t *sorted_slot, int32_t *block_expert,
+                                                          int32_t *expert_off, int32_t *n_padded)
+{
+    extern __shared__ int smem[];
+    int *off = smem;          // [E+1]
+    int *count = off + E + 1; // [E]
+    int *wt = count + E;      // [33]
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < n_chunks; ++c) {
+            int v = chunk_cnt[(size_t)c * E + e];
+            chunk_cnt[(size_t)c * E + e] = run;
+            run += v;
+        }
+        count[e] = run;
+        off[e] = (run + B - 1) / B * B;
+    }
+    __syncthreads();
+    int total = block_exclusive_scan(off, E, wt);
+    if (tid == 0) off[E] = total;
+    __syncthreads();
+    fill_blocks(off, count, E, B, n, total, sorted_slot, block_expert);
+    for (int e = tid; e <= E; e += blockDim.x) expert_off[e] = off[e];
+    if (tid == 0) *n_padded = total;
+}
+
+// Pass 3: every slot to its place.
+__global__ void align_place_kernel(const int32_t *__restrict__ ids, int n, int E, const int *chunk_base,
+                                   const int *rank, const int32_t *expert_off, int32_t *sorted_slot)
+{
+    int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= n) return;
+    int e = __ldg(ids + s);
+    if (e < 0 || e >= E) return;
+    int c = s / kAlignChunk;
+    sorted_slot[expert_off[e] + chunk_base[(size_t)c * E + e] + rank[s]] = s;
+}
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t align_scratch_bytes(int n_slots, int E)
+{
+    if (n_slots <= kAlignFusedMax) return 0;
+    size_t chunks = (size_t)(n_slots + kAlignChunk - 1) / kAlignChunk;
+    return round_up(chunks * E * sizeof(int), 256) + round_up((size_t)n_slots * sizeof(int), 256);
+}
+
+cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t *sorted_slot,
+                         int32_t *block_expert, int32_t *expert_off, int32_t *n_padded, int *status,
+                         void *scratch, cudaStream_t s)
+{
+    const int n = T * k;
+    if (n <= kAlignFusedMax) {
+        size_t smem = sizeof(int) * ((size_t)32 * E + n + (E + 1) + E + 33);
+        cudaError_t err = cudaFuncSetAttribute(align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+        if (err != cudaSuccess) return err;
+        align_fused_kernel<<<1, 1024, smem, s>>>(ids, n, k, E, B, sorted_slot, block_expert, expert_off,
+                                                 n_padded, status);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    const int chunks = (n + kAlignChunk - 1) / kAlignChunk;
+    int *chunk_cnt = static_cast<int *>(scratch);
+    int *rank = reinterpret_cast<int *>(static_cast<char *>(scratch) + round_up((size_t)chunks * E * sizeof(int), 256));
+    size_t smem1 = sizeof(int) * 8 * (size_t)E;
+    cudaError_t err = cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+    if (err != cudaSuccess) return err;
+    align_count_kernel<<<chunks, 256, smem1, s>>>(ids, n, k, E, chunk_cnt, rank, status);
+    size_t smem2 = sizeof(int) * ((size_t)(E + 1) + E + 33);
+    align_scan_kernel<<<1, 1024, smem2, s>>>(chunk_cnt, chunks, E, B, n, sorted_slot, block_expert, expert_off,
+                                             n_padded);
+    align_place_kernel<<<(n + 255) / 256, 256, 0, s>>>(ids, n, E, chunk_cnt, rank, expert_off, sorted_slot);
+    count_launches(3);
+    return cudaGetLastError();
+}
+
+}  // namespace ftmoe

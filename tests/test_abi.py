@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol,
+and validates geometry and arguments before touching a GPU (no kernel runs here)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ft():
+    from nvfp4_quantized_moe_gb300 import build
+    build.build()
+    import nvfp4_quantized_moe_gb300 as ft
+    ft.load()
+    return ft
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "ft_moe.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^(?:ft_status|const char \*|int64_t)\s*(ft_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(ft):
+    declared = _declared_symbols()
+    assert declared == sorted(ft.EXPORTS)
+    lib = ctypes.CDLL(ft.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_layout_matches_pages_bank_shapes(ft):
+    with open(os.path.join(ROOT, "tests", "golden", "bank_layout_qwen36.json")) as f:
+        g = json.load(f)
+    for tp, want in g["per_tp"].items():
+        cfg = ft.MoEConfig(g["hidden"], g["intermediate"], g["num_experts"], 8, g["group"], 512, 0, int(tp))
+        got = {name: list(shape) for name, shape, _, _ in ft.ft_moe_layout(cfg, 0)}
+        assert got == want, tp
+
+
+def test_layout_bytes_and_shared(ft):
+    cfg = ft.MoEConfig.of(synth.SHAPES["qwen36"])
+    specs = ft.ft_moe_layout(cfg, 0)
+    per_expert = sum(b for *_, b in specs) // 256
+    assert per_expert == 1024 * 1024 + 1024 * 128 + 1024 * 4 + 2048 * 256 + 2048 * 32 + 2048 * 4 == 1781760
+    sh = ft.ft_moe_layout(cfg, 1)
+    assert [s for _, s, _, _ in sh][0] == (1, 1024, 1024)
+    c4 = ft.MoEConfig.of(synth.SHAPES["dsv4"], 0, 4)
+    assert sum(b for *_, b in ft.ft_moe_layout(c4, 0)) // 256 == (1024 * 2048 + 1024 * 128 + 1024 * 4 +
+                                                                   4096 * 256 + 4096 * 16 + 4096 * 4)
+
+
+@pytest.mark.parametrize("fields,code", [
+    (dict(tp_size=3), 2),                      # 512 % 3
+    (dict(tp_size=64), 2),                     # 512/64 = 8 not a multiple of 16
+    (dict(group=8), 3),                        # unsupported block size
+    (dict(num_experts=2048), 3),
+    (dict(top_k=0), 1),
+    (dict(tp_rank=2, tp_size=2), 1),
+    (dict(hidden=2056), 2),                    # not a multiple of 16
+    (dict(hidden=2064), 3),                    # multiple of 16, not of 128
+    (dict(shared_intermediate=200), 2),        # 200 % 16 at tp=1
+])
+def test_layout_rejects_bad_geometry(ft, fields, code):
+    base = dict(hidden=2048, intermediate=512, num_experts=256, top_k=8, group=16, shared_intermediate=512,
+                tp_rank=0, tp_size=1)
+    base.update(fields)
+    cfg = ft.MoEConfig(*[base[n] for n, _ in ft.MoEConfig._fields_])
+    with pytest.raises(ft.FtMoeError) as ei:
+        ft.ft_moe_layout(cfg, 0)
+    assert ei.value.status == code
+    assert ft.ft_last_error()
+
+
+def test_layout_shared_without_shared_expert(ft):
+    cfg = ft.MoEConfig.of(synth.SHAPES["tiny"])
+    with pytest.raises(ft.FtMoeError) as ei:
+        ft.ft_moe_layout(cfg, 1)
+    assert ei.value.status == 3
+
+
+def test_forward_argument_checks_happen_before_launch(ft):
+    lib = ft.load()
+    cfg = ft.MoEConfig.of(synth.SHAPES["qwen36"])
+    fake = ft._Banks()
+    for i in range(6):
+        fake.p[i] = 4096 * (i + 1)
+    need = ctypes.c_size_t()
+    assert lib.ft_moe_workspace_size(ctypes.byref(cfg), 64, ctypes.byref(need)) == 0
+    assert need.value > 64 * 8 * 2048 * 4
+    # T = 0 is a no-op
+    assert lib.ft_moe_forward(ctypes.byref(cfg), ctypes.byref(fake), ctypes.byref(fake), None, 0, None, None,
+                              None, ft.FT_DTYPE_F32, None, 0, None) == 0
+    # missing shared banks when the layer has a shared expert
+    assert lib.ft_moe_forward(ctypes.byref(cfg), ctypes.byref(fake), None, 4096, 4, 4096, 4096, 4096,
+                              ft.FT_DTYPE_F32, 4096, need.value, None) == 1
+    # misaligned activations
+    assert lib.ft_moe_forward(ctypes.byref(cfg), ctypes.byref(fake), ctypes.byref(fake), 4098, 4, 4096, 4096,
+                              4096, ft.FT_DTYPE_F32, 4096, 1 << 40, None) == 1
+    # workspace too small
+    assert lib.ft_moe_forward(ctypes.byref(cfg), ctypes.byref(fake), ctypes.byref(fake), 4096, 64, 4096, 4096,
+                              8192, ft.FT_DTYPE_F32, 4096, need.value - 1, None) == 4
+    # bad output dtype
+    assert lib.ft_moe_forward(ctypes.byref(cfg), ctypes.byref(fake), ctypes.byref(fake), 4096, 4, 4096, 4096,
+                              4096, 7, 4096, 1 << 40, None) == 1
+    # routing limits
+    assert lib.ft_moe_route(4096, 4, 2048, 8, 4096, 4096, None) == 3
+    assert lib.ft_moe_route(4096, 4, 8, 9, 4096, 4096, None) == 3
+    assert lib.ft_moe_route(None, 0, 8, 2, None, None, None) == 0
+    n = ctypes.c_size_t()
+    assert lib.ft_moe_align_workspace_size(8192, 8, 256, ctypes.byref(n)) == 0 and n.value > 8192 * 8 * 4
+    assert lib.ft_moe_align(4096, 4, 2, 8, 0, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 1
+
+
+def test_pack_rejects_overlap(ft):
+    lib = ft.load()
+    cfg = ft.MoEConfig.of(synth.SHAPES["tiny"])
+    banks = ft._Banks()
+    for i in range(6):
+        banks.p[i] = 1 << 20 + i
+    pieces = ft._Pieces(*([1 << 20] * 9), 1)
+    assert lib.ft_moe_pack(ctypes.byref(cfg), 0, ctypes.byref(pieces), ctypes.byref(banks), None) == 1

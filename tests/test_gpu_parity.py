@@ -1,0 +1,309 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer stages (router ids, align order, pack bytes, dequantised bf16 values) must be
+bit-exact; floating outputs must reach relative L2 error <= 1e-2 and max-abs error
+<= 3e-2 x RMS of the oracle output; routing weights agree to 1e-6 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from moe_cases import ROUTE_W_RTOL, GpuLayer, assert_close, logits_for, oracle_banks, pieces
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from nvfp4_quantized_moe_gb300 import build
+    build.build()
+    import nvfp4_quantized_moe_gb300 as ft
+    ft.load()
+
+
+@pytest.fixture(scope="module")
+def ft():
+    import nvfp4_quantized_moe_gb300 as ft
+    return ft
+
+
+_layers = {}
+
+
+def layer(name, tp_rank=0, tp_size=1):
+    key = (name, tp_rank, tp_size)
+    if key not in _layers:
+        if len(_layers) > 6:
+            _layers.clear()
+            torch.cuda.empty_cache()
+        _layers[key] = GpuLayer(name, tp_rank, tp_size)
+    return _layers[key]
+
+
+# ------------------------------------------------------------------ dequant (bit-exact)
+
+def test_dequant_all_code_scale_pairs(ft):
+    """Every (e2m1 code, e4m3 scale byte) pair through the kernels' dequant routine."""
+    shape = synth.LayerShape(hidden=256, intermediate=64, num_experts=1, top_k=1)
+    cfg = ft.MoEConfig.of(shape)
+    rows, K, g = 128, 256, 16
+    nib = np.arange(16, dtype=np.uint8)
+    group_bytes = (nib[1::2] << 4 | nib[0::2]).astype(np.uint8)          # elements 0..15 = codes 0..15
+    gu = np.tile(group_bytes, (rows, K // 16))
+    sc = (np.arange(rows * (K // g)) % 256).astype(np.uint8).reshape(rows, K // g)
+    banks = ft.alloc_banks(cfg, 0)
+    banks[0].copy_(torch.from_numpy(gu.reshape(1, rows, K // 2)))
+    banks[1].copy_(torch.from_numpy(sc.reshape(1, rows, K // g)))
+    for b in banks[2:]:
+        b.zero_()
+    out = torch.empty((rows, K), dtype=torch.bfloat16, device="cuda")
+    ft.ft_moe_dequant(cfg, 0, banks, ft.FT_GU, 0, out)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    checked = 0
+    for n in range(rows):
+        for kk in range(K):
+            s = int(sc[n, kk // g])
+            if s in (0x7F, 0xFF):
+                continue
+            assert got[n, kk] == oracle.dequant_bf16(kk % 16, s), (n, kk, s)
+            checked += 1
+    assert checked == rows * K - 2 * 8 * 16
+
+
+def test_dequant_real_bank_matches_oracle(ft):
+    L = layer("qwen36")
+    rb, _ = oracle_banks("qwen36")
+    for which, e in ((ft.FT_GU, 0), (ft.FT_GU, 255), (ft.FT_DN, 17)):
+        rows, K = (1024, 2048) if which == ft.FT_GU else (2048, 512)
+        out = torch.empty((rows, K), dtype=torch.bfloat16, device="cuda")
+        ft.ft_moe_dequant(L.cfg, 0, L.routed, which, e, out)
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        codes = rb["gu"][e] if which == ft.FT_GU else rb["dn"][e]
+        sc = rb["gu_scale"][e] if which == ft.FT_GU else rb["dn_scale"][e]
+        ref = oracle.dequant_matrix(codes, sc, np.ones(rows, np.float32), 16)
+        gotf = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        assert np.array_equal(gotf, ref)
+
+
+# ------------------------------------------------------------------ pack (bit-exact)
+
+@pytest.mark.parametrize("name,tp", [("tiny", 1), ("tiny", 2), ("tiny", 4), ("qwen36", 2)])
+@pytest.mark.parametrize("from_host", [True, False])
+def test_pack_matches_oracle_slicer(ft, name, tp, from_host):
+    shape = synth.SHAPES[name]
+    routed, shared = pieces(name)
+    for r in range(tp):
+        L = GpuLayer(name, r, tp, from_host=from_host)
+        rb, sb = oracle_banks(name, r, tp)
+        for i, key in enumerate(("gu", "gu_scale", "gu_global", "dn", "dn_scale", "dn_global")):
+            assert np.array_equal(L.routed[i].cpu().numpy(), rb[key]), (key, r)
+            if shared is not None:
+                assert np.array_equal(L.shared[i].cpu().numpy(), sb[key]), (key, r)
+        # banks own their storage
+        assert all(b.untyped_storage().data_ptr() != 0 for b in L.routed)
+    del shape
+
+
+# ------------------------------------------------------------------ router
+
+@pytest.mark.parametrize("T,E,k,zipf", [(16, 8, 2, False), (1, 256, 8, False), (64, 256, 8, False),
+                                        (2048, 256, 8, True), (37, 1024, 32, True), (5, 33, 3, False),
+                                        (3, 32, 32, False)])
+def test_route_matches_oracle(ft, T, E, k, zipf):
+    logits = synth.zipf_logits(T, E, seed=T) if zipf else synth.make_logits(T, E, seed=T)
+    lg = torch.from_numpy(logits).cuda()
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ft.ft_moe_route(lg, k, ids, w)
+    ref_ids, ref_w = oracle.route(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.cpu().numpy().astype(np.float64), ref_w, rtol=ROUTE_W_RTOL, atol=0)
+
+
+def test_route_ties_go_to_lower_index(ft):
+    logits = np.zeros((4, 64), np.float32)
+    logits[1, ::3] = 2.0
+    logits[2, [5, 9, 40]] = 1.0
+    lg = torch.from_numpy(logits).cuda()
+    ids = torch.empty((4, 8), dtype=torch.int32, device="cuda")
+    w = torch.empty((4, 8), dtype=torch.float32, device="cuda")
+    ft.ft_moe_route(lg, 8, ids, w)
+    ref_ids, ref_w = oracle.route(logits, 8)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=ROUTE_W_RTOL)
+
+
+# ------------------------------------------------------------------ align (bit-exact)
+
+@pytest.mark.parametrize("T,E,k,B,zipf", [(16, 8, 2, 8, False), (1, 256, 8, 8, False), (64, 256, 8, 8, False),
+                                          (1024, 256, 8, 16, True), (2048, 256, 8, 8, True),
+                                          (8192, 256, 8, 128, True), (3000, 1024, 8, 64, True),
+                                          (7, 5, 3, 1, False)])
+def test_align_matches_oracle(ft, T, E, k, B, zipf):
+    logits = synth.zipf_logits(T, E, seed=1) if zipf else synth.make_logits(T, E, seed=1)
+    ids_np, _ = oracle.route(logits, k)
+    ids = torch.from_numpy(ids_np).cuda()
+    cap = T * k + min(E, T * k) * (B - 1)
+    sorted_slot = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+    block_expert = torch.full((cap // B + 1,), -7, dtype=torch.int32, device="cuda")
+    expert_off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    n_padded = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(ft.ft_moe_align_workspace_size(T, k, E), dtype=torch.uint8, device="cuda")
+    ft.ft_moe_align(ids, E, B, sorted_slot, block_expert, expert_off, n_padded, ws)
+    assert ft.ft_moe_read_status(ws) == 0
+    ref_sorted, ref_block, ref_off, ref_n = oracle.align(ids_np, E, B)
+    n = int(n_padded.item())
+    assert n == ref_n
+    assert np.array_equal(sorted_slot[:n].cpu().numpy(), ref_sorted)
+    assert np.array_equal(block_expert[:n // B].cpu().numpy(), ref_block)
+    assert np.array_equal(expert_off.cpu().numpy(), ref_off)
+
+
+def test_align_flags_invalid_ids(ft):
+    ids = torch.tensor([[0, 1], [2, 9], [3, 3]], dtype=torch.int32, device="cuda")
+    E, B = 8, 4
+    cap = 6 + 6 * (B - 1)
+    bufs = [torch.empty(cap, dtype=torch.int32, device="cuda"), torch.empty(cap, dtype=torch.int32, device="cuda"),
+            torch.empty(E + 1, dtype=torch.int32, device="cuda"), torch.empty(1, dtype=torch.int32, device="cuda")]
+    ws = torch.empty(ft.ft_moe_align_workspace_size(3, 2, E), dtype=torch.uint8, device="cuda")
+    ft.ft_moe_align(ids, E, B, *bufs, ws)
+    assert ft.ft_moe_read_status(ws) == 6      # FT_ERR_INVALID_ROUTING
+    # the out-of-range slot (expert 9) is skipped, the rest are placed
+    n = int(bufs[3].item())
+    placed = sorted(v for v in bufs[0][:n].cpu().tolist() if v < 6)
+    assert placed == [0, 1, 2, 4, 5]
+
+
+# ------------------------------------------------------------------ forward
+
+def _run_and_compare(name, T, zipf, tp_rank=0, tp_size=1, sample=None, out_dtype=torch.float32):
+    L = layer(name, tp_rank, tp_size)
+    shape = synth.SHAPES[name]
+    logits = logits_for(name, T, zipf)
+    x = synth.make_activations(T, shape.hidden)
+    ids, w = L.route(logits)
+    out, _ = L.forward(x, ids, w, out_dtype=out_dtype)
+    ref_ids, ref_w = oracle.route(logits, shape.top_k)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    rb, sb = oracle_banks(name, tp_rank, tp_size)
+    tokens = np.arange(T) if sample is None else sample
+    ref = oracle.moe_forward(rb, sb, shape.group, x, ref_ids, ref_w, tokens=tokens,
+                             nthreads=oracle.default_threads())
+    got = out.float().cpu().numpy()[tokens]
+    return got, ref
+
+
+@pytest.mark.parametrize("tp", [1, 2])
+def test_forward_tiny(tp):
+    for r in range(tp):
+        got, ref = _run_and_compare("tiny", 16, False, r, tp)
+        assert_close(got, ref, f"tiny tp={tp} rank={r}")
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
+def test_forward_qwen36_decode(T):
+    got, ref = _run_and_compare("qwen36", T, False)
+    assert_close(got, ref, f"qwen36 decode T={T}")
+
+
+def test_forward_bf16_output():
+    got, ref = _run_and_compare("qwen36", 8, False, out_dtype=torch.bfloat16)
+    assert_close(got, ref, "bf16 out")
+
+
+@pytest.mark.parametrize("T", [2048, 8192])
+def test_forward_qwen36_prefill_sampled(T):
+    rng = np.random.default_rng(T)
+    sample = np.sort(rng.choice(T, size=24, replace=False))
+    sample[0], sample[-1] = 0, T - 1
+    got, ref = _run_and_compare("qwen36", T, True, sample=sample)
+    assert_close(got, ref, f"qwen36 prefill T={T}")
+
+
+@pytest.mark.parametrize("tp,T,zipf", [(2, 32, False), (4, 32, False), (2, 2048, True), (4, 2048, True)])
+def test_forward_tp_partials_sum_to_full(tp, T, zipf):
+    """Each rank-local partial matches the oracle's; their host sum matches the tp=1 output."""
+    shape = synth.SHAPES["qwen36"]
+    sample = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(5).choice(T, 16, replace=False))
+    total = 0
+    for r in range(tp):
+        got, ref = _run_and_compare("qwen36", T, zipf, r, tp, sample=sample)
+        assert_close(got, ref, f"rank {r}/{tp}")
+        total = total + got.astype(np.float64)
+    logits = logits_for("qwen36", T, zipf)
+    ids, w = oracle.route(logits, shape.top_k)
+    rb, sb = oracle_banks("qwen36")
+    x = synth.make_activations(T, shape.hidden)
+    full = oracle.moe_forward(rb, sb, shape.group, x, ids, w, tokens=sample, nthreads=oracle.default_threads())
+    assert_close(total, full, f"sum of {tp} partials vs tp=1")
+
+
+@pytest.mark.parametrize("T,tp", [(1, 1), (16, 1), (1, 4), (16, 4)])
+def test_forward_dsv4_group32(T, tp):
+    for r in range(tp) if T == 1 else [0, tp - 1]:
+        got, ref = _run_and_compare("dsv4", T, True, r, tp)
+        assert_close(got, ref, f"dsv4 T={T} tp={tp} rank={r}")
+
+
+def test_forward_dsv4_prefill_sampled():
+    sample = np.array([0, 1, 777, 2048, 4095])
+    got, ref = _run_and_compare("dsv4", 4096, True, sample=sample)
+    assert_close(got, ref, "dsv4 T=4096")
+
+
+def test_forward_deterministic_and_untouched_experts():
+    L = layer("qwen36")
+    x = synth.make_activations(32, 2048, seed=3)
+    ids, w = L.route(logits_for("qwen36", 32, False, seed=3))
+    a, _ = L.forward(x, ids, w)
+    b, _ = L.forward(x, ids, w)
+    assert torch.equal(a, b)
+    # scribble over an expert nobody uses: bitwise-identical output
+    used = set(ids.cpu().numpy().reshape(-1).tolist())
+    free = next(e for e in range(256) if e not in used)
+    saved = [t[free].clone() for t in L.routed]
+    for t in L.routed:
+        t[free].copy_(torch.randint_like(t[free], 0, 100) if t.dtype == torch.uint8 else torch.rand_like(t[free]))
+    c, _ = L.forward(x, ids, w)
+    for t, s in zip(L.routed, saved):
+        t[free].copy_(s)
+    assert torch.equal(a, c)
+
+
+def test_forward_invalid_ids_flagged():
+    L = layer("tiny")
+    x = synth.make_activations(4, 256)
+    ids = torch.tensor([[0, 1], [2, 2], [3, 4], [5, 6]], dtype=torch.int32, device="cuda")
+    w = torch.full((4, 2), 0.5, device="cuda")
+    _, st = L.forward(x, ids, w, check_status=False)
+    assert st == 6
+
+
+def test_forward_in_cuda_graph():
+    L = layer("qwen36")
+    T = 8
+    x_bits = synth.make_activations(T, 2048, seed=9)
+    logits = torch.from_numpy(logits_for("qwen36", T, False, seed=9)).cuda()
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.empty((T, 8), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, 8), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, 2048), dtype=torch.float32, device="cuda")
+    ws = torch.empty(L.ft.ft_moe_workspace_size(L.cfg, T), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        L.ft.ft_moe_route(logits, 8, ids, w)
+        L.ft.ft_moe_forward(L.cfg, L.routed, L.shared, x, ids, w, out, ws)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        L.ft.ft_moe_route(logits, 8, ids, w)
+        L.ft.ft_moe_forward(L.cfg, L.routed, L.shared, x, ids, w, out, ws)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
