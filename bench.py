@@ -210,6 +210,9 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(dev)
     n_stage = ft.FT_NSTAGES + 1
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(L)]
+    for row in ev:
+        for e_ in row:
+            e_.record(stream)  # torch creates the CUDA event lazily, on first record
 
     def step(profile: bool):
         for l in range(L):
