@@ -203,6 +203,23 @@ ft_status ft_moe_align(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
                        int32_t *sorted_slot, int32_t *block_expert, int32_t *expert_off,
                        int32_t *n_padded, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ft_moe_align without a workspace, for callers that cannot allocate device memory
+ * (for instance code running in a host callback on a stream, where CUDA calls are not
+ * allowed, or an engine that fixes every device allocation at start-up). The pages
+ * have no counterpart: it is the same sort as ft_moe_align, with the scratch and the
+ * status word in a static array of 393,472 bytes that the library holds on every GPU
+ * that loads it, until the process exits.
+ *   Limits: T*k <= 65536 slots, E <= 1024, k <= 32; larger inputs return
+ *   FT_ERR_UNSUPPORTED (use ft_moe_align with a workspace).
+ *   status  device i32 [1] (out, may be NULL): FT_OK or FT_ERR_INVALID_ROUTING.
+ * Other arguments as ft_moe_align. The first call on each device looks up the array's
+ * device address; make that first call before any stream capture on that device.
+ * All calls share the one array: calls that overlap on the GPU (other streams, other
+ * threads) race and must be ordered by the caller. Allocates nothing. */
+ft_status ft_moe_align_static(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E, int32_t block,
+                              int32_t *sorted_slot, int32_t *block_expert, int32_t *expert_off,
+                              int32_t *n_padded, int32_t *status, void *stream);
+
 /* Dequantised weights of one expert without the per-row global:
  * out[n, k] = bf16(e2m1(code[n][k]) * e4m3(scale[n][k/group])), exact in bf16.
  * which = FT_GU (rows 2*I_l, K = H) or FT_DN (rows H, K = I_l); `banks` are

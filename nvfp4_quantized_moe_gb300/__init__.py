@@ -33,7 +33,7 @@ BANK_NAMES = ("gate_up", "gate_up_scale", "gate_up_global", "down", "down_scale"
 # Every symbol include/ft_moe.h declares.
 EXPORTS = ("ft_moe_layout", "ft_moe_pack", "ft_moe_route", "ft_moe_workspace_size", "ft_moe_forward",
            "ft_moe_align_workspace_size", "ft_moe_align", "ft_moe_dequant", "ft_moe_read_status",
-           "ft_last_error", "ft_moe_set_stage_events", "ft_moe_launch_count")
+           "ft_last_error", "ft_moe_set_stage_events", "ft_moe_launch_count", "ft_moe_align_static")
 FT_NSTAGES = 6
 STAGES = ("align", "gate_up", "shared_gate_up", "down", "shared_down", "combine")
 

@@ -43,6 +43,12 @@ static ft_status ok()
     return FT_OK;
 }
 
+ft_status report_error(ft_status code, const char *message)
+{
+    if (code == FT_OK) return ok();
+    return fail(code, "%s", message);
+}
+
 static ft_status cuda_fail(cudaError_t e, const char *what)
 {
     return fail(FT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));

@@ -44,6 +44,8 @@ struct GemvParams {
 };
 
 int sm_count();
+// Sets the thread-local error message (cleared for FT_OK) and returns `code`.
+ft_status report_error(ft_status code, const char *message);
 // Adds n to the calling thread's launch counter (ft_moe_launch_count).
 void count_launches(int n);
 
