@@ -357,7 +357,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
 
     const int max_blocks = L.pmax / kGemvBlock;
     const int tpad = (T + kGemvBlock - 1) / kGemvBlock;
-    auto down_ksplit = [](int K) { int ks = K / 256; return ks >= 8 ? 8 : ks >= 4 ? 4 : ks >= 2 ? 2 : 1; };
+    auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
 
     // gate_up + SwiGLU
     GemvParams gp = {};
@@ -368,10 +368,11 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il;
     gp.act = static_cast<const uint16_t *>(x);
     gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp;
-    gp.n_slots = n_slots; gp.top_k = G.k; gp.n_tiles = G.Il / 16; gp.num_experts = G.E;
+    const int gks = gemv_ksplit(max_blocks, cdiv(G.Il, 128), G.H);
+    gp.n_slots = n_slots; gp.top_k = G.k; gp.n_tiles = cdiv(G.Il, 16 * (8 / gks)); gp.num_experts = G.E;
     gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
     if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-    e = launch_gemv_gated(gp, max_blocks * gp.n_tiles, s);
+    e = launch_gemv_gated(gp, gks, max_blocks * gp.n_tiles, s);
     if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
 
     GemvParams sp = {};
@@ -384,9 +385,10 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         sp.e_codes = (int64_t)G.Isl * G.H; sp.e_scales = (int64_t)2 * G.Isl * G.H / G.g; sp.e_glob = 2 * G.Isl;
         sp.R = 2 * G.Isl; sp.up_off = G.Isl;
         sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
-        sp.n_slots = T; sp.top_k = 1; sp.n_tiles = G.Isl / 16; sp.num_experts = 1;
+        const int sks = gemv_ksplit(tpad, cdiv(G.Isl, 128), G.H);
+        sp.n_slots = T; sp.top_k = 1; sp.n_tiles = cdiv(G.Isl, 16 * (8 / sks)); sp.num_experts = 1;
         sp.h_out = h_sh; sp.h_ld = G.Isl;
-        e = launch_gemv_gated(sp, tpad * sp.n_tiles, s);
+        e = launch_gemv_gated(sp, sks, tpad * sp.n_tiles, s);
         if (e != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
     }
 
@@ -394,7 +396,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     {
         GemvParams dp = {};
-        const int ks = down_ksplit(G.Il), rows_per_cta = 16 * (8 / ks);
+        const int ks = gemv_ksplit(max_blocks, cdiv(G.H, 128), G.Il), rows_per_cta = 16 * (8 / ks);
         dp.codes = static_cast<const uint8_t *>(routed->p[FT_DN]);
         dp.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
         dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
@@ -410,7 +412,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     if (G.Is) {
         GemvParams dp = {};
-        const int ks = down_ksplit(G.Isl), rows_per_cta = 16 * (8 / ks);
+        const int ks = gemv_ksplit(tpad, cdiv(G.H, 128), G.Isl), rows_per_cta = 16 * (8 / ks);
         dp.codes = static_cast<const uint8_t *>(shared->p[FT_DN]);
         dp.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
         dp.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);

@@ -84,7 +84,41 @@ __device__ __forceinline__ void dequant8(uint32_t codes, uint32_t scale_bf16x2, 
     for (int i = 0; i < 4; ++i) out[i] = bf16x2_mul(f16x2_codes_to_bf16x2_scaled(f[i]), scale_bf16x2);
 }
 
+// Two e4m3 scale bytes (low byte = first) -> two f16x2 registers, each holding one
+// scale in both halves (every e4m3 value is an f16 value).
+__device__ __forceinline__ void e4m3x2_to_f16x2_bcast(uint32_t two_bytes, uint32_t &s0, uint32_t &s1)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(h2)
+        : "r"(two_bytes));
+    s0 = __byte_perm(h2, 0, 0x1010);
+    s1 = __byte_perm(h2, 0, 0x3232);
+}
+
+// Eight codes sharing one scale -> four f16x2 registers of exact code*scale values:
+// |code*scale| lies in [2^-10, 2688] with at most 6 significant bits, so the f16
+// product is exact.
+__device__ __forceinline__ void dequant8_f16(uint32_t codes, uint32_t scale_f16x2, uint32_t (&out)[4])
+{
+    uint32_t f[4];
+    e2m1x8_to_f16x2(codes, f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(f[i]), "r"(scale_f16x2));
+}
+
 // ---------------------------------------------------------------- warp MMA
+
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 // D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col).
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -102,6 +136,15 @@ __device__ __forceinline__ uint2 ldg_nc_v2(const void *p)
     uint2 v;
     asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
                  : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
 }

@@ -58,8 +58,12 @@ cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t
                          int32_t *block_expert, int32_t *expert_off, int32_t *n_padded, int *status,
                          void *scratch, cudaStream_t s);
 
-cudaError_t launch_gemv_gated(const GemvParams &p, int max_units, cudaStream_t s);
-cudaError_t launch_gemv_down(const GemvParams &p, int ksplit, int max_units, cudaStream_t s);
+// K-split (1, 2, 4 or 8 warps per row tile) for a launch whose CTA-unit count at
+// K-split 1 is max_blocks * units_per_block_ks1.
+int gemv_ksplit(int max_blocks, int units_per_block_ks1, int K);
+// p.n_tiles = CTA units per block: ceil(rows / (16 * 8 / ks)) with rows = I_l (gated) or H.
+cudaError_t launch_gemv_gated(const GemvParams &p, int ks, int max_units, cudaStream_t s);
+cudaError_t launch_gemv_down(const GemvParams &p, int ks, int max_units, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, int H, void *out, int out_dtype,
                            cudaStream_t s);
 

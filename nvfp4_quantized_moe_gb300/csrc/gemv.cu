@@ -1,21 +1,25 @@
 // Decode-regime grouped GEMV for the NVFP4 experts, on warp-level tensor-core MMAs.
 //
-// Work unit = (block of 8 expert-sorted slots, tile of 16 weight rows). Only the
-// experts that own a block are ever read, so the HBM stream is the touched experts'
-// packed codes and scales. Each warp multiplies a 16-row tile against the block's
-// activation rows over a K range: the packed codes are loaded with 8-byte
-// coalesced loads, dequantised in registers to exact bf16 code*scale values, and fed
-// to m16n8k16 MMAs with fp32 accumulation (weights as M, tokens as N). The K order
-// inside an MMA is permuted identically for weights and activations so that each
-// lane reads 16 consecutive elements (one block scale) per step.
+// Work unit = (block of 8 expert-sorted slots, group of weight-row tiles). Only the
+// experts that own a block are read, so the HBM stream is exactly the touched experts'
+// packed codes and scales. A CTA stages the block's 8 activation rows once in shared
+// memory as f16, each row scaled by a power of two 2^-e so that its largest magnitude
+// lies in [2^14, 2^15) (exact for every bf16 value of normal f16 range; the scale is
+// undone on the fp32 accumulator). Each warp then streams a 16-row weight tile with
+// 16-byte coalesced loads, prefetched two K steps ahead, dequantises in registers to
+// the exact f16 value code*scale (e2m1 and e4m3 values and their products are all
+// exact f16 numbers), and feeds m16n8k16 MMAs with fp32 accumulation: weights are
+// the M side, the block's tokens the N side. Inside an MMA the K order is permuted
+// identically for weights and activations, so each lane reads 32 consecutive elements
+// of a row per step.
 //
-// gate_up (gated): rows i and I_l+i of the rank-local gate_up bank share a warp, the
-// epilogue applies the per-row globals and SwiGLU h = silu(gate)*up ("[TP=2]
-// Quantized MoE expert parallelism ... NVFP4 port", section 4: MoE output =
-// sum_i silu(gate_i)*up_i @ down_i) and stores h in bf16.
-// down: the epilogue applies the per-row global and the routing weight and stores
-// y[slot] in fp32; the combine kernel then adds the k routed rows of a token in
-// order j = 0..k-1 and the shared expert's row.
+// gate_up (gated): gate rows i and up rows I_l + i of the rank-local bank share a
+// warp; the epilogue applies the row globals and SwiGLU h = silu(gate) * up ("[TP=2]
+// Quantized MoE expert parallelism ... NVFP4 port", section 4: the MoE output is
+// sum_i silu(gate_i) * up_i @ down_i) and stores h in bf16.
+// down: the epilogue applies the row global and the routing weight and stores y[slot]
+// in fp32; the combine kernel adds the k routed rows of a token in order j = 0..k-1,
+// then the shared expert's row.
 #include <cuda_runtime.h>
 
 #include "ftmoe_device.cuh"
@@ -25,149 +29,233 @@ namespace ftmoe {
 
 namespace {
 
-struct BlockInfo {
-    int expert;
-    int n_pos;
-};
+constexpr int kThreads = 256;  // 8 warps per CTA
+constexpr int kStep = 128;     // K elements per warp step (4 lanes x 32)
 
 __device__ __forceinline__ int load_n_pos(const GemvParams &p)
 {
     return p.n_pos_dev ? *p.n_pos_dev : (p.n_pos_static + kGemvBlock - 1) / kGemvBlock * kGemvBlock;
 }
 
-// Activation row for block position `pos`, or -1 when the position is padding.
-__device__ __forceinline__ int act_row_gated(const GemvParams &p, int pos, int n_pos)
+// Source row of block position `pos` (x row for gate_up, h row for down), or -1 for padding.
+__device__ __forceinline__ int source_row(const GemvParams &p, int pos, int n_pos, bool gated)
 {
     if (pos >= n_pos) return -1;
     if (p.sorted_slot) {
-        int s = __ldg(p.sorted_slot + pos);
-        return (s < p.n_slots) ? s / p.top_k : -1;
+        const int s = __ldg(p.sorted_slot + pos);
+        if (s >= p.n_slots) return -1;
+        return gated ? s / p.top_k : pos;
     }
     return (pos < p.n_pos_static) ? pos : -1;
 }
 
-__device__ __forceinline__ int act_row_down(const GemvParams &p, int pos, int n_pos)
+// Physical 16-byte chunk of logical chunk q in staged row r. With a row pitch that is a
+// multiple of 128 bytes, the 8 lanes of each LDS.128 phase (rows 2m, 2m+1; lanes c = 0..3
+// reading chunks base + 4c + j) land in 8 distinct bank quads.
+__device__ __forceinline__ int swz(int q, int r) { return q ^ (((q >> 3) & 1) << 1) ^ (r & 1); }
+
+// Stage the block's 8 activation rows (bf16, length K) into shared memory as f16 scaled
+// by 2^-e_r; inv[r] = 2^e_r. Warp r handles row r. The row pitch is Kp >= K elements
+// (a multiple of kStep) and the tail [K, Kp) is zero.
+__device__ void stage_block(const uint16_t *__restrict__ src, int K, int Kp, const int *rows, uint4 *sm,
+                            float *inv)
 {
-    if (pos >= n_pos) return -1;
-    if (p.sorted_slot) return (__ldg(p.sorted_slot + pos) < p.n_slots) ? pos : -1;
-    return (pos < p.n_pos_static) ? pos : -1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = warp;
+    const int row = rows[r];
+    uint4 *dst = sm + (size_t)r * (Kp / 8);
+    if (row < 0) {
+        for (int q = lane; q < Kp / 8; q += 32) dst[swz(q, r)] = make_uint4(0, 0, 0, 0);
+        if (lane == 0) inv[r] = 0.f;
+        return;
+    }
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)row * K);
+    float m = 0.f;
+    for (int q = lane; q < K / 8; q += 32) {
+        const uint4 v = __ldg(s4 + q);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+            m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    // 2^e with m * 2^-e in [2^14, 2^15); non-finite or zero rows keep e = 0.
+    int e = 0;
+    if (m > 0.f && m <= 3.3895314e38f) e = ilogbf(m) - 14;
+    const float down = exp2f((float)-e);
+    for (int q = lane; q < Kp / 8; q += 32) {
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (q < K / 8) {
+            const uint4 v = __ldg(s4 + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half2 hh = __floats2half2_rn(__uint_as_float(w[i] << 16) * down,
+                                                     __uint_as_float(w[i] & 0xFFFF0000u) * down);
+                h[i] = *reinterpret_cast<const uint32_t *>(&hh);
+            }
+            o = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        dst[swz(q, r)] = o;
+    }
+    if (lane == 0) inv[r] = exp2f((float)e);
 }
 
-// One K step of a 16-row tile: lane (g = lane/4, c = lane%4) holds rows g and g+8,
-// elements [kk, kk+16) of its piece, and the activation row of block column g.
-struct TileStep {
-    uint2 c_lo, c_hi;  // codes of rows g and g+8 (8 bytes each)
-    uint32_t s_lo, s_hi;
+// Codes and scales of one K step for rows g and g+8 of a 16-row tile.
+struct Frag {
+    uint4 lo, hi;       // 32 codes of row g / row g+8 (16 bytes each)
+    uint32_t slo, shi;  // two e4m3 scale bytes (first in the low byte)
 };
 
-__device__ __forceinline__ void load_tile_step(const uint8_t *codes_e, const uint8_t *scales_e, int K, int group,
-                                               int row, int kk, bool ok, TileStep &st)
+__device__ __forceinline__ void load_frag(const uint8_t *codes_row_lo, const uint8_t *scales_row_lo, int K, int group,
+                                          int kk, int valid, Frag &f)
 {
-    if (ok) {
-        st.c_lo = ldg_nc_v2(codes_e + (size_t)row * (K / 2) + kk / 2);
-        st.c_hi = ldg_nc_v2(codes_e + (size_t)(row + 8) * (K / 2) + kk / 2);
-        st.s_lo = __ldg(scales_e + (size_t)row * (K / group) + kk / group);
-        st.s_hi = __ldg(scales_e + (size_t)(row + 8) * (K / group) + kk / group);
+    // valid: elements of the 32-element piece inside K (0, 16 or 32)
+    const size_t rs = (size_t)8 * (K / 2);  // 8 rows further
+    const size_t ss = (size_t)8 * (K / group);
+    if (valid == 32 && (K & 31) == 0) {
+        f.lo = ldg_nc_v4(codes_row_lo + kk / 2);
+        f.hi = ldg_nc_v4(codes_row_lo + rs + kk / 2);
+    } else if (valid > 0) {
+        uint2 a = ldg_nc_v2(codes_row_lo + kk / 2), b = ldg_nc_v2(codes_row_lo + rs + kk / 2);
+        uint2 a2 = make_uint2(0, 0), b2 = make_uint2(0, 0);
+        if (valid == 32) {
+            a2 = ldg_nc_v2(codes_row_lo + kk / 2 + 8);
+            b2 = ldg_nc_v2(codes_row_lo + rs + kk / 2 + 8);
+        }
+        f.lo = make_uint4(a.x, a.y, a2.x, a2.y);
+        f.hi = make_uint4(b.x, b.y, b2.x, b2.y);
     } else {
-        st.c_lo = make_uint2(0, 0);
-        st.c_hi = make_uint2(0, 0);
-        st.s_lo = st.s_hi = 0x38;  // 1.0, multiplies zero codes
+        f.lo = f.hi = make_uint4(0, 0, 0, 0);
     }
-}
-
-__device__ __forceinline__ void mma_tile_step(const TileStep &st, const uint32_t (&b)[8], float (&acc)[4])
-{
-    uint32_t sl, sh;
-    e4m3x2_to_bf16x2_scaled(st.s_lo | (st.s_hi << 8), sl, sh);
-    uint32_t lo[8], hi[8];
-    {
-        uint32_t t[4];
-        dequant8(st.c_lo.x, sl, t);
-        lo[0] = t[0]; lo[1] = t[1]; lo[2] = t[2]; lo[3] = t[3];
-        dequant8(st.c_lo.y, sl, t);
-        lo[4] = t[0]; lo[5] = t[1]; lo[6] = t[2]; lo[7] = t[3];
-        dequant8(st.c_hi.x, sh, t);
-        hi[0] = t[0]; hi[1] = t[1]; hi[2] = t[2]; hi[3] = t[3];
-        dequant8(st.c_hi.y, sh, t);
-        hi[4] = t[0]; hi[5] = t[1]; hi[6] = t[2]; hi[7] = t[3];
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        mma_bf16_16816(acc, lo[2 * j], hi[2 * j], lo[2 * j + 1], hi[2 * j + 1], b[2 * j], b[2 * j + 1]);
-}
-
-__device__ __forceinline__ void load_act(const uint16_t *act, int K, int row, int kk, bool ok, uint32_t (&b)[8])
-{
-    if (ok && row >= 0) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(act + (size_t)row * K + kk);
-        uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-        b[0] = v0.x; b[1] = v0.y; b[2] = v0.z; b[3] = v0.w;
-        b[4] = v1.x; b[5] = v1.y; b[6] = v1.z; b[7] = v1.w;
+    if (valid > 0) {
+        const int q0 = kk / group, q1 = (kk + 16) / group;
+        const uint32_t l0 = __ldg(scales_row_lo + q0), h0 = __ldg(scales_row_lo + ss + q0);
+        const uint32_t l1 = (valid == 32) ? (uint32_t)__ldg(scales_row_lo + q1) : l0;
+        const uint32_t h1 = (valid == 32) ? (uint32_t)__ldg(scales_row_lo + ss + q1) : h0;
+        f.slo = l0 | (l1 << 8);
+        f.shi = h0 | (h1 << 8);
     } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) b[i] = 0;
+        f.slo = f.shi = 0x3838;  // 1.0, multiplies zero codes
     }
 }
 
-constexpr int kUnroll = 4;
+// 8 MMAs of one K step: A from the fragment, B (4 x 16 bytes of f16) from shared memory.
+__device__ __forceinline__ void mma_frag(const Frag &f, const uint4 (&b)[4], float (&acc)[4])
+{
+    uint32_t s_lo[2], s_hi[2];
+    e4m3x2_to_f16x2_bcast(f.slo, s_lo[0], s_lo[1]);
+    e4m3x2_to_f16x2_bcast(f.shi, s_hi[0], s_hi[1]);
+    const uint32_t cl[4] = {f.lo.x, f.lo.y, f.lo.z, f.lo.w};
+    const uint32_t ch[4] = {f.hi.x, f.hi.y, f.hi.z, f.hi.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {  // 8 elements per code word; words 0,1 use scale 0, words 2,3 scale 1
+        uint32_t al[4], ah[4];
+        dequant8_f16(cl[w], s_lo[w >> 1], al);
+        dequant8_f16(ch[w], s_hi[w >> 1], ah);
+        const uint32_t bw[4] = {b[w].x, b[w].y, b[w].z, b[w].w};
+        mma_f16_16816(acc, al[0], ah[0], al[1], ah[1], bw[0], bw[1]);
+        mma_f16_16816(acc, al[2], ah[2], al[3], ah[3], bw[2], bw[3]);
+    }
+}
+
+__device__ __forceinline__ void load_b(const uint4 *sm_row, int q0, int r, uint4 (&b)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) b[j] = sm_row[swz(q0 + j, r)];
+}
 
 }  // namespace
 
 // ---------------------------------------------------------------- gate_up + SwiGLU
 
-// CTA = KSPLIT warps on one tile pair (gate rows [i0, i0+16), up rows I_l + same).
-template <int KSPLIT>
-__global__ void __launch_bounds__(KSPLIT * 32) gemv_gated_kernel(const GemvParams p)
+// CTA = TPW tile pairs x KS K-splits (TPW * KS = 8 warps). A tile pair is gate rows
+// [i0, i0+16) and up rows I_l + [i0, i0+16).
+template <int KS>
+__global__ void __launch_bounds__(kThreads, 2) gemv_gated_kernel(const GemvParams p)
 {
-    __shared__ float red[KSPLIT][32][8];
-    const int lane = threadIdx.x & 31, ks = threadIdx.x >> 5;
+    constexpr int TPW = 8 / KS;
+    extern __shared__ uint4 smem_b[];
+    __shared__ float inv[kGemvBlock];
+    __shared__ float red[KS > 1 ? 8 : 1][32][8];
+    __shared__ int rows[kGemvBlock];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ks = warp % KS, tp = warp / KS;
     const int g = lane >> 2, c = lane & 3;
+    const int Kp = (p.K + kStep - 1) / kStep * kStep;
     const int n_pos = load_n_pos(p);
-    const int n_units = (n_pos / kGemvBlock) * p.n_tiles;
-    const int Kw = p.K / KSPLIT, k0 = ks * Kw;
-    const int n_steps = (Kw + 63) / 64;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int blk = u / p.n_tiles, tile = u - blk * p.n_tiles;
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
-        const int i0 = tile * 16;
-        const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
-        const uint8_t *scales_e = p.scales + (size_t)e * p.e_scales;
-        const int arow = act_row_gated(p, blk * kGemvBlock + g, n_pos);
-        float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s0 = 0; s0 < n_steps; s0 += kUnroll) {
-            TileStep sg[kUnroll], su[kUnroll];
-            uint32_t b[kUnroll][8];
-#pragma unroll
-            for (int q = 0; q < kUnroll; ++q) {
-                const int piece = 4 * (s0 + q) + c;
-                const bool ok = (s0 + q) < n_steps && 16 * piece < Kw;
-                const int kk = k0 + 16 * piece;
-                load_tile_step(codes_e, scales_e, p.K, p.group, i0 + g, kk, ok, sg[q]);
-                load_tile_step(codes_e, scales_e, p.K, p.group, p.up_off + i0 + g, kk, ok, su[q]);
-                load_act(p.act, p.K, arow, kk, ok, b[q]);
-            }
-#pragma unroll
-            for (int q = 0; q < kUnroll; ++q) {
-                mma_tile_step(sg[q], b[q], accg);
-                mma_tile_step(su[q], b[q], accu);
-            }
+    const int n_groups = p.n_tiles;  // tile-pair groups per block
+    const int n_units = (n_pos / kGemvBlock) * n_groups;
+    const int Kw = p.K / KS, k0 = ks * Kw;
+    const int n_steps = (Kw + kStep - 1) / kStep;
+    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    int staged = -1;
+    for (int u = u_lo; u < u_hi; ++u) {
+        const int blk = u / n_groups, grp = u - blk * n_groups;
+        if (blk != staged) {
+            __syncthreads();
+            if (threadIdx.x < kGemvBlock) rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, true);
+            __syncthreads();
+            stage_block(p.act, p.K, Kp, rows, smem_b, inv);
+            __syncthreads();
+            staged = blk;
         }
-        if (KSPLIT > 1) {
+        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int i0 = (grp * TPW + tp) * 16;
+        const bool tile_ok = i0 < p.up_off;
+        const uint8_t *gcodes = p.codes + (size_t)e * p.e_codes + (size_t)(i0 + g) * (p.K / 2);
+        const uint8_t *gscales = p.scales + (size_t)e * p.e_scales + (size_t)(i0 + g) * (p.K / p.group);
+        const uint8_t *ucodes = gcodes + (size_t)p.up_off * (p.K / 2);
+        const uint8_t *uscales = gscales + (size_t)p.up_off * (p.K / p.group);
+        const uint4 *brow = smem_b + (size_t)g * (Kp / 8);
+        float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+        auto piece_k = [&](int s) { return k0 + kStep * s + 32 * c; };
+        auto valid = [&](int s) {
+            return (tile_ok && s < n_steps) ? max(0, min(32, Kw - (kStep * s + 32 * c))) : 0;
+        };
+        Frag fg0, fu0, fg1, fu1;
+        load_frag(gcodes, gscales, p.K, p.group, piece_k(0), valid(0), fg0);
+        load_frag(ucodes, uscales, p.K, p.group, piece_k(0), valid(0), fu0);
+        load_frag(gcodes, gscales, p.K, p.group, piece_k(1), valid(1), fg1);
+        load_frag(ucodes, uscales, p.K, p.group, piece_k(1), valid(1), fu1);
+        for (int s = 0; s < n_steps; s += 2) {
+            Frag fg2, fu2, fg3, fu3;
+            load_frag(gcodes, gscales, p.K, p.group, piece_k(s + 2), valid(s + 2), fg2);
+            load_frag(ucodes, uscales, p.K, p.group, piece_k(s + 2), valid(s + 2), fu2);
+            load_frag(gcodes, gscales, p.K, p.group, piece_k(s + 3), valid(s + 3), fg3);
+            load_frag(ucodes, uscales, p.K, p.group, piece_k(s + 3), valid(s + 3), fu3);
+            uint4 b[4];
+            load_b(brow, (k0 + kStep * s) / 8 + 4 * c, g, b);
+            mma_frag(fg0, b, accg);
+            mma_frag(fu0, b, accu);
+            if (s + 1 < n_steps) {
+                load_b(brow, (k0 + kStep * (s + 1)) / 8 + 4 * c, g, b);
+                mma_frag(fg1, b, accg);
+                mma_frag(fu1, b, accu);
+            }
+            fg0 = fg2; fu0 = fu2; fg1 = fg3; fu1 = fu3;
+        }
+        if (KS > 1) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                red[ks][lane][i] = accg[i];
-                red[ks][lane][4 + i] = accu[i];
+                red[warp][lane][i] = accg[i];
+                red[warp][lane][4 + i] = accu[i];
             }
             __syncthreads();
         }
-        if (ks == 0) {
-            if (KSPLIT > 1) {
+        if (ks == 0 && tile_ok) {
+            if (KS > 1) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float a = 0.f, b2 = 0.f;
-                    for (int w = 0; w < KSPLIT; ++w) {
-                        a += red[w][lane][i];
-                        b2 += red[w][lane][4 + i];
+                    for (int w = 0; w < KS; ++w) {
+                        a += red[tp * KS + w][lane][i];
+                        b2 += red[tp * KS + w][lane][4 + i];
                     }
                     accg[i] = a;
                     accu[i] = b2;
@@ -181,68 +269,89 @@ __global__ void __launch_bounds__(KSPLIT * 32) gemv_gated_kernel(const GemvParam
 #pragma unroll
                 for (int col = 0; col < 2; ++col) {
                     const int pos = blk * kGemvBlock + 2 * c + col;
-                    if (pos < n_pos) {
-                        const float gate = accg[2 * half + col] * gg;
-                        const float up = accu[2 * half + col] * gu;
-                        __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
-                        p.h_out[(size_t)pos * p.h_ld + i] = *reinterpret_cast<uint16_t *>(&hv);
-                    }
+                    const float sc = inv[2 * c + col];
+                    const float gate = accg[2 * half + col] * sc * gg;
+                    const float up = accu[2 * half + col] * sc * gu;
+                    __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
+                    p.h_out[(size_t)pos * p.h_ld + i] = *reinterpret_cast<uint16_t *>(&hv);
                 }
             }
         }
-        if (KSPLIT > 1) __syncthreads();
+        if (KS > 1) __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------- down + routing weight
 
-// CTA = (8 / KSPLIT) row tiles x KSPLIT K-splits.
-template <int KSPLIT>
-__global__ void __launch_bounds__(256) gemv_down_kernel(const GemvParams p)
+// CTA = TPW row tiles of 16 rows x KS K-splits.
+template <int KS>
+__global__ void __launch_bounds__(kThreads, 2) gemv_down_kernel(const GemvParams p)
 {
-    constexpr int TPC = 8 / KSPLIT;
-    __shared__ float red[8][32][4];
+    constexpr int TPW = 8 / KS;
+    extern __shared__ uint4 smem_b[];
+    __shared__ float inv[kGemvBlock];
+    __shared__ float red[KS > 1 ? 8 : 1][32][4];
+    __shared__ int rows[kGemvBlock];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int ks = warp % KSPLIT, tw = warp / KSPLIT;
+    const int ks = warp % KS, tw = warp / KS;
     const int g = lane >> 2, c = lane & 3;
+    const int Kp = (p.K + kStep - 1) / kStep * kStep;
     const int n_pos = load_n_pos(p);
-    const int n_units = (n_pos / kGemvBlock) * p.n_tiles;
-    const int Kw = p.K / KSPLIT, k0 = ks * Kw;
-    const int n_steps = (Kw + 63) / 64;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int blk = u / p.n_tiles, tile = u - blk * p.n_tiles;
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
-        const int n0 = (tile * TPC + tw) * 16;
-        const bool tile_ok = n0 < p.R;
-        const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
-        const uint8_t *scales_e = p.scales + (size_t)e * p.e_scales;
-        const int arow = act_row_down(p, blk * kGemvBlock + g, n_pos);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s0 = 0; s0 < n_steps; s0 += kUnroll) {
-            TileStep st[kUnroll];
-            uint32_t b[kUnroll][8];
-#pragma unroll
-            for (int q = 0; q < kUnroll; ++q) {
-                const int piece = 4 * (s0 + q) + c;
-                const bool ok = tile_ok && (s0 + q) < n_steps && 16 * piece < Kw;
-                const int kk = k0 + 16 * piece;
-                load_tile_step(codes_e, scales_e, p.K, p.group, n0 + g, kk, ok, st[q]);
-                load_act(p.act, p.K, arow, kk, ok, b[q]);
-            }
-#pragma unroll
-            for (int q = 0; q < kUnroll; ++q) mma_tile_step(st[q], b[q], acc);
+    const int n_groups = p.n_tiles;
+    const int n_units = (n_pos / kGemvBlock) * n_groups;
+    const int Kw = p.K / KS, k0 = ks * Kw;
+    const int n_steps = (Kw + kStep - 1) / kStep;
+    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    int staged = -1;
+    for (int u = u_lo; u < u_hi; ++u) {
+        const int blk = u / n_groups, grp = u - blk * n_groups;
+        if (blk != staged) {
+            __syncthreads();
+            if (threadIdx.x < kGemvBlock) rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, false);
+            __syncthreads();
+            stage_block(p.act, p.K, Kp, rows, smem_b, inv);
+            __syncthreads();
+            staged = blk;
         }
-        if (KSPLIT > 1) {
+        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int n0 = (grp * TPW + tw) * 16;
+        const bool tile_ok = n0 < p.R;
+        const uint8_t *codes = p.codes + (size_t)e * p.e_codes + (size_t)(n0 + g) * (p.K / 2);
+        const uint8_t *scales = p.scales + (size_t)e * p.e_scales + (size_t)(n0 + g) * (p.K / p.group);
+        const uint4 *brow = smem_b + (size_t)g * (Kp / 8);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        auto piece_k = [&](int s) { return k0 + kStep * s + 32 * c; };
+        auto valid = [&](int s) {
+            return (tile_ok && s < n_steps) ? max(0, min(32, Kw - (kStep * s + 32 * c))) : 0;
+        };
+        Frag f0, f1;
+        load_frag(codes, scales, p.K, p.group, piece_k(0), valid(0), f0);
+        load_frag(codes, scales, p.K, p.group, piece_k(1), valid(1), f1);
+        for (int s = 0; s < n_steps; s += 2) {
+            Frag f2, f3;
+            load_frag(codes, scales, p.K, p.group, piece_k(s + 2), valid(s + 2), f2);
+            load_frag(codes, scales, p.K, p.group, piece_k(s + 3), valid(s + 3), f3);
+            uint4 b[4];
+            load_b(brow, (k0 + kStep * s) / 8 + 4 * c, g, b);
+            mma_frag(f0, b, acc);
+            if (s + 1 < n_steps) {
+                load_b(brow, (k0 + kStep * (s + 1)) / 8 + 4 * c, g, b);
+                mma_frag(f1, b, acc);
+            }
+            f0 = f2; f1 = f3;
+        }
+        if (KS > 1) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) red[warp][lane][i] = acc[i];
             __syncthreads();
         }
         if (ks == 0 && tile_ok) {
-            if (KSPLIT > 1) {
+            if (KS > 1) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float a = 0.f;
-                    for (int w = 0; w < KSPLIT; ++w) a += red[tw * KSPLIT + w][lane][i];
+                    for (int w = 0; w < KS; ++w) a += red[tw * KS + w][lane][i];
                     acc[i] = a;
                 }
             }
@@ -252,11 +361,11 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(const GemvParams p)
                 const int pos = blk * kGemvBlock + 2 * c + col;
                 if (pos >= n_pos) continue;
                 int dst;
-                float wgt = 1.0f;
+                float wgt = inv[2 * c + col];
                 if (p.sorted_slot) {
                     dst = __ldg(p.sorted_slot + pos);
                     if (dst >= p.n_slots) continue;
-                    if (p.route_w) wgt = __ldg(p.route_w + dst);
+                    if (p.route_w) wgt *= __ldg(p.route_w + dst);
                 } else {
                     dst = pos;
                     if (dst >= p.n_pos_static) continue;
@@ -268,7 +377,7 @@ __global__ void __launch_bounds__(256) gemv_down_kernel(const GemvParams p)
                 }
             }
         }
-        if (KSPLIT > 1) __syncthreads();
+        if (KS > 1) __syncthreads();
     }
 }
 
@@ -304,31 +413,52 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
 
 // ---------------------------------------------------------------- launchers
 
-static int grid_for(int max_units, int per_sm)
-{
-    int g = sm_count() * per_sm;
-    if (max_units < g) g = max_units;
-    return g < 1 ? 1 : g;
-}
+static size_t stage_bytes(int K) { return (size_t)kGemvBlock * ((K + kStep - 1) / kStep * kStep) * 2; }
 
-cudaError_t launch_gemv_gated(const GemvParams &p, int max_units, cudaStream_t s)
+template <typename Kern>
+static cudaError_t launch_persistent(Kern kern, const GemvParams &p, int max_units, cudaStream_t s)
 {
-    gemv_gated_kernel<8><<<grid_for(max_units, 4), 256, 0, s>>>(p);
+    const size_t smem = stage_bytes(p.K);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int grid = sm_count() * 2;
+    if (max_units < grid) grid = max_units;
+    if (grid < 1) grid = 1;
+    kern<<<grid, kThreads, smem, s>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemv_down(const GemvParams &p, int ksplit, int max_units, cudaStream_t s)
+// K-split so that the unit count covers the GPU: the smallest of 1, 2, 4, 8 with
+// enough units, keeping each warp's K range a multiple of the 128-element step.
+int gemv_ksplit(int max_blocks, int rows_units_per_block_at_ks1, int K)
 {
-    const int grid = grid_for(max_units, 4);
-    switch (ksplit) {
-    case 1: gemv_down_kernel<1><<<grid, 256, 0, s>>>(p); break;
-    case 2: gemv_down_kernel<2><<<grid, 256, 0, s>>>(p); break;
-    case 4: gemv_down_kernel<4><<<grid, 256, 0, s>>>(p); break;
-    default: gemv_down_kernel<8><<<grid, 256, 0, s>>>(p); break;
+    const int target = 2 * sm_count();
+    int ks = 1;
+    while (ks < 8 && max_blocks * rows_units_per_block_at_ks1 * ks < target && (K / (ks * 2)) % kStep == 0 &&
+           K / (ks * 2) >= kStep)
+        ks *= 2;
+    return ks;
+}
+
+cudaError_t launch_gemv_gated(const GemvParams &p, int ks, int max_units, cudaStream_t s)
+{
+    switch (ks) {
+    case 1: return launch_persistent(gemv_gated_kernel<1>, p, max_units, s);
+    case 2: return launch_persistent(gemv_gated_kernel<2>, p, max_units, s);
+    case 4: return launch_persistent(gemv_gated_kernel<4>, p, max_units, s);
+    default: return launch_persistent(gemv_gated_kernel<8>, p, max_units, s);
     }
-    count_launches(1);
-    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_down(const GemvParams &p, int ks, int max_units, cudaStream_t s)
+{
+    switch (ks) {
+    case 1: return launch_persistent(gemv_down_kernel<1>, p, max_units, s);
+    case 2: return launch_persistent(gemv_down_kernel<2>, p, max_units, s);
+    case 4: return launch_persistent(gemv_down_kernel<4>, p, max_units, s);
+    default: return launch_persistent(gemv_down_kernel<8>, p, max_units, s);
+    }
 }
 
 cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, int H, void *out, int out_dtype,
