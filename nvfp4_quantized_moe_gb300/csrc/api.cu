@@ -155,6 +155,47 @@ static WsLayout ws_layout(const Geometry &G, int T)
     return L;
 }
 
+// One grouped GEMV launch: the bulk-copy-fed kernel when the shape allows it, else the
+// register-fed one. `rows` = I_l (gated) or H (down); max_blocks bounds the blocks.
+#ifndef FTMOE_GEMV_USE_TMA
+#define FTMOE_GEMV_USE_TMA 0  // 1: prefer the bulk-copy-fed kernel where the shape allows it
+#endif
+
+static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, cudaStream_t s)
+{
+    auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
+    if (!FTMOE_GEMV_USE_TMA) {
+        const int pr = gated ? 16 : 32;
+        int ks = 1;
+        while (ks < 8 && max_blocks * cdiv(rows, pr * (8 / ks)) < 2 * sm_count() && (p.K / (2 * ks)) % 128 == 0)
+            ks *= 2;
+        if (gemv_fast_ok(p.K, p.group, ks)) {
+            p.n_tiles = cdiv(rows, pr * (8 / ks));
+            return launch_gemv_fast(p, gated, ks, max_blocks * p.n_tiles, s);
+        }
+    }
+    if (FTMOE_GEMV_USE_TMA) {
+    const int pair_rows = gated ? 16 : 32;
+    int ks = 1;
+    while (ks < 8 && max_blocks * cdiv(rows, pair_rows * (8 / ks)) < sm_count() && (p.K / (2 * ks)) % 128 == 0)
+        ks *= 2;
+    int kc = 0;
+    for (; ks >= 1; ks /= 2)
+        if ((kc = gemv_tma_chunk(p.K, p.group, ks)) != 0) break;
+    if (kc) {
+        const int nw = gemv_tma_warps(p.K, p.group, kc);
+        if (nw && ks <= nw) {
+            p.n_tiles = cdiv(rows, pair_rows * (nw / ks));
+            return launch_gemv_tma(p, gated, ks, kc, nw, max_blocks * p.n_tiles, s);
+        }
+    }
+    }
+    const int ks2 = gemv_ksplit(max_blocks, cdiv(rows, 128), p.K);
+    p.n_tiles = cdiv(rows, 16 * (8 / ks2));
+    return gated ? launch_gemv_gated(p, ks2, max_blocks * p.n_tiles, s)
+                 : launch_gemv_down(p, ks2, max_blocks * p.n_tiles, s);
+}
+
 static bool banks_ok(const ft_moe_banks *b)
 {
     if (!b) return false;
@@ -357,7 +398,6 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
 
     const int max_blocks = L.pmax / kGemvBlock;
     const int tpad = (T + kGemvBlock - 1) / kGemvBlock;
-    auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
 
     // gate_up + SwiGLU
     GemvParams gp = {};
@@ -368,35 +408,29 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il;
     gp.act = static_cast<const uint16_t *>(x);
     gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp;
-    const int gks = gemv_ksplit(max_blocks, cdiv(G.Il, 128), G.H);
-    gp.n_slots = n_slots; gp.top_k = G.k; gp.n_tiles = cdiv(G.Il, 16 * (8 / gks)); gp.num_experts = G.E;
+    gp.n_slots = n_slots; gp.top_k = G.k; gp.num_experts = G.E;
     gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
     if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-    e = launch_gemv_gated(gp, gks, max_blocks * gp.n_tiles, s);
-    if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
+    if ((e = run_gemv(gp, true, max_blocks, G.Il, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
 
-    GemvParams sp = {};
     if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     if (G.Is) {
-        sp = gp;
+        GemvParams sp = gp;
         sp.codes = static_cast<const uint8_t *>(shared->p[FT_GU]);
         sp.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
         sp.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
         sp.e_codes = (int64_t)G.Isl * G.H; sp.e_scales = (int64_t)2 * G.Isl * G.H / G.g; sp.e_glob = 2 * G.Isl;
         sp.R = 2 * G.Isl; sp.up_off = G.Isl;
         sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
-        const int sks = gemv_ksplit(tpad, cdiv(G.Isl, 128), G.H);
-        sp.n_slots = T; sp.top_k = 1; sp.n_tiles = cdiv(G.Isl, 16 * (8 / sks)); sp.num_experts = 1;
+        sp.n_slots = T; sp.top_k = 1; sp.num_experts = 1;
         sp.h_out = h_sh; sp.h_ld = G.Isl;
-        e = launch_gemv_gated(sp, sks, tpad * sp.n_tiles, s);
-        if (e != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
+        if ((e = run_gemv(sp, true, tpad, G.Isl, s)) != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
     }
 
     // down + routing weight
     if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     {
         GemvParams dp = {};
-        const int ks = gemv_ksplit(max_blocks, cdiv(G.H, 128), G.Il), rows_per_cta = 16 * (8 / ks);
         dp.codes = static_cast<const uint8_t *>(routed->p[FT_DN]);
         dp.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
         dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
@@ -404,25 +438,22 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         dp.R = G.H; dp.K = G.Il; dp.group = G.g;
         dp.act = h;
         dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp;
-        dp.n_slots = n_slots; dp.top_k = G.k; dp.n_tiles = (G.H + rows_per_cta - 1) / rows_per_cta;
+        dp.n_slots = n_slots; dp.top_k = G.k;
         dp.num_experts = G.E; dp.y_out = y; dp.route_w = topk_w; dp.status = status;
-        e = launch_gemv_down(dp, ks, max_blocks * dp.n_tiles, s);
-        if (e != cudaSuccess) return cuda_fail(e, "down launch");
+        if ((e = run_gemv(dp, false, max_blocks, G.H, s)) != cudaSuccess) return cuda_fail(e, "down launch");
     }
     if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     if (G.Is) {
         GemvParams dp = {};
-        const int ks = gemv_ksplit(tpad, cdiv(G.H, 128), G.Isl), rows_per_cta = 16 * (8 / ks);
         dp.codes = static_cast<const uint8_t *>(shared->p[FT_DN]);
         dp.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
         dp.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
         dp.e_codes = (int64_t)G.H * G.Isl / 2; dp.e_scales = (int64_t)G.H * G.Isl / G.g; dp.e_glob = G.H;
         dp.R = G.H; dp.K = G.Isl; dp.group = G.g;
         dp.act = h_sh;
-        dp.n_pos_static = T; dp.n_slots = T; dp.top_k = 1; dp.n_tiles = (G.H + rows_per_cta - 1) / rows_per_cta;
+        dp.n_pos_static = T; dp.n_slots = T; dp.top_k = 1;
         dp.num_experts = 1; dp.y_out = y_sh; dp.route_w = nullptr; dp.status = status;
-        e = launch_gemv_down(dp, ks, tpad * dp.n_tiles, s);
-        if (e != cudaSuccess) return cuda_fail(e, "shared down launch");
+        if ((e = run_gemv(dp, false, tpad, G.H, s)) != cudaSuccess) return cuda_fail(e, "shared down launch");
     }
     if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);

@@ -64,6 +64,16 @@ int gemv_ksplit(int max_blocks, int units_per_block_ks1, int K);
 // p.n_tiles = CTA units per block: ceil(rows / (16 * 8 / ks)) with rows = I_l (gated) or H.
 cudaError_t launch_gemv_gated(const GemvParams &p, int ks, int max_units, cudaStream_t s);
 cudaError_t launch_gemv_down(const GemvParams &p, int ks, int max_units, cudaStream_t s);
+// Bulk-copy-fed GEMV: K chunk per stage (0 = shape not supported), warps per CTA
+// (0 = does not fit), launch. p.n_tiles = ceil(rows / (pair_rows * nw / ks)) with
+// pair_rows = 16 (gated, rows = I_l) or 32 (down, rows = H).
+int gemv_tma_chunk(int K, int group, int ks);
+// Lean register-fed GEMV (two 16-row tiles per warp): usable when K % 32 == 0 and
+// (K / ks) % 128 == 0. p.n_tiles = ceil(rows / (pair_rows * 8 / ks)).
+bool gemv_fast_ok(int K, int group, int ks);
+cudaError_t launch_gemv_fast(const GemvParams &p, bool gated, int ks, int max_units, cudaStream_t s);
+int gemv_tma_warps(int K, int group, int kc);
+cudaError_t launch_gemv_tma(const GemvParams &p, bool gated, int ks, int kc, int nw, int max_units, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, int H, void *out, int out_dtype,
                            cudaStream_t s);
 

@@ -24,86 +24,17 @@
 
 #include "ftmoe_device.cuh"
 #include "ftmoe_internal.h"
+#include "gemv_common.cuh"
+
+#ifndef FTMOE_GEMV_MIN_BLOCKS
+#define FTMOE_GEMV_MIN_BLOCKS 2  // resident CTAs per SM the register budget is sized for
+#endif
 
 namespace ftmoe {
 
+using namespace gemv;
+
 namespace {
-
-constexpr int kThreads = 256;  // 8 warps per CTA
-constexpr int kStep = 128;     // K elements per warp step (4 lanes x 32)
-
-__device__ __forceinline__ int load_n_pos(const GemvParams &p)
-{
-    return p.n_pos_dev ? *p.n_pos_dev : (p.n_pos_static + kGemvBlock - 1) / kGemvBlock * kGemvBlock;
-}
-
-// Source row of block position `pos` (x row for gate_up, h row for down), or -1 for padding.
-__device__ __forceinline__ int source_row(const GemvParams &p, int pos, int n_pos, bool gated)
-{
-    if (pos >= n_pos) return -1;
-    if (p.sorted_slot) {
-        const int s = __ldg(p.sorted_slot + pos);
-        if (s >= p.n_slots) return -1;
-        return gated ? s / p.top_k : pos;
-    }
-    return (pos < p.n_pos_static) ? pos : -1;
-}
-
-// Physical 16-byte chunk of logical chunk q in staged row r. With a row pitch that is a
-// multiple of 128 bytes, the 8 lanes of each LDS.128 phase (rows 2m, 2m+1; lanes c = 0..3
-// reading chunks base + 4c + j) land in 8 distinct bank quads.
-__device__ __forceinline__ int swz(int q, int r) { return q ^ (((q >> 3) & 1) << 1) ^ (r & 1); }
-
-// Stage the block's 8 activation rows (bf16, length K) into shared memory as f16 scaled
-// by 2^-e_r; inv[r] = 2^e_r. Warp r handles row r. The row pitch is Kp >= K elements
-// (a multiple of kStep) and the tail [K, Kp) is zero.
-__device__ void stage_block(const uint16_t *__restrict__ src, int K, int Kp, const int *rows, uint4 *sm,
-                            float *inv)
-{
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = warp;
-    const int row = rows[r];
-    uint4 *dst = sm + (size_t)r * (Kp / 8);
-    if (row < 0) {
-        for (int q = lane; q < Kp / 8; q += 32) dst[swz(q, r)] = make_uint4(0, 0, 0, 0);
-        if (lane == 0) inv[r] = 0.f;
-        return;
-    }
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)row * K);
-    float m = 0.f;
-    for (int q = lane; q < K / 8; q += 32) {
-        const uint4 v = __ldg(s4 + q);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
-            m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    // 2^e with m * 2^-e in [2^14, 2^15); non-finite or zero rows keep e = 0.
-    int e = 0;
-    if (m > 0.f && m <= 3.3895314e38f) e = ilogbf(m) - 14;
-    const float down = exp2f((float)-e);
-    for (int q = lane; q < Kp / 8; q += 32) {
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (q < K / 8) {
-            const uint4 v = __ldg(s4 + q);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t h[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __half2 hh = __floats2half2_rn(__uint_as_float(w[i] << 16) * down,
-                                                     __uint_as_float(w[i] & 0xFFFF0000u) * down);
-                h[i] = *reinterpret_cast<const uint32_t *>(&hh);
-            }
-            o = make_uint4(h[0], h[1], h[2], h[3]);
-        }
-        dst[swz(q, r)] = o;
-    }
-    if (lane == 0) inv[r] = exp2f((float)e);
-}
 
 // Codes and scales of one K step for rows g and g+8 of a 16-row tile.
 struct Frag {
@@ -147,26 +78,7 @@ __device__ __forceinline__ void load_frag(const uint8_t *codes_row_lo, const uin
 // 8 MMAs of one K step: A from the fragment, B (4 x 16 bytes of f16) from shared memory.
 __device__ __forceinline__ void mma_frag(const Frag &f, const uint4 (&b)[4], float (&acc)[4])
 {
-    uint32_t s_lo[2], s_hi[2];
-    e4m3x2_to_f16x2_bcast(f.slo, s_lo[0], s_lo[1]);
-    e4m3x2_to_f16x2_bcast(f.shi, s_hi[0], s_hi[1]);
-    const uint32_t cl[4] = {f.lo.x, f.lo.y, f.lo.z, f.lo.w};
-    const uint32_t ch[4] = {f.hi.x, f.hi.y, f.hi.z, f.hi.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {  // 8 elements per code word; words 0,1 use scale 0, words 2,3 scale 1
-        uint32_t al[4], ah[4];
-        dequant8_f16(cl[w], s_lo[w >> 1], al);
-        dequant8_f16(ch[w], s_hi[w >> 1], ah);
-        const uint32_t bw[4] = {b[w].x, b[w].y, b[w].z, b[w].w};
-        mma_f16_16816(acc, al[0], ah[0], al[1], ah[1], bw[0], bw[1]);
-        mma_f16_16816(acc, al[2], ah[2], al[3], ah[3], bw[2], bw[3]);
-    }
-}
-
-__device__ __forceinline__ void load_b(const uint4 *sm_row, int q0, int r, uint4 (&b)[4])
-{
-#pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = sm_row[swz(q0 + j, r)];
+    mma_step(f.lo, f.hi, f.slo, f.shi, b, acc);
 }
 
 }  // namespace
@@ -176,7 +88,7 @@ __device__ __forceinline__ void load_b(const uint4 *sm_row, int q0, int r, uint4
 // CTA = TPW tile pairs x KS K-splits (TPW * KS = 8 warps). A tile pair is gate rows
 // [i0, i0+16) and up rows I_l + [i0, i0+16).
 template <int KS>
-__global__ void __launch_bounds__(kThreads, 2) gemv_gated_kernel(const GemvParams p)
+__global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_gated_kernel(const GemvParams p)
 {
     constexpr int TPW = 8 / KS;
     extern __shared__ uint4 smem_b[];
@@ -285,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_gated_kernel(const GemvParam
 
 // CTA = TPW row tiles of 16 rows x KS K-splits.
 template <int KS>
-__global__ void __launch_bounds__(kThreads, 2) gemv_down_kernel(const GemvParams p)
+__global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_down_kernel(const GemvParams p)
 {
     constexpr int TPW = 8 / KS;
     extern __shared__ uint4 smem_b[];
@@ -421,7 +333,7 @@ static cudaError_t launch_persistent(Kern kern, const GemvParams &p, int max_uni
     const size_t smem = stage_bytes(p.K);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    int grid = sm_count() * 2;
+    int grid = sm_count() * FTMOE_GEMV_MIN_BLOCKS;
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
     kern<<<grid, kThreads, smem, s>>>(p);

@@ -1,0 +1,234 @@
+// Decode-regime grouped GEMV, lean register-fed variant for the common shapes
+// (K a multiple of 32 and each warp's K range a multiple of 128).
+//
+// Same arithmetic as gemv.cu: exact f16 code*scale weights against f16 activations
+// staged per block with a power-of-two row scale, m16n8k16 MMAs with fp32
+// accumulation, weights as M and the block's 8 tokens as N. Each warp owns two 16-row
+// tiles (gate rows i and up rows I_l + i for gate_up; rows n and n + 16 for down) over
+// its K range. Loads run two 128-element steps ahead through a 4-slot register ring;
+// every address is a per-lane base plus a step offset; scales arrive as one 16-bit load
+// per row and step; the activation swizzle reduces to a per-lane XOR, precomputed.
+#include <cuda_runtime.h>
+
+#include "ftmoe_device.cuh"
+#include "ftmoe_internal.h"
+#include "gemv_common.cuh"
+
+namespace ftmoe {
+
+using namespace gemv;
+
+namespace {
+
+struct FastFrag {
+    uint4 a_lo, a_hi, b_lo, b_hi;  // codes: tile 0 rows g / g+8, tile 1 rows g / g+8
+    uint32_t sa, sb;               // scales: tile 0 (row g low 16 bits, row g+8 high), tile 1
+};
+
+struct FastPtrs {
+    const uint8_t *ca, *cb, *sa, *sb;  // lane bases for tile 0 / tile 1 codes and scales
+    size_t crow8, srow8;               // byte offsets to the row 8 further down
+    int group;
+};
+
+__device__ __forceinline__ uint32_t scale_pair(const uint8_t *p, int group)
+{
+    if (group == 16) return __ldg(reinterpret_cast<const uint16_t *>(p));
+    const uint32_t b = __ldg(p);
+    return b | (b << 8);
+}
+
+__device__ __forceinline__ void fast_load(const FastPtrs &P, int s, FastFrag &f)
+{
+    const int co = 64 * s;                     // 128 elements = 64 code bytes per step
+    const int so = (P.group == 16) ? 8 * s : 4 * s;
+    f.a_lo = ldg_nc_v4(P.ca + co);
+    f.a_hi = ldg_nc_v4(P.ca + P.crow8 + co);
+    f.b_lo = ldg_nc_v4(P.cb + co);
+    f.b_hi = ldg_nc_v4(P.cb + P.crow8 + co);
+    f.sa = scale_pair(P.sa + so, P.group) | (scale_pair(P.sa + P.srow8 + so, P.group) << 16);
+    f.sb = scale_pair(P.sb + so, P.group) | (scale_pair(P.sb + P.srow8 + so, P.group) << 16);
+}
+
+__device__ __forceinline__ void fast_compute(const FastFrag &f, const uint4 *bb, const int (&boff)[4], int s,
+                                             float (&acc0)[4], float (&acc1)[4])
+{
+    uint4 b[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) b[j] = bb[16 * s + boff[j]];
+    mma_step(f.a_lo, f.a_hi, f.sa & 0xFFFFu, f.sa >> 16, b, acc0);
+    mma_step(f.b_lo, f.b_hi, f.sb & 0xFFFFu, f.sb >> 16, b, acc1);
+}
+
+}  // namespace
+
+template <bool GATED, int KS>
+__global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const GemvParams p)
+{
+    constexpr int TPW = 8 / KS;
+    extern __shared__ uint4 smem_b[];
+    __shared__ float inv[kGemvBlock];
+    __shared__ int rows[kGemvBlock];
+    __shared__ float red[KS > 1 ? 8 : 1][32][8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ks = warp % KS, tp = warp / KS;
+    const int g = lane >> 2, c = lane & 3;
+    const int K = p.K;
+    const int n_pos = load_n_pos(p);
+    const int n_groups = p.n_tiles;
+    const int n_units = (n_pos / kGemvBlock) * n_groups;
+    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    const int Kw = K / KS, k0 = ks * Kw, nstep = Kw / kStep;
+    const int pair_rows = GATED ? 16 : 32;
+    const int rows_limit = GATED ? p.up_off : p.R;
+    // chunk j of step s of this lane lives at 16 s + 4 c + (j ^ m) (see swz)
+    const int m = ((c >> 1) << 1) ^ (g & 1);
+    const int boff[4] = {4 * c + (0 ^ m), 4 * c + (1 ^ m), 4 * c + (2 ^ m), 4 * c + (3 ^ m)};
+    int staged = -1;
+    for (int u = u_lo; u < u_hi; ++u) {
+        const int blk = u / n_groups, grp = u - blk * n_groups;
+        if (blk != staged) {
+            __syncthreads();
+            if (threadIdx.x < kGemvBlock)
+                rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, GATED);
+            __syncthreads();
+            stage_block(p.act, K, K, rows, smem_b, inv);
+            __syncthreads();
+            staged = blk;
+        }
+        const int r0 = (grp * TPW + tp) * pair_rows;
+        const bool ok = r0 < rows_limit;
+        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ok) {
+            const int row_a = r0 + g, row_b = GATED ? p.up_off + r0 + g : r0 + 16 + g;
+            const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
+            const uint8_t *scales_e = p.scales + (size_t)e * p.e_scales;
+            FastPtrs P;
+            P.ca = codes_e + (size_t)row_a * (K / 2) + k0 / 2 + 16 * c;
+            P.cb = codes_e + (size_t)row_b * (K / 2) + k0 / 2 + 16 * c;
+            P.sa = scales_e + (size_t)row_a * (K / p.group) + (k0 + 32 * c) / p.group;
+            P.sb = scales_e + (size_t)row_b * (K / p.group) + (k0 + 32 * c) / p.group;
+            P.crow8 = (size_t)8 * (K / 2);
+            P.srow8 = (size_t)8 * (K / p.group);
+            P.group = p.group;
+            const uint4 *bb = smem_b + (size_t)g * (K / 8) + k0 / 8;
+            FastFrag ring[4];
+            fast_load(P, 0, ring[0]);
+            if (nstep > 1) fast_load(P, 1, ring[1]);
+            for (int s0 = 0; s0 < nstep; s0 += 4) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int s = s0 + q;
+                    if (s + 2 < nstep) fast_load(P, s + 2, ring[(q + 2) & 3]);
+                    if (s < nstep) fast_compute(ring[q], bb, boff, s, acc0, acc1);
+                }
+            }
+        }
+        if (KS > 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                red[warp][lane][i] = acc0[i];
+                red[warp][lane][4 + i] = acc1[i];
+            }
+            __syncthreads();
+        }
+        if (ks == 0 && ok) {
+            if (KS > 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float a = 0.f, b2 = 0.f;
+                    for (int w = 0; w < KS; ++w) {
+                        a += red[tp * KS + w][lane][i];
+                        b2 += red[tp * KS + w][lane][4 + i];
+                    }
+                    acc0[i] = a;
+                    acc1[i] = b2;
+                }
+            }
+            const float *glob_e = p.glob + (size_t)e * p.e_glob;
+            if (GATED) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int i = r0 + g + 8 * half;
+                    const float gg = __ldg(glob_e + i), gu = __ldg(glob_e + p.up_off + i);
+#pragma unroll
+                    for (int col = 0; col < 2; ++col) {
+                        const int pos = blk * kGemvBlock + 2 * c + col;
+                        const float scl = inv[2 * c + col];
+                        const float gate = acc0[2 * half + col] * scl * gg;
+                        const float up = acc1[2 * half + col] * scl * gu;
+                        __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
+                        p.h_out[(size_t)pos * p.h_ld + i] = *reinterpret_cast<uint16_t *>(&hv);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int col = 0; col < 2; ++col) {
+                    const int pos = blk * kGemvBlock + 2 * c + col;
+                    if (pos >= n_pos) continue;
+                    int dst;
+                    float wgt = inv[2 * c + col];
+                    if (p.sorted_slot) {
+                        dst = __ldg(p.sorted_slot + pos);
+                        if (dst >= p.n_slots) continue;
+                        if (p.route_w) wgt *= __ldg(p.route_w + dst);
+                    } else {
+                        dst = pos;
+                        if (dst >= p.n_pos_static) continue;
+                    }
+                    float *yrow = p.y_out + (size_t)dst * p.R;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int n = r0 + g + 8 * half;
+                        yrow[n] = acc0[2 * half + col] * __ldg(glob_e + n) * wgt;
+                        yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * wgt;
+                    }
+                }
+            }
+        }
+        if (KS > 1) __syncthreads();
+    }
+}
+
+// Usable for this shape and K-split?
+bool gemv_fast_ok(int K, int group, int ks)
+{
+    return K % 32 == 0 && (K / ks) % kStep == 0 && (group == 16 || group == 32);
+}
+
+template <bool GATED, int KS>
+static cudaError_t launch_fast_t(const GemvParams &p, int max_units, cudaStream_t s)
+{
+    auto kern = gemv_fast_kernel<GATED, KS>;
+    const size_t smem = (size_t)kGemvBlock * p.K * 2;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int grid = sm_count() * 2;
+    if (max_units < grid) grid = max_units;
+    if (grid < 1) grid = 1;
+    kern<<<grid, kThreads, smem, s>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_fast(const GemvParams &p, bool gated, int ks, int max_units, cudaStream_t s)
+{
+    if (gated) {
+        switch (ks) {
+        case 1: return launch_fast_t<true, 1>(p, max_units, s);
+        case 2: return launch_fast_t<true, 2>(p, max_units, s);
+        case 4: return launch_fast_t<true, 4>(p, max_units, s);
+        default: return launch_fast_t<true, 8>(p, max_units, s);
+        }
+    }
+    switch (ks) {
+    case 1: return launch_fast_t<false, 1>(p, max_units, s);
+    case 2: return launch_fast_t<false, 2>(p, max_units, s);
+    case 4: return launch_fast_t<false, 4>(p, max_units, s);
+    default: return launch_fast_t<false, 8>(p, max_units, s);
+    }
+}
+
+}  // namespace ftmoe
