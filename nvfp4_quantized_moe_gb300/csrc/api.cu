@@ -128,7 +128,8 @@ static void bank_specs(const Geometry &G, int shared, ft_bank_spec out[FT_NBANKS
 
 // Workspace regions of ft_moe_forward, each 256-byte aligned.
 struct WsLayout {
-    size_t status, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    size_t status, counters, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    size_t zero_bytes;  // [status, counters) cleared at the start of every forward
     int pmax;
 };
 
@@ -141,6 +142,8 @@ static WsLayout ws_layout(const Geometry &G, int T)
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = round_up(o + bytes, 256); return at; };
     L.status = take(256);
+    L.counters = take(sizeof(int) * (size_t)T * (G.H / 32));
+    L.zero_bytes = o;
     L.sorted = take(sizeof(int) * (size_t)pmax);
     L.block_expert = take(sizeof(int) * (size_t)(pmax / kGemvBlock + 1));
     L.expert_off = take(sizeof(int) * (size_t)(G.E + 1));
@@ -157,6 +160,18 @@ static WsLayout ws_layout(const Geometry &G, int T)
 
 // One grouped GEMV launch: the bulk-copy-fed kernel when the shape allows it, else the
 // register-fed one. `rows` = I_l (gated) or H (down); max_blocks bounds the blocks.
+// K-split for a merged lean launch: the smallest of 1, 2, 4, 8 that gives at least two
+// CTA units per SM, as long as every K range stays a multiple of 128.
+static int fast_ksplit(int blocks, int units_per_block_ks1, int K0, int K1 = 0)
+{
+    if (!K1) K1 = K0;
+    int ks = 1;
+    while (ks < 8 && blocks * units_per_block_ks1 * ks < 2 * sm_count() && (K0 / (2 * ks)) % 128 == 0 &&
+           (K1 / (2 * ks)) % 128 == 0)
+        ks *= 2;
+    return ks;
+}
+
 #ifndef FTMOE_GEMV_USE_TMA
 #define FTMOE_GEMV_USE_TMA 0  // 1: prefer the bulk-copy-fed kernel where the shape allows it
 #endif
@@ -164,16 +179,6 @@ static WsLayout ws_layout(const Geometry &G, int T)
 static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, cudaStream_t s)
 {
     auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
-    if (!FTMOE_GEMV_USE_TMA) {
-        const int pr = gated ? 16 : 32;
-        int ks = 1;
-        while (ks < 8 && max_blocks * cdiv(rows, pr * (8 / ks)) < 2 * sm_count() && (p.K / (2 * ks)) % 128 == 0)
-            ks *= 2;
-        if (gemv_fast_ok(p.K, p.group, ks)) {
-            p.n_tiles = cdiv(rows, pr * (8 / ks));
-            return launch_gemv_fast(p, gated, ks, max_blocks * p.n_tiles, s);
-        }
-    }
     if (FTMOE_GEMV_USE_TMA) {
     const int pair_rows = gated ? 16 : 32;
     int ks = 1;
@@ -390,7 +395,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     const int n_slots = T * G.k;
 
     struct Disarm { ~Disarm() { g_stage_armed = false; } } disarm_on_return;
-    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+    cudaError_t e = cudaMemsetAsync(status, 0, L.zero_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     e = launch_align(topk_ids, T, G.k, G.E, kGemvBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s);
@@ -398,6 +403,78 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
 
     const int max_blocks = L.pmax / kGemvBlock;
     const int tpad = (T + kGemvBlock - 1) / kGemvBlock;
+    auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
+
+    // Lean kernels, routed and shared expert in one launch per stage, combine fused
+    // into the down stage.
+    const int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H);
+    const int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
+    if (!FTMOE_GEMV_USE_TMA && gemv_fast_ok(G.H, G.g, ks_gu) && gemv_fast_ok(G.Il, G.g, ks_dn) &&
+        (!G.Is || gemv_fast_ok(G.Isl, G.g, ks_dn))) {
+        FastLaunch F = {};
+        GemvParams &r = F.prob[0];
+        r.codes = static_cast<const uint8_t *>(routed->p[FT_GU]);
+        r.scales = static_cast<const uint8_t *>(routed->p[FT_GU_SCALE]);
+        r.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
+        r.e_codes = (int64_t)G.Il * G.H; r.e_scales = (int64_t)2 * G.Il * G.H / G.g; r.e_glob = 2 * G.Il;
+        r.R = 2 * G.Il; r.K = G.H; r.group = G.g; r.up_off = G.Il;
+        r.act = static_cast<const uint16_t *>(x);
+        r.n_pos_dev = npad; r.sorted_slot = sorted; r.block_expert = bexp;
+        r.n_slots = n_slots; r.top_k = G.k; r.num_experts = G.E; r.status = status;
+        r.n_tiles = cdiv(G.Il, 16 * (8 / ks_gu)); r.h_out = h; r.h_ld = G.Il;
+        F.nprob = 1;
+        if (G.Is) {
+            GemvParams &q = F.prob[1];
+            q = r;
+            q.codes = static_cast<const uint8_t *>(shared->p[FT_GU]);
+            q.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
+            q.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
+            q.e_codes = (int64_t)G.Isl * G.H; q.e_scales = (int64_t)2 * G.Isl * G.H / G.g; q.e_glob = 2 * G.Isl;
+            q.R = 2 * G.Isl; q.up_off = G.Isl;
+            q.n_pos_dev = nullptr; q.n_pos_static = T; q.sorted_slot = nullptr; q.block_expert = nullptr;
+            q.n_slots = T; q.top_k = 1; q.num_experts = 1;
+            q.n_tiles = cdiv(G.Isl, 16 * (8 / ks_gu)); q.h_out = h_sh; q.h_ld = G.Isl;
+            F.nprob = 2;
+        }
+        if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        int max_units = max_blocks * r.n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
+        if ((e = launch_gemv_fast(F, true, ks_gu, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
+        if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+
+        FastLaunch D = {};
+        GemvParams &d = D.prob[0];
+        d.codes = static_cast<const uint8_t *>(routed->p[FT_DN]);
+        d.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
+        d.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
+        d.e_codes = (int64_t)G.H * G.Il / 2; d.e_scales = (int64_t)G.H * G.Il / G.g; d.e_glob = G.H;
+        d.R = G.H; d.K = G.Il; d.group = G.g; d.act = h;
+        d.n_pos_dev = npad; d.sorted_slot = sorted; d.block_expert = bexp;
+        d.n_slots = n_slots; d.top_k = G.k; d.num_experts = G.E; d.y_out = y; d.route_w = topk_w; d.status = status;
+        d.n_tiles = cdiv(G.H, 32 * (8 / ks_dn));
+        D.nprob = 1;
+        if (G.Is) {
+            GemvParams &q = D.prob[1];
+            q = d;
+            q.codes = static_cast<const uint8_t *>(shared->p[FT_DN]);
+            q.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
+            q.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
+            q.e_codes = (int64_t)G.H * G.Isl / 2; q.e_scales = (int64_t)G.H * G.Isl / G.g;
+            q.K = G.Isl; q.act = h_sh;
+            q.n_pos_dev = nullptr; q.n_pos_static = T; q.sorted_slot = nullptr; q.block_expert = nullptr;
+            q.n_slots = T; q.top_k = 1; q.num_experts = 1; q.y_out = y_sh; q.route_w = nullptr;
+            D.nprob = 2;
+        }
+        D.counters = reinterpret_cast<int *>(ws + L.counters);
+        D.combine_target = G.k + (G.Is ? 1 : 0);
+        D.y = y; D.y_sh = G.Is ? y_sh : nullptr; D.out = out; D.out_dtype = out_dtype;
+        D.T = T; D.H = G.H; D.k = G.k;
+        if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        max_units = (max_blocks + (G.Is ? tpad : 0)) * d.n_tiles;
+        if ((e = launch_gemv_fast(D, false, ks_dn, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
+        for (int st = FT_STAGE_SHARED_DOWN; st <= FT_NSTAGES; ++st)
+            if ((e = stage_mark(st, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        return ok();
+    }
 
     // gate_up + SwiGLU
     GemvParams gp = {};

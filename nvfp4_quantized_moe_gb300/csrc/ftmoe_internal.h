@@ -71,7 +71,19 @@ int gemv_tma_chunk(int K, int group, int ks);
 // Lean register-fed GEMV (two 16-row tiles per warp): usable when K % 32 == 0 and
 // (K / ks) % 128 == 0. p.n_tiles = ceil(rows / (pair_rows * 8 / ks)).
 bool gemv_fast_ok(int K, int group, int ks);
-cudaError_t launch_gemv_fast(const GemvParams &p, bool gated, int ks, int max_units, cudaStream_t s);
+
+// One lean-GEMV launch over up to two problems (routed experts, shared expert). For
+// the down stage, non-null `counters` ([T][H/32] ints, zero on entry) fuse the combine.
+struct FastLaunch {
+    GemvParams prob[2];
+    int nprob;
+    int *counters;
+    int combine_target;  // k, or k + 1 with a shared expert
+    const float *y, *y_sh;
+    void *out;
+    int out_dtype, T, H, k;
+};
+cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
 int gemv_tma_warps(int K, int group, int kc);
 cudaError_t launch_gemv_tma(const GemvParams &p, bool gated, int ks, int kc, int nw, int max_units, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, int H, void *out, int out_dtype,

@@ -60,135 +60,211 @@ __device__ __forceinline__ void fast_compute(const FastFrag &f, const uint4 *bb,
     mma_step(f.b_lo, f.b_hi, f.sb & 0xFFFFu, f.sb >> 16, b, acc1);
 }
 
+// Fused combine: after a warp stores y for rows [r0, r0+32) of its block's tokens, it
+// counts one contribution per token for that row range; the warp that brings a
+// counter to k (+1 with a shared expert) sums that token's k routed rows in order
+// j = 0..k-1 and then the shared row, and writes the output. Only the identity of the
+// summing warp depends on timing, not the order of the sum.
+__device__ __forceinline__ void fast_combine(const GemvParams &p, const FastLaunch &L, int blk, int n_pos, int r0)
+{
+    const int lane = threadIdx.x & 31;
+    // The warp's y stores are ordered before the counting atomics by the warp barrier;
+    // the acq_rel atomic releases them (cumulatively) and acquires the other writers'.
+    __syncwarp();
+    int t = -1;
+    if (lane < kGemvBlock) {
+        const int pos = blk * kGemvBlock + lane;
+        if (pos < n_pos) {
+            if (p.sorted_slot) {
+                const int sl = __ldg(p.sorted_slot + pos);
+                if (sl < p.n_slots) t = sl / p.top_k;
+            } else if (pos < p.n_pos_static) {
+                t = pos;
+            }
+        }
+    }
+    bool last = false;
+    if (t >= 0) {
+        int old;
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
+                     : "=r"(old)
+                     : "l"(L.counters + (size_t)t * (L.H / 32) + r0 / 32)
+                     : "memory");
+        last = old == L.combine_target - 1;
+    }
+    uint32_t mask = __ballot_sync(0xFFFFFFFFu, last);
+    if (!mask) return;
+    const int n = r0 + lane;
+    while (mask) {
+        const int src = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int tt = __shfl_sync(0xFFFFFFFFu, t, src);
+        float acc = 0.f;
+        for (int j = 0; j < L.k; ++j) acc += __ldcg(L.y + ((size_t)tt * L.k + j) * L.H + n);
+        if (L.y_sh) acc += __ldcg(L.y_sh + (size_t)tt * L.H + n);
+        if (L.out_dtype == FT_DTYPE_F32) {
+            static_cast<float *>(L.out)[(size_t)tt * L.H + n] = acc;
+        } else {
+            __nv_bfloat16 b = __float2bfloat16_rn(acc);
+            static_cast<uint16_t *>(L.out)[(size_t)tt * L.H + n] = *reinterpret_cast<uint16_t *>(&b);
+        }
+    }
+}
+
 }  // namespace
 
+// One unit of work: a block of 8 positions of problem `p` and one pair-tile per warp.
 template <bool GATED, int KS>
-__global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const GemvParams p)
+__device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch &L, int lu, int n_pos, uint4 *smem_b,
+                                          const float *inv, float (&red)[KS > 1 ? 8 : 1][32][8])
 {
     constexpr int TPW = 8 / KS;
-    extern __shared__ uint4 smem_b[];
-    __shared__ float inv[kGemvBlock];
-    __shared__ int rows[kGemvBlock];
-    __shared__ float red[KS > 1 ? 8 : 1][32][8];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ks = warp % KS, tp = warp / KS;
     const int g = lane >> 2, c = lane & 3;
     const int K = p.K;
-    const int n_pos = load_n_pos(p);
-    const int n_groups = p.n_tiles;
-    const int n_units = (n_pos / kGemvBlock) * n_groups;
-    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
-    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    const int blk = lu / p.n_tiles, grp = lu - blk * p.n_tiles;
     const int Kw = K / KS, k0 = ks * Kw, nstep = Kw / kStep;
     const int pair_rows = GATED ? 16 : 32;
     const int rows_limit = GATED ? p.up_off : p.R;
-    // chunk j of step s of this lane lives at 16 s + 4 c + (j ^ m) (see swz)
     const int m = ((c >> 1) << 1) ^ (g & 1);
     const int boff[4] = {4 * c + (0 ^ m), 4 * c + (1 ^ m), 4 * c + (2 ^ m), 4 * c + (3 ^ m)};
-    int staged = -1;
-    for (int u = u_lo; u < u_hi; ++u) {
-        const int blk = u / n_groups, grp = u - blk * n_groups;
-        if (blk != staged) {
-            __syncthreads();
-            if (threadIdx.x < kGemvBlock)
-                rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, GATED);
-            __syncthreads();
-            stage_block(p.act, K, K, rows, smem_b, inv);
-            __syncthreads();
-            staged = blk;
-        }
-        const int r0 = (grp * TPW + tp) * pair_rows;
-        const bool ok = r0 < rows_limit;
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
-        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-        if (ok) {
-            const int row_a = r0 + g, row_b = GATED ? p.up_off + r0 + g : r0 + 16 + g;
-            const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
-            const uint8_t *scales_e = p.scales + (size_t)e * p.e_scales;
-            FastPtrs P;
-            P.ca = codes_e + (size_t)row_a * (K / 2) + k0 / 2 + 16 * c;
-            P.cb = codes_e + (size_t)row_b * (K / 2) + k0 / 2 + 16 * c;
-            P.sa = scales_e + (size_t)row_a * (K / p.group) + (k0 + 32 * c) / p.group;
-            P.sb = scales_e + (size_t)row_b * (K / p.group) + (k0 + 32 * c) / p.group;
-            P.crow8 = (size_t)8 * (K / 2);
-            P.srow8 = (size_t)8 * (K / p.group);
-            P.group = p.group;
-            const uint4 *bb = smem_b + (size_t)g * (K / 8) + k0 / 8;
-            FastFrag ring[4];
-            fast_load(P, 0, ring[0]);
-            if (nstep > 1) fast_load(P, 1, ring[1]);
-            for (int s0 = 0; s0 < nstep; s0 += 4) {
+    const int r0 = (grp * TPW + tp) * pair_rows;
+    const bool ok = r0 < rows_limit;
+    const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+        const int row_a = r0 + g, row_b = GATED ? p.up_off + r0 + g : r0 + 16 + g;
+        const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
+        const uint8_t *scales_e = p.scales + (size_t)e * p.e_scales;
+        FastPtrs P;
+        P.ca = codes_e + (size_t)row_a * (K / 2) + k0 / 2 + 16 * c;
+        P.cb = codes_e + (size_t)row_b * (K / 2) + k0 / 2 + 16 * c;
+        P.sa = scales_e + (size_t)row_a * (K / p.group) + (k0 + 32 * c) / p.group;
+        P.sb = scales_e + (size_t)row_b * (K / p.group) + (k0 + 32 * c) / p.group;
+        P.crow8 = (size_t)8 * (K / 2);
+        P.srow8 = (size_t)8 * (K / p.group);
+        P.group = p.group;
+        const uint4 *bb = smem_b + (size_t)g * (K / 8) + k0 / 8;
+        FastFrag ring[4];
+        fast_load(P, 0, ring[0]);
+        if (nstep > 1) fast_load(P, 1, ring[1]);
+        for (int s0 = 0; s0 < nstep; s0 += 4) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int s = s0 + q;
-                    if (s + 2 < nstep) fast_load(P, s + 2, ring[(q + 2) & 3]);
-                    if (s < nstep) fast_compute(ring[q], bb, boff, s, acc0, acc1);
-                }
+            for (int q = 0; q < 4; ++q) {
+                const int s = s0 + q;
+                if (s + 2 < nstep) fast_load(P, s + 2, ring[(q + 2) & 3]);
+                if (s < nstep) fast_compute(ring[q], bb, boff, s, acc0, acc1);
             }
         }
+    }
+    if (KS > 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            red[warp][lane][i] = acc0[i];
+            red[warp][lane][4 + i] = acc1[i];
+        }
+        __syncthreads();
+    }
+    if (ks == 0 && ok) {
         if (KS > 1) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                red[warp][lane][i] = acc0[i];
-                red[warp][lane][4 + i] = acc1[i];
+                float a = 0.f, b2 = 0.f;
+                for (int w = 0; w < KS; ++w) {
+                    a += red[tp * KS + w][lane][i];
+                    b2 += red[tp * KS + w][lane][4 + i];
+                }
+                acc0[i] = a;
+                acc1[i] = b2;
             }
-            __syncthreads();
         }
-        if (ks == 0 && ok) {
-            if (KS > 1) {
+        const float *glob_e = p.glob + (size_t)e * p.e_glob;
+        if (GATED) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float a = 0.f, b2 = 0.f;
-                    for (int w = 0; w < KS; ++w) {
-                        a += red[tp * KS + w][lane][i];
-                        b2 += red[tp * KS + w][lane][4 + i];
-                    }
-                    acc0[i] = a;
-                    acc1[i] = b2;
-                }
-            }
-            const float *glob_e = p.glob + (size_t)e * p.e_glob;
-            if (GATED) {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int i = r0 + g + 8 * half;
-                    const float gg = __ldg(glob_e + i), gu = __ldg(glob_e + p.up_off + i);
-#pragma unroll
-                    for (int col = 0; col < 2; ++col) {
-                        const int pos = blk * kGemvBlock + 2 * c + col;
-                        const float scl = inv[2 * c + col];
-                        const float gate = acc0[2 * half + col] * scl * gg;
-                        const float up = acc1[2 * half + col] * scl * gu;
-                        __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
-                        p.h_out[(size_t)pos * p.h_ld + i] = *reinterpret_cast<uint16_t *>(&hv);
-                    }
-                }
-            } else {
+            for (int half = 0; half < 2; ++half) {
+                const int i = r0 + g + 8 * half;
+                const float gg = __ldg(glob_e + i), gu = __ldg(glob_e + p.up_off + i);
 #pragma unroll
                 for (int col = 0; col < 2; ++col) {
                     const int pos = blk * kGemvBlock + 2 * c + col;
-                    if (pos >= n_pos) continue;
-                    int dst;
-                    float wgt = inv[2 * c + col];
-                    if (p.sorted_slot) {
-                        dst = __ldg(p.sorted_slot + pos);
-                        if (dst >= p.n_slots) continue;
-                        if (p.route_w) wgt *= __ldg(p.route_w + dst);
-                    } else {
-                        dst = pos;
-                        if (dst >= p.n_pos_static) continue;
-                    }
-                    float *yrow = p.y_out + (size_t)dst * p.R;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int n = r0 + g + 8 * half;
-                        yrow[n] = acc0[2 * half + col] * __ldg(glob_e + n) * wgt;
-                        yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * wgt;
-                    }
+                    const float scl = inv[2 * c + col];
+                    const float gate = acc0[2 * half + col] * scl * gg;
+                    const float up = acc1[2 * half + col] * scl * gu;
+                    __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
+                    p.h_out[(size_t)pos * p.h_ld + i] = *reinterpret_cast<uint16_t *>(&hv);
                 }
             }
+        } else {
+#pragma unroll
+            for (int col = 0; col < 2; ++col) {
+                const int pos = blk * kGemvBlock + 2 * c + col;
+                if (pos >= n_pos) continue;
+                int dst;
+                float wgt = inv[2 * c + col];
+                if (p.sorted_slot) {
+                    dst = __ldg(p.sorted_slot + pos);
+                    if (dst >= p.n_slots) continue;
+                    if (p.route_w) wgt *= __ldg(p.route_w + dst);
+                } else {
+                    dst = pos;
+                    if (dst >= p.n_pos_static) continue;
+                }
+                float *yrow = p.y_out + (size_t)dst * p.R;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int n = r0 + g + 8 * half;
+                    yrow[n] = acc0[2 * half + col] * __ldg(glob_e + n) * wgt;
+                    yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * wgt;
+                }
+            }
+            if (L.counters) fast_combine(p, L, blk, n_pos, r0);
         }
-        if (KS > 1) __syncthreads();
+    }
+    if (KS > 1) __syncthreads();
+}
+
+// Stage the activation rows of block `blk` of problem `p` (CTA-wide, with barriers).
+template <bool GATED>
+__device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_pos, int *rows, uint4 *smem_b,
+                                           float *inv)
+{
+    __syncthreads();
+    if (threadIdx.x < kGemvBlock) rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, GATED);
+    __syncthreads();
+    stage_block(p.act, p.K, p.K, rows, smem_b, inv);
+    __syncthreads();
+}
+
+// Grid-strided over the concatenated unit lists of up to two problems (the routed
+// experts and the shared expert); each CTA takes a contiguous range of units.
+template <bool GATED, int KS>
+__global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_constant__ FastLaunch L)
+{
+    extern __shared__ uint4 smem_b[];
+    __shared__ float inv[kGemvBlock];
+    __shared__ int rows[kGemvBlock];
+    __shared__ float red[KS > 1 ? 8 : 1][32][8];
+    const int n_pos0 = load_n_pos(L.prob[0]);
+    const int n_pos1 = L.nprob > 1 ? load_n_pos(L.prob[1]) : 0;
+    const int units0 = (n_pos0 / kGemvBlock) * L.prob[0].n_tiles;
+    const int units1 = L.nprob > 1 ? (n_pos1 / kGemvBlock) * L.prob[1].n_tiles : 0;
+    const int n_units = units0 + units1;
+    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    int staged = -1;
+    for (int u = u_lo; u < u_hi; ++u) {
+        const int pi = u < units0 ? 0 : 1;
+        const GemvParams &p = L.prob[pi];
+        const int lu = pi ? u - units0 : u;
+        const int n_pos = pi ? n_pos1 : n_pos0;
+        const int blk = lu / p.n_tiles;
+        const int key = pi * (1 << 30) + blk;
+        if (key != staged) {
+            fast_stage<GATED>(p, blk, n_pos, rows, smem_b, inv);
+            staged = key;
+        }
+        fast_unit<GATED, KS>(p, L, lu, n_pos, smem_b, inv, red);
     }
 }
 
@@ -199,35 +275,36 @@ bool gemv_fast_ok(int K, int group, int ks)
 }
 
 template <bool GATED, int KS>
-static cudaError_t launch_fast_t(const GemvParams &p, int max_units, cudaStream_t s)
+static cudaError_t launch_fast_t(const FastLaunch &L, int max_units, cudaStream_t s)
 {
     auto kern = gemv_fast_kernel<GATED, KS>;
-    const size_t smem = (size_t)kGemvBlock * p.K * 2;
+    const int Kmax = L.nprob > 1 && L.prob[1].K > L.prob[0].K ? L.prob[1].K : L.prob[0].K;
+    const size_t smem = (size_t)kGemvBlock * Kmax * 2;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int grid = sm_count() * 2;
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, kThreads, smem, s>>>(p);
+    kern<<<grid, kThreads, smem, s>>>(L);
     count_launches(1);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemv_fast(const GemvParams &p, bool gated, int ks, int max_units, cudaStream_t s)
+cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s)
 {
     if (gated) {
         switch (ks) {
-        case 1: return launch_fast_t<true, 1>(p, max_units, s);
-        case 2: return launch_fast_t<true, 2>(p, max_units, s);
-        case 4: return launch_fast_t<true, 4>(p, max_units, s);
-        default: return launch_fast_t<true, 8>(p, max_units, s);
+        case 1: return launch_fast_t<true, 1>(L, max_units, s);
+        case 2: return launch_fast_t<true, 2>(L, max_units, s);
+        case 4: return launch_fast_t<true, 4>(L, max_units, s);
+        default: return launch_fast_t<true, 8>(L, max_units, s);
         }
     }
     switch (ks) {
-    case 1: return launch_fast_t<false, 1>(p, max_units, s);
-    case 2: return launch_fast_t<false, 2>(p, max_units, s);
-    case 4: return launch_fast_t<false, 4>(p, max_units, s);
-    default: return launch_fast_t<false, 8>(p, max_units, s);
+    case 1: return launch_fast_t<false, 1>(L, max_units, s);
+    case 2: return launch_fast_t<false, 2>(L, max_units, s);
+    case 4: return launch_fast_t<false, 4>(L, max_units, s);
+    default: return launch_fast_t<false, 8>(L, max_units, s);
     }
 }
 
