@@ -137,8 +137,9 @@ static WsLayout ws_layout(const Geometry &G, int T)
 {
     WsLayout L;
     const int64_t n = (int64_t)T * G.k;
-    const int64_t pmax = n + (int64_t)(n < G.E ? n : G.E) * (kGemvBlock - 1);
-    const int64_t tpad = (T + kGemvBlock - 1) / kGemvBlock * kGemvBlock;
+    // sized for the larger padding block of the two paths (warp-MMA and tensor-core)
+    const int64_t pmax = n + (int64_t)(n < G.E ? n : G.E) * (kTcBlock - 1);
+    const int64_t tpad = (T + kTcBlock - 1) / kTcBlock * kTcBlock;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = round_up(o + bytes, 256); return at; };
     L.status = take(256);
@@ -199,6 +200,16 @@ static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, 
     p.n_tiles = cdiv(rows, 16 * (8 / ks2));
     return gated ? launch_gemv_gated(p, ks2, max_blocks * p.n_tiles, s)
                  : launch_gemv_down(p, ks2, max_blocks * p.n_tiles, s);
+}
+
+// Tensor-core (prefill) path when the routing gives the experts at least 32 slots on
+// average and every tile shape fits; the warp-MMA (decode) path otherwise.
+static bool use_tc(const Geometry &G, int T)
+{
+    if ((int64_t)T * G.k < (int64_t)32 * G.E) return false;
+    if (!tc_shape_ok(G.H, G.g, G.Il) || !tc_shape_ok(G.Il, G.g, G.H)) return false;
+    if (G.Is && (!tc_shape_ok(G.H, G.g, G.Isl) || !tc_shape_ok(G.Isl, G.g, G.H))) return false;
+    return true;
 }
 
 static bool banks_ok(const ft_moe_banks *b)
@@ -398,12 +409,65 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     cudaError_t e = cudaMemsetAsync(status, 0, L.zero_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+
+    auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
+    if (use_tc(G, T)) {
+        // ---------------------------------------------------------------- tensor-core path
+        e = launch_align(topk_ids, T, G.k, G.E, kTcBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s);
+        if (e != cudaSuccess) return cuda_fail(e, "align launch");
+        const int max_blocks_tc = L.pmax / kTcBlock, tpad_tc = cdiv(T, kTcBlock);
+        uint16_t *yb = reinterpret_cast<uint16_t *>(y), *yb_sh = reinterpret_cast<uint16_t *>(y_sh);
+        TcParams gp = {};
+        gp.scales = static_cast<const uint8_t *>(routed->p[FT_GU_SCALE]);
+        gp.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
+        gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il; gp.n_mtiles = G.Il / 128;
+        gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp; gp.n_slots = n_slots; gp.top_k = G.k;
+        gp.act = static_cast<const uint16_t *>(x); gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
+        if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        e = launch_tc_gemm(gp, true, routed->p[FT_GU], (int64_t)G.E * 2 * G.Il, x, T, max_blocks_tc * gp.n_mtiles, s);
+        if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
+        if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if (G.Is) {
+            TcParams sp = gp;
+            sp.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
+            sp.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
+            sp.R = 2 * G.Isl; sp.up_off = G.Isl; sp.n_mtiles = G.Isl / 128;
+            sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
+            sp.n_slots = T; sp.top_k = 1; sp.h_out = h_sh; sp.h_ld = G.Isl;
+            e = launch_tc_gemm(sp, true, shared->p[FT_GU], 2 * (int64_t)G.Isl, x, T, tpad_tc * sp.n_mtiles, s);
+            if (e != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
+        }
+        if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        TcParams dp = {};
+        dp.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
+        dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
+        dp.R = G.H; dp.K = G.Il; dp.group = G.g; dp.up_off = 0; dp.n_mtiles = G.H / 128;
+        dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp; dp.n_slots = n_slots; dp.top_k = G.k;
+        dp.y_out = yb; dp.y_ld = G.H; dp.route_w = topk_w; dp.status = status;
+        e = launch_tc_gemm(dp, false, routed->p[FT_DN], (int64_t)G.E * G.H, h, L.pmax, max_blocks_tc * dp.n_mtiles, s);
+        if (e != cudaSuccess) return cuda_fail(e, "down launch");
+        if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if (G.Is) {
+            TcParams sd = dp;
+            sd.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
+            sd.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
+            sd.K = G.Isl; sd.n_pos_dev = nullptr; sd.n_pos_static = T; sd.sorted_slot = nullptr;
+            sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.y_out = yb_sh; sd.route_w = nullptr;
+            e = launch_tc_gemm(sd, false, shared->p[FT_DN], G.H, h_sh, (int64_t)tpad_tc * kTcBlock,
+                               tpad_tc * sd.n_mtiles, s);
+            if (e != cudaSuccess) return cuda_fail(e, "shared down launch");
+        }
+        if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        e = launch_combine_bf16(yb, G.Is ? yb_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+        if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        return ok();
+    }
+
     e = launch_align(topk_ids, T, G.k, G.E, kGemvBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s);
     if (e != cudaSuccess) return cuda_fail(e, "align launch");
-
-    const int max_blocks = L.pmax / kGemvBlock;
+    const int max_blocks = (int)(((int64_t)n_slots + (n_slots < G.E ? n_slots : G.E) * (kGemvBlock - 1)) / kGemvBlock);
     const int tpad = (T + kGemvBlock - 1) / kGemvBlock;
-    auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
 
     // Lean kernels, routed and shared expert in one launch per stage, combine fused
     // into the down stage.

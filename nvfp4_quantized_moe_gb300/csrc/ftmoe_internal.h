@@ -43,6 +43,38 @@ struct GemvParams {
     int *status;
 };
 
+// Positions per block (the MMA N side) of the tensor-core prefill path.
+constexpr int kTcBlock = 128;
+
+// One grouped GEMM launch of the tensor-core path. Rows of expert e's matrix are
+// e * R .. e * R + R - 1 of the bank; a unit is (block of kTcBlock positions, tile of
+// 128 rows); gate_up units pair gate rows with the up rows up_off further down.
+struct TcParams {
+    const uint8_t *scales;   // [E][R][K/group]
+    const float *glob;       // [E][R]
+    int R, K, group, up_off, n_mtiles;
+    const int *n_pos_dev;    // routed: device count of padded positions
+    int n_pos_static;        // shared: number of tokens
+    const int *sorted_slot;  // routed: position -> slot
+    const int *block_expert; // routed: block -> expert
+    int n_slots, top_k;
+    const uint16_t *act;     // gate_up: x [T][K] bf16 (gathered per position)
+    uint16_t *h_out;         // gate_up: bf16 [positions][h_ld]
+    int h_ld;
+    uint16_t *y_out;         // down: bf16 [slots][y_ld]
+    int y_ld;
+    const float *route_w;    // down, routed: [T*k]
+    int *status;
+};
+bool tc_shape_ok(int K, int group, int rows_per_expert);
+size_t tc_smem_bytes(bool gated, int K, int group);
+// codes: the bank's packed codes (rows_total rows of K/2 bytes); act: the activation
+// matrix the B operand comes from (gate_up: x, act_rows = T; down: h, act_rows = its rows).
+cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total, const void *act,
+                           int64_t act_rows, int max_units, cudaStream_t s);
+cudaError_t launch_combine_bf16(const uint16_t *y, const uint16_t *y_shared, int T, int k, int H, void *out,
+                                int out_dtype, cudaStream_t s);
+
 int sm_count();
 // Sets the thread-local error message (cleared for FT_OK) and returns `code`.
 ft_status report_error(ft_status code, const char *message);

@@ -46,6 +46,8 @@ class LayerShape:
 SHAPES = {
     # tiny layer: T=16, H=256, E=8, top-2, I=64, no shared expert
     "tiny": LayerShape(hidden=256, intermediate=64, num_experts=8, top_k=2),
+    # small layer whose tiles fit the 128-row tensor-core path (full-oracle parity)
+    "mini": LayerShape(hidden=256, intermediate=256, num_experts=8, top_k=2, group=16, shared_intermediate=128),
     # Qwen3.6-35B-A3B-shaped MoE layer (decode and prefill)
     "qwen36": LayerShape(hidden=2048, intermediate=512, num_experts=256, top_k=8,
                          group=16, shared_intermediate=512),

@@ -215,6 +215,15 @@ def test_forward_bf16_output():
     assert_close(got, ref, "bf16 out")
 
 
+@pytest.mark.parametrize("T,tp,zipf", [(256, 1, False), (1000, 1, True), (384, 2, True), (256, 1, True)])
+def test_forward_mini_tensor_core_path(T, tp, zipf):
+    """Every token against the oracle on a layer small enough for it (tensor-core path:
+    T * k >= 32 * E and 128-row tiles)."""
+    for r in range(tp):
+        got, ref = _run_and_compare("mini", T, zipf, r, tp)
+        assert_close(got, ref, f"mini T={T} tp={tp} rank={r}")
+
+
 @pytest.mark.parametrize("T", [2048, 8192])
 def test_forward_qwen36_prefill_sampled(T):
     rng = np.random.default_rng(T)
