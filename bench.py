@@ -170,6 +170,52 @@ def cpu_baseline(T, budget_s=10.0):
             "sample": f"{layers} layers x {T} tokens (route + forward, fp64), {t_total:.1f} s"}
 
 
+def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
+    """One qwen36 layer at T tokens (Zipf routing), L2 flushed before every repetition."""
+    import torch
+    rb, sb = ft.alloc_banks(cfg, 0, dev), ft.alloc_banks(cfg, 1, dev)
+    ft.ft_moe_pack(cfg, 0, routed_d, rb)
+    ft.ft_moe_pack(cfg, 1, shared_d, sb)
+    H, E, k = shape.hidden, shape.num_experts, shape.top_k
+    x = torch.from_numpy(synth.make_activations(T, H, seed=7).view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(synth.zipf_logits(T, E, seed=7)).to(dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(ft.ft_moe_workspace_size(cfg, T), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    n_ev = ft.FT_NSTAGES + 1
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream(dev)
+    for e_ in ev:
+        e_.record(stream)
+    times, stages = [], []
+    for r in range(reps + 2):
+        flush.fill_(r & 0xFF)
+        start.record(stream)
+        ft.ft_moe_route(lg, k, ids, w)
+        ft.ft_moe_set_stage_events(ev)
+        ft.ft_moe_forward(cfg, rb, sb, x, ids, w, out, ws)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if r >= 2:
+            times.append(start.elapsed_time(stop))
+            stages.append([ev[i].elapsed_time(ev[i + 1]) for i in range(ft.FT_NSTAGES)])
+    assert ft.ft_moe_read_status(ws) == 0
+    ms = float(np.median(times))
+    flops = 56623104.0 * T   # 2 * 3 * H * I per routed expert x 8 + shared, per token
+    _, tfl, peak_kind = _peaks()
+    st = np.median(np.array(stages), axis=0)
+    counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=E)
+    del rb, sb, ws, flush
+    return {"T": T, "routing": "zipf(1.1)", "us": ms * 1e3, "tokens_per_s": T / (ms / 1e3),
+            "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tfl,
+            "peak_source": f"{peak_kind} bf16 dense", "l2": "512 MB written before every repetition",
+            "stage_us": {n: float(v * 1e3) for n, v in zip(ft.STAGES, st)},
+            "expert_tokens_max_over_mean": float(counts.max() / counts.mean())}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import nvfp4_quantized_moe_gb300 as ft
@@ -198,6 +244,9 @@ def run_ours(args, world, rank, local):
         ft.ft_moe_pack(cfg, 0, routed_d, rb)
         ft.ft_moe_pack(cfg, 1, shared_d, sb)
         layers.append((rb, sb))
+    prefill = None
+    if not args.no_prefill:
+        prefill = [measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T_) for T_ in (2048, 8192)]
     del routed_d, shared_d
     x_host = [synth.make_activations(T, H, seed=l) for l in range(L)]
     lg_host = [synth.make_logits(T, E, seed=l) for l in range(L)]
@@ -329,7 +378,8 @@ def run_ours(args, world, rank, local):
         "roofline": roofline, "layer": {"us": layer_us, "touched_experts_mean": float(np.mean(touched)),
                                         "weight_bytes_mean": float(np.mean(layer_bytes)), "gbs": layer_gbs,
                                         "frac_of_hbm": layer_gbs / hbm},
-        "stage_us": stage_mean_us, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps),
+        "stage_us": stage_mean_us, "prefill": prefill, "e2e": e2e,
+        "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -347,6 +397,7 @@ def main():
     ap.add_argument("--layers", type=int, default=40)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
