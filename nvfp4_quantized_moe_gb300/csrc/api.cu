@@ -126,9 +126,21 @@ static void bank_specs(const Geometry &G, int shared, ft_bank_spec out[FT_NBANKS
     spec(out[FT_DN_GLOBAL], FT_DTYPE_F32, E, G.H, 0, 2);
 }
 
+// Tensor-core (prefill) path when the routing gives the experts at least 32 slots on
+// average and every tile shape fits; the warp-MMA (decode) path otherwise.
+static bool use_tc(const Geometry &G, int T)
+{
+    if ((int64_t)T * G.k < (int64_t)32 * G.E || G.H % 256) return false;
+    if (!tc_shape_ok(G.H, G.g, G.Il) || !tc_shape_ok(G.Il, G.g, G.H)) return false;
+    if (G.Is && (!tc_shape_ok(G.H, G.g, G.Isl) || !tc_shape_ok(G.Isl, G.g, G.H))) return false;
+    return true;
+}
+
 // Workspace regions of ft_moe_forward, each 256-byte aligned.
 struct WsLayout {
     size_t status, counters, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    // tensor-core path only: f16 copies of the B operands and their per-row scales
+    size_t xs, xs_scale, x16, x16_scale, h16, h16_scale, hsh16, hsh16_scale;
     size_t zero_bytes;  // [status, counters) cleared at the start of every forward
     int pmax;
 };
@@ -154,6 +166,15 @@ static WsLayout ws_layout(const Geometry &G, int T)
     L.h_sh = take(G.Is ? 2 * (size_t)tpad * G.Isl : 0);
     L.y = take(4 * (size_t)n * G.H);
     L.y_sh = take(G.Is ? 4 * (size_t)T * G.H : 0);
+    const bool tc = use_tc(G, T);
+    L.xs = take(tc ? 2 * (size_t)pmax * G.H : 0);
+    L.xs_scale = take(tc ? 4 * (size_t)pmax : 0);
+    L.x16 = take(tc && G.Is ? 2 * (size_t)tpad * G.H : 0);
+    L.x16_scale = take(tc && G.Is ? 4 * (size_t)tpad : 0);
+    L.h16 = take(tc ? 2 * (size_t)pmax * G.Il : 0);
+    L.h16_scale = take(tc ? 4 * (size_t)pmax : 0);
+    L.hsh16 = take(tc && G.Is ? 2 * (size_t)tpad * G.Isl : 0);
+    L.hsh16_scale = take(tc && G.Is ? 4 * (size_t)tpad : 0);
     L.total = o;
     L.pmax = (int)pmax;
     return L;
@@ -200,16 +221,6 @@ static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, 
     p.n_tiles = cdiv(rows, 16 * (8 / ks2));
     return gated ? launch_gemv_gated(p, ks2, max_blocks * p.n_tiles, s)
                  : launch_gemv_down(p, ks2, max_blocks * p.n_tiles, s);
-}
-
-// Tensor-core (prefill) path when the routing gives the experts at least 32 slots on
-// average and every tile shape fits; the warp-MMA (decode) path otherwise.
-static bool use_tc(const Geometry &G, int T)
-{
-    if ((int64_t)T * G.k < (int64_t)32 * G.E) return false;
-    if (!tc_shape_ok(G.H, G.g, G.Il) || !tc_shape_ok(G.Il, G.g, G.H)) return false;
-    if (G.Is && (!tc_shape_ok(G.H, G.g, G.Isl) || !tc_shape_ok(G.Isl, G.g, G.H))) return false;
-    return true;
 }
 
 static bool banks_ok(const ft_moe_banks *b)
@@ -422,9 +433,16 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         gp.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
         gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il; gp.n_mtiles = G.Il / 128;
         gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp; gp.n_slots = n_slots; gp.top_k = G.k;
-        gp.act = static_cast<const uint16_t *>(x); gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
+        gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
         if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-        e = launch_tc_gemm(gp, true, routed->p[FT_GU], (int64_t)G.E * 2 * G.Il, x, T, max_blocks_tc * gp.n_mtiles, s);
+        auto f16buf = [&](size_t off) { return reinterpret_cast<uint16_t *>(ws + off); };
+        auto f32buf = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+        const uint16_t *xb = static_cast<const uint16_t *>(x);
+        e = launch_rows_to_f16(xb, G.H, sorted, npad, 0, n_slots, G.k, L.pmax, f16buf(L.xs), f32buf(L.xs_scale), s);
+        if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
+        gp.act_scale = f32buf(L.xs_scale);
+        e = launch_tc_gemm(gp, true, routed->p[FT_GU], (int64_t)G.E * 2 * G.Il, f16buf(L.xs), L.pmax,
+                           max_blocks_tc * gp.n_mtiles, s);
         if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
         if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         if (G.Is) {
@@ -434,17 +452,27 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sp.R = 2 * G.Isl; sp.up_off = G.Isl; sp.n_mtiles = G.Isl / 128;
             sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
             sp.n_slots = T; sp.top_k = 1; sp.h_out = h_sh; sp.h_ld = G.Isl;
-            e = launch_tc_gemm(sp, true, shared->p[FT_GU], 2 * (int64_t)G.Isl, x, T, tpad_tc * sp.n_mtiles, s);
+            sp.act_scale = f32buf(L.x16_scale);
+            const int tp = tpad_tc * kTcBlock;
+            e = launch_rows_to_f16(xb, G.H, nullptr, nullptr, tp, T, 1, tp, f16buf(L.x16), f32buf(L.x16_scale), s);
+            if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
+            e = launch_tc_gemm(sp, true, shared->p[FT_GU], 2 * (int64_t)G.Isl, f16buf(L.x16), tp,
+                               tpad_tc * sp.n_mtiles, s);
             if (e != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
         }
         if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         TcParams dp = {};
         dp.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
         dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
-        dp.R = G.H; dp.K = G.Il; dp.group = G.g; dp.up_off = 0; dp.n_mtiles = G.H / 128;
+        dp.R = G.H; dp.K = G.Il; dp.group = G.g; dp.up_off = 0; dp.n_mtiles = G.H / 256;
         dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp; dp.n_slots = n_slots; dp.top_k = G.k;
         dp.y_out = yb; dp.y_ld = G.H; dp.route_w = topk_w; dp.status = status;
-        e = launch_tc_gemm(dp, false, routed->p[FT_DN], (int64_t)G.E * G.H, h, L.pmax, max_blocks_tc * dp.n_mtiles, s);
+        dp.act_scale = f32buf(L.h16_scale);
+        // h rows are already in sorted-position order: convert them in place of a gather
+        e = launch_rows_to_f16(h, G.Il, nullptr, npad, 0, L.pmax, 1, L.pmax, f16buf(L.h16), f32buf(L.h16_scale), s);
+        if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
+        e = launch_tc_gemm(dp, false, routed->p[FT_DN], (int64_t)G.E * G.H, f16buf(L.h16), L.pmax,
+                           max_blocks_tc * dp.n_mtiles, s);
         if (e != cudaSuccess) return cuda_fail(e, "down launch");
         if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         if (G.Is) {
@@ -453,7 +481,12 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sd.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
             sd.K = G.Isl; sd.n_pos_dev = nullptr; sd.n_pos_static = T; sd.sorted_slot = nullptr;
             sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.y_out = yb_sh; sd.route_w = nullptr;
-            e = launch_tc_gemm(sd, false, shared->p[FT_DN], G.H, h_sh, (int64_t)tpad_tc * kTcBlock,
+            sd.act_scale = f32buf(L.hsh16_scale);
+            const int tp = tpad_tc * kTcBlock;
+            e = launch_rows_to_f16(h_sh, G.Isl, nullptr, nullptr, tp, T, 1, tp, f16buf(L.hsh16),
+                                   f32buf(L.hsh16_scale), s);
+            if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
+            e = launch_tc_gemm(sd, false, shared->p[FT_DN], G.H, f16buf(L.hsh16), (int64_t)tpad_tc * kTcBlock,
                                tpad_tc * sd.n_mtiles, s);
             if (e != cudaSuccess) return cuda_fail(e, "shared down launch");
         }

@@ -58,20 +58,26 @@ struct TcParams {
     const int *sorted_slot;  // routed: position -> slot
     const int *block_expert; // routed: block -> expert
     int n_slots, top_k;
-    const uint16_t *act;     // gate_up: x [T][K] bf16 (gathered per position)
     uint16_t *h_out;         // gate_up: bf16 [positions][h_ld]
     int h_ld;
     uint16_t *y_out;         // down: bf16 [slots][y_ld]
     int y_ld;
     const float *route_w;    // down, routed: [T*k]
+    const float *act_scale;  // per position: factor that undoes the B rows' f16 scaling (or null)
     int *status;
 };
 bool tc_shape_ok(int K, int group, int rows_per_expert);
 size_t tc_smem_bytes(bool gated, int K, int group);
 // codes: the bank's packed codes (rows_total rows of K/2 bytes); act: the activation
 // matrix the B operand comes from (gate_up: x, act_rows = T; down: h, act_rows = its rows).
-cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total, const void *act,
-                           int64_t act_rows, int max_units, cudaStream_t s);
+cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total,
+                           const void *act, int64_t act_rows, int max_units, cudaStream_t s);
+// B rows for the f16 tensor-core path: out[pos] = f16(src[row] * 2^-e), scale[pos] = 2^e,
+// row = token of sorted_slot[pos] (or pos when sorted_slot is null; rows >= n_slots and
+// padding slots give zero rows). pos < *n_pos_dev, or < n_pos_static when that is null.
+cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
+                               int n_pos_static, int n_slots, int top_k, int max_rows, uint16_t *out, float *scale,
+                               cudaStream_t s);
 cudaError_t launch_combine_bf16(const uint16_t *y, const uint16_t *y_shared, int T, int k, int H, void *out,
                                 int out_dtype, cudaStream_t s);
 

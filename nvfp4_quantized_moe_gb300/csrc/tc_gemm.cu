@@ -1,20 +1,27 @@
 // Prefill-regime grouped GEMM for the NVFP4 experts on the 5th-generation tensor cores.
 //
-// A work unit is (block of NT = 128 expert-sorted positions, tile of MT = 128 weight
-// rows). Warp roles in a persistent CTA:
-//   warp 0      TMA producer: per 64-element K chunk, the raw packed codes of the weight
-//               tile(s) (box 32 bytes x 128 rows) and the block's activation rows
-//               (bf16, 128-byte swizzled, K-major); per unit, the tile's block scales
-//               (one contiguous bulk copy);
-//   warp 1      allocates tensor memory and, from one thread, issues tcgen05.mma
-//               (kind::f16, bf16 x bf16 -> fp32, M = 128, N = 128, K = 16 per
-//               instruction) and commits to the stage barriers;
-//   warps 2..5  dequantise the raw codes to the exact bf16 value code*scale, written in
-//               the 128-byte swizzled K-major layout the MMA descriptors describe, and
-//               after the last K chunk read the accumulators back with tcgen05.ld for
-//               the epilogue: SwiGLU with the row globals for gate_up (gate and up
-//               tiles accumulate side by side in tensor memory), routing weight and row
-//               global for down.
+// A work unit is (block of NT = 128 expert-sorted positions, two tiles of 128 weight
+// rows): for gate_up the gate rows [i0, i0+128) and the matching up rows I_l + i0 + ..,
+// whose accumulators sit side by side in tensor memory so SwiGLU fuses into the
+// epilogue; for down the rows [n0, n0+256) as two tiles. Warp roles, persistent CTA:
+//   warp 0      one thread issues every TMA: per unit the two tiles' block scales
+//               (double-buffered, prefetched a unit ahead); per 64-element K chunk the
+//               raw packed codes of both tiles (box 32 bytes x 128 rows) and the block's
+//               activations (f16 box 64 x 128, 128-byte swizzled, K-major) -- gate_up
+//               reads them from the expert-sorted f16 copy of x, down from the f16 copy
+//               of h; each activation row carries a power-of-two scale (see
+//               rows_to_f16_kernel) that the epilogue multiplies back;
+//   warp 1      allocates tensor memory and from one thread issues tcgen05.mma
+//               (kind::f16, f16 x f16 -> fp32, M = 128, N = 128, K = 16 per
+//               instruction, two per K step) and commits to the stage barriers;
+//   warps 2..9  dequantise the raw codes to the exact f16 code*scale, written in the
+//               128-byte swizzled K-major layout the MMA descriptors describe (warp
+//               half 0 tile 0, half 1 tile 1), then read the accumulators with
+//               tcgen05.ld for the epilogue.
+// f16 operands instead of bf16: code*scale is exact in both; a bf16 activation row
+// scaled by its power of two (maximum in [2^14, 2^15)) converts to f16 exactly except
+// for elements below 2^-31 of the row maximum, which move by less than 2^-38 of it;
+// and the f16 dequantisation needs fewer instructions.
 // Every wait on an mbarrier is bounded (about two seconds): on expiry the CTA records
 // FT_ERR_TIMEOUT, stops, lets its issued copies land, frees its tensor memory and
 // returns.
@@ -29,12 +36,13 @@ namespace ftmoe {
 
 namespace {
 
-constexpr int NT = kTcBlock;  // tokens (positions) per unit
-constexpr int MT = 128;       // weight rows per tile
-constexpr int KC = 64;        // K elements per chunk (128 bytes of bf16)
-constexpr int NS = 4;         // TMA stages
+constexpr int NT = kTcBlock;  // positions per unit (MMA N)
+constexpr int MT = 128;       // weight rows per tile (MMA M)
+constexpr int KC = 64;        // K elements per chunk (128 bytes of f16)
+constexpr int NSMAX = 4;      // TMA stages (at most)
 constexpr int NA = 2;         // dequantised A buffers
-constexpr int kThreadsTc = 192;
+constexpr int kThreadsTc = 320;  // producer, MMA, 8 dequant/epilogue warps
+constexpr int kDq = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint64_t globaltimer()
@@ -58,25 +66,32 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
 }
 
+__device__ __forceinline__ void arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 struct TcSmem {
-    uint32_t a_bytes, b_bytes, raw_bytes, scale_bytes;  // per buffer
+    uint32_t a_bytes, b_bytes, raw_bytes, scale_bytes, scale_row;
     uint32_t a_off, b_off, raw_off, scale_off, bar_off, total;
+    int ns;
 };
 
-__host__ __device__ inline TcSmem tc_smem(bool gated, int K, int group)
+__host__ __device__ inline TcSmem tc_smem(int K, int group, int ns)
 {
     TcSmem s;
-    const int ntile = gated ? 2 : 1;
-    s.a_bytes = (uint32_t)ntile * MT * 128;
+    s.a_bytes = 2u * MT * 128;
     s.b_bytes = (uint32_t)NT * 128;
-    s.raw_bytes = (uint32_t)ntile * MT * 32;
-    s.scale_bytes = (uint32_t)MT * (K / group);
+    s.raw_bytes = 2u * MT * 32;
+    s.scale_row = (uint32_t)(K / group);
+    s.scale_bytes = (uint32_t)MT * s.scale_row;  // per tile
+    s.ns = ns;
     s.a_off = 0;
     s.b_off = s.a_off + NA * s.a_bytes;
-    s.raw_off = s.b_off + NS * s.b_bytes;
-    s.scale_off = s.raw_off + NS * s.raw_bytes;
-    s.bar_off = s.scale_off + (uint32_t)ntile * s.scale_bytes;
-    s.total = s.bar_off + 256;
+    s.raw_off = s.b_off + ns * s.b_bytes;
+    s.scale_off = s.raw_off + ns * s.raw_bytes;
+    s.bar_off = s.scale_off + 4 * s.scale_bytes;  // 2 buffers x 2 tiles
+    s.total = s.bar_off + 512;
     return s;
 }
 
@@ -85,34 +100,30 @@ __host__ __device__ inline TcSmem tc_smem(bool gated, int K, int group)
 template <bool GATED>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap b_map,
-                   const __grid_constant__ TcParams p)
+                   const __grid_constant__ CUtensorMap scale_map, const __grid_constant__ TcParams p, int ns)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte alignment for the swizzled tiles
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int K = p.K;
-    const TcSmem L = tc_smem(GATED, K, p.group);
+    const TcSmem L = tc_smem(K, p.group, ns);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-    uint64_t *full = bars, *empty = bars + NS, *a_full = bars + 2 * NS, *a_empty = bars + 2 * NS + NA;
-    uint64_t *scale_full = bars + 2 * NS + 2 * NA, *scale_empty = scale_full + 1;
-    uint64_t *acc_full = scale_full + 2, *acc_empty = scale_full + 3;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(scale_full + 4);
+    uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
+    uint64_t *scale_full = a_empty + NA, *scale_empty = scale_full + 2;
+    uint64_t *acc_full = scale_empty + 2, *acc_empty = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntile = GATED ? 2 : 1;
-    const uint32_t tmem_cols = GATED ? 2 * NT : NT;
+    const uint32_t tmem_cols = 2 * NT;
+    const bool sw_scales = L.scale_row == 128;  // scale rows TMA-loaded 128-byte swizzled
 
     if (threadIdx.x == 0) {
-        // full: the codes' TMA byte count (+ for gate_up, the producer's arrival once its
-        // cp.async gather of the activation rows has landed)
-        for (int i = 0; i < NS; ++i) { mbar_init(full + i, GATED ? 2 : 1); mbar_init(empty + i, 1); }
-        for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, 128); mbar_init(a_empty + i, 1); }
-        mbar_init(scale_full, 1);
-        mbar_init(scale_empty, 128);
+        for (int i = 0; i < NSMAX; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
+        for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq); mbar_init(a_empty + i, 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(scale_full + i, 1); mbar_init(scale_empty + i, kDq); }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 128);
+        mbar_init(acc_empty, kDq);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -120,6 +131,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (warp == 0 && lane == 0) {
         tc::prefetch_map(&codes_map);
         tc::prefetch_map(&b_map);
+        tc::prefetch_map(&scale_map);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -129,103 +141,47 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int n_pos = p.n_pos_dev ? *p.n_pos_dev : (p.n_pos_static + NT - 1) / NT * NT;
     const int n_units = (n_pos / NT) * p.n_mtiles;
     const int nk = K / KC;
-    const uint32_t sbytes = (uint32_t)(MT * (K / p.group));
+    const int tile_rows = GATED ? MT : 2 * MT;  // row stride of the unit index m
     bool dead = false;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // gate_up gathers activation rows with cp.async (16 bytes per copy) straight into
-        // the 128-byte swizzled K-major layout; it waits for its own copies LAG chunks
-        // later, makes them visible to the tensor core (async proxy) and arrives.
-        constexpr int LAG = 2;
-        int it = 0, uc = 0;
-        for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
-            const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
-            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
-            const int row_a = e * p.R + m * MT;
-            const int row_b = row_a + p.up_off;  // gated: the matching up rows
-            if (lane == 0) {
-                if (!wait_bar(scale_empty, (uc & 1) ^ 1, abort_flag)) dead = true;
-                if (!dead) {
-                    mbar_arrive_expect_tx(scale_full, ntile * sbytes);
-                    bulk_g2s(smem + L.scale_off, p.scales + (size_t)row_a * (K / p.group), sbytes, scale_full);
-                    if (GATED)
-                        bulk_g2s(smem + L.scale_off + L.scale_bytes, p.scales + (size_t)row_b * (K / p.group), sbytes,
-                                 scale_full);
-                }
-            }
-            dead = __shfl_sync(0xFFFFFFFFu, dead, 0);
-            // lane l copies chunk l % 8 of rows l / 8 + 4 i (i = 0..31) of each K chunk
-            const int jc = lane & 7;
-            const uint16_t *src_row[NT / 4];
-            if (GATED) {
-#pragma unroll
-                for (int i = 0; i < NT / 4; ++i) {
-                    const int pos = b * NT + (lane >> 3) + 4 * i;
-                    int r = 0;
-                    if (p.sorted_slot) {
-                        const int sl = __ldg(p.sorted_slot + pos);
-                        r = sl < p.n_slots ? sl / p.top_k : 0;
-                    } else {
-                        r = pos < p.n_pos_static ? pos : 0;
-                    }
-                    src_row[i] = p.act + (size_t)r * K + jc * 8;
-                }
-            }
-            for (int c = 0; c < nk && !dead; ++c, ++it) {
-                const int slot = it % NS;
-                if (lane == 0 && !wait_bar(empty + slot, ((it / NS) & 1) ^ 1, abort_flag)) dead = true;
-                dead = __shfl_sync(0xFFFFFFFFu, dead, 0);
-                if (dead) break;
-                unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
-                unsigned char *bt = smem + L.b_off + slot * L.b_bytes;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(full + slot, ntile * MT * 32 + (GATED ? 0u : (uint32_t)NT * 128));
+        if (lane == 0) {
+            int it = 0, uc = 0;
+            for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
+                const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
+                const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+                const int row_a = e * p.R + m * tile_rows;
+                const int row_b = GATED ? row_a + p.up_off : row_a + MT;
+                const int sb = uc & 1;
+                if (!wait_bar(scale_empty + sb, ((uc >> 1) & 1) ^ 1, abort_flag)) { dead = true; break; }
+                mbar_arrive_expect_tx(scale_full + sb, 2 * L.scale_bytes);
+                tc::tma_load_2d(smem + L.scale_off + (2 * sb) * L.scale_bytes, &scale_map, 0, row_a, scale_full + sb);
+                tc::tma_load_2d(smem + L.scale_off + (2 * sb + 1) * L.scale_bytes, &scale_map, 0, row_b,
+                                scale_full + sb);
+                for (int c = 0; c < nk; ++c, ++it) {
+                    const int slot = it % ns;
+                    if (!wait_bar(empty + slot, ((it / ns) & 1) ^ 1, abort_flag)) { dead = true; break; }
+                    unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
+                    mbar_arrive_expect_tx(full + slot, L.raw_bytes + L.b_bytes);
                     tc::tma_load_2d(raw, &codes_map, c * 32, row_a, full + slot);
-                    if (GATED) tc::tma_load_2d(raw + MT * 32, &codes_map, c * 32, row_b, full + slot);
-                    else tc::tma_load_2d(bt, &b_map, c * KC, b * NT, full + slot);
-                }
-                if (GATED) {
-#pragma unroll
-                    for (int i = 0; i < NT / 4; ++i) {
-                        const int t = (lane >> 3) + 4 * i;
-                        cp_async_16(bt + t * 128 + ((jc ^ (t & 7)) << 4), src_row[i] + c * KC);
-                    }
-                    cp_async_commit();
-                    if (c >= LAG) {
-                        cp_async_wait<LAG>();
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0)
-                            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(full + (it - LAG) % NS))
-                                         : "memory");
-                    }
+                    tc::tma_load_2d(raw + MT * 32, &codes_map, c * 32, row_b, full + slot);
+                    tc::tma_load_2d(smem + L.b_off + slot * L.b_bytes, &b_map, c * KC, b * NT, full + slot);
                 }
             }
-            if (GATED && !dead) {
-                // this unit's last chunks: their gathers must land before the next unit
-                // waits on the scale buffer, which needs this unit fully consumed
-                cp_async_wait<0>();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    for (int j = it - (nk < LAG ? nk : LAG); j < it; ++j)
-                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(full + j % NS))
-                                     : "memory");
-            }
+            if (dead) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
         }
-        if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16_f32(MT, NT);
+            const uint32_t idesc = tc::idesc_f16_f32(MT, NT);
             int it = 0, ia = 0, uc = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
                 if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag)) { dead = true; break; }
                 tc::fence_after_sync();
                 for (int c = 0; c < nk; ++c, ++it, ++ia) {
-                    const int slot = it % NS, ab = ia % NA;
-                    if (!wait_bar(full + slot, (it / NS) & 1, abort_flag) ||
+                    const int slot = it % ns, ab = ia % NA;
+                    if (!wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
                         !wait_bar(a_full + ab, (ia / NA) & 1, abort_flag)) {
                         dead = true;
                         break;
@@ -236,10 +192,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
                     for (int kk = 0; kk < KC / 16; ++kk) {
                         const uint64_t bd = tc::sw128_desc(b0 + kk * 32);
-                        tc::mma_bf16(tmem, tc::sw128_desc(a0 + kk * 32), bd, idesc, (c | kk) != 0);
-                        if (GATED)
-                            tc::mma_bf16(tmem + NT, tc::sw128_desc(a0 + MT * 128 + kk * 32), bd, idesc,
-                                         (c | kk) != 0);
+                        tc::mma_f16(tmem, tc::sw128_desc(a0 + kk * 32), bd, idesc, (c | kk) != 0);
+                        tc::mma_f16(tmem + NT, tc::sw128_desc(a0 + MT * 128 + kk * 32), bd, idesc, (c | kk) != 0);
                     }
                     tc::commit(empty + slot);
                     tc::commit(a_empty + ab);
@@ -251,52 +205,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
     } else {
         // ------------------------------------------------------------ dequant + epilogue
-        const int quarter = warp & 3;
-        const int r = 32 * quarter + lane;  // weight row in the tile == TMEM lane
+        // warp (quarter, half): TMEM lanes / tile rows 32*quarter .. +32 of tile `half`;
+        // epilogue positions [64 half, 64 half + 64) of both tiles.
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        const int r = 32 * quarter + lane;
+        const int cpl = 16 * p.group / KC;  // K chunks covered by 16 scale bytes
         int it = 0, ia = 0, uc = 0;
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
             const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
-            if (!wait_bar(scale_full, uc & 1, abort_flag)) { dead = true; break; }
-            const unsigned char *sc0 = smem + L.scale_off + r * (K / p.group);
+            const int sb = uc & 1;
+            if (!wait_bar(scale_full + sb, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
+            const unsigned char *sc = smem + L.scale_off + (2 * sb + half) * L.scale_bytes + r * L.scale_row;
+            uint4 s16 = make_uint4(0, 0, 0, 0);
             for (int c = 0; c < nk; ++c, ++it, ++ia) {
-                const int slot = it % NS, ab = ia % NA;
-                if (!wait_bar(full + slot, (it / NS) & 1, abort_flag) ||
+                const int slot = it % ns, ab = ia % NA;
+                if (!wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
                     !wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag)) {
                     dead = true;
                     break;
                 }
-                const unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
-                unsigned char *at = smem + L.a_off + ab * L.a_bytes;
+                if (c % cpl == 0) {
+                    const int q = c / cpl;
+                    s16 = *reinterpret_cast<const uint4 *>(sc + ((sw_scales ? (q ^ (r & 7)) : q) << 4));
+                }
+                const int ci = c % cpl;
+                uint32_t sw;
+                if (p.group == 16) {
+                    sw = ci == 0 ? s16.x : ci == 1 ? s16.y : ci == 2 ? s16.z : s16.w;
+                } else {
+                    const int wi = ci >> 1;
+                    const uint32_t wv = wi == 0 ? s16.x : wi == 1 ? s16.y : wi == 2 ? s16.z : s16.w;
+                    const uint32_t two = (ci & 1) ? (wv >> 16) : (wv & 0xFFFFu);
+                    sw = (two & 0xFFu) * 0x0101u | ((two >> 8) * 0x0101u) << 16;
+                }
+                uint32_t sv[4];
+                e4m3x2_to_f16x2_bcast(sw & 0xFFFFu, sv[0], sv[1]);
+                e4m3x2_to_f16x2_bcast(sw >> 16, sv[2], sv[3]);
+                // 32 code bytes of row r; the two 16-byte reads alternate order with row
+                // bit 2 so that 8 consecutive rows hit 8 different bank quads
+                const unsigned char *rw = smem + L.raw_off + slot * L.raw_bytes + half * MT * 32 + r * 32;
+                const int j0 = (r >> 2) & 1;
+                const uint4 qa = *reinterpret_cast<const uint4 *>(rw + 16 * j0);
+                const uint4 qb = *reinterpret_cast<const uint4 *>(rw + 16 * (j0 ^ 1));
+                const uint4 q0 = j0 ? qb : qa, q1 = j0 ? qa : qb;
+                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                unsigned char *arow = smem + L.a_off + ab * L.a_bytes + half * MT * 128 + r * 128;
 #pragma unroll
-                for (int t = 0; t < (GATED ? 2 : 1); ++t) {
-                    const uint4 *rw = reinterpret_cast<const uint4 *>(raw + t * MT * 32 + r * 32);
-                    const uint4 q0 = rw[0], q1 = rw[1];
-                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    const unsigned char *sc = sc0 + t * L.scale_bytes;
-                    uint32_t sv[4];
-                    if (p.group == 16) {
-                        const uint32_t s4 = *reinterpret_cast<const uint32_t *>(sc + c * 4);
-                        e4m3x2_to_bf16x2_scaled(s4 & 0xFFFFu, sv[0], sv[1]);
-                        e4m3x2_to_bf16x2_scaled(s4 >> 16, sv[2], sv[3]);
-                    } else {
-                        const uint32_t s2 = *reinterpret_cast<const uint16_t *>(sc + c * 2);
-                        e4m3x2_to_bf16x2_scaled(s2, sv[0], sv[2]);
-                        sv[1] = sv[0];
-                        sv[3] = sv[2];
-                    }
-                    unsigned char *arow = at + t * MT * 128 + r * 128;
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        uint32_t o[4];
-                        dequant8(words[w], sv[w >> 1], o);
-                        *reinterpret_cast<uint4 *>(arow + ((w ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
+                for (int w = 0; w < 8; ++w) {
+                    uint32_t o[4];
+                    dequant8_f16(words[w], sv[w >> 1], o);
+                    *reinterpret_cast<uint4 *>(arow + ((w ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 fence_proxy_async_smem();
-                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(a_full + ab)) : "memory");
+                arrive(a_full + ab);
             }
             if (dead) break;
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(scale_empty)) : "memory");
+            arrive(scale_empty + sb);
 
             // epilogue
             if (!wait_bar(acc_full, uc & 1, abort_flag)) { dead = true; break; }
@@ -304,10 +268,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
             const float *glob_e = p.glob + (size_t)e * p.R;
             const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-            const int row = m * MT + r;
             if (GATED) {
+                const int row = m * MT + r;
                 const float gg = __ldg(glob_e + row), gu = __ldg(glob_e + p.up_off + row);
-                for (int cb = 0; cb < NT / 32; ++cb) {
+                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     uint32_t dg[32], du[32];
                     tc::ld32(lane_addr + cb * 32, dg);
                     tc::ld32(lane_addr + NT + cb * 32, du);
@@ -315,16 +279,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int pos = b * NT + cb * 32 + j;
-                        const float gate = __uint_as_float(dg[j]) * gg, up = __uint_as_float(du[j]) * gu;
+                        const float sc_pos = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
+                        const float gate = __uint_as_float(dg[j]) * sc_pos * gg;
+                        const float up = __uint_as_float(du[j]) * sc_pos * gu;
                         __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
                         p.h_out[(size_t)pos * p.h_ld + row] = *reinterpret_cast<uint16_t *>(&hv);
                     }
                 }
             } else {
-                const float dg = __ldg(glob_e + row);
-                for (int cb = 0; cb < NT / 32; ++cb) {
-                    uint32_t d[32];
-                    tc::ld32(lane_addr + cb * 32, d);
+                const int row0 = m * 2 * MT + r, row1 = row0 + MT;
+                const float d0 = __ldg(glob_e + row0), d1 = __ldg(glob_e + row1);
+                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
+                    uint32_t a0[32], a1[32];
+                    tc::ld32(lane_addr + cb * 32, a0);
+                    tc::ld32(lane_addr + NT + cb * 32, a1);
                     tc::wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -339,31 +307,96 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             dst = pos;
                             if (dst >= p.n_pos_static) continue;
                         }
-                        __nv_bfloat16 yv = __float2bfloat16_rn(__uint_as_float(d[j]) * dg * wgt);
-                        p.y_out[(size_t)dst * p.y_ld + row] = *reinterpret_cast<uint16_t *>(&yv);
+                        if (p.act_scale) wgt *= __ldg(p.act_scale + pos);
+                        uint16_t *yrow = p.y_out + (size_t)dst * p.y_ld;
+                        __nv_bfloat16 y0 = __float2bfloat16_rn(__uint_as_float(a0[j]) * d0 * wgt);
+                        __nv_bfloat16 y1 = __float2bfloat16_rn(__uint_as_float(a1[j]) * d1 * wgt);
+                        yrow[row0] = *reinterpret_cast<uint16_t *>(&y0);
+                        yrow[row1] = *reinterpret_cast<uint16_t *>(&y1);
                     }
                 }
             }
             tc::fence_before_sync();
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(acc_empty)) : "memory");
+            arrive(acc_empty);
         }
         if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     }
 
-    // wind down: every issued stage has landed or been consumed once all roles are here
+    // wind down
     tc::fence_before_sync();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
         // let copies still in flight land before the CTA's shared memory is released
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NSMAX; ++i) {
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(full + i, 0) && !mbar_try_wait(full + i, 1) && globaltimer() - t0 < kWaitNs) {
+            }
+        }
+        for (int i = 0; i < 2; ++i) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(scale_full + i, 0) && !mbar_try_wait(scale_full + i, 1) &&
+                   globaltimer() - t0 < kWaitNs) {
             }
         }
     }
     __syncthreads();
     tc::fence_after_sync();
     if (warp == 1) tc::tmem_dealloc(tmem, tmem_cols);
+}
+
+// out[pos] = f16(src[row(pos)] * 2^-e_pos), scale[pos] = 2^e_pos with e_pos chosen so that
+// the row's largest magnitude lands in [2^14, 2^15); row(pos) = token of the position's
+// slot (sorted_slot given) or pos itself; padding positions get zero rows and scale 0.
+// One warp per position.
+__global__ void rows_to_f16_kernel(const uint16_t *__restrict__ src, int K, const int *__restrict__ sorted_slot,
+                                   const int *__restrict__ n_pos_dev, int n_pos_static, int n_slots, int top_k,
+                                   uint16_t *__restrict__ out, float *__restrict__ scale)
+{
+    const int n_pos = n_pos_dev ? *n_pos_dev : n_pos_static;
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n_pos; pos += warps) {
+        int row = pos;
+        if (sorted_slot) {
+            const int sl = __ldg(sorted_slot + pos);
+            row = sl < n_slots ? sl / top_k : -1;
+        } else if (pos >= n_slots) {
+            row = -1;
+        }
+        uint4 *o = reinterpret_cast<uint4 *>(out + (size_t)pos * K);
+        if (row < 0) {
+            for (int q = lane; q < K / 8; q += 32) o[q] = make_uint4(0, 0, 0, 0);
+            if (lane == 0) scale[pos] = 0.f;
+            continue;
+        }
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)row * K);
+        float m = 0.f;
+        for (int q = lane; q < K / 8; q += 32) {
+            const uint4 v = __ldg(s4 + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
+                                                           fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        int e = 0;
+        if (m > 0.f && m <= 3.3895314e38f) e = min(max(ilogbf(m) - 14, -126), 127);
+        const float down = __int_as_float((127 - e) << 23);
+        for (int q = lane; q < K / 8; q += 32) {
+            const uint4 v = __ldg(s4 + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half2 hh = __floats2half2_rn(__uint_as_float(w[i] << 16) * down,
+                                                     __uint_as_float(w[i] & 0xFFFF0000u) * down);
+                h[i] = *reinterpret_cast<const uint32_t *>(&hh);
+            }
+            o[q] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        if (lane == 0) scale[pos] = __int_as_float((127 + e) << 23);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -399,36 +432,70 @@ static bool make_map(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint6
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tc_shape_ok(int K, int group, int rows_per_expert) { return K % KC == 0 && K >= KC && rows_per_expert % MT == 0 && (K / group) % 4 == 0; }
-
-size_t tc_smem_bytes(bool gated, int K, int group) { return tc_smem(gated, K, group).total + 1024; }
-
-// codes: raw code bank (rows_total x K/2 bytes); act: gate_up -> x [T, K] bf16 (rows
-// gathered per position), down -> h [act_rows, K] bf16 (consecutive positions).
-cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total, const void *act,
-                           int64_t act_rows, int max_units, cudaStream_t s)
+bool tc_shape_ok(int K, int group, int rows_per_expert)
 {
-    CUtensorMap cmap, bmap;
+    return K % KC == 0 && K >= KC && rows_per_expert % MT == 0 && (K / group) % 16 == 0 && K / group <= 256;
+}
+
+// Deepest TMA ring (4, 3 or 2 stages) that fits the opt-in shared memory.
+static int tc_stages(int K, int group)
+{
+    int optin = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    for (int ns : {4, 3, 2})
+        if (tc_smem(K, group, ns).total + 1024 <= (uint32_t)optin) return ns;
+    return 0;
+}
+
+size_t tc_smem_bytes(bool gated, int K, int group)
+{
+    (void)gated;
+    const int ns = tc_stages(K, group);
+    return ns ? tc_smem(K, group, ns).total + 1024 : 0;
+}
+
+cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
+                               int n_pos_static, int n_slots, int top_k, int max_rows, uint16_t *out, float *scale,
+                               cudaStream_t s)
+{
+    int blocks = (max_rows + 7) / 8;
+    const int cap = sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    rows_to_f16_kernel<<<blocks, 256, 0, s>>>(src, K, sorted_slot, n_pos_dev, n_pos_static, n_slots, top_k, out,
+                                               scale);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// codes: the bank's packed codes (rows_total rows of K/2 bytes); act: the B operand
+// rows (gate_up: the f16 expert-sorted copy of x or, for the shared expert, the f16 copy
+// of x; down: the f16 copy of h), act_rows rows of K f16, read in blocks of 128
+// consecutive rows.
+cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total,
+                           const void *act, int64_t act_rows, int max_units, cudaStream_t s)
+{
+    const int ns = tc_stages(p.K, p.group);
+    if (!ns) return cudaErrorInvalidValue;
+    CUtensorMap cmap, bmap, smap;
+    const uint32_t srow = (uint32_t)(p.K / p.group);
     if (!make_map(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(codes), (uint64_t)p.K / 2,
-                  (uint64_t)rows_total, (uint64_t)p.K / 2, 32, MT, CU_TENSOR_MAP_SWIZZLE_NONE))
+                  (uint64_t)rows_total, (uint64_t)p.K / 2, 32, MT, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void *>(act), (uint64_t)p.K,
+                  (uint64_t)act_rows, (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(static_cast<const void *>(p.scales)), srow,
+                  (uint64_t)rows_total, srow, srow, MT,
+                  srow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    if (!make_map(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(act), (uint64_t)p.K,
-                  (uint64_t)act_rows, (uint64_t)p.K * 2, KC, gated ? 1 : NT, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    const size_t smem = tc_smem_bytes(gated, p.K, p.group);
+    const size_t smem = tc_smem(p.K, p.group, ns).total + 1024;
     int grid = sm_count();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
-    cudaError_t e;
-    if (gated) {
-        e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        tc_gemm_kernel<true><<<grid, kThreadsTc, smem, s>>>(cmap, bmap, p);
-    } else {
-        e = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        tc_gemm_kernel<false><<<grid, kThreadsTc, smem, s>>>(cmap, bmap, p);
-    }
+    auto kern = gated ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreadsTc, smem, s>>>(cmap, bmap, smap, p, ns);
     count_launches(1);
     return cudaGetLastError();
 }

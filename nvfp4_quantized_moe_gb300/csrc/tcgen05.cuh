@@ -47,15 +47,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr)
     return d;
 }
 
-// Instruction descriptor for kind::f16: bf16 A and B, fp32 accumulator, both K-major,
-// M x N tile.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+// Instruction descriptor for kind::f16: f16 A and B (type fields 0), fp32 accumulator
+// (bit 4), both operands K-major, M x N tile (N/8 at bit 17, M/16 at bit 24).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] x B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// D[tmem] (+)= A[smem] x B[smem]^T (kind::f16, both operands f16), issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
     asm volatile(

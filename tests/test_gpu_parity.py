@@ -264,6 +264,38 @@ def test_forward_dsv4_prefill_sampled():
     assert_close(got, ref, "dsv4 T=4096")
 
 
+def _scale_rows_bf16(x_bits: np.ndarray, exps) -> np.ndarray:
+    """Rows of bf16 bit patterns times 2**e (exact: power of two, no overflow); e=None
+    zeroes the row."""
+    f = (x_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for t, e in enumerate(exps):
+        f[t] = 0.0 if e is None else np.ldexp(f[t], e)
+    return (f.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("T", [16, 256])
+def test_forward_rows_of_mixed_magnitude(T):
+    """Token rows 2^-40 .. 2^40 apart and all-zero rows, on the warp-MMA path (T=16) and
+    the tensor-core path (T=256): both stage each activation row with its own
+    power-of-two scale, so every row keeps its own relative accuracy."""
+    L = layer("mini")
+    shape = synth.SHAPES["mini"]
+    cycle = [0, 40, -40, None, 17, -23]
+    x = _scale_rows_bf16(synth.make_activations(T, shape.hidden, seed=11), [cycle[t % 6] for t in range(T)])
+    logits = logits_for("mini", T, False, seed=11)
+    ids, w = L.route(logits)
+    out, _ = L.forward(x, ids, w)
+    ref_ids, ref_w = oracle.route(logits, shape.top_k)
+    rb, sb = oracle_banks("mini")
+    ref = oracle.moe_forward(rb, sb, shape.group, x, ref_ids, ref_w, nthreads=oracle.default_threads())
+    got = out.cpu().numpy()
+    for t in range(T):
+        if cycle[t % 6] is None:
+            assert not got[t].any(), f"token {t}: zero row gives nonzero output"
+        else:
+            assert_close(got[t], ref[t], f"token {t} (row scale 2^{cycle[t % 6]})")
+
+
 def test_forward_deterministic_and_untouched_experts():
     L = layer("qwen36")
     x = synth.make_activations(32, 2048, seed=3)
