@@ -180,8 +180,6 @@ static WsLayout ws_layout(const Geometry &G, int T)
     return L;
 }
 
-// One grouped GEMV launch: the bulk-copy-fed kernel when the shape allows it, else the
-// register-fed one. `rows` = I_l (gated) or H (down); max_blocks bounds the blocks.
 // K-split for a merged lean launch: the smallest of 1, 2, 4, 8 that gives at least two
 // CTA units per SM, as long as every K range stays a multiple of 128.
 static int fast_ksplit(int blocks, int units_per_block_ks1, int K0, int K1 = 0)
@@ -194,29 +192,22 @@ static int fast_ksplit(int blocks, int units_per_block_ks1, int K0, int K1 = 0)
     return ks;
 }
 
-#ifndef FTMOE_GEMV_USE_TMA
-#define FTMOE_GEMV_USE_TMA 0  // 1: prefer the bulk-copy-fed kernel where the shape allows it
-#endif
+// Decode kernel family: the lean register-fed kernels (default) or, with the
+// environment variable FTMOE_DECODE=stream, the TMA-streamed ones. Read once per process.
+static bool decode_streamed()
+{
+    static const bool v = [] {
+        const char *e = getenv("FTMOE_DECODE");
+        return e && strcmp(e, "stream") == 0;
+    }();
+    return v;
+}
 
+// Generic register-fed launch for one problem (shapes the lean kernels do not cover).
+// `rows` = I_l (gated) or H (down); max_blocks bounds the blocks.
 static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, cudaStream_t s)
 {
     auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
-    if (FTMOE_GEMV_USE_TMA) {
-    const int pair_rows = gated ? 16 : 32;
-    int ks = 1;
-    while (ks < 8 && max_blocks * cdiv(rows, pair_rows * (8 / ks)) < sm_count() && (p.K / (2 * ks)) % 128 == 0)
-        ks *= 2;
-    int kc = 0;
-    for (; ks >= 1; ks /= 2)
-        if ((kc = gemv_tma_chunk(p.K, p.group, ks)) != 0) break;
-    if (kc) {
-        const int nw = gemv_tma_warps(p.K, p.group, kc);
-        if (nw && ks <= nw) {
-            p.n_tiles = cdiv(rows, pair_rows * (nw / ks));
-            return launch_gemv_tma(p, gated, ks, kc, nw, max_blocks * p.n_tiles, s);
-        }
-    }
-    }
     const int ks2 = gemv_ksplit(max_blocks, cdiv(rows, 128), p.K);
     p.n_tiles = cdiv(rows, 16 * (8 / ks2));
     return gated ? launch_gemv_gated(p, ks2, max_blocks * p.n_tiles, s)
@@ -502,133 +493,144 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     const int max_blocks = (int)(((int64_t)n_slots + (n_slots < G.E ? n_slots : G.E) * (kGemvBlock - 1)) / kGemvBlock);
     const int tpad = (T + kGemvBlock - 1) / kGemvBlock;
 
-    // Lean kernels, routed and shared expert in one launch per stage, combine fused
-    // into the down stage.
+    // The four problems of the decode regime: routed and shared gate_up (+ SwiGLU into
+    // h / h_sh), routed and shared down (+ routing weight into y / y_sh).
+    GemvParams gu = {}, gu_sh = {}, dn = {}, dn_sh = {};
+    gu.codes = static_cast<const uint8_t *>(routed->p[FT_GU]);
+    gu.scales = static_cast<const uint8_t *>(routed->p[FT_GU_SCALE]);
+    gu.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
+    gu.e_codes = (int64_t)G.Il * G.H; gu.e_scales = (int64_t)2 * G.Il * G.H / G.g; gu.e_glob = 2 * G.Il;
+    gu.R = 2 * G.Il; gu.K = G.H; gu.group = G.g; gu.up_off = G.Il;
+    gu.act = static_cast<const uint16_t *>(x);
+    gu.n_pos_dev = npad; gu.sorted_slot = sorted; gu.block_expert = bexp;
+    gu.n_slots = n_slots; gu.top_k = G.k; gu.num_experts = G.E; gu.status = status;
+    gu.h_out = h; gu.h_ld = G.Il;
+    dn.codes = static_cast<const uint8_t *>(routed->p[FT_DN]);
+    dn.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
+    dn.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
+    dn.e_codes = (int64_t)G.H * G.Il / 2; dn.e_scales = (int64_t)G.H * G.Il / G.g; dn.e_glob = G.H;
+    dn.R = G.H; dn.K = G.Il; dn.group = G.g; dn.act = h;
+    dn.n_pos_dev = npad; dn.sorted_slot = sorted; dn.block_expert = bexp;
+    dn.n_slots = n_slots; dn.top_k = G.k; dn.num_experts = G.E; dn.status = status;
+    dn.y_out = y; dn.route_w = topk_w;
+    if (G.Is) {
+        gu_sh = gu;
+        gu_sh.codes = static_cast<const uint8_t *>(shared->p[FT_GU]);
+        gu_sh.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
+        gu_sh.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
+        gu_sh.e_codes = (int64_t)G.Isl * G.H; gu_sh.e_scales = (int64_t)2 * G.Isl * G.H / G.g;
+        gu_sh.e_glob = 2 * G.Isl; gu_sh.R = 2 * G.Isl; gu_sh.up_off = G.Isl;
+        gu_sh.n_pos_dev = nullptr; gu_sh.n_pos_static = T; gu_sh.sorted_slot = nullptr;
+        gu_sh.block_expert = nullptr; gu_sh.n_slots = T; gu_sh.top_k = 1; gu_sh.num_experts = 1;
+        gu_sh.h_out = h_sh; gu_sh.h_ld = G.Isl;
+        dn_sh = dn;
+        dn_sh.codes = static_cast<const uint8_t *>(shared->p[FT_DN]);
+        dn_sh.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
+        dn_sh.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
+        dn_sh.e_codes = (int64_t)G.H * G.Isl / 2; dn_sh.e_scales = (int64_t)G.H * G.Isl / G.g;
+        dn_sh.K = G.Isl; dn_sh.act = h_sh;
+        dn_sh.n_pos_dev = nullptr; dn_sh.n_pos_static = T; dn_sh.sorted_slot = nullptr;
+        dn_sh.block_expert = nullptr; dn_sh.n_slots = T; dn_sh.top_k = 1; dn_sh.num_experts = 1;
+        dn_sh.y_out = y_sh; dn_sh.route_w = nullptr;
+    }
+    int *counters = reinterpret_cast<int *>(ws + L.counters);
+    auto set_combine = [&](auto &D) {
+        D.counters = counters;
+        D.combine_target = G.k + (G.Is ? 1 : 0);
+        D.y = y; D.y_sh = G.Is ? y_sh : nullptr; D.out = out; D.out_dtype = out_dtype;
+        D.T = T; D.H = G.H; D.k = G.k;
+    };
+    auto trailing_marks = [&]() -> cudaError_t {
+        for (int st = FT_STAGE_SHARED_DOWN; st <= FT_NSTAGES; ++st) {
+            cudaError_t err = stage_mark(st, s);
+            if (err != cudaSuccess) return err;
+        }
+        return cudaSuccess;
+    };
+
+    // TMA-streamed kernels, routed and shared expert in one launch per stage, combine
+    // fused into the down stage.
+    {
+        StreamLaunch SG = {}, SD = {};
+        const int kmax = G.H > G.Il ? (G.H > G.Isl ? G.H : G.Isl) : (G.Il > G.Isl ? G.Il : G.Isl);
+        bool use = decode_streamed() && gemv_stream_fits(kmax) &&
+                   gemv_stream_geom(G.H, G.g, G.Il, true, SG.prob[0]) &&
+                   gemv_stream_geom(G.Il, G.g, G.H, false, SD.prob[0]);
+        if (use && G.Is)
+            use = gemv_stream_geom(G.H, G.g, G.Isl, true, SG.prob[1]) &&
+                  gemv_stream_geom(G.Isl, G.g, G.H, false, SD.prob[1]);
+        if (use) {
+            SG.prob[0].p = gu; SD.prob[0].p = dn;
+            SG.nprob = SD.nprob = 1;
+            if (G.Is) {
+                SG.prob[1].p = gu_sh; SD.prob[1].p = dn_sh;
+                SG.nprob = SD.nprob = 2;
+            }
+            set_combine(SD);
+            SD.counters = nullptr;  // combine in its own launch (below)
+            auto units = [&](const StreamLaunch &S) {
+                return max_blocks * S.prob[0].n_ptiles + (G.Is ? tpad * S.prob[1].n_ptiles : 0);
+            };
+            if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            if ((e = launch_gemv_stream(SG, true, units(SG), s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
+            if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            if ((e = launch_gemv_stream(SD, false, units(SD), s)) != cudaSuccess) return cuda_fail(e, "down launch");
+            if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
+            if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+            if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            return ok();
+        }
+    }
+
+    // Lean register-fed kernels, same launch structure.
     const int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H);
     const int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
-    if (!FTMOE_GEMV_USE_TMA && gemv_fast_ok(G.H, G.g, ks_gu) && gemv_fast_ok(G.Il, G.g, ks_dn) &&
+    if (gemv_fast_ok(G.H, G.g, ks_gu) && gemv_fast_ok(G.Il, G.g, ks_dn) &&
         (!G.Is || gemv_fast_ok(G.Isl, G.g, ks_dn))) {
         FastLaunch F = {};
-        GemvParams &r = F.prob[0];
-        r.codes = static_cast<const uint8_t *>(routed->p[FT_GU]);
-        r.scales = static_cast<const uint8_t *>(routed->p[FT_GU_SCALE]);
-        r.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
-        r.e_codes = (int64_t)G.Il * G.H; r.e_scales = (int64_t)2 * G.Il * G.H / G.g; r.e_glob = 2 * G.Il;
-        r.R = 2 * G.Il; r.K = G.H; r.group = G.g; r.up_off = G.Il;
-        r.act = static_cast<const uint16_t *>(x);
-        r.n_pos_dev = npad; r.sorted_slot = sorted; r.block_expert = bexp;
-        r.n_slots = n_slots; r.top_k = G.k; r.num_experts = G.E; r.status = status;
-        r.n_tiles = cdiv(G.Il, 16 * (8 / ks_gu)); r.h_out = h; r.h_ld = G.Il;
+        F.prob[0] = gu;
+        F.prob[0].n_tiles = cdiv(G.Il, 16 * (8 / ks_gu));
         F.nprob = 1;
         if (G.Is) {
-            GemvParams &q = F.prob[1];
-            q = r;
-            q.codes = static_cast<const uint8_t *>(shared->p[FT_GU]);
-            q.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
-            q.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
-            q.e_codes = (int64_t)G.Isl * G.H; q.e_scales = (int64_t)2 * G.Isl * G.H / G.g; q.e_glob = 2 * G.Isl;
-            q.R = 2 * G.Isl; q.up_off = G.Isl;
-            q.n_pos_dev = nullptr; q.n_pos_static = T; q.sorted_slot = nullptr; q.block_expert = nullptr;
-            q.n_slots = T; q.top_k = 1; q.num_experts = 1;
-            q.n_tiles = cdiv(G.Isl, 16 * (8 / ks_gu)); q.h_out = h_sh; q.h_ld = G.Isl;
+            F.prob[1] = gu_sh;
+            F.prob[1].n_tiles = cdiv(G.Isl, 16 * (8 / ks_gu));
             F.nprob = 2;
         }
         if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-        int max_units = max_blocks * r.n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
+        int max_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
         if ((e = launch_gemv_fast(F, true, ks_gu, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
         if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
 
         FastLaunch D = {};
-        GemvParams &d = D.prob[0];
-        d.codes = static_cast<const uint8_t *>(routed->p[FT_DN]);
-        d.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
-        d.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
-        d.e_codes = (int64_t)G.H * G.Il / 2; d.e_scales = (int64_t)G.H * G.Il / G.g; d.e_glob = G.H;
-        d.R = G.H; d.K = G.Il; d.group = G.g; d.act = h;
-        d.n_pos_dev = npad; d.sorted_slot = sorted; d.block_expert = bexp;
-        d.n_slots = n_slots; d.top_k = G.k; d.num_experts = G.E; d.y_out = y; d.route_w = topk_w; d.status = status;
-        d.n_tiles = cdiv(G.H, 32 * (8 / ks_dn));
+        D.prob[0] = dn;
+        D.prob[0].n_tiles = cdiv(G.H, 32 * (8 / ks_dn));
         D.nprob = 1;
         if (G.Is) {
-            GemvParams &q = D.prob[1];
-            q = d;
-            q.codes = static_cast<const uint8_t *>(shared->p[FT_DN]);
-            q.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
-            q.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
-            q.e_codes = (int64_t)G.H * G.Isl / 2; q.e_scales = (int64_t)G.H * G.Isl / G.g;
-            q.K = G.Isl; q.act = h_sh;
-            q.n_pos_dev = nullptr; q.n_pos_static = T; q.sorted_slot = nullptr; q.block_expert = nullptr;
-            q.n_slots = T; q.top_k = 1; q.num_experts = 1; q.y_out = y_sh; q.route_w = nullptr;
+            D.prob[1] = dn_sh;
+            D.prob[1].n_tiles = D.prob[0].n_tiles;
             D.nprob = 2;
         }
-        D.counters = reinterpret_cast<int *>(ws + L.counters);
-        D.combine_target = G.k + (G.Is ? 1 : 0);
-        D.y = y; D.y_sh = G.Is ? y_sh : nullptr; D.out = out; D.out_dtype = out_dtype;
-        D.T = T; D.H = G.H; D.k = G.k;
+        set_combine(D);
         if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-        max_units = (max_blocks + (G.Is ? tpad : 0)) * d.n_tiles;
+        max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
         if ((e = launch_gemv_fast(D, false, ks_dn, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
-        for (int st = FT_STAGE_SHARED_DOWN; st <= FT_NSTAGES; ++st)
-            if ((e = stage_mark(st, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if ((e = trailing_marks()) != cudaSuccess) return cuda_fail(e, "stage event");
         return ok();
     }
 
-    // gate_up + SwiGLU
-    GemvParams gp = {};
-    gp.codes = static_cast<const uint8_t *>(routed->p[FT_GU]);
-    gp.scales = static_cast<const uint8_t *>(routed->p[FT_GU_SCALE]);
-    gp.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
-    gp.e_codes = (int64_t)2 * G.Il * G.H / 2; gp.e_scales = (int64_t)2 * G.Il * G.H / G.g; gp.e_glob = 2 * G.Il;
-    gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il;
-    gp.act = static_cast<const uint16_t *>(x);
-    gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp;
-    gp.n_slots = n_slots; gp.top_k = G.k; gp.num_experts = G.E;
-    gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
+    // Generic kernels, one launch per problem, separate combine.
     if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-    if ((e = run_gemv(gp, true, max_blocks, G.Il, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
-
+    if ((e = run_gemv(gu, true, max_blocks, G.Il, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
     if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-    if (G.Is) {
-        GemvParams sp = gp;
-        sp.codes = static_cast<const uint8_t *>(shared->p[FT_GU]);
-        sp.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
-        sp.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
-        sp.e_codes = (int64_t)G.Isl * G.H; sp.e_scales = (int64_t)2 * G.Isl * G.H / G.g; sp.e_glob = 2 * G.Isl;
-        sp.R = 2 * G.Isl; sp.up_off = G.Isl;
-        sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
-        sp.n_slots = T; sp.top_k = 1; sp.num_experts = 1;
-        sp.h_out = h_sh; sp.h_ld = G.Isl;
-        if ((e = run_gemv(sp, true, tpad, G.Isl, s)) != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
-    }
-
-    // down + routing weight
+    if (G.Is && (e = run_gemv(gu_sh, true, tpad, G.Isl, s)) != cudaSuccess)
+        return cuda_fail(e, "shared gate_up launch");
     if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-    {
-        GemvParams dp = {};
-        dp.codes = static_cast<const uint8_t *>(routed->p[FT_DN]);
-        dp.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
-        dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
-        dp.e_codes = (int64_t)G.H * G.Il / 2; dp.e_scales = (int64_t)G.H * G.Il / G.g; dp.e_glob = G.H;
-        dp.R = G.H; dp.K = G.Il; dp.group = G.g;
-        dp.act = h;
-        dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp;
-        dp.n_slots = n_slots; dp.top_k = G.k;
-        dp.num_experts = G.E; dp.y_out = y; dp.route_w = topk_w; dp.status = status;
-        if ((e = run_gemv(dp, false, max_blocks, G.H, s)) != cudaSuccess) return cuda_fail(e, "down launch");
-    }
+    if ((e = run_gemv(dn, false, max_blocks, G.H, s)) != cudaSuccess) return cuda_fail(e, "down launch");
     if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-    if (G.Is) {
-        GemvParams dp = {};
-        dp.codes = static_cast<const uint8_t *>(shared->p[FT_DN]);
-        dp.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
-        dp.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
-        dp.e_codes = (int64_t)G.H * G.Isl / 2; dp.e_scales = (int64_t)G.H * G.Isl / G.g; dp.e_glob = G.H;
-        dp.R = G.H; dp.K = G.Isl; dp.group = G.g;
-        dp.act = h_sh;
-        dp.n_pos_static = T; dp.n_slots = T; dp.top_k = 1;
-        dp.num_experts = 1; dp.y_out = y_sh; dp.route_w = nullptr; dp.status = status;
-        if ((e = run_gemv(dp, false, tpad, G.H, s)) != cudaSuccess) return cuda_fail(e, "shared down launch");
-    }
+    if (G.Is && (e = run_gemv(dn_sh, false, tpad, G.H, s)) != cudaSuccess) return cuda_fail(e, "shared down launch");
     if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");

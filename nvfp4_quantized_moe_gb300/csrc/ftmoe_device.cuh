@@ -107,6 +107,20 @@ __device__ __forceinline__ void dequant8_f16(uint32_t codes, uint32_t scale_f16x
     for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(f[i]), "r"(scale_f16x2));
 }
 
+// ---------------------------------------------------------------- activation row scaling
+
+// 2^e for integer e in [-126, 127], built from its bits (exact).
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// Row scale exponent e for a row whose largest magnitude is m: m * 2^-e lies in
+// [2^14, 2^15), clamped to [-126, 127] so that 2^e and 2^-e stay finite normals;
+// zero and non-finite rows keep e = 0.
+__device__ __forceinline__ int row_scale_exp(float m)
+{
+    if (!(m > 0.f && m <= 3.3895314e38f)) return 0;
+    return min(max(ilogbf(m) - 14, -126), 127);
+}
+
 // ---------------------------------------------------------------- warp MMA
 
 // D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col).
@@ -239,6 +253,57 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Limit of every mbarrier wait in the pipelined kernels: about two seconds.
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` nanoseconds
+// while the phase is incomplete (it resumes as soon as the phase completes), so that
+// waiting warps do not spin on the issue slots the math warps need.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`: false after about two seconds, or as soon as
+// another role of the CTA has set *abort_flag (non-null) after giving up itself.
+// Between polls the thread sleeps (32 ns doubling to 256 ns), so that a waiting warp
+// leaves the issue slots of its scheduler to the warps that have work.
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t sleep_ns = 32;
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 256) sleep_ns <<= 1;
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) return false;
+        }
+    }
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt()

@@ -1,6 +1,7 @@
 // Host-side declarations shared by the libftmoe translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -81,6 +82,11 @@ cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slo
 cudaError_t launch_combine_bf16(const uint16_t *y, const uint16_t *y_shared, int T, int k, int H, void *out,
                                 int out_dtype, cudaStream_t s);
 
+// 2D tiled tensor map (rows of `row_bytes` bytes, `inner` elements used per row) through
+// the driver's cuTensorMapEncodeTiled; false when the driver refuses the shape.
+bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
+
 int sm_count();
 // Sets the thread-local error message (cleared for FT_OK) and returns `code`.
 ft_status report_error(ft_status code, const char *message);
@@ -102,10 +108,6 @@ int gemv_ksplit(int max_blocks, int units_per_block_ks1, int K);
 // p.n_tiles = CTA units per block: ceil(rows / (16 * 8 / ks)) with rows = I_l (gated) or H.
 cudaError_t launch_gemv_gated(const GemvParams &p, int ks, int max_units, cudaStream_t s);
 cudaError_t launch_gemv_down(const GemvParams &p, int ks, int max_units, cudaStream_t s);
-// Bulk-copy-fed GEMV: K chunk per stage (0 = shape not supported), warps per CTA
-// (0 = does not fit), launch. p.n_tiles = ceil(rows / (pair_rows * nw / ks)) with
-// pair_rows = 16 (gated, rows = I_l) or 32 (down, rows = H).
-int gemv_tma_chunk(int K, int group, int ks);
 // Lean register-fed GEMV (two 16-row tiles per warp): usable when K % 32 == 0 and
 // (K / ks) % 128 == 0. p.n_tiles = ceil(rows / (pair_rows * 8 / ks)).
 bool gemv_fast_ok(int K, int group, int ks);
@@ -122,8 +124,31 @@ struct FastLaunch {
     int out_dtype, T, H, k;
 };
 cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
-int gemv_tma_warps(int K, int group, int kc);
-cudaError_t launch_gemv_tma(const GemvParams &p, bool gated, int ks, int kc, int nw, int max_units, cudaStream_t s);
+
+// TMA-streamed decode GEMV (one persistent CTA per SM). Per problem: lps lines of 256 K
+// elements x tps pair tiles per stage, nst stages per unit, n_ptiles units per block of
+// positions, sbytes scale bytes per row and stage (gemv_stream_geom fills these).
+struct StreamProb {
+    GemvParams p;
+    int lps, tps, nst, n_ptiles, sbytes;
+};
+struct StreamLaunch {
+    CUtensorMap cmap[2], smap[2];  // per problem: packed codes, block scales (set by the launch)
+    StreamProb prob[2];
+    int nprob;
+    int *counters;                 // down: fused combine as in FastLaunch
+    int combine_target;
+    const float *y, *y_sh;
+    void *out;
+    int out_dtype, T, H, k;
+    int ns, act_bytes;             // stages, activation bytes (set by the launch)
+};
+// Geometry for a problem of K columns and `rows` rows (I_l for gate_up, H for down);
+// false when the shape is outside the kernel's coverage.
+bool gemv_stream_geom(int K, int group, int rows, bool gated, StreamProb &P);
+// Enough shared memory for at least two stages next to Kmax-long activations?
+bool gemv_stream_fits(int Kmax);
+cudaError_t launch_gemv_stream(StreamLaunch &L, bool gated, int max_units, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, int H, void *out, int out_dtype,
                            cudaStream_t s);
 

@@ -304,6 +304,9 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
     if (idx >= (size_t)T * H4) return;
     const int t = (int)(idx / H4), n4 = (int)(idx % H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // unrolled so that the loads of a group of rows are in flight together; the
+    // additions stay in the order j = 0 .. k-1
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
         float4 v = __ldg(reinterpret_cast<const float4 *>(y + ((size_t)t * k + j) * H) + n4);
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
@@ -341,6 +344,7 @@ __global__ void combine_bf16_kernel(const uint16_t *__restrict__ y, const uint16
             acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
         }
     };
+#pragma unroll 8
     for (int j = 0; j < k; ++j) add(y + ((size_t)t * k + j) * H);
     if (ysh) add(ysh + (size_t)t * H);
     if (out_dtype == FT_DTYPE_F32) {

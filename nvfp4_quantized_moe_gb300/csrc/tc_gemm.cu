@@ -43,33 +43,13 @@ constexpr int NSMAX = 4;      // TMA stages (at most)
 constexpr int NA = 2;         // dequantised A buffers
 constexpr int kThreadsTc = 320;  // producer, MMA, 8 dequant/epilogue warps
 constexpr int kDq = 256;
-constexpr uint64_t kWaitNs = 2000000000ull;
 
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait: false after about two seconds (or once another role gave up).
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitNs) return false;
-        }
-    }
+    return mbar_wait_timed(bar, parity, abort_flag);
 }
 
-__device__ __forceinline__ void arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
+__device__ __forceinline__ void arrive(uint64_t *bar) { mbar_arrive(bar); }
 
 struct TcSmem {
     uint32_t a_bytes, b_bytes, raw_bytes, scale_bytes, scale_row;
@@ -103,8 +83,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                    const __grid_constant__ CUtensorMap scale_map, const __grid_constant__ TcParams p, int ns)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base by pointer arithmetic on the shared array itself, so that the
+    // compiler keeps every access derived from it in the shared state space
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int K = p.K;
     const TcSmem L = tc_smem(K, p.group, ns);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -380,9 +361,8 @@ __global__ void rows_to_f16_kernel(const uint16_t *__restrict__ src, int K, cons
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-        int e = 0;
-        if (m > 0.f && m <= 3.3895314e38f) e = min(max(ilogbf(m) - 14, -126), 127);
-        const float down = __int_as_float((127 - e) << 23);
+        const int e = row_scale_exp(m);
+        const float down = pow2f(-e);
         for (int q = lane; q < K / 8; q += 32) {
             const uint4 v = __ldg(s4 + q);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -395,7 +375,7 @@ __global__ void rows_to_f16_kernel(const uint16_t *__restrict__ src, int K, cons
             }
             o[q] = make_uint4(h[0], h[1], h[2], h[3]);
         }
-        if (lane == 0) scale[pos] = __int_as_float((127 + e) << 23);
+        if (lane == 0) scale[pos] = pow2f(e);
     }
 }
 
@@ -419,8 +399,8 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-static bool make_map(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint64_t inner, uint64_t rows,
-                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz)
+bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -428,7 +408,7 @@ static bool make_map(CUtensorMap *map, CUtensorMapDataType dt, void *base, uint6
     const cuuint64_t strides[1] = {row_bytes};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -480,11 +460,11 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
     if (!ns) return cudaErrorInvalidValue;
     CUtensorMap cmap, bmap, smap;
     const uint32_t srow = (uint32_t)(p.K / p.group);
-    if (!make_map(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(codes), (uint64_t)p.K / 2,
+    if (!make_tensor_map_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(codes), (uint64_t)p.K / 2,
                   (uint64_t)rows_total, (uint64_t)p.K / 2, 32, MT, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void *>(act), (uint64_t)p.K,
+        !make_tensor_map_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void *>(act), (uint64_t)p.K,
                   (uint64_t)act_rows, (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(static_cast<const void *>(p.scales)), srow,
+        !make_tensor_map_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(static_cast<const void *>(p.scales)), srow,
                   (uint64_t)rows_total, srow, srow, MT,
                   srow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
