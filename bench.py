@@ -141,6 +141,29 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def _sources_sha256(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic(stage):
+    """DRAM bytes (read + write) per launch of the stage's kernel from the committed ncu
+    capture (profiles/kernel_traffic.json), or None when that kernel's sources have
+    changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "kernel_traffic.json")) as f:
+            rec = json.load(f).get(stage)
+        if rec and _sources_sha256(rec["sources"]) == rec["sources_sha256"]:
+            return rec
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
 def _config(args):
     return {"workload": f"qwen36-moe-decode-T{args.T}", "T": args.T, "layers": args.layers, "hidden": 2048,
             "num_experts": 256, "top_k": 8, "intermediate": 512, "shared_intermediate": 512, "group": 16,
@@ -325,15 +348,19 @@ def run_ours(args, world, rank, local):
     stage_mean_us = {name: float(stage_ms[:, :, i].mean() * 1e3) for i, name in enumerate(ft.STAGES)}
     dominant = max(stage_mean_us, key=stage_mean_us.get)
     hbm, tfl, peak_kind = _peaks()
-    gu_alg = float(np.mean([t * gu_bytes_per_expert for t in touched]))
-    dn_alg = float(np.mean([t * (2048 * 256 + 2048 * 32 + 2048 * 4) for t in touched]))
+    # the routed and the shared expert run in the same launch per stage (decode regime)
+    gu_alg = float(np.mean([(t + 1) * gu_bytes_per_expert for t in touched]))
+    dn_alg = float(np.mean([(t + 1) * (2048 * 256 + 2048 * 32 + 2048 * 4) for t in touched]))
     alg = {"gate_up": gu_alg, "down": dn_alg, "shared_gate_up": float(gu_bytes_per_expert),
            "shared_down": float(2048 * 256 + 2048 * 32 + 2048 * 4)}
     dom_bytes = alg.get(dominant, 0.0)
     dom_s = stage_mean_us[dominant] * 1e-6
     achieved = dom_bytes / dom_s / 1e9 if dom_bytes else None
+    tr = _traffic(dominant)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm if achieved else None, "traffic": None,
+                "frac": achieved / hbm if achieved else None,
+                "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "traffic_alg_bytes": tr["alg_bytes_of_captured_launch"] if tr else None,
                 "peak_source": f"{peak_kind} HBM copy bandwidth",
                 "alg_bytes_per_launch": dom_bytes, "avg_launch_us": stage_mean_us[dominant]}
     layer_us = ms_step * 1e3 / L
@@ -374,7 +401,7 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(args),
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": _config(args),
         "roofline": roofline, "layer": {"us": layer_us, "touched_experts_mean": float(np.mean(touched)),
                                         "weight_bytes_mean": float(np.mean(layer_bytes)), "gbs": layer_gbs,
                                         "frac_of_hbm": layer_gbs / hbm},
