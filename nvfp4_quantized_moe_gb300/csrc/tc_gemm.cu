@@ -16,8 +16,12 @@
 //               instruction, two per K step) and commits to the stage barriers;
 //   warps 2..9  dequantise the raw codes to the exact f16 code*scale, written in the
 //               128-byte swizzled K-major layout the MMA descriptors describe (warp
-//               half 0 tile 0, half 1 tile 1), then read the accumulators with
-//               tcgen05.ld for the epilogue.
+//               half 0 tile 0, half 1 tile 1);
+//   warps 10-13 the epilogue: read an accumulator with tcgen05.ld (one TMEM lane = one
+//               weight row per thread), apply globals, row scales and SwiGLU or the
+//               routing weight, store. Tensor memory holds two accumulators (512
+//               columns), so the MMAs of the next unit run while the epilogue drains
+//               the previous one.
 // f16 operands instead of bf16: code*scale is exact in both; a bf16 activation row
 // scaled by its power of two (maximum in [2^14, 2^15)) converts to f16 exactly except
 // for elements below 2^-31 of the row maximum, which move by less than 2^-38 of it;
@@ -41,8 +45,10 @@ constexpr int MT = 128;       // weight rows per tile (MMA M)
 constexpr int KC = 64;        // K elements per chunk (128 bytes of f16)
 constexpr int NSMAX = 4;      // TMA stages (at most)
 constexpr int NA = 2;         // dequantised A buffers
-constexpr int kThreadsTc = 320;  // producer, MMA, 8 dequant/epilogue warps
-constexpr int kDq = 256;
+constexpr int kThreadsTc = 448;  // producer, MMA, 8 dequant warps, 4 epilogue warps
+constexpr int kDq = 256;         // dequantising threads
+constexpr int kEp = 128;         // epilogue threads (one TMEM lane each)
+constexpr int kEpWarp0 = 10;     // first epilogue warp
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
@@ -53,7 +59,7 @@ __device__ __forceinline__ void arrive(uint64_t *bar) { mbar_arrive(bar); }
 
 struct TcSmem {
     uint32_t a_bytes, b_bytes, raw_bytes, scale_bytes, scale_row;
-    uint32_t a_off, b_off, raw_off, scale_off, bar_off, total;
+    uint32_t a_off, b_off, raw_off, scale_off, tbl_off, bar_off, total;
     int ns;
 };
 
@@ -70,7 +76,8 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns)
     s.b_off = s.a_off + NA * s.a_bytes;
     s.raw_off = s.b_off + ns * s.b_bytes;
     s.scale_off = s.raw_off + ns * s.raw_bytes;
-    s.bar_off = s.scale_off + 4 * s.scale_bytes;  // 2 buffers x 2 tiles
+    s.tbl_off = s.scale_off + 4 * s.scale_bytes;  // scales: 2 buffers x 2 tiles
+    s.bar_off = s.tbl_off + 4 * NT * 8;           // per epilogue warp: [NT] slots + [NT] factors
     s.total = s.bar_off + 512;
     return s;
 }
@@ -91,20 +98,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
     uint64_t *scale_full = a_empty + NA, *scale_empty = scale_full + 2;
-    uint64_t *acc_full = scale_empty + 2, *acc_empty = acc_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+    uint64_t *acc_full = scale_empty + 2, *acc_empty = acc_full + 2;  // two accumulators
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tmem_cols = 2 * NT;
+    const uint32_t tmem_cols = 4 * NT;  // two accumulators of two 128-column tiles
     const bool sw_scales = L.scale_row == 128;  // scale rows TMA-loaded 128-byte swizzled
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSMAX; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
         for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq); mbar_init(a_empty + i, 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(scale_full + i, 1); mbar_init(scale_empty + i, kDq); }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kDq);
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEp); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -158,8 +164,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint32_t idesc = tc::idesc_f16_f32(MT, NT);
             int it = 0, ia = 0, uc = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
-                if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag)) { dead = true; break; }
+                const int ab2 = uc & 1;  // accumulator of this unit
+                if (!wait_bar(acc_empty + ab2, ((uc >> 1) & 1) ^ 1, abort_flag)) { dead = true; break; }
                 tc::fence_after_sync();
+                const uint32_t acc = tmem + (uint32_t)(ab2 * 2 * NT);
                 for (int c = 0; c < nk; ++c, ++it, ++ia) {
                     const int slot = it % ns, ab = ia % NA;
                     if (!wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
@@ -173,27 +181,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
                     for (int kk = 0; kk < KC / 16; ++kk) {
                         const uint64_t bd = tc::sw128_desc(b0 + kk * 32);
-                        tc::mma_f16(tmem, tc::sw128_desc(a0 + kk * 32), bd, idesc, (c | kk) != 0);
-                        tc::mma_f16(tmem + NT, tc::sw128_desc(a0 + MT * 128 + kk * 32), bd, idesc, (c | kk) != 0);
+                        tc::mma_f16(acc, tc::sw128_desc(a0 + kk * 32), bd, idesc, (c | kk) != 0);
+                        tc::mma_f16(acc + NT, tc::sw128_desc(a0 + MT * 128 + kk * 32), bd, idesc, (c | kk) != 0);
                     }
                     tc::commit(empty + slot);
                     tc::commit(a_empty + ab);
                 }
                 if (dead) break;
-                tc::commit(acc_full);
+                tc::commit(acc_full + ab2);
             }
             if (dead) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
         }
-    } else {
-        // ------------------------------------------------------------ dequant + epilogue
-        // warp (quarter, half): TMEM lanes / tile rows 32*quarter .. +32 of tile `half`;
-        // epilogue positions [64 half, 64 half + 64) of both tiles.
+    } else if (warp < kEpWarp0) {
+        // ------------------------------------------------------------ dequantisation
+        // warp (quarter, half): rows 32*quarter .. +32 of tile `half`.
         const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;
         const int cpl = 16 * p.group / KC;  // K chunks covered by 16 scale bytes
         int it = 0, ia = 0, uc = 0;
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
-            const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
             const int sb = uc & 1;
             if (!wait_bar(scale_full + sb, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
             const unsigned char *sc = smem + L.scale_off + (2 * sb + half) * L.scale_bytes + r * L.scale_row;
@@ -242,63 +248,76 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             if (dead) break;
             arrive(scale_empty + sb);
-
-            // epilogue
-            if (!wait_bar(acc_full, uc & 1, abort_flag)) { dead = true; break; }
-            tc::fence_after_sync();
-            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
-            const float *glob_e = p.glob + (size_t)e * p.R;
-            const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-            if (GATED) {
-                const int row = m * MT + r;
-                const float gg = __ldg(glob_e + row), gu = __ldg(glob_e + p.up_off + row);
-                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
-                    uint32_t dg[32], du[32];
-                    tc::ld32(lane_addr + cb * 32, dg);
-                    tc::ld32(lane_addr + NT + cb * 32, du);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int pos = b * NT + cb * 32 + j;
-                        const float sc_pos = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
-                        const float gate = __uint_as_float(dg[j]) * sc_pos * gg;
-                        const float up = __uint_as_float(du[j]) * sc_pos * gu;
-                        __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
-                        p.h_out[(size_t)pos * p.h_ld + row] = *reinterpret_cast<uint16_t *>(&hv);
+        }
+        if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        // Thread = TMEM lane = tile row r (warp w may read lanes 32 (w % 4) ..); every
+        // thread handles all NT positions of its row in both tiles of the accumulator.
+        // Per unit the warp first builds its own table of the block's positions (slot and
+        // routing weight x activation row scale, or the row scale alone) in shared memory,
+        // while the MMAs of the unit are still running.
+        const int quarter = warp & 3;
+        const int r = 32 * quarter + lane;
+        int *tbl_slot = reinterpret_cast<int *>(smem + L.tbl_off) + (warp - kEpWarp0) * 2 * NT;
+        float *tbl_w = reinterpret_cast<float *>(tbl_slot + NT);
+        int uc = 0;
+        for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
+            const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
+            __syncwarp();
+            for (int t = lane; t < NT; t += 32) {
+                const int pos = b * NT + t;
+                float w = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
+                int dst = pos;
+                if (!GATED) {
+                    if (p.sorted_slot) {
+                        dst = __ldg(p.sorted_slot + pos);
+                        if (dst >= p.n_slots) dst = -1;
+                        else if (p.route_w) w *= __ldg(p.route_w + dst);
+                    } else if (dst >= p.n_pos_static) {
+                        dst = -1;
                     }
                 }
-            } else {
-                const int row0 = m * 2 * MT + r, row1 = row0 + MT;
-                const float d0 = __ldg(glob_e + row0), d1 = __ldg(glob_e + row1);
-                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
-                    uint32_t a0[32], a1[32];
-                    tc::ld32(lane_addr + cb * 32, a0);
-                    tc::ld32(lane_addr + NT + cb * 32, a1);
-                    tc::wait_ld();
+                tbl_slot[t] = dst;
+                tbl_w[t] = w;
+            }
+            __syncwarp();
+            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+            const float *glob_e = p.glob + (size_t)e * p.R;
+            const int row0 = GATED ? m * MT + r : m * 2 * MT + r;
+            const float g0 = __ldg(glob_e + row0);
+            const float g1 = __ldg(glob_e + (GATED ? p.up_off + row0 : row0 + MT));
+            const int ab2 = uc & 1;
+            if (!wait_bar(acc_full + ab2, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
+            tc::fence_after_sync();
+            const uint32_t lane_addr = tmem + (uint32_t)(ab2 * 2 * NT) + ((uint32_t)(32 * quarter) << 16);
+            for (int cb = 0; cb < NT / 32; ++cb) {
+                uint32_t v0[32], v1[32];
+                tc::ld32(lane_addr + cb * 32, v0);
+                tc::ld32(lane_addr + NT + cb * 32, v1);
+                tc::wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int pos = b * NT + cb * 32 + j;
-                        int dst;
-                        float wgt = 1.f;
-                        if (p.sorted_slot) {
-                            dst = __ldg(p.sorted_slot + pos);
-                            if (dst >= p.n_slots) continue;
-                            if (p.route_w) wgt = __ldg(p.route_w + dst);
-                        } else {
-                            dst = pos;
-                            if (dst >= p.n_pos_static) continue;
-                        }
-                        if (p.act_scale) wgt *= __ldg(p.act_scale + pos);
+                for (int j = 0; j < 32; ++j) {
+                    const int t = cb * 32 + j;
+                    const float w = tbl_w[t];
+                    if (GATED) {
+                        const float gate = __uint_as_float(v0[j]) * w * g0;
+                        const float up = __uint_as_float(v1[j]) * w * g1;
+                        __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
+                        p.h_out[(size_t)(b * NT + t) * p.h_ld + row0] = *reinterpret_cast<uint16_t *>(&hv);
+                    } else {
+                        const int dst = tbl_slot[t];
+                        if (dst < 0) continue;
                         uint16_t *yrow = p.y_out + (size_t)dst * p.y_ld;
-                        __nv_bfloat16 y0 = __float2bfloat16_rn(__uint_as_float(a0[j]) * d0 * wgt);
-                        __nv_bfloat16 y1 = __float2bfloat16_rn(__uint_as_float(a1[j]) * d1 * wgt);
+                        __nv_bfloat16 y0 = __float2bfloat16_rn(__uint_as_float(v0[j]) * g0 * w);
+                        __nv_bfloat16 y1 = __float2bfloat16_rn(__uint_as_float(v1[j]) * g1 * w);
                         yrow[row0] = *reinterpret_cast<uint16_t *>(&y0);
-                        yrow[row1] = *reinterpret_cast<uint16_t *>(&y1);
+                        yrow[row0 + MT] = *reinterpret_cast<uint16_t *>(&y1);
                     }
                 }
             }
             tc::fence_before_sync();
-            arrive(acc_empty);
+            arrive(acc_empty + ab2);
         }
         if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     }
