@@ -408,14 +408,14 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     const int n_slots = T * G.k;
 
     struct Disarm { ~Disarm() { g_stage_armed = false; } } disarm_on_return;
-    cudaError_t e = cudaMemsetAsync(status, 0, L.zero_bytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    cudaError_t e;
     if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
 
     auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
     if (use_tc(G, T)) {
         // ---------------------------------------------------------------- tensor-core path
-        e = launch_align(topk_ids, T, G.k, G.E, kTcBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s);
+        e = launch_align(topk_ids, T, G.k, G.E, kTcBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s,
+                         status, L.zero_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "align launch");
         const int max_blocks_tc = L.pmax / kTcBlock, tpad_tc = cdiv(T, kTcBlock);
         uint16_t *yb = reinterpret_cast<uint16_t *>(y), *yb_sh = reinterpret_cast<uint16_t *>(y_sh);
@@ -488,7 +488,8 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         return ok();
     }
 
-    e = launch_align(topk_ids, T, G.k, G.E, kGemvBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s);
+    e = launch_align(topk_ids, T, G.k, G.E, kGemvBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s,
+                         status, L.zero_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "align launch");
     const int max_blocks = (int)(((int64_t)n_slots + (n_slots < G.E ? n_slots : G.E) * (kGemvBlock - 1)) / kGemvBlock);
     const int tpad = (T + kGemvBlock - 1) / kGemvBlock;

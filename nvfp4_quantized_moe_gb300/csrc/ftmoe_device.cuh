@@ -107,6 +107,20 @@ __device__ __forceinline__ void dequant8_f16(uint32_t codes, uint32_t scale_f16x
     for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[i]) : "r"(f[i]), "r"(scale_f16x2));
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Every kernel of the library starts with pdl_wait(): it returns once the kernels before
+// it in the stream have completed and their memory is visible, so a kernel launched
+// early (programmatic dependent launch) never reads or overwrites what they still use.
+// pdl_trigger() then lets the next kernel's CTAs be scheduled while this one runs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter()
+{
+    pdl_wait();
+    pdl_trigger();
+}
+
 // ---------------------------------------------------------------- activation row scaling
 
 // 2^e for integer e in [-126, 127], built from its bits (exact).
@@ -291,18 +305,21 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
 
 // Wait for phase `parity` of `bar`: false after about two seconds, or as soon as
 // another role of the CTA has set *abort_flag (non-null) after giving up itself.
-// Between polls the thread sleeps (32 ns doubling to 256 ns), so that a waiting warp
-// leaves the issue slots of its scheduler to the warps that have work.
+// The first 2048 polls spin (the pipelines' waits are short and latency-critical); after
+// that the thread sleeps between polls (32 ns doubling to 256 ns), so that a warp left
+// waiting for long leaves the issue slots of its scheduler to the warps that have work.
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     uint32_t sleep_ns = 32;
     for (uint32_t i = 1;; ++i) {
-        __nanosleep(sleep_ns);
-        if (sleep_ns < 256) sleep_ns <<= 1;
+        if (i > 2048) {
+            __nanosleep(sleep_ns);
+            if (sleep_ns < 256) sleep_ns <<= 1;
+        }
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0) {
+        if ((i & 255u) == 0) {
             if (abort_flag && *abort_flag) return false;
             if (globaltimer() - t0 > kWaitNs) return false;
         }

@@ -88,6 +88,31 @@ bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ba
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
 
 int sm_count();
+
+// Launch with programmatic stream serialization: the kernel may be scheduled before its
+// predecessor in the stream finishes; it waits for it in pdl_wait() before touching
+// memory (every kernel of the library starts with pdl_enter()).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+// launch_pdl inside a function returning cudaError_t: return the launch error, if any.
+#define FT_LAUNCH(...)                                                                                         \
+    do {                                                                                                       \
+        const cudaError_t le_ = launch_pdl(__VA_ARGS__);                                                       \
+        if (le_ != cudaSuccess) return le_;                                                                    \
+    } while (0)
 // Sets the thread-local error message (cleared for FT_OK) and returns `code`.
 ft_status report_error(ft_status code, const char *message);
 // Adds n to the calling thread's launch counter (ft_moe_launch_count).
@@ -96,11 +121,13 @@ void count_launches(int n);
 cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t s);
 
 // Align into caller buffers; `scratch` holds kAlignChunk-sized chunk counts and
-// per-slot ranks (align_scratch_bytes).
+// per-slot ranks (align_scratch_bytes). The zero_bytes at `zero` (a multiple of 4, the
+// status word among them) are cleared first, in the align launch itself when it is a
+// single CTA.
 size_t align_scratch_bytes(int n_slots, int E);
 cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t *sorted_slot,
                          int32_t *block_expert, int32_t *expert_off, int32_t *n_padded, int *status,
-                         void *scratch, cudaStream_t s);
+                         void *scratch, cudaStream_t s, int *zero = nullptr, size_t zero_bytes = 0);
 
 // K-split (1, 2, 4 or 8 warps per row tile) for a launch whose CTA-unit count at
 // K-split 1 is max_blocks * units_per_block_ks1.

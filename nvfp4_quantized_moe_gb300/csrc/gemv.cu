@@ -90,6 +90,7 @@ __device__ __forceinline__ void mma_frag(const Frag &f, const uint4 (&b)[4], flo
 template <int KS>
 __global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_gated_kernel(const GemvParams p)
 {
+    pdl_enter();
     constexpr int TPW = 8 / KS;
     extern __shared__ uint4 smem_b[];
     __shared__ float inv[kGemvBlock];
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_gated_ke
 template <int KS>
 __global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_down_kernel(const GemvParams p)
 {
+    pdl_enter();
     constexpr int TPW = 8 / KS;
     extern __shared__ uint4 smem_b[];
     __shared__ float inv[kGemvBlock];
@@ -299,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_down_ker
 __global__ void combine_kernel(const float *__restrict__ y, const float *__restrict__ ysh, int T, int k, int H,
                                void *out, int out_dtype)
 {
+    pdl_enter();
     const int H4 = H / 4;
     size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)T * H4) return;
@@ -330,6 +333,7 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
 __global__ void combine_bf16_kernel(const uint16_t *__restrict__ y, const uint16_t *__restrict__ ysh, int T, int k,
                                     int H, void *out, int out_dtype)
 {
+    pdl_enter();
     const int H8 = H / 8;
     size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)T * H8) return;
@@ -367,8 +371,8 @@ cudaError_t launch_combine_bf16(const uint16_t *y, const uint16_t *y_shared, int
 {
     const size_t n = (size_t)T * (H / 8);
     const int threads = 256;
-    combine_bf16_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(y, y_shared, T, k, H, out,
-                                                                                     out_dtype);
+    FT_LAUNCH(combine_bf16_kernel, dim3((unsigned)((n + threads - 1) / threads)), dim3(threads), 0, s, y,
+              y_shared, T, k, H, out, out_dtype);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -386,7 +390,7 @@ static cudaError_t launch_persistent(Kern kern, const GemvParams &p, int max_uni
     int grid = sm_count() * FTMOE_GEMV_MIN_BLOCKS;
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, kThreads, smem, s>>>(p);
+    FT_LAUNCH(kern, dim3(grid), dim3(kThreads), smem, s, p);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -428,7 +432,8 @@ cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, 
 {
     const size_t n = (size_t)T * (H / 4);
     const int threads = 256;
-    combine_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(y, y_shared, T, k, H, out, out_dtype);
+    FT_LAUNCH(combine_kernel, dim3((unsigned)((n + threads - 1) / threads)), dim3(threads), 0, s, y, y_shared,
+              T, k, H, out, out_dtype);
     count_launches(1);
     return cudaGetLastError();
 }

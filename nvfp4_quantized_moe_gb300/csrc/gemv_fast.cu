@@ -190,6 +190,7 @@ __device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_p
 template <bool GATED, int KS>
 __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_constant__ FastLaunch L)
 {
+    pdl_enter();
     extern __shared__ uint4 smem_b[];
     __shared__ float inv[kGemvBlock];
     __shared__ int rows[kGemvBlock];
@@ -234,7 +235,7 @@ static cudaError_t launch_fast_t(const FastLaunch &L, int max_units, cudaStream_
     int grid = sm_count() * 2;
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, kThreads, smem, s>>>(L);
+    FT_LAUNCH(kern, dim3(grid), dim3(kThreads), smem, s, L);
     count_launches(1);
     return cudaGetLastError();
 }

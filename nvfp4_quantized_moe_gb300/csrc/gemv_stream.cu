@@ -148,6 +148,7 @@ __device__ __forceinline__ UnitPos unit_pos(const Geo2 &geo, int u, int units0)
 template <bool GATED>
 __global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const __grid_constant__ StreamLaunch L)
 {
+    pdl_enter();
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte aligned base by pointer arithmetic on the shared array itself, so that the
     // compiler keeps every access derived from it in the shared state space
@@ -529,7 +530,7 @@ cudaError_t launch_gemv_stream(StreamLaunch &L, bool gated, int max_units, cudaS
     int grid = sm_count();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, kStreamThreads, smem, s>>>(L);
+    FT_LAUNCH(kern, dim3(grid), dim3(kStreamThreads), smem, s, L);
     count_launches(1);
     return cudaGetLastError();
 }

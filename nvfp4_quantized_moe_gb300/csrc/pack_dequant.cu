@@ -11,6 +11,7 @@ namespace ftmoe {
 __global__ void copy2d_kernel(const uint8_t *__restrict__ src, size_t src_pitch, uint8_t *__restrict__ dst,
                               size_t dst_pitch, size_t width, size_t height, int vec)
 {
+    pdl_enter();
     const size_t per_row = vec ? width / 16 : width;
     const size_t total = per_row * height;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -33,7 +34,8 @@ cudaError_t launch_pack_copy2d(const uint8_t *src, size_t src_pitch, uint8_t *ds
     size_t blocks = (total + 255) / 256;
     const size_t cap = (size_t)sm_count() * 16;
     if (blocks > cap) blocks = cap;
-    copy2d_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, src_pitch, dst, dst_pitch, width, height, vec);
+    FT_LAUNCH(copy2d_kernel, dim3((unsigned)blocks), dim3(256), 0, s, src, src_pitch, dst, dst_pitch, width,
+              height, vec);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -43,6 +45,7 @@ cudaError_t launch_pack_copy2d(const uint8_t *src, size_t src_pitch, uint8_t *ds
 __global__ void dequant_kernel(const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, int rows,
                                int K, int group, uint16_t *__restrict__ out)
 {
+    pdl_enter();
     const size_t words = (size_t)rows * (K / 8);
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= words) return;
@@ -63,7 +66,8 @@ cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *scales, int rows
 {
     const size_t words = (size_t)rows * (K / 8);
     if (words == 0) return cudaSuccess;
-    dequant_kernel<<<(unsigned)((words + 255) / 256), 256, 0, s>>>(codes, scales, rows, K, group, out);
+    FT_LAUNCH(dequant_kernel, dim3((unsigned)((words + 255) / 256)), dim3(256), 0, s, codes, scales, rows, K,
+              group, out);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -25,6 +25,7 @@ template <int VPL>
 __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int T, int E, int k,
                                                     int32_t *__restrict__ ids, float *__restrict__ w)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -73,12 +74,12 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
     const int warps = 8;
     dim3 grid((T + warps - 1) / warps), block(warps * 32);
     int vpl = (E + 31) / 32;
-    if (vpl <= 1) route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-    else if (vpl <= 2) route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-    else if (vpl <= 4) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-    else if (vpl <= 8) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-    else if (vpl <= 16) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-    else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+    if (vpl <= 1) FT_LAUNCH(route_kernel<1>, dim3(grid), dim3(block), 0, s, logits, T, E, k, ids, w);
+    else if (vpl <= 2) FT_LAUNCH(route_kernel<2>, dim3(grid), dim3(block), 0, s, logits, T, E, k, ids, w);
+    else if (vpl <= 4) FT_LAUNCH(route_kernel<4>, dim3(grid), dim3(block), 0, s, logits, T, E, k, ids, w);
+    else if (vpl <= 8) FT_LAUNCH(route_kernel<8>, dim3(grid), dim3(block), 0, s, logits, T, E, k, ids, w);
+    else if (vpl <= 16) FT_LAUNCH(route_kernel<16>, dim3(grid), dim3(block), 0, s, logits, T, E, k, ids, w);
+    else FT_LAUNCH(route_kernel<32>, dim3(grid), dim3(block), 0, s, logits, T, E, k, ids, w);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -175,8 +176,13 @@ __device__ void fill_blocks(const int *off, const int *count, int E, int B, int 
 // then per-expert prefixes over warps, padded offsets, placement.
 __global__ void __launch_bounds__(1024) align_fused_kernel(const int32_t *__restrict__ ids, int n, int k, int E,
                                                            int B, int32_t *sorted_slot, int32_t *block_expert,
-                                                           int32_t *expert_off, int32_t *n_padded, int *status)
+                                                           int32_t *expert_off, int32_t *n_padded, int *status,
+                                                           int *zero, int zero_words)
 {
+    pdl_enter();
+    // the forward's status word and combine counters start at zero (cleared here instead
+    // of by a separate memset); the __syncthreads below orders this before any error report
+    for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero[i] = 0;
     extern __shared__ int smem[];
     int *cnt = smem;                    // [32][E]
     int *rank = cnt + 32 * E;           // [n]
@@ -222,6 +228,7 @@ __global__ void __launch_bounds__(1024) align_fused_kernel(const int32_t *__rest
 __global__ void __launch_bounds__(256) align_count_kernel(const int32_t *__restrict__ ids, int n, int k, int E,
                                                           int *chunk_cnt, int *rank, int *status)
 {
+    pdl_enter();
     extern __shared__ int smem[];
     int *cnt = smem;  // [8][E]
     const int tid = threadIdx.x, wid = tid >> 5;
@@ -253,6 +260,7 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int *chunk_cnt, int n_
                                                           int32_t *sorted_slot, int32_t *block_expert,
                                                           int32_t *expert_off, int32_t *n_padded)
 {
+    pdl_enter();
     extern __shared__ int smem[];
     int *off = smem;          // [E+1]
     int *count = off + E + 1; // [E]
@@ -281,6 +289,7 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int *chunk_cnt, int n_
 __global__ void align_place_kernel(const int32_t *__restrict__ ids, int n, int E, const int *chunk_base,
                                    const int *rank, const int32_t *expert_off, int32_t *sorted_slot)
 {
+    pdl_enter();
     int s = blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= n) return;
     int e = __ldg(ids + s);
@@ -300,7 +309,7 @@ size_t align_scratch_bytes(int n_slots, int E)
 
 cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t *sorted_slot,
                          int32_t *block_expert, int32_t *expert_off, int32_t *n_padded, int *status,
-                         void *scratch, cudaStream_t s)
+                         void *scratch, cudaStream_t s, int *zero, size_t zero_bytes)
 {
     const int n = T * k;
     if (n <= kAlignFusedMax) {
@@ -308,10 +317,14 @@ cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t
         cudaError_t err = cudaFuncSetAttribute(align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)smem);
         if (err != cudaSuccess) return err;
-        align_fused_kernel<<<1, 1024, smem, s>>>(ids, n, k, E, B, sorted_slot, block_expert, expert_off,
-                                                 n_padded, status);
+        FT_LAUNCH(align_fused_kernel, dim3(1), dim3(1024), smem, s, ids, n, k, E, B, sorted_slot, block_expert,
+                  expert_off, n_padded, status, zero, (int)(zero_bytes / sizeof(int)));
         count_launches(1);
         return cudaGetLastError();
+    }
+    if (zero_bytes) {
+        cudaError_t err = cudaMemsetAsync(zero, 0, zero_bytes, s);
+        if (err != cudaSuccess) return err;
     }
     const int chunks = (n + kAlignChunk - 1) / kAlignChunk;
     int *chunk_cnt = static_cast<int *>(scratch);
@@ -319,11 +332,12 @@ cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t
     size_t smem1 = sizeof(int) * 8 * (size_t)E;
     cudaError_t err = cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
     if (err != cudaSuccess) return err;
-    align_count_kernel<<<chunks, 256, smem1, s>>>(ids, n, k, E, chunk_cnt, rank, status);
+    FT_LAUNCH(align_count_kernel, dim3(chunks), dim3(256), smem1, s, ids, n, k, E, chunk_cnt, rank, status);
     size_t smem2 = sizeof(int) * ((size_t)(E + 1) + E + 33);
-    align_scan_kernel<<<1, 1024, smem2, s>>>(chunk_cnt, chunks, E, B, n, sorted_slot, block_expert, expert_off,
-                                             n_padded);
-    align_place_kernel<<<(n + 255) / 256, 256, 0, s>>>(ids, n, E, chunk_cnt, rank, expert_off, sorted_slot);
+    FT_LAUNCH(align_scan_kernel, dim3(1), dim3(1024), smem2, s, chunk_cnt, chunks, E, B, n, sorted_slot,
+              block_expert, expert_off, n_padded);
+    FT_LAUNCH(align_place_kernel, dim3((n + 255) / 256), dim3(256), 0, s, ids, n, E, chunk_cnt, rank,
+              expert_off, sorted_slot);
     count_launches(3);
     return cudaGetLastError();
 }

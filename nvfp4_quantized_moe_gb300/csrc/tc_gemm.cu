@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ CUtensorMap scale_map, const __grid_constant__ TcParams p, int ns)
 {
+    pdl_enter();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base by pointer arithmetic on the shared array itself, so that the
     // compiler keeps every access derived from it in the shared state space
@@ -352,6 +353,7 @@ __global__ void rows_to_f16_kernel(const uint16_t *__restrict__ src, int K, cons
                                    const int *__restrict__ n_pos_dev, int n_pos_static, int n_slots, int top_k,
                                    uint16_t *__restrict__ out, float *__restrict__ scale)
 {
+    pdl_enter();
     const int n_pos = n_pos_dev ? *n_pos_dev : n_pos_static;
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -462,8 +464,8 @@ cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slo
     const int cap = sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    rows_to_f16_kernel<<<blocks, 256, 0, s>>>(src, K, sorted_slot, n_pos_dev, n_pos_static, n_slots, top_k, out,
-                                               scale);
+    FT_LAUNCH(rows_to_f16_kernel, dim3(blocks), dim3(256), 0, s, src, K, sorted_slot, n_pos_dev, n_pos_static,
+              n_slots, top_k, out, scale);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -494,7 +496,7 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
     auto kern = gated ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsTc, smem, s>>>(cmap, bmap, smap, p, ns);
+    FT_LAUNCH(kern, dim3(grid), dim3(kThreadsTc), smem, s, cmap, bmap, smap, p, ns);
     count_launches(1);
     return cudaGetLastError();
 }
