@@ -239,6 +239,32 @@ def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
             "expert_tokens_max_over_mean": float(counts.max() / counts.mean())}
 
 
+def measure_router(ft, dev, T, E=256, H=2048, reps=6):
+    """ft_moe_route_gemm (router logit GEMM + top-8) for one layer's router, L2 flushed."""
+    import torch
+    x = torch.from_numpy(synth.make_activations(T, H, seed=5).view(np.int16)).to(dev).view(torch.bfloat16)
+    wr = torch.from_numpy(synth.make_router_weights(E, H, seed=5).view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
+    w = torch.empty((T, 8), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    for r in range(reps + 2):
+        flush.fill_(r & 0xFF)
+        start.record(stream)
+        ft.ft_moe_route_gemm(x, wr, 8, logits, ids, w)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if r >= 2:
+            times.append(start.elapsed_time(stop))
+    us = float(np.median(times)) * 1e3
+    del flush
+    return {"T": T, "E": E, "H": H, "us": us, "weight_gbs": E * H * 2 / (us * 1e-6) / 1e9,
+            "tflops": 2.0 * T * E * H / (us * 1e-6) / 1e12, "l2": "512 MB written before every repetition"}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import nvfp4_quantized_moe_gb300 as ft
@@ -270,6 +296,7 @@ def run_ours(args, world, rank, local):
     prefill = None
     if not args.no_prefill:
         prefill = [measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T_) for T_ in (2048, 8192)]
+    router = [measure_router(ft, dev, T_) for T_ in (T, 2048)]
     del routed_d, shared_d
     x_host = [synth.make_activations(T, H, seed=l) for l in range(L)]
     lg_host = [synth.make_logits(T, E, seed=l) for l in range(L)]
@@ -405,7 +432,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline, "layer": {"us": layer_us, "touched_experts_mean": float(np.mean(touched)),
                                         "weight_bytes_mean": float(np.mean(layer_bytes)), "gbs": layer_gbs,
                                         "frac_of_hbm": layer_gbs / hbm},
-        "stage_us": stage_mean_us, "prefill": prefill, "e2e": e2e,
+        "stage_us": stage_mean_us, "prefill": prefill, "router_gemm": router, "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk.summary(),
     }

@@ -159,6 +159,21 @@ ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pie
 ft_status ft_moe_route(const float *logits, int32_t T, int32_t E, int32_t k,
                        int32_t *topk_ids, float *topk_w, void *stream);
 
+/* Router with its logit GEMM: logits[t, e] = sum_h x[t, h] * w_router[e, h] over the
+ * bf16 values, accumulated in fp32 (the router is replicated on every rank and every
+ * rank computes the same routing: "[1/3] feat(dsv4): add tensor-parallel DeepSeek-V4
+ * runtime", table "Tensor ownership and collectives"), then exactly ft_moe_route on
+ * those logits.
+ *   x         device bf16 [T, H], row-major, 16-byte aligned
+ *   w_router  device bf16 [E, H], row-major, 16-byte aligned (caller-owned)
+ *   logits    device f32 [T, E] (out, also the router's input), 4-byte aligned
+ *   topk_ids  device i32 [T, k] (out); topk_w device f32 [T, k] (out)
+ * H must be a multiple of 32. T = 0 is a no-op. Errors:
+ * FT_ERR_INVALID_ARG (NULL or misaligned pointer, H not a positive multiple of 32),
+ * FT_ERR_UNSUPPORTED (E > 1024, k > 32, k > E), FT_ERR_CUDA. */
+ft_status ft_moe_route_gemm(const void *x, int32_t T, int32_t H, const void *w_router, int32_t E, int32_t k,
+                            float *logits, int32_t *topk_ids, float *topk_w, void *stream);
+
 /* Bytes of workspace ft_moe_forward needs for this config and token count
  * (256-byte aligned buffer). Host-only. */
 ft_status ft_moe_workspace_size(const ft_moe_config *cfg, int32_t T, size_t *bytes);

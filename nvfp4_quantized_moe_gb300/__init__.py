@@ -14,7 +14,7 @@ import os
 import torch
 
 __all__ = [
-    "FtMoeError", "MoEConfig", "load", "ft_moe_layout", "ft_moe_pack", "ft_moe_route",
+    "FtMoeError", "MoEConfig", "load", "ft_moe_layout", "ft_moe_pack", "ft_moe_route", "ft_moe_route_gemm",
     "ft_moe_workspace_size", "ft_moe_forward", "ft_moe_align_workspace_size", "ft_moe_align",
     "ft_moe_dequant", "ft_moe_read_status", "ft_last_error", "alloc_banks", "EXPORTS",
     "FT_GU", "FT_GU_SCALE", "FT_GU_GLOBAL", "FT_DN", "FT_DN_SCALE", "FT_DN_GLOBAL",
@@ -31,8 +31,8 @@ STATUS = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_INDIVISIBLE", 3: "FT_E
 BANK_NAMES = ("gate_up", "gate_up_scale", "gate_up_global", "down", "down_scale", "down_global")
 
 # Every symbol include/ft_moe.h declares.
-EXPORTS = ("ft_moe_layout", "ft_moe_pack", "ft_moe_route", "ft_moe_workspace_size", "ft_moe_forward",
-           "ft_moe_align_workspace_size", "ft_moe_align", "ft_moe_dequant", "ft_moe_read_status",
+EXPORTS = ("ft_moe_layout", "ft_moe_pack", "ft_moe_route", "ft_moe_route_gemm", "ft_moe_workspace_size",
+           "ft_moe_forward", "ft_moe_align_workspace_size", "ft_moe_align", "ft_moe_dequant", "ft_moe_read_status",
            "ft_last_error", "ft_moe_set_stage_events", "ft_moe_launch_count", "ft_moe_align_static")
 FT_NSTAGES = 6
 STAGES = ("align", "gate_up", "shared_gate_up", "down", "shared_down", "combine")
@@ -84,6 +84,7 @@ def load():
             "ft_moe_layout": [P, I32, P],
             "ft_moe_pack": [P, I32, P, P, P],
             "ft_moe_route": [P, I32, I32, I32, P, P, P],
+            "ft_moe_route_gemm": [P, I32, I32, P, I32, I32, P, P, P, P],
             "ft_moe_workspace_size": [P, I32, P],
             "ft_moe_forward": [P, P, P, P, I32, P, P, P, I32, P, SZ, P],
             "ft_moe_align_workspace_size": [I32, I32, I32, P],
@@ -174,6 +175,15 @@ def ft_moe_pack(cfg: MoEConfig, shared: int, pieces: dict, banks, stream=None):
 def ft_moe_route(logits: torch.Tensor, k: int, topk_ids: torch.Tensor, topk_w: torch.Tensor, stream=None):
     T, E = logits.shape
     _check(load().ft_moe_route(_ptr(logits), T, E, k, _ptr(topk_ids), _ptr(topk_w), _stream(stream, logits)))
+
+
+def ft_moe_route_gemm(x: torch.Tensor, w_router: torch.Tensor, k: int, logits: torch.Tensor, topk_ids: torch.Tensor,
+                      topk_w: torch.Tensor, stream=None):
+    """Router logits = x . w_router^T (bf16 in, fp32 [T, E] out), then the top-k of ft_moe_route."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    _check(load().ft_moe_route_gemm(_ptr(x), T, H, _ptr(w_router), E, k, _ptr(logits), _ptr(topk_ids),
+                                    _ptr(topk_w), _stream(stream, x)))
 
 
 def ft_moe_workspace_size(cfg: MoEConfig, T: int) -> int:

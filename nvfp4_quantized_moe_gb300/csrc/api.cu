@@ -341,6 +341,25 @@ ft_status ft_moe_route(const float *logits, int32_t T, int32_t E, int32_t k, int
     return ok();
 }
 
+ft_status ft_moe_route_gemm(const void *x, int32_t T, int32_t H, const void *w_router, int32_t E, int32_t k,
+                            float *logits, int32_t *topk_ids, float *topk_w, void *stream)
+{
+    if (T < 0 || E <= 0 || k <= 0 || H <= 0) return fail(FT_ERR_INVALID_ARG, "need T >= 0, H, E, k > 0");
+    if (H % 32) return fail(FT_ERR_INVALID_ARG, "need H a multiple of 32");
+    if (E > 1024 || k > 32 || k > E) return fail(FT_ERR_UNSUPPORTED, "need k <= 32, k <= E <= 1024");
+    if (T == 0) return ok();
+    if (!x || !w_router || !logits || !topk_ids || !topk_w || !aligned(x, 16) || !aligned(w_router, 16) ||
+        !aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return fail(FT_ERR_INVALID_ARG, "router pointers must be non-NULL; x and w_router 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_router_gemm(static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(w_router), T, H,
+                                       E, logits, s);
+    if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");
+    e = launch_route(logits, T, E, k, topk_ids, topk_w, s);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    return ok();
+}
+
 ft_status ft_moe_align_workspace_size(int32_t T, int32_t k, int32_t E, size_t *bytes)
 {
     if (!bytes || T < 0 || k <= 0 || E <= 0) return fail(FT_ERR_INVALID_ARG, "bad align arguments");

@@ -119,6 +119,9 @@ ft_status report_error(ft_status code, const char *message);
 void count_launches(int n);
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t s);
+// logits [T][E] (fp32) = x [T][H] . w [E][H]^T over bf16; H % 32 == 0.
+cudaError_t launch_router_gemm(const uint16_t *x, const uint16_t *w, int T, int H, int E, float *logits,
+                               cudaStream_t s);
 
 // Align into caller buffers; `scratch` holds kAlignChunk-sized chunk counts and
 // per-slot ranks (align_scratch_bytes). The zero_bytes at `zero` (a multiple of 4, the

@@ -4,9 +4,8 @@
 // rows): for gate_up the gate rows [i0, i0+128) and the matching up rows I_l + i0 + ..,
 // whose accumulators sit side by side in tensor memory so SwiGLU fuses into the
 // epilogue; for down the rows [n0, n0+256) as two tiles. Warp roles, persistent CTA:
-//   warp 0      one thread issues every TMA: per unit the two tiles' block scales
-//               (double-buffered, prefetched a unit ahead); per 64-element K chunk the
-//               raw packed codes of both tiles (box 32 bytes x 128 rows) and the block's
+//   warp 0      one thread issues every TMA: per 64-element K chunk the raw packed
+//               codes of both tiles (box 32 bytes x 128 rows) and the block's
 //               activations (f16 box 64 x 128, 128-byte swizzled, K-major) -- gate_up
 //               reads them from the expert-sorted f16 copy of x, down from the f16 copy
 //               of h; each activation row carries a power-of-two scale (see
@@ -14,7 +13,8 @@
 //   warp 1      allocates tensor memory and from one thread issues tcgen05.mma
 //               (kind::f16, f16 x f16 -> fp32, M = 128, N = 128, K = 16 per
 //               instruction, two per K step) and commits to the stage barriers;
-//   warps 2..9  dequantise the raw codes to the exact f16 code*scale, written in the
+//   warps 2..9  dequantise the raw codes to the exact f16 code*scale (each thread reads
+//               its row's block scales from global memory, 16 bytes a group ahead), written in the
 //               128-byte swizzled K-major layout the MMA descriptors describe (warp
 //               half 0 tile 0, half 1 tile 1);
 //   warps 10-13 the epilogue: read an accumulator with tcgen05.ld (one TMEM lane = one
@@ -44,7 +44,7 @@ constexpr int NT = kTcBlock;  // positions per unit (MMA N)
 constexpr int MT = 128;       // weight rows per tile (MMA M)
 constexpr int KC = 64;        // K elements per chunk (128 bytes of f16)
 constexpr int NSMAX = 4;      // TMA stages (at most)
-constexpr int NA = 2;         // dequantised A buffers
+constexpr int NA = 4;         // dequantised A buffers
 constexpr int kThreadsTc = 448;  // producer, MMA, 8 dequant warps, 4 epilogue warps
 constexpr int kDq = 256;         // dequantising threads
 constexpr int kEp = 128;         // epilogue threads (one TMEM lane each)
@@ -55,11 +55,19 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     return mbar_wait_timed(bar, parity, abort_flag);
 }
 
+// The same, for a whole warp: every lane waits (and so acquires what the phase
+// publishes); the result is the same on all lanes, so the warp leaves its loops together.
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    const bool ok = mbar_wait_timed(bar, parity, abort_flag);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 __device__ __forceinline__ void arrive(uint64_t *bar) { mbar_arrive(bar); }
 
 struct TcSmem {
-    uint32_t a_bytes, b_bytes, raw_bytes, scale_bytes, scale_row;
-    uint32_t a_off, b_off, raw_off, scale_off, tbl_off, bar_off, total;
+    uint32_t a_bytes, b_bytes, raw_bytes;
+    uint32_t a_off, b_off, raw_off, tbl_off, bar_off, total;
     int ns;
 };
 
@@ -69,14 +77,13 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns)
     s.a_bytes = 2u * MT * 128;
     s.b_bytes = (uint32_t)NT * 128;
     s.raw_bytes = 2u * MT * 32;
-    s.scale_row = (uint32_t)(K / group);
-    s.scale_bytes = (uint32_t)MT * s.scale_row;  // per tile
+    (void)K;
+    (void)group;
     s.ns = ns;
     s.a_off = 0;
     s.b_off = s.a_off + NA * s.a_bytes;
     s.raw_off = s.b_off + ns * s.b_bytes;
-    s.scale_off = s.raw_off + ns * s.raw_bytes;
-    s.tbl_off = s.scale_off + 4 * s.scale_bytes;  // scales: 2 buffers x 2 tiles
+    s.tbl_off = s.raw_off + ns * s.raw_bytes;
     s.bar_off = s.tbl_off + 4 * NT * 8;           // per epilogue warp: [NT] slots + [NT] factors
     s.total = s.bar_off + 512;
     return s;
@@ -87,7 +94,7 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns)
 template <bool GATED>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap b_map,
-                   const __grid_constant__ CUtensorMap scale_map, const __grid_constant__ TcParams p, int ns)
+                   const __grid_constant__ TcParams p, int ns)
 {
     pdl_enter();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -98,20 +105,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const TcSmem L = tc_smem(K, p.group, ns);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
-    uint64_t *scale_full = a_empty + NA, *scale_empty = scale_full + 2;
-    uint64_t *acc_full = scale_empty + 2, *acc_empty = acc_full + 2;  // two accumulators
+    uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + 2;  // two accumulators
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t tmem_cols = 4 * NT;  // two accumulators of two 128-column tiles
-    const bool sw_scales = L.scale_row == 128;  // scale rows TMA-loaded 128-byte swizzled
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSMAX; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
-        for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq); mbar_init(a_empty + i, 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(scale_full + i, 1); mbar_init(scale_empty + i, kDq); }
-        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEp); }
+        // consumer barriers count warps: each warp arrives once, from lane 0 after __syncwarp
+        for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq / 32); mbar_init(a_empty + i, 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEp / 32); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -119,7 +124,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (warp == 0 && lane == 0) {
         tc::prefetch_map(&codes_map);
         tc::prefetch_map(&b_map);
-        tc::prefetch_map(&scale_map);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -135,18 +139,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int it = 0, uc = 0;
-            for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
+            int it = 0;
+            for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
                 const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
                 const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
                 const int row_a = e * p.R + m * tile_rows;
                 const int row_b = GATED ? row_a + p.up_off : row_a + MT;
-                const int sb = uc & 1;
-                if (!wait_bar(scale_empty + sb, ((uc >> 1) & 1) ^ 1, abort_flag)) { dead = true; break; }
-                mbar_arrive_expect_tx(scale_full + sb, 2 * L.scale_bytes);
-                tc::tma_load_2d(smem + L.scale_off + (2 * sb) * L.scale_bytes, &scale_map, 0, row_a, scale_full + sb);
-                tc::tma_load_2d(smem + L.scale_off + (2 * sb + 1) * L.scale_bytes, &scale_map, 0, row_b,
-                                scale_full + sb);
                 for (int c = 0; c < nk; ++c, ++it) {
                     const int slot = it % ns;
                     if (!wait_bar(empty + slot, ((it / ns) & 1) ^ 1, abort_flag)) { dead = true; break; }
@@ -158,6 +156,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
             }
             if (dead) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
+            // let every issued copy land before the CTA's shared memory can be released:
+            // wait for the last issued phase of each stage (already complete unless a
+            // consumer gave up)
+            for (int i = 0; i < ns && i < it; ++i) {
+                const int last = it - 1 - i;
+                mbar_wait_timed(full + last % ns, (last / ns) & 1, nullptr);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -196,25 +201,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     } else if (warp < kEpWarp0) {
         // ------------------------------------------------------------ dequantisation
         // warp (quarter, half): rows 32*quarter .. +32 of tile `half`.
+        // Block scales come straight from global memory: each thread reads its own row's
+        // 16-byte groups (one group covers cpl chunks), one group ahead, across units.
         const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;
         const int cpl = 16 * p.group / KC;  // K chunks covered by 16 scale bytes
-        int it = 0, ia = 0, uc = 0;
-        for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
-            const int sb = uc & 1;
-            if (!wait_bar(scale_full + sb, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
-            const unsigned char *sc = smem + L.scale_off + (2 * sb + half) * L.scale_bytes + r * L.scale_row;
+        const int ngroups = nk / cpl;
+        const size_t srow_bytes = (size_t)(K / p.group);
+        auto scale_row = [&](int uu) {
+            const int bb = uu / p.n_mtiles, mm = uu - bb * p.n_mtiles;
+            const int ee = p.block_expert ? __ldg(p.block_expert + bb) : 0;
+            const int row = ee * p.R + mm * tile_rows + (half ? (GATED ? p.up_off : MT) : 0) + r;
+            return p.scales + (size_t)row * srow_bytes;
+        };
+        int it = 0, ia = 0;
+        const uint8_t *srow = blockIdx.x < n_units ? scale_row(blockIdx.x) : p.scales;
+        uint4 s_next = blockIdx.x < n_units ? __ldg(reinterpret_cast<const uint4 *>(srow)) : make_uint4(0, 0, 0, 0);
+        for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
+            const int u_next = u + gridDim.x;
+            const uint8_t *srow_next = u_next < n_units ? scale_row(u_next) : nullptr;
             uint4 s16 = make_uint4(0, 0, 0, 0);
             for (int c = 0; c < nk; ++c, ++it, ++ia) {
                 const int slot = it % ns, ab = ia % NA;
-                if (!wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
-                    !wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag)) {
+                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
+                    !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag)) {
                     dead = true;
                     break;
                 }
                 if (c % cpl == 0) {
                     const int q = c / cpl;
-                    s16 = *reinterpret_cast<const uint4 *>(sc + ((sw_scales ? (q ^ (r & 7)) : q) << 4));
+                    s16 = s_next;
+                    if (q + 1 < ngroups) s_next = __ldg(reinterpret_cast<const uint4 *>(srow + 16 * (q + 1)));
+                    else if (srow_next) s_next = __ldg(reinterpret_cast<const uint4 *>(srow_next));
                 }
                 const int ci = c % cpl;
                 uint32_t sw;
@@ -244,11 +262,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     dequant8_f16(words[w], sv[w >> 1], o);
                     *reinterpret_cast<uint4 *>(arow + ((w ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
+                // every thread orders its A writes before the tensor core's reads, then
+                // the warp arrives once
                 fence_proxy_async_smem();
-                arrive(a_full + ab);
+                __syncwarp();
+                if (lane == 0) arrive(a_full + ab);
             }
             if (dead) break;
-            arrive(scale_empty + sb);
+            srow = srow_next;
         }
         if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else {
@@ -289,7 +310,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const float g0 = __ldg(glob_e + row0);
             const float g1 = __ldg(glob_e + (GATED ? p.up_off + row0 : row0 + MT));
             const int ab2 = uc & 1;
-            if (!wait_bar(acc_full + ab2, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
+            if (!warp_wait_bar(acc_full + ab2, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
             tc::fence_after_sync();
             const uint32_t lane_addr = tmem + (uint32_t)(ab2 * 2 * NT) + ((uint32_t)(32 * quarter) << 16);
             for (int cb = 0; cb < NT / 32; ++cb) {
@@ -318,28 +339,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
             }
             tc::fence_before_sync();
-            arrive(acc_empty + ab2);
+            __syncwarp();
+            if (lane == 0) arrive(acc_empty + ab2);
         }
         if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     }
 
-    // wind down
+    // wind down (the producer has let its copies land before reaching this barrier)
     tc::fence_before_sync();
-    __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
-        // let copies still in flight land before the CTA's shared memory is released
-        for (int i = 0; i < NSMAX; ++i) {
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(full + i, 0) && !mbar_try_wait(full + i, 1) && globaltimer() - t0 < kWaitNs) {
-            }
-        }
-        for (int i = 0; i < 2; ++i) {
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(scale_full + i, 0) && !mbar_try_wait(scale_full + i, 1) &&
-                   globaltimer() - t0 < kWaitNs) {
-            }
-        }
-    }
     __syncthreads();
     tc::fence_after_sync();
     if (warp == 1) tc::tmem_dealloc(tmem, tmem_cols);
@@ -479,15 +486,11 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
 {
     const int ns = tc_stages(p.K, p.group);
     if (!ns) return cudaErrorInvalidValue;
-    CUtensorMap cmap, bmap, smap;
-    const uint32_t srow = (uint32_t)(p.K / p.group);
-    if (!make_tensor_map_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(codes), (uint64_t)p.K / 2,
-                  (uint64_t)rows_total, (uint64_t)p.K / 2, 32, MT, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tensor_map_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<void *>(act), (uint64_t)p.K,
-                  (uint64_t)act_rows, (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(static_cast<const void *>(p.scales)), srow,
-                  (uint64_t)rows_total, srow, srow, MT,
-                  srow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
+    CUtensorMap cmap, bmap;
+    if (!make_tensor_map_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)p.K / 2, (uint64_t)rows_total,
+                            (uint64_t)p.K / 2, 32, MT, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, (uint64_t)p.K, (uint64_t)act_rows,
+                            (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const size_t smem = tc_smem(p.K, p.group, ns).total + 1024;
     int grid = sm_count();
@@ -496,7 +499,7 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
     auto kern = gated ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    FT_LAUNCH(kern, dim3(grid), dim3(kThreadsTc), smem, s, cmap, bmap, smap, p, ns);
+    FT_LAUNCH(kern, dim3(grid), dim3(kThreadsTc), smem, s, cmap, bmap, p, ns);
     count_launches(1);
     return cudaGetLastError();
 }

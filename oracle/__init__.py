@@ -52,6 +52,7 @@ def lib():
             L.orc_dequant_matrix.restype = None
             L.orc_dequant_matrix.argtypes = [P, P, P, I, I, I, P]
             L.orc_route.restype = I; L.orc_route.argtypes = [P, I, I, I, P, P]
+            L.orc_router_logits.restype = None; L.orc_router_logits.argtypes = [P, P, I, I, I, P, P]
             L.orc_align.restype = I; L.orc_align.argtypes = [P, I, I, I, I, P, P, P, P]
             L.orc_slice.restype = I; L.orc_slice.argtypes = [I] * 6 + [P] * 15
             L.orc_expert_gate_up.restype = None
@@ -86,7 +87,7 @@ def mutation(code: int):
 MUTATIONS = {
     "nibble_order": 1, "swap_gate_up": 2, "drop_global": 3, "scale_index": 4, "e2m1_sign": 5,
     "no_renorm": 6, "tie_high": 7, "down_rows": 8, "drop_shared": 9, "drop_route_w": 10,
-    "e4m3_bias": 11, "up_slice": 12,
+    "e4m3_bias": 11, "up_slice": 12, "router_transposed": 13,
 }
 
 
@@ -122,6 +123,20 @@ def route(logits: np.ndarray, k: int):
     if lib().orc_route(_p(logits), T, E, k, _p(ids), _p(w)) != 0:
         raise ValueError("bad routing arguments")
     return ids, w
+
+
+def router_logits(x_bits: np.ndarray, w_bits: np.ndarray):
+    """logits [T, E] = x [T, H] . W [E, H]^T over bf16 values in fp64, and absum
+    [T, E] = sum |x * w| (the scale of rounding errors of lower-precision sums)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    T, H = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == H
+    logits = np.zeros((T, E), dtype=np.float64)
+    absum = np.zeros((T, E), dtype=np.float64)
+    lib().orc_router_logits(_p(x), _p(w), T, H, E, _p(logits), _p(absum))
+    return logits, absum
 
 
 def align(ids: np.ndarray, E: int, block: int):

@@ -62,6 +62,7 @@ enum {
     ORC_MUT_DROP_ROUTE_W = 10,  /* routed terms not weighted */
     ORC_MUT_E4M3_BIAS = 11,     /* e4m3 exponent bias 8 instead of 7 */
     ORC_MUT_UP_SLICE = 12,      /* up rows taken from the gate half */
+    ORC_MUT_ROUTER_T = 13,      /* router weight read transposed (square shapes only) */
 };
 
 /* ---------------------------------------------------------------- formats */
@@ -209,6 +210,30 @@ int orc_route(const float *logits, int T, int E, int k, int32_t *ids, double *w)
  *   (start of each expert's padded run; expert_off[E] = n_padded).
  * Returns 0, or -1 on an out-of-range id or bad arguments. Caller sizes
  * sorted_slot for T*k + E*(B-1) entries. */
+/* Router logits of the replicated router ("[1/3] feat(dsv4): add tensor-parallel
+ * DeepSeek-V4 runtime", table "Tensor ownership and collectives": the router is
+ * replicated and every rank computes the same routing): logits[t][e] = sum_h
+ * x[t][h] * W[e][h] over the bf16 values of x [T][H] and W [E][H]. Every product of
+ * two bf16 values is exact in fp64 (16 significant bits), so the only rounding is
+ * the fp64 summation (relative error below H * 2^-53 of absum). absum[t][e] = sum_h
+ * |x[t][h] * W[e][h]|, the scale of any rounding error of a lower-precision sum. */
+void orc_router_logits(const uint16_t *x, const uint16_t *w, int T, int H, int E, double *logits, double *absum)
+{
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0, mag = 0.0;
+            for (int h = 0; h < H; ++h) {
+                const uint16_t wb = orc_mutation == ORC_MUT_ROUTER_T ? w[(size_t)h * E + e] : w[(size_t)e * H + h];
+                const double prod = orc_bf16_to_double(x[(size_t)t * H + h]) * orc_bf16_to_double(wb);
+                acc += prod;
+                mag += fabs(prod);
+            }
+            logits[(size_t)t * E + e] = acc;
+            absum[(size_t)t * E + e] = mag;
+        }
+    }
+}
+
 int orc_align(const int32_t *ids, int T, int k, int E, int B,
               int32_t *sorted_slot, int32_t *block_expert, int32_t *expert_off, int32_t *n_padded)
 {

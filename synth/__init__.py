@@ -18,6 +18,8 @@ group size 16) and the "Offloaded MoE ignores tensor parallelism" page
 * code bytes      uniform over 0..255 (two independent uniform e2m1 nibbles)
 * block scales    continuous U[0.25, 2] rounded to nearest-even e4m3
 * weight_global   fp32 U[0.5, 1.5], one per output row
+* router weights  bf16 ~ N(0, 1/H) [E, H] (replicated on every rank), so that with
+                  N(0,1) activations the router logits are again ~ N(0, 1)
 """
 from __future__ import annotations
 
@@ -27,7 +29,7 @@ import numpy as np
 
 __all__ = [
     "LayerShape", "SHAPES", "rng_for", "bf16_bits_from_f32", "e4m3_rne_bytes",
-    "make_pieces", "make_activations", "make_logits", "zipf_logits",
+    "make_pieces", "make_activations", "make_logits", "zipf_logits", "make_router_weights",
 ]
 
 
@@ -158,3 +160,8 @@ def zipf_logits(T: int, E: int, s: float = 1.1, seed: int = 0, stream: int = 400
     noise = rng.standard_normal((T, E))
     return (noise + log_prior[None, :]).astype(np.float32)
 
+
+def make_router_weights(E: int, H: int, seed: int = 0, stream: int = 500) -> np.ndarray:
+    """Router weights bf16 ~ N(0, 1/H), returned as uint16 bit patterns [E, H]."""
+    w = rng_for(seed, stream, E, H).standard_normal((E, H), dtype=np.float32) / np.float32(np.sqrt(H))
+    return bf16_bits_from_f32(w)

@@ -118,6 +118,18 @@ def test_forward_argument_checks_happen_before_launch(ft):
     assert lib.ft_moe_align(4096, 4, 2, 8, 0, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 1
 
 
+def test_route_gemm_argument_checks_happen_before_launch(ft):
+    lib = ft.load()
+    a = 4096  # aligned stand-in address; nothing is launched for these calls
+    assert lib.ft_moe_route_gemm(None, 0, 2048, None, 256, 8, None, None, None, None) == 0   # T = 0
+    assert lib.ft_moe_route_gemm(a, 4, 2040, a, 256, 8, a, a, a, None) == 1     # H not a multiple of 32
+    assert lib.ft_moe_route_gemm(a, 4, 2048, a, 0, 8, a, a, a, None) == 1       # E = 0
+    assert lib.ft_moe_route_gemm(a, 4, 2048, a, 2048, 8, a, a, a, None) == 3    # E > 1024
+    assert lib.ft_moe_route_gemm(a, 4, 2048, a, 16, 17, a, a, a, None) == 3     # k > E
+    assert lib.ft_moe_route_gemm(a + 8, 4, 2048, a, 256, 8, a, a, a, None) == 1  # x misaligned
+    assert lib.ft_moe_route_gemm(a, 4, 2048, None, 256, 8, a, a, a, None) == 1  # no router weight
+
+
 def test_pack_rejects_overlap(ft):
     lib = ft.load()
     cfg = ft.MoEConfig.of(synth.SHAPES["tiny"])

@@ -163,6 +163,36 @@ def test_align_matches_oracle(ft, T, E, k, B, zipf):
     assert np.array_equal(expert_off.cpu().numpy(), ref_off)
 
 
+@pytest.mark.parametrize("T,E,H", [(1, 256, 2048), (33, 256, 2048), (64, 256, 2048), (2048, 256, 2048),
+                                   (16, 8, 256), (5, 40, 64), (16, 256, 4096)])
+def test_route_gemm_matches_oracle(ft, T, E, H):
+    """Router logit GEMM + top-k. Logits: within the fp32 summation bound H * 2^-23 * sum|x*w|
+    of the oracle's fp64 logits. Top-k: bit-exact with the oracle routing the GPU's own fp32
+    logits; against the fp64 logits the selected set may differ only where the boundary
+    logits lie within that bound of each other (either choice is then a valid top-k)."""
+    k = min(8, E)
+    x_bits = synth.make_activations(T, H, seed=31)
+    w_bits = synth.make_router_weights(E, H, seed=31)
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    wr = torch.from_numpy(w_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ft.ft_moe_route_gemm(x, wr, k, logits, ids, w)
+    got = logits.cpu().numpy().astype(np.float64)
+    ref, absum = oracle.router_logits(x_bits, w_bits)
+    bound = H * 2.0 ** -23 * absum
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / np.maximum(absum, 1e-30)))
+    own_ids, own_w = oracle.route(logits.cpu().numpy(), k)
+    got_ids = ids.cpu().numpy()
+    assert np.array_equal(got_ids, own_ids)
+    assert np.allclose(w.cpu().numpy(), own_w, rtol=ROUTE_W_RTOL, atol=0)
+    ref_ids, _ = oracle.route(ref.astype(np.float32), k)
+    for t in np.nonzero(np.any(np.sort(got_ids, 1) != np.sort(ref_ids, 1), axis=1))[0]:
+        kth = np.sort(ref[t])[::-1][k - 1]
+        assert np.all(ref[t][got_ids[t]] >= kth - 2 * bound[t][got_ids[t]]), f"token {t}: not a valid top-{k}"
+
+
 def test_align_flags_invalid_ids(ft):
     ids = torch.tensor([[0, 1], [2, 9], [3, 3]], dtype=torch.int32, device="cuda")
     E, B = 8, 4

@@ -336,10 +336,39 @@ def pin_tp_partial_sum():
         assert np.abs(parts[0] - full).max() / np.abs(full).max() > 1e-3
 
 
+def pin_router_logits_exact():
+    """Router logits against exact rational arithmetic: with these magnitudes every
+    bf16 product and every partial sum fits 53 bits, so fp64 must be exact; absum too.
+    Square E == H so that a transposed read would still index inside W (and differ)."""
+    T, H, E = 3, 16, 16
+    x = synth.make_activations(T, H, seed=21)
+    w = synth.make_router_weights(E, H, seed=21)
+    logits, absum = oracle.router_logits(x, w)
+    xv = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wv = (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for t in range(T):
+        for e in range(E):
+            exact = sum((Fraction(a) * Fraction(b) for a, b in zip(xv[t], wv[e])), Fraction(0))
+            mag = sum((abs(Fraction(a) * Fraction(b)) for a, b in zip(xv[t], wv[e])), Fraction(0))
+            assert Fraction(logits[t, e]) == exact and Fraction(absum[t, e]) == mag
+
+
+def pin_router_one_hot():
+    """A one-hot token selects one column of the router weight: logits[e] = W[e][i]."""
+    H = E = 16
+    w = synth.make_router_weights(E, H, seed=22)
+    wv = (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    x = np.zeros((H, H), np.uint16)
+    x[np.arange(H), np.arange(H)] = synth.bf16_bits_from_f32(np.ones(1, np.float32))[0]
+    logits, _ = oracle.router_logits(x, w)
+    assert np.array_equal(logits, wv.T)
+
+
 PINS = [pin_e2m1, pin_e4m3, pin_dequant_bf16, pin_route_worked_example, pin_route_brute_force,
         pin_route_library, pin_route_ties_and_shift, pin_align, pin_slice_identity_and_tiling,
         pin_one_hot_columns, pin_linear_parts_exact, pin_dense_mlp_special_case,
-        pin_routed_combination, pin_untouched_experts_and_tokens, pin_tp_partial_sum]
+        pin_routed_combination, pin_untouched_experts_and_tokens, pin_tp_partial_sum,
+        pin_router_logits_exact, pin_router_one_hot]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
