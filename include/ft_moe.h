@@ -71,7 +71,9 @@ typedef enum {
  * `shared_intermediate` are the FULL (unsliced) sizes; the rank-local sizes are
  * I_l = intermediate / tp_size and I_sl = shared_intermediate / tp_size
  * ("MoEConfig ... local_intermediate = intermediate // tp_size", NVFP4 port
- * section 3a). shared_intermediate = 0 means the layer has no shared expert. */
+ * section 3a), or the explicit shard sizes below. shared_intermediate = 0 means the
+ * layer has no shared expert. A shard range that is negative, empty, not a multiple
+ * of group or past the full size is FT_ERR_INDIVISIBLE. */
 typedef struct {
     int32_t hidden;               /* H */
     int32_t intermediate;         /* I (full) */
@@ -81,6 +83,18 @@ typedef struct {
     int32_t shared_intermediate;  /* I_s (full), 0 = none */
     int32_t tp_rank;              /* r in [0, tp_size) */
     int32_t tp_size;              /* >= 1 */
+    /* Asymmetric split (optional): with shard_size > 0 this rank owns the explicit
+     * intermediate range [shard_begin, shard_begin + shard_size) instead of the even
+     * share [r*I/tp, (r+1)*I/tp). The pages leave such a ratio open ("[TP=2] Quantized
+     * MoE expert parallelism ... NVFP4 port", section 8: a split weighted toward the
+     * faster card was not attempted); the slicing rule and the exact sum of partials
+     * over any partition of [0, I) carry over from the even split (section 4). Both
+     * values must be multiples of group; 0 = even split. The shared expert likewise
+     * with shared_shard_begin / shared_shard_size (0 = its even share). */
+    int32_t shard_begin;
+    int32_t shard_size;
+    int32_t shared_shard_begin;
+    int32_t shared_shard_size;
 } ft_moe_config;
 
 enum { FT_DTYPE_U8 = 0, FT_DTYPE_E4M3 = 1, FT_DTYPE_F32 = 2, FT_DTYPE_BF16 = 3 };

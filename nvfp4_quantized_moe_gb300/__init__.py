@@ -47,12 +47,17 @@ class FtMoeError(RuntimeError):
 class MoEConfig(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("group", ctypes.c_int32), ("shared_intermediate", ctypes.c_int32),
-                ("tp_rank", ctypes.c_int32), ("tp_size", ctypes.c_int32)]
+                ("tp_rank", ctypes.c_int32), ("tp_size", ctypes.c_int32), ("shard_begin", ctypes.c_int32),
+                ("shard_size", ctypes.c_int32), ("shared_shard_begin", ctypes.c_int32),
+                ("shared_shard_size", ctypes.c_int32)]
 
     @classmethod
-    def of(cls, shape, tp_rank: int = 0, tp_size: int = 1) -> "MoEConfig":
+    def of(cls, shape, tp_rank: int = 0, tp_size: int = 1, shard=None, shared_shard=None) -> "MoEConfig":
+        """Even split (tp_rank of tp_size) or explicit (begin, size) ranges of the intermediate."""
+        sb, ss = shard if shard else (0, 0)
+        hb, hs = shared_shard if shared_shard else (0, 0)
         return cls(shape.hidden, shape.intermediate, shape.num_experts, shape.top_k, shape.group,
-                   shape.shared_intermediate, tp_rank, tp_size)
+                   shape.shared_intermediate, tp_rank, tp_size, sb, ss, hb, hs)
 
 
 class _BankSpec(ctypes.Structure):

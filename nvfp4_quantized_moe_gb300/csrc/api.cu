@@ -75,7 +75,8 @@ static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 
 struct Geometry {
     int H, I, E, k, g, Is, r, tp;
-    int Il, Isl;
+    int Il, Isl;     // rank-local intermediate sizes (routed, shared)
+    int rb, sb;      // first intermediate column of the rank's range (routed, shared)
 };
 
 static ft_status check_config(const ft_moe_config *cfg, Geometry &G)
@@ -85,23 +86,43 @@ static ft_status check_config(const ft_moe_config *cfg, Geometry &G)
     G.g = cfg->group; G.Is = cfg->shared_intermediate; G.r = cfg->tp_rank; G.tp = cfg->tp_size;
     if (G.H <= 0 || G.I <= 0 || G.E <= 0 || G.k <= 0 || G.Is < 0 || G.tp <= 0 || G.r < 0 || G.r >= G.tp)
         return fail(FT_ERR_INVALID_ARG, "config fields must be positive and 0 <= tp_rank < tp_size");
+    if (cfg->shard_size < 0 || cfg->shared_shard_size < 0)
+        return fail(FT_ERR_INVALID_ARG, "shard sizes must be >= 0 (0 = even split by tp_rank/tp_size)");
     if (G.g != 16 && G.g != 32) return fail(FT_ERR_UNSUPPORTED, "group must be 16 or 32 (got %d)", G.g);
     if (G.E > 1024 || G.k > 32 || G.k > G.E)
         return fail(FT_ERR_UNSUPPORTED, "need top_k <= 32, top_k <= num_experts <= 1024");
     if (G.H % G.g || G.H % 2)
         return fail(FT_ERR_INDIVISIBLE, "hidden %d is not a multiple of the %d-element scale block", G.H, G.g);
-    if (G.I % G.tp)
-        return fail(FT_ERR_INDIVISIBLE, "intermediate %d does not split across %d tp ranks", G.I, G.tp);
-    G.Il = G.I / G.tp;
-    if (G.Il % G.g)
-        return fail(FT_ERR_INDIVISIBLE, "local intermediate %d is not a multiple of the %d-element scale block",
-                    G.Il, G.g);
-    if (G.Is % G.tp)
-        return fail(FT_ERR_INDIVISIBLE, "shared intermediate %d does not split across %d tp ranks", G.Is, G.tp);
-    G.Isl = G.Is / G.tp;
-    if (G.Isl % G.g)
-        return fail(FT_ERR_INDIVISIBLE, "local shared intermediate %d is not a multiple of the %d-element block",
-                    G.Isl, G.g);
+    if (cfg->shard_size > 0) {  // explicit (possibly asymmetric) range
+        G.rb = cfg->shard_begin;
+        G.Il = cfg->shard_size;
+        if (G.rb < 0 || G.rb % G.g || G.Il % G.g || G.rb + G.Il > G.I)
+            return fail(FT_ERR_INDIVISIBLE, "shard [%d, %d) is not a range of whole %d-element blocks inside [0, %d)",
+                        G.rb, G.rb + G.Il, G.g, G.I);
+    } else {
+        if (G.I % G.tp)
+            return fail(FT_ERR_INDIVISIBLE, "intermediate %d does not split across %d tp ranks", G.I, G.tp);
+        G.Il = G.I / G.tp;
+        G.rb = G.r * G.Il;
+        if (G.Il % G.g)
+            return fail(FT_ERR_INDIVISIBLE, "local intermediate %d is not a multiple of the %d-element scale block",
+                        G.Il, G.g);
+    }
+    if (G.Is > 0 && cfg->shared_shard_size > 0) {
+        G.sb = cfg->shared_shard_begin;
+        G.Isl = cfg->shared_shard_size;
+        if (G.sb < 0 || G.sb % G.g || G.Isl % G.g || G.sb + G.Isl > G.Is)
+            return fail(FT_ERR_INDIVISIBLE, "shared shard [%d, %d) is not a range of whole %d-element blocks",
+                        G.sb, G.sb + G.Isl, G.g);
+    } else {
+        if (G.Is % G.tp)
+            return fail(FT_ERR_INDIVISIBLE, "shared intermediate %d does not split across %d tp ranks", G.Is, G.tp);
+        G.Isl = G.Is / G.tp;
+        G.sb = G.r * G.Isl;
+        if (G.Isl % G.g)
+            return fail(FT_ERR_INDIVISIBLE,
+                        "local shared intermediate %d is not a multiple of the %d-element block", G.Isl, G.g);
+    }
     if (G.H % 128) return fail(FT_ERR_UNSUPPORTED, "hidden must be a multiple of 128 (got %d)", G.H);
     return FT_OK;
 }
@@ -288,7 +309,9 @@ ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pie
         return fail(FT_ERR_INVALID_ARG, "a source piece is NULL");
     if (!banks_ok(dst)) return fail(FT_ERR_INVALID_ARG, "destination banks must be non-NULL and 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t E = shared ? 1 : G.E, I = shared ? G.Is : G.I, Il = I / G.tp, r = G.r, H = G.H, g = G.g;
+    // the rank's range [b0, b0 + Il) of the intermediate dimension (even or explicit split)
+    const size_t E = shared ? 1 : G.E, I = shared ? G.Is : G.I, Il = shared ? G.Isl : G.Il, H = G.H, g = G.g;
+    const size_t b0 = shared ? G.sb : G.rb;
     ft_bank_spec specs[FT_NBANKS];
     bank_specs(G, shared, specs);
     const size_t src_bytes[9] = {E * I * H / 2, E * I * H / g, E * I * 4, E * I * H / 2, E * I * H / g, E * I * 4,
@@ -305,15 +328,15 @@ ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pie
     auto u8 = [](const void *p, size_t off) { return static_cast<const uint8_t *>(p) + off; };
     auto w8 = [](void *p, size_t off) { return static_cast<uint8_t *>(p) + off; };
     const Copy copies[9] = {
-        {u8(src->gate, r * Il * H / 2), I * H / 2, w8(dst->p[FT_GU], 0), 2 * Il * H / 2, Il * H / 2, E},
-        {u8(src->up, r * Il * H / 2), I * H / 2, w8(dst->p[FT_GU], Il * H / 2), 2 * Il * H / 2, Il * H / 2, E},
-        {u8(src->gate_scale, r * Il * H / g), I * H / g, w8(dst->p[FT_GU_SCALE], 0), 2 * Il * H / g, Il * H / g, E},
-        {u8(src->up_scale, r * Il * H / g), I * H / g, w8(dst->p[FT_GU_SCALE], Il * H / g), 2 * Il * H / g,
+        {u8(src->gate, b0 * H / 2), I * H / 2, w8(dst->p[FT_GU], 0), 2 * Il * H / 2, Il * H / 2, E},
+        {u8(src->up, b0 * H / 2), I * H / 2, w8(dst->p[FT_GU], Il * H / 2), 2 * Il * H / 2, Il * H / 2, E},
+        {u8(src->gate_scale, b0 * H / g), I * H / g, w8(dst->p[FT_GU_SCALE], 0), 2 * Il * H / g, Il * H / g, E},
+        {u8(src->up_scale, b0 * H / g), I * H / g, w8(dst->p[FT_GU_SCALE], Il * H / g), 2 * Il * H / g,
          Il * H / g, E},
-        {u8(src->gate_global, r * Il * 4), I * 4, w8(dst->p[FT_GU_GLOBAL], 0), 2 * Il * 4, Il * 4, E},
-        {u8(src->up_global, r * Il * 4), I * 4, w8(dst->p[FT_GU_GLOBAL], Il * 4), 2 * Il * 4, Il * 4, E},
-        {u8(src->down, r * Il / 2), I / 2, w8(dst->p[FT_DN], 0), Il / 2, Il / 2, E * H},
-        {u8(src->down_scale, r * Il / g), I / g, w8(dst->p[FT_DN_SCALE], 0), Il / g, Il / g, E * H},
+        {u8(src->gate_global, b0 * 4), I * 4, w8(dst->p[FT_GU_GLOBAL], 0), 2 * Il * 4, Il * 4, E},
+        {u8(src->up_global, b0 * 4), I * 4, w8(dst->p[FT_GU_GLOBAL], Il * 4), 2 * Il * 4, Il * 4, E},
+        {u8(src->down, b0 / 2), I / 2, w8(dst->p[FT_DN], 0), Il / 2, Il / 2, E * H},
+        {u8(src->down_scale, b0 / g), I / g, w8(dst->p[FT_DN_SCALE], 0), Il / g, Il / g, E * H},
         {u8(src->down_global, 0), E * H * 4, w8(dst->p[FT_DN_GLOBAL], 0), E * H * 4, E * H * 4, 1},
     };
     for (const Copy &c : copies) {

@@ -55,6 +55,7 @@ def lib():
             L.orc_router_logits.restype = None; L.orc_router_logits.argtypes = [P, P, I, I, I, P, P]
             L.orc_align.restype = I; L.orc_align.argtypes = [P, I, I, I, I, P, P, P, P]
             L.orc_slice.restype = I; L.orc_slice.argtypes = [I] * 6 + [P] * 15
+            L.orc_slice_range.restype = I; L.orc_slice_range.argtypes = [I] * 6 + [P] * 15
             L.orc_expert_gate_up.restype = None
             L.orc_expert_gate_up.argtypes = [ctypes.POINTER(Bank), I, P, P]
             L.orc_swiglu.restype = None; L.orc_swiglu.argtypes = [P, I, P]
@@ -155,14 +156,15 @@ def align(ids: np.ndarray, E: int, block: int):
     return sorted_slot[:n].copy(), block_expert[:n // block].copy(), expert_off, n
 
 
-def slice_bank(pieces: dict, group: int, tp_rank: int = 0, tp_size: int = 1) -> dict:
-    """Rank-local bank {gu, gu_scale, gu_global, dn, dn_scale, dn_global} from full pieces."""
+def slice_bank(pieces: dict, group: int, tp_rank: int = 0, tp_size: int = 1, shard: tuple | None = None) -> dict:
+    """Rank-local bank {gu, gu_scale, gu_global, dn, dn_scale, dn_global} from full pieces:
+    the even split (tp_rank of tp_size) or, with shard = (begin, size), that explicit range."""
     c = {k: np.ascontiguousarray(v) for k, v in pieces.items()}
     E, I, H2 = c["gate"].shape
     H = H2 * 2
-    if I % tp_size:
+    if shard is None and I % tp_size:
         raise ValueError("intermediate not divisible by tp_size")
-    Il = I // tp_size
+    Il = I // tp_size if shard is None else shard[1]
     out = {
         "gu": np.zeros((E, 2 * Il, H // 2), np.uint8),
         "gu_scale": np.zeros((E, 2 * Il, H // group), np.uint8),
@@ -171,11 +173,12 @@ def slice_bank(pieces: dict, group: int, tp_rank: int = 0, tp_size: int = 1) -> 
         "dn_scale": np.zeros((E, H, Il // group), np.uint8),
         "dn_global": np.zeros((E, H), np.float32),
     }
-    rc = lib().orc_slice(E, H, I, group, tp_rank, tp_size,
-                         *[_p(c[n]) for n in ("gate", "gate_scale", "gate_global", "up", "up_scale",
-                                              "up_global", "down", "down_scale", "down_global")],
-                         *[_p(out[n]) for n in ("gu", "gu_scale", "gu_global", "dn", "dn_scale",
-                                                "dn_global")])
+    fn, a, b = (lib().orc_slice, tp_rank, tp_size) if shard is None else (lib().orc_slice_range, shard[0], shard[1])
+    rc = fn(E, H, I, group, a, b,
+            *[_p(c[n]) for n in ("gate", "gate_scale", "gate_global", "up", "up_scale",
+                                 "up_global", "down", "down_scale", "down_global")],
+            *[_p(out[n]) for n in ("gu", "gu_scale", "gu_global", "dn", "dn_scale",
+                                   "dn_global")])
     if rc != 0:
         raise ValueError("indivisible or invalid tp geometry")
     return out

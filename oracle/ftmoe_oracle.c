@@ -303,6 +303,45 @@ int orc_slice(int E, int H, int I, int g, int tp_rank, int tp_size,
     return 0;
 }
 
+/* Rank-local bank for an explicit intermediate range [begin, begin + len), the
+ * asymmetric split the "[TP=2] Quantized MoE expert parallelism ... NVFP4 port" page
+ * leaves open (section 8: a shard ratio weighted toward the faster card was not
+ * attempted). The slicing rule is the even split's (section 4, _shard_expert_tensor:
+ * gate and up rows of the range, down columns of the range, globals of those rows,
+ * down_global whole) with the range given instead of derived; the linearity argument
+ * of section 4 makes the partials of any partition of [0, I) sum to the full output.
+ * begin and len must be multiples of the scale block. */
+int orc_slice_range(int E, int H, int I, int g, int begin, int len,
+                    const uint8_t *gate, const uint8_t *gate_scale, const float *gate_global,
+                    const uint8_t *up, const uint8_t *up_scale, const float *up_global,
+                    const uint8_t *down, const uint8_t *down_scale, const float *down_global,
+                    uint8_t *gu, uint8_t *gu_scale, float *gu_global,
+                    uint8_t *dn, uint8_t *dn_scale, float *dn_global)
+{
+    if (begin < 0 || len <= 0 || begin + len > I || begin % g || len % g || H % g || H % 2) return -1;
+    size_t hr = (size_t)H / 2, hs = (size_t)H / g;
+    for (int e = 0; e < E; ++e) {
+        for (int i = 0; i < len; ++i) {
+            size_t src = (size_t)e * I + (size_t)begin + i;
+            size_t up_src = (orc_mutation == ORC_MUT_UP_SLICE) ? (size_t)e * I + i : src;
+            size_t dg = (size_t)e * 2 * len + i, du = dg + len;
+            memcpy(gu + dg * hr, gate + src * hr, hr);
+            memcpy(gu + du * hr, up + up_src * hr, hr);
+            memcpy(gu_scale + dg * hs, gate_scale + src * hs, hs);
+            memcpy(gu_scale + du * hs, up_scale + up_src * hs, hs);
+            gu_global[dg] = gate_global[src];
+            gu_global[du] = up_global[up_src];
+        }
+        for (int n = 0; n < H; ++n) {
+            size_t row = (size_t)e * H + n;
+            memcpy(dn + row * (len / 2), down + row * (I / 2) + (size_t)begin / 2, (size_t)len / 2);
+            memcpy(dn_scale + row * (len / g), down_scale + row * (I / g) + (size_t)begin / g, (size_t)len / g);
+            dn_global[row] = down_global[row];
+        }
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------- expert MLP */
 
 typedef struct {

@@ -31,11 +31,14 @@ def logits_for(shape_name: str, T: int, zipf: bool, seed: int = 0):
     return synth.zipf_logits(T, E, seed=seed) if zipf else synth.make_logits(T, E, seed=seed)
 
 
-def oracle_banks(shape_name: str, tp_rank: int = 0, tp_size: int = 1, seed: int = 0):
+def oracle_banks(shape_name: str, tp_rank: int = 0, tp_size: int = 1, seed: int = 0, shard=None,
+                 shared_shard=None):
+    """Rank-local banks: even split (tp_rank of tp_size) or explicit (begin, size) ranges."""
     shape = synth.SHAPES[shape_name]
     routed, shared = pieces(shape_name, seed)
-    rb = oracle.slice_bank(routed, shape.group, tp_rank, tp_size)
-    sb = oracle.slice_bank(shared, shape.group, tp_rank, tp_size) if shared is not None else None
+    rb = oracle.slice_bank(routed, shape.group, tp_rank, tp_size, shard=shard)
+    sb = (oracle.slice_bank(shared, shape.group, tp_rank, tp_size, shard=shared_shard)
+          if shared is not None else None)
     return rb, sb
 
 
@@ -55,11 +58,12 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
 class GpuLayer:
     """Rank-local banks of one layer on the GPU, packed through ft_moe_pack."""
 
-    def __init__(self, shape_name: str, tp_rank: int = 0, tp_size: int = 1, seed: int = 0, from_host: bool = True):
+    def __init__(self, shape_name: str, tp_rank: int = 0, tp_size: int = 1, seed: int = 0, from_host: bool = True,
+                 shard=None, shared_shard=None):
         import nvfp4_quantized_moe_gb300 as ft
         self.ft = ft
         self.shape = synth.SHAPES[shape_name]
-        self.cfg = ft.MoEConfig.of(self.shape, tp_rank, tp_size)
+        self.cfg = ft.MoEConfig.of(self.shape, tp_rank, tp_size, shard=shard, shared_shard=shared_shard)
         routed, shared = pieces(shape_name, seed)
         self.routed = ft.alloc_banks(self.cfg, 0)
         src = routed if from_host else {k: torch.from_numpy(v).cuda() for k, v in routed.items()}

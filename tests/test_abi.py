@@ -56,6 +56,20 @@ def test_layout_bytes_and_shared(ft):
                                                                    4096 * 256 + 4096 * 16 + 4096 * 4)
 
 
+def test_layout_follows_explicit_shard(ft):
+    """An explicit range sizes the rank's banks by its own length, not intermediate/tp_size."""
+    shape = synth.SHAPES["qwen36"]
+    a = ft.MoEConfig.of(shape, 0, 2, shard=(0, 320), shared_shard=(0, 192))
+    b = ft.MoEConfig.of(shape, 1, 2, shard=(320, 192), shared_shard=(192, 320))
+    ra = {n: tuple(s) for n, s, _, _ in ft.ft_moe_layout(a, 0)}
+    rb = {n: tuple(s) for n, s, _, _ in ft.ft_moe_layout(b, 0)}
+    assert ra["gate_up"] == (256, 640, 1024) and rb["gate_up"] == (256, 384, 1024)
+    assert ra["down"] == (256, 2048, 160) and rb["down"] == (256, 2048, 96)
+    sa = {n: tuple(s) for n, s, _, _ in ft.ft_moe_layout(a, 1)}
+    sb = {n: tuple(s) for n, s, _, _ in ft.ft_moe_layout(b, 1)}
+    assert sa["gate_up"] == (1, 384, 1024) and sb["gate_up"] == (1, 640, 1024)
+
+
 @pytest.mark.parametrize("fields,code", [
     (dict(tp_size=3), 2),                      # 512 % 3
     (dict(tp_size=64), 2),                     # 512/64 = 8 not a multiple of 16
@@ -66,10 +80,15 @@ def test_layout_bytes_and_shared(ft):
     (dict(hidden=2056), 2),                    # not a multiple of 16
     (dict(hidden=2064), 3),                    # multiple of 16, not of 128
     (dict(shared_intermediate=200), 2),        # 200 % 16 at tp=1
+    (dict(shard_begin=8, shard_size=64), 2),   # begin not on a block boundary
+    (dict(shard_begin=0, shard_size=40), 2),   # size not a whole number of blocks
+    (dict(shard_begin=448, shard_size=128), 2),  # runs past the intermediate
+    (dict(shard_size=-16), 1),
+    (dict(shared_shard_begin=256, shared_shard_size=272), 2),  # shared range past 512
 ])
 def test_layout_rejects_bad_geometry(ft, fields, code):
     base = dict(hidden=2048, intermediate=512, num_experts=256, top_k=8, group=16, shared_intermediate=512,
-                tp_rank=0, tp_size=1)
+                tp_rank=0, tp_size=1, shard_begin=0, shard_size=0, shared_shard_begin=0, shared_shard_size=0)
     base.update(fields)
     cfg = ft.MoEConfig(*[base[n] for n, _ in ft.MoEConfig._fields_])
     with pytest.raises(ft.FtMoeError) as ei:

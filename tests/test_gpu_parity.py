@@ -34,13 +34,13 @@ def ft():
 _layers = {}
 
 
-def layer(name, tp_rank=0, tp_size=1):
-    key = (name, tp_rank, tp_size)
+def layer(name, tp_rank=0, tp_size=1, shard=None, shared_shard=None):
+    key = (name, tp_rank, tp_size, shard, shared_shard)
     if key not in _layers:
         if len(_layers) > 6:
             _layers.clear()
             torch.cuda.empty_cache()
-        _layers[key] = GpuLayer(name, tp_rank, tp_size)
+        _layers[key] = GpuLayer(name, tp_rank, tp_size, shard=shard, shared_shard=shared_shard)
     return _layers[key]
 
 
@@ -210,8 +210,9 @@ def test_align_flags_invalid_ids(ft):
 
 # ------------------------------------------------------------------ forward
 
-def _run_and_compare(name, T, zipf, tp_rank=0, tp_size=1, sample=None, out_dtype=torch.float32):
-    L = layer(name, tp_rank, tp_size)
+def _run_and_compare(name, T, zipf, tp_rank=0, tp_size=1, sample=None, out_dtype=torch.float32, shard=None,
+                     shared_shard=None):
+    L = layer(name, tp_rank, tp_size, shard, shared_shard)
     shape = synth.SHAPES[name]
     logits = logits_for(name, T, zipf)
     x = synth.make_activations(T, shape.hidden)
@@ -219,7 +220,7 @@ def _run_and_compare(name, T, zipf, tp_rank=0, tp_size=1, sample=None, out_dtype
     out, _ = L.forward(x, ids, w, out_dtype=out_dtype)
     ref_ids, ref_w = oracle.route(logits, shape.top_k)
     assert np.array_equal(ids.cpu().numpy(), ref_ids)
-    rb, sb = oracle_banks(name, tp_rank, tp_size)
+    rb, sb = oracle_banks(name, tp_rank, tp_size, shard=shard, shared_shard=shared_shard)
     tokens = np.arange(T) if sample is None else sample
     ref = oracle.moe_forward(rb, sb, shape.group, x, ref_ids, ref_w, tokens=tokens,
                              nthreads=oracle.default_threads())
@@ -279,6 +280,39 @@ def test_forward_tp_partials_sum_to_full(tp, T, zipf):
     x = synth.make_activations(T, shape.hidden)
     full = oracle.moe_forward(rb, sb, shape.group, x, ids, w, tokens=sample, nthreads=oracle.default_threads())
     assert_close(total, full, f"sum of {tp} partials vs tp=1")
+
+
+# Two ranks with unequal shares of the intermediate dimension (routed 320 + 192 of 512,
+# shared 192 + 320 of 512): every range is whole scale blocks, and 320 / 192 are not
+# multiples of the tensor-core path's 128-row tiles, so both paths see ragged K and N.
+ASYM = [((0, 320), (0, 192)), ((320, 192), (192, 320))]
+
+
+def test_pack_explicit_shard_matches_oracle_slicer(ft):
+    for shard, shared_shard in ASYM:
+        L = GpuLayer("qwen36", shard=shard, shared_shard=shared_shard)
+        rb, sb = oracle_banks("qwen36", shard=shard, shared_shard=shared_shard)
+        for i, key in enumerate(("gu", "gu_scale", "gu_global", "dn", "dn_scale", "dn_global")):
+            assert np.array_equal(L.routed[i].cpu().numpy(), rb[key]), (key, shard)
+            assert np.array_equal(L.shared[i].cpu().numpy(), sb[key]), (key, shared_shard)
+
+
+@pytest.mark.parametrize("T,zipf", [(1, False), (32, False), (2048, True)])
+def test_forward_asymmetric_shards_sum_to_full(T, zipf):
+    """Partials over unequal ranges match the oracle's and add up to the unsharded output."""
+    shape = synth.SHAPES["qwen36"]
+    sample = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(7).choice(T, 16, replace=False))
+    total = 0
+    for shard, shared_shard in ASYM:
+        got, ref = _run_and_compare("qwen36", T, zipf, sample=sample, shard=shard, shared_shard=shared_shard)
+        assert_close(got, ref, f"shard {shard} shared {shared_shard}")
+        total = total + got.astype(np.float64)
+    logits = logits_for("qwen36", T, zipf)
+    ids, w = oracle.route(logits, shape.top_k)
+    rb, sb = oracle_banks("qwen36")
+    x = synth.make_activations(T, shape.hidden)
+    full = oracle.moe_forward(rb, sb, shape.group, x, ids, w, tokens=sample, nthreads=oracle.default_threads())
+    assert_close(total, full, "sum of asymmetric partials vs unsharded")
 
 
 @pytest.mark.parametrize("T,tp", [(1, 1), (16, 1), (1, 4), (16, 4)])

@@ -336,6 +336,29 @@ def pin_tp_partial_sum():
         assert np.abs(parts[0] - full).max() / np.abs(full).max() > 1e-3
 
 
+def pin_asymmetric_partition():
+    """Explicit uneven ranges: equal to the even split when the range is the rank's share,
+    tile the intermediate axis, and their partials sum to the full output (linearity)."""
+    shape = synth.LayerShape(hidden=256, intermediate=128, num_experts=8, top_k=2, shared_intermediate=64)
+    pieces, sp = _tiny_layer(seed=12, shared=True, shape=shape)
+    for r in range(4):
+        even, rng_ = oracle.slice_bank(pieces, 16, r, 4), oracle.slice_bank(pieces, 16, shard=(32 * r, 32))
+        assert all(np.array_equal(even[n], rng_[n]) for n in even)
+    cuts = [(0, 48), (48, 64), (112, 16)]
+    banks = [oracle.slice_bank(pieces, 16, shard=c) for c in cuts]
+    gate_rows = np.concatenate([b["gu"][:, :c[1]] for b, c in zip(banks, cuts)], axis=1)
+    assert np.array_equal(gate_rows, pieces["gate"])
+    T = 8
+    x = synth.make_activations(T, 256, seed=12)
+    ids, w = oracle.route(synth.make_logits(T, 8, seed=12), 2)
+    full = oracle.moe_forward(oracle.slice_bank(pieces, 16), oracle.slice_bank(sp, 16), 16, x, ids, w)
+    shared_cuts = [(0, 16), (16, 32), (48, 16)]
+    parts = [oracle.moe_forward(b, oracle.slice_bank(sp, 16, shard=sc), 16, x, ids, w)
+             for b, sc in zip(banks, shared_cuts)]
+    rel = np.abs(np.sum(parts, axis=0) - full).max() / np.abs(full).max()
+    assert rel < 1e-12, rel
+
+
 def pin_router_logits_exact():
     """Router logits against exact rational arithmetic: with these magnitudes every
     bf16 product and every partial sum fits 53 bits, so fp64 must be exact; absum too.
@@ -368,7 +391,7 @@ PINS = [pin_e2m1, pin_e4m3, pin_dequant_bf16, pin_route_worked_example, pin_rout
         pin_route_library, pin_route_ties_and_shift, pin_align, pin_slice_identity_and_tiling,
         pin_one_hot_columns, pin_linear_parts_exact, pin_dense_mlp_special_case,
         pin_routed_combination, pin_untouched_experts_and_tokens, pin_tp_partial_sum,
-        pin_router_logits_exact, pin_router_one_hot]
+        pin_router_logits_exact, pin_router_one_hot, pin_asymmetric_partition]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
