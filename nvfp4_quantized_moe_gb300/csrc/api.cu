@@ -215,12 +215,21 @@ static int fast_ksplit(int blocks, int units_per_block_ks1, int K0, int K1 = 0)
 
 // Decode kernel family: the lean register-fed kernels (default) or, with the
 // environment variable FTMOE_DECODE=stream, the TMA-streamed ones. Read once per process.
+static bool decode_mode_is(const char *name)
+{
+    const char *e = getenv("FTMOE_DECODE");
+    return e && strcmp(e, name) == 0;
+}
+
 static bool decode_streamed()
 {
-    static const bool v = [] {
-        const char *e = getenv("FTMOE_DECODE");
-        return e && strcmp(e, "stream") == 0;
-    }();
+    static const bool v = decode_mode_is("stream");
+    return v;
+}
+
+static bool decode_tensor_core()
+{
+    static const bool v = decode_mode_is("tc");
     return v;
 }
 
@@ -619,6 +628,47 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
             if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
             if ((e = launch_gemv_stream(SD, false, units(SD), s)) != cudaSuccess) return cuda_fail(e, "down launch");
+            if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
+            if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+            if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            return ok();
+        }
+    }
+
+    // Tensor-core kernels (A operand dequantised into tensor memory), same launch structure.
+    {
+        const int kmax = G.H > G.Il ? (G.H > G.Isl ? G.H : G.Isl) : (G.Il > G.Isl ? G.Il : G.Isl);
+        if (decode_tensor_core() && tc_gemv_ok(G.H, G.g) && tc_gemv_ok(G.Il, G.g) &&
+            (!G.Is || tc_gemv_ok(G.Isl, G.g)) && tc_gemv_fits(kmax)) {
+            FastLaunch F = {};
+            F.prob[0] = gu;
+            F.prob[0].n_tiles = cdiv(G.Il, 128);
+            F.nprob = 1;
+            if (G.Is) {
+                F.prob[1] = gu_sh;
+                F.prob[1].n_tiles = cdiv(G.Isl, 128);
+                F.nprob = 2;
+            }
+            if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            int max_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
+            if ((e = launch_tc_gemv(F, true, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
+            if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            FastLaunch D = {};
+            D.prob[0] = dn;
+            D.prob[0].n_tiles = cdiv(G.H, 256);
+            D.nprob = 1;
+            if (G.Is) {
+                D.prob[1] = dn_sh;
+                D.prob[1].n_tiles = D.prob[0].n_tiles;
+                D.nprob = 2;
+            }
+            set_combine(D);
+            D.counters = nullptr;  // combine in its own launch (below): no atomics in the epilogue
+            if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
+            if ((e = launch_tc_gemv(D, false, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
             if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
             if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
             e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);

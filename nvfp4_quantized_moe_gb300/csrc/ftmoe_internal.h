@@ -155,6 +155,12 @@ struct FastLaunch {
 };
 cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
 
+// Tensor-core decode GEMV (A operand dequantised into tensor memory, one persistent CTA
+// per SM). Units per block: prob[i].n_tiles = ceil(I/128) for gate_up, ceil(H/256) for down.
+bool tc_gemv_ok(int K, int group);
+bool tc_gemv_fits(int kmax);
+cudaError_t launch_tc_gemv(const FastLaunch &L, bool gated, int max_units, cudaStream_t s);
+
 // TMA-streamed decode GEMV (one persistent CTA per SM). Per problem: lps lines of 256 K
 // elements x tps pair tiles per stage, nst stages per unit, n_ptiles units per block of
 // positions, sbytes scale bytes per row and stage (gemv_stream_geom fills these).
