@@ -1,4 +1,4 @@
-"""CPU oracle for the NVFP4 routed-MoE expert forward (TEST INFRASTRUCTURE ONLY).
+"""CPU oracle for the NVFP4 (and fp8_block) routed-MoE expert forward (TEST INFRASTRUCTURE ONLY).
 
 A ctypes front end over ``ftmoe_oracle.c``, the plain fp64 C statement of the
 layer. Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
@@ -35,7 +35,8 @@ def build(force: bool = False) -> str:
 class Bank(ctypes.Structure):
     _fields_ = [("gu", ctypes.c_void_p), ("gu_scale", ctypes.c_void_p), ("gu_global", ctypes.c_void_p),
                 ("dn", ctypes.c_void_p), ("dn_scale", ctypes.c_void_p), ("dn_global", ctypes.c_void_p),
-                ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("Il", ctypes.c_int32), ("g", ctypes.c_int32)]
+                ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("Il", ctypes.c_int32), ("g", ctypes.c_int32),
+                ("fmt", ctypes.c_int32)]
 
 
 def lib():
@@ -56,6 +57,9 @@ def lib():
             L.orc_align.restype = I; L.orc_align.argtypes = [P, I, I, I, I, P, P, P, P]
             L.orc_slice.restype = I; L.orc_slice.argtypes = [I] * 6 + [P] * 15
             L.orc_slice_range.restype = I; L.orc_slice_range.argtypes = [I] * 6 + [P] * 15
+            L.orc_slice_fp8_range.restype = I; L.orc_slice_fp8_range.argtypes = [I] * 5 + [P] * 10
+            L.orc_dequant_fp8_matrix.restype = None
+            L.orc_dequant_fp8_matrix.argtypes = [P, P, I, I, P]
             L.orc_expert_gate_up.restype = None
             L.orc_expert_gate_up.argtypes = [ctypes.POINTER(Bank), I, P, P]
             L.orc_swiglu.restype = None; L.orc_swiglu.argtypes = [P, I, P]
@@ -88,7 +92,7 @@ def mutation(code: int):
 MUTATIONS = {
     "nibble_order": 1, "swap_gate_up": 2, "drop_global": 3, "scale_index": 4, "e2m1_sign": 5,
     "no_renorm": 6, "tie_high": 7, "down_rows": 8, "drop_shared": 9, "drop_route_w": 10,
-    "e4m3_bias": 11, "up_slice": 12, "router_transposed": 13,
+    "e4m3_bias": 11, "up_slice": 12, "router_transposed": 13, "fp8_block_transposed": 14,
 }
 
 
@@ -112,6 +116,17 @@ def dequant_matrix(codes: np.ndarray, scales: np.ndarray, glob: np.ndarray, grou
     rows, K = codes.shape[0], codes.shape[1] * 2
     out = np.empty((rows, K), np.float64)
     lib().orc_dequant_matrix(_p(codes), _p(scales), _p(glob), rows, K, group, _p(out))
+    return out
+
+
+def dequant_fp8_matrix(codes: np.ndarray, sinv: np.ndarray) -> np.ndarray:
+    """Dense fp64 [rows, K] of one fp8_block expert matrix (codes [rows, K] u8,
+    scale_inv [rows/128, K/128] f32)."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    sinv = np.ascontiguousarray(sinv, np.float32)
+    rows, K = codes.shape
+    out = np.empty((rows, K), np.float64)
+    lib().orc_dequant_fp8_matrix(_p(codes), _p(sinv), rows, K, _p(out))
     return out
 
 
@@ -184,10 +199,41 @@ def slice_bank(pieces: dict, group: int, tp_rank: int = 0, tp_size: int = 1, sha
     return out
 
 
+def slice_fp8_bank(pieces: dict, tp_rank: int = 0, tp_size: int = 1, shard: tuple | None = None) -> dict:
+    """fp8_block rank-local bank {gu, gu_scale, dn, dn_scale, fmt} from full pieces
+    (gate/up [E, I, H] u8 + [E, I/128, H/128] f32, down [E, H, I] u8 + [E, H/128, I/128]):
+    the even split (tp_rank of tp_size) or the explicit range shard = (begin, size)."""
+    c = {k: np.ascontiguousarray(v) for k, v in pieces.items()}
+    E, I, H = c["gate"].shape
+    if shard is None:
+        if I % tp_size:
+            raise ValueError("intermediate not divisible by tp_size")
+        shard = (tp_rank * (I // tp_size), I // tp_size)
+    b, n = shard
+    out = {
+        "gu": np.zeros((E, 2 * n, H), np.uint8),
+        "gu_scale": np.zeros((E, 2 * n // 128, H // 128), np.float32),
+        "dn": np.zeros((E, H, n), np.uint8),
+        "dn_scale": np.zeros((E, H // 128, n // 128), np.float32),
+        "fmt": "fp8_block",
+    }
+    rc = lib().orc_slice_fp8_range(E, H, I, b, n,
+                                   *[_p(c[k]) for k in ("gate", "gate_scale", "up", "up_scale", "down",
+                                                        "down_scale")],
+                                   *[_p(out[k]) for k in ("gu", "gu_scale", "dn", "dn_scale")])
+    if rc != 0:
+        raise ValueError("range not made of whole 128-element blocks")
+    return out
+
+
 def _bank(b: dict, group: int) -> Bank:
+    if b.get("fmt") == "fp8_block":
+        E, rows, H = b["gu"].shape
+        return Bank(_p(b["gu"]), _p(b["gu_scale"]), None, _p(b["dn"]), _p(b["dn_scale"]), None,
+                    E, H, rows // 2, 128, 1)
     E, rows, H2 = b["gu"].shape
     return Bank(_p(b["gu"]), _p(b["gu_scale"]), _p(b["gu_global"]), _p(b["dn"]), _p(b["dn_scale"]),
-                _p(b["dn_global"]), E, H2 * 2, rows // 2, group)
+                _p(b["dn_global"]), E, H2 * 2, rows // 2, group, 0)
 
 
 def expert_gate_up(bank: dict, group: int, e: int, x_row: np.ndarray) -> np.ndarray:

@@ -35,6 +35,15 @@
  *  - SwiGLU h_i = silu(g_i) * u_i with silu(z) = z / (1 + e^-z), gate rows first;
  *  - the shared expert is added with weight 1 after the k routed terms.
  *
+ * fp8_block experts (the second expert format of the same pages: "feat(qwen3_5_moe):
+ * tensor-parallel weight sharding", Summary and Implementation notes -- an fp8-block
+ * weight carries a 128-block weight_scale_inv, split along the same axis as its weight;
+ * "[1/3] feat(dsv4)...", Checkpoint loading -- FP8 128x128 blocks cannot be cut at
+ * arbitrary boundaries; "Offloaded MoE ignores tensor parallelism", item 2 -- I/tp a
+ * multiple of 128): W[n][k] = e4m3(code[n][k]) * scale_inv[n/128][k/128], one code byte
+ * per element, no per-row global. Reading where the pages are silent: scale_inv is the
+ * fp32 multiplier that dequantises (the weight is code times scale_inv).
+ *
  * Parity pins for every function here live in tests/test_oracle_pins.py.
  * The absolute output values are "parity unpinned" against the pages: they print
  * no worked numeric example of the MoE arithmetic.
@@ -63,6 +72,7 @@ enum {
     ORC_MUT_E4M3_BIAS = 11,     /* e4m3 exponent bias 8 instead of 7 */
     ORC_MUT_UP_SLICE = 12,      /* up rows taken from the gate half */
     ORC_MUT_ROUTER_T = 13,      /* router weight read transposed (square shapes only) */
+    ORC_MUT_FP8_BLOCK_T = 14,   /* fp8_block: scale block indexed [k/128][n/128] */
 };
 
 /* ---------------------------------------------------------------- formats */
@@ -150,6 +160,22 @@ static double weight_at(const uint8_t *codes, const uint8_t *scales, const float
                e4m3_tab[scales[(size_t)n * (K / g) + grp]];
     if (orc_mutation != ORC_MUT_DROP_GLOBAL) w *= (double)glob[n];
     return w;
+}
+
+/* fp8_block: W[n][k] = e4m3(code[n][k]) * scale_inv[n/128][k/128] for one expert's
+ * [rows, K] matrix stored as codes [rows][K] and scale_inv [rows/128][K/128]. */
+static double fp8_weight_at(const uint8_t *codes, const float *sinv, int n, int k, int K)
+{
+    int nb = n / 128, kb = k / 128, kblocks = K / 128;
+    size_t s = (orc_mutation == ORC_MUT_FP8_BLOCK_T) ? (size_t)kb * kblocks + nb : (size_t)nb * kblocks + kb;
+    return e4m3_tab[codes[(size_t)n * K + k]] * (double)sinv[s];
+}
+
+void orc_dequant_fp8_matrix(const uint8_t *codes, const float *sinv, int rows, int K, double *out)
+{
+    fill_tables();
+    for (int n = 0; n < rows; ++n)
+        for (int k = 0; k < K; ++k) out[(size_t)n * K + k] = fp8_weight_at(codes, sinv, n, k, K);
 }
 
 /* Dense dequantised matrix of one expert, W as above, row-major [rows][K]. */
@@ -342,6 +368,45 @@ int orc_slice_range(int E, int H, int I, int g, int begin, int len,
     return 0;
 }
 
+/* fp8_block rank-local bank for the intermediate range [begin, begin + len) (begin
+ * and len multiples of 128, the scale block): gate and up rows of the range with their
+ * scale_inv block rows (gate first), down columns of the range with their scale_inv
+ * block columns -- the rule of "feat(qwen3_5_moe): tensor-parallel weight sharding"
+ * (gate/up split along output rows, down along input columns, companions with their
+ * weight). Pieces: gate, up [E][I][H] u8 and [E][I/128][H/128] f32; down [E][H][I] u8
+ * and [E][H/128][I/128] f32. Bank: gu [E][2len][H], gu_sinv [E][2len/128][H/128],
+ * dn [E][H][len], dn_sinv [E][H/128][len/128]. */
+int orc_slice_fp8_range(int E, int H, int I, int begin, int len,
+                        const uint8_t *gate, const float *gate_sinv, const uint8_t *up, const float *up_sinv,
+                        const uint8_t *down, const float *down_sinv,
+                        uint8_t *gu, float *gu_sinv, uint8_t *dn, float *dn_sinv)
+{
+    if (begin < 0 || len <= 0 || begin + len > I || begin % 128 || len % 128 || H % 128 || I % 128) return -1;
+    size_t hb = (size_t)H / 128, ib = (size_t)I / 128, lb = (size_t)len / 128;
+    for (int e = 0; e < E; ++e) {
+        for (int i = 0; i < len; ++i) {
+            size_t src = (size_t)e * I + (size_t)begin + i;
+            size_t up_src = (orc_mutation == ORC_MUT_UP_SLICE) ? (size_t)e * I + i : src;
+            memcpy(gu + ((size_t)e * 2 * len + i) * H, gate + src * H, (size_t)H);
+            memcpy(gu + ((size_t)e * 2 * len + len + i) * H, up + up_src * H, (size_t)H);
+        }
+        for (size_t b = 0; b < lb; ++b) {
+            size_t src = (size_t)e * ib + (size_t)begin / 128 + b;
+            memcpy(gu_sinv + ((size_t)e * 2 * lb + b) * hb, gate_sinv + src * hb, hb * sizeof(float));
+            memcpy(gu_sinv + ((size_t)e * 2 * lb + lb + b) * hb, up_sinv + src * hb, hb * sizeof(float));
+        }
+        for (int n = 0; n < H; ++n) {
+            size_t row = (size_t)e * H + n;
+            memcpy(dn + row * len, down + row * I + begin, (size_t)len);
+        }
+        for (size_t nb = 0; nb < hb; ++nb) {
+            size_t row = (size_t)e * hb + nb;
+            memcpy(dn_sinv + row * lb, down_sinv + row * ib + (size_t)begin / 128, lb * sizeof(float));
+        }
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------- expert MLP */
 
 typedef struct {
@@ -350,19 +415,34 @@ typedef struct {
     const uint8_t *dn, *dn_scale;   /* [E][H][Il/2], [E][H][Il/g] */
     const float *dn_global;         /* [E][H] */
     int32_t E, H, Il, g;
+    int32_t fmt;                    /* 0: NVFP4 as above; 1: fp8_block -- gu [E][2*Il][H] and
+                                       dn [E][H][Il] code bytes, gu_scale / dn_scale fp32
+                                       scale_inv [E][2*Il/128][H/128] / [E][H/128][Il/128],
+                                       no globals */
 } orc_bank;
+
+/* W of expert e's gate_up (which = 0) or down (which = 1) matrix at [n][k]. */
+static double bank_weight(const orc_bank *b, int which, int e, int n, int k)
+{
+    int rows = which ? b->H : 2 * b->Il, K = which ? b->Il : b->H;
+    const uint8_t *codes = which ? b->dn : b->gu;
+    if (b->fmt == 1) {
+        const float *sinv = (const float *)(which ? b->dn_scale : b->gu_scale);
+        return fp8_weight_at(codes + (size_t)e * rows * K, sinv + (size_t)e * (rows / 128) * (K / 128), n, k, K);
+    }
+    const uint8_t *scales = which ? b->dn_scale : b->gu_scale;
+    const float *glob = which ? b->dn_global : b->gu_global;
+    return weight_at(codes + (size_t)e * rows * (K / 2), scales + (size_t)e * rows * (K / b->g),
+                     glob + (size_t)e * rows, n, k, K, b->g);
+}
 
 /* Pre-activations G[n] = sum_k x[k] * W_gu[e][n][k], n < 2*Il (gate rows first). */
 static void expert_gate_up(const orc_bank *b, int e, const uint16_t *x_row, double *G)
 {
     int H = b->H, rows = 2 * b->Il;
-    const uint8_t *codes = b->gu + (size_t)e * rows * (H / 2);
-    const uint8_t *scales = b->gu_scale + (size_t)e * rows * (H / b->g);
-    const float *glob = b->gu_global + (size_t)e * rows;
     for (int n = 0; n < rows; ++n) {
         double acc = 0.0;
-        for (int k = 0; k < H; ++k)
-            acc += orc_bf16_to_double(x_row[k]) * weight_at(codes, scales, glob, n, k, H, b->g);
+        for (int k = 0; k < H; ++k) acc += orc_bf16_to_double(x_row[k]) * bank_weight(b, 0, e, n, k);
         G[n] = acc;
     }
 }
@@ -381,12 +461,9 @@ void orc_swiglu(const double *G, int Il, double *h)
 static void expert_down(const orc_bank *b, int e, const double *h, double *y)
 {
     int H = b->H, Il = b->Il;
-    const uint8_t *codes = b->dn + (size_t)e * H * (Il / 2);
-    const uint8_t *scales = b->dn_scale + (size_t)e * H * (Il / b->g);
-    const float *glob = b->dn_global + (size_t)e * H;
     for (int n = 0; n < H; ++n) {
         double acc = 0.0;
-        for (int i = 0; i < Il; ++i) acc += h[i] * weight_at(codes, scales, glob, n, i, Il, b->g);
+        for (int i = 0; i < Il; ++i) acc += h[i] * bank_weight(b, 1, e, n, i);
         y[n] = acc;
     }
 }

@@ -20,6 +20,13 @@ group size 16) and the "Offloaded MoE ignores tensor parallelism" page
 * weight_global   fp32 U[0.5, 1.5], one per output row
 * router weights  bf16 ~ N(0, 1/H) [E, H] (replicated on every rank), so that with
                   N(0,1) activations the router logits are again ~ N(0, 1)
+
+fp8_block experts (the Qwen3.6-35B-A3B-FP8 checkpoint of the "feat(qwen3_5_moe):
+tensor-parallel weight sharding" page, Testing: same layer geometry, fp8 weights with a
+128x128-block weight_scale_inv):
+
+* weight codes    e4m3 (round-to-nearest-even, saturating at 448) of N(0, 1) * 32
+* scale_inv       fp32 U[0.5, 1.5] * 2^-8, one per 128 x 128 block
 """
 from __future__ import annotations
 
@@ -30,6 +37,7 @@ import numpy as np
 __all__ = [
     "LayerShape", "SHAPES", "rng_for", "bf16_bits_from_f32", "e4m3_rne_bytes",
     "make_pieces", "make_activations", "make_logits", "zipf_logits", "make_router_weights",
+    "e4m3_rne_signed_bytes", "make_fp8_pieces",
 ]
 
 
@@ -42,6 +50,7 @@ class LayerShape:
     top_k: int
     group: int = 16
     shared_intermediate: int = 0
+    fmt: str = "nvfp4"  # or "fp8_block" (group is then the 128-element scale block)
 
 
 # The layer families exercised by the tests and the bench.
@@ -56,6 +65,11 @@ SHAPES = {
     # DeepSeek-V4-Flash-like routed FP4 layer, 32-element scale blocks
     "dsv4": LayerShape(hidden=4096, intermediate=2048, num_experts=256, top_k=8,
                        group=32, shared_intermediate=2048),
+    # fp8_block experts: a small layer (full-oracle parity) and the Qwen3.6-FP8 layer
+    "mini_fp8": LayerShape(hidden=256, intermediate=256, num_experts=8, top_k=2, group=128,
+                           shared_intermediate=128, fmt="fp8_block"),
+    "qwen36_fp8": LayerShape(hidden=2048, intermediate=512, num_experts=256, top_k=8,
+                             group=128, shared_intermediate=512, fmt="fp8_block"),
 }
 
 
@@ -87,6 +101,25 @@ def e4m3_rne_bytes(v: np.ndarray) -> np.ndarray:
     m = np.where(carry, 0, m)
     e = np.where(carry, e + 1, e)
     return ((e + 7) << 3 | m).astype(np.uint8)
+
+
+def e4m3_rne_signed_bytes(v: np.ndarray) -> np.ndarray:
+    """Encode any finite values as OCP e4m3 bytes, round-to-nearest-even, saturating at
+    +-448 (subnormals 2^-9 * m below 2^-6). Used only to draw fp8 weight codes."""
+    v = np.asarray(v, dtype=np.float64)
+    sign = (v < 0).astype(np.int64) << 7
+    a = np.minimum(np.abs(v), 448.0)
+    sub = a < 2.0 ** -6
+    m_sub = np.rint(a * 2.0 ** 9).astype(np.int64)  # subnormal: a = m * 2^-9, m in 0..8
+    safe = np.where(sub, 1.0, a)
+    e = np.floor(np.log2(safe)).astype(np.int64)
+    m = np.rint((safe / np.exp2(e.astype(np.float64)) - 1.0) * 8.0).astype(np.int64)
+    carry = m == 8
+    m = np.where(carry, 0, m)
+    e = np.where(carry, e + 1, e)
+    normal = ((e + 7) << 3) | m
+    code = np.where(sub, m_sub, normal)  # m_sub == 8 is the smallest normal, byte 8
+    return (sign | code).astype(np.uint8)
 
 
 def _codes(rng, shape):
@@ -134,6 +167,31 @@ def make_pieces(shape: LayerShape, seed: int = 0, shared: bool = False) -> dict[
         "down": _codes(r(7), (E, H, I // 2)),
         "down_scale": _scales(r(8), (E, H, I // g)),
         "down_global": _globals(r(9), (E, H)),
+    }
+
+
+def make_fp8_pieces(shape: LayerShape, seed: int = 0, shared: bool = False) -> dict[str, np.ndarray]:
+    """Checkpoint-shaped fp8_block expert tensors at full intermediate size, expert-major:
+
+      gate, up           u8  [E, I, H]           e4m3 codes
+      gate_scale, ...    f32 [E, I/128, H/128]   scale_inv per 128 x 128 block
+      down               u8  [E, H, I]
+      down_scale         f32 [E, H/128, I/128]
+    """
+    H = shape.hidden
+    if shared:
+        E, I, base = 1, shape.shared_intermediate, 700
+        if I == 0:
+            raise ValueError("layer has no shared expert")
+    else:
+        E, I, base = shape.num_experts, shape.intermediate, 600
+    r = lambda i: rng_for(seed, base + i)
+    codes = lambda g, sh: e4m3_rne_signed_bytes(g.standard_normal(sh) * 32.0)
+    sinv = lambda g, sh: (g.uniform(0.5, 1.5, size=sh) * 2.0 ** -8).astype(np.float32)
+    return {
+        "gate": codes(r(1), (E, I, H)), "gate_scale": sinv(r(2), (E, I // 128, H // 128)),
+        "up": codes(r(3), (E, I, H)), "up_scale": sinv(r(4), (E, I // 128, H // 128)),
+        "down": codes(r(5), (E, H, I)), "down_scale": sinv(r(6), (E, H // 128, I // 128)),
     }
 
 

@@ -387,11 +387,85 @@ def pin_router_one_hot():
     assert np.array_equal(logits, wv.T)
 
 
+# ------------------------------------------------------------------ fp8_block experts
+
+FP8 = synth.LayerShape(hidden=256, intermediate=256, num_experts=4, top_k=2, group=128,
+                       shared_intermediate=256, fmt="fp8_block")
+
+
+def _dense_fp8(codes, sinv):
+    """Test-side fp8_block dequantisation: torch's e4m3 times the 128 x 128 block grid
+    expanded with np.kron (an independent statement of "one scale per block")."""
+    return _torch_e4m3(codes) * np.kron(np.asarray(sinv, np.float64), np.ones((128, 128)))
+
+
+def pin_fp8_slice_identity_and_tiling():
+    pieces = synth.make_fp8_pieces(FP8, seed=31)
+    b1 = oracle.slice_fp8_bank(pieces)
+    assert np.array_equal(b1["gu"], np.concatenate([pieces["gate"], pieces["up"]], axis=1))
+    assert np.array_equal(b1["gu_scale"], np.concatenate([pieces["gate_scale"], pieces["up_scale"]], 1))
+    assert np.array_equal(b1["dn"], pieces["down"]) and np.array_equal(b1["dn_scale"], pieces["down_scale"])
+    banks = [oracle.slice_fp8_bank(pieces, r, 2) for r in range(2)]
+    assert np.array_equal(np.concatenate([b["gu"][:, :128] for b in banks], 1), pieces["gate"])
+    assert np.array_equal(np.concatenate([b["gu"][:, 128:] for b in banks], 1), pieces["up"])
+    assert np.array_equal(np.concatenate([b["gu_scale"][:, 1:] for b in banks], 1), pieces["up_scale"])
+    assert np.array_equal(np.concatenate([b["dn"] for b in banks], 2), pieces["down"])
+    assert np.array_equal(np.concatenate([b["dn_scale"] for b in banks], 2), pieces["down_scale"])
+    with pytest.raises(ValueError):
+        oracle.slice_fp8_bank(pieces, 0, 4)      # 64 is not a whole 128-element block
+    with pytest.raises(ValueError):
+        oracle.slice_fp8_bank(pieces, shard=(64, 128))
+
+
+def pin_fp8_one_hot_columns():
+    """x = e_k gives column k of the block-scaled fp8 matrix, for k in both K blocks and
+    rows in all four row blocks of gate_up (and the same through down with h = e_i)."""
+    pieces = synth.make_fp8_pieces(FP8, seed=32)
+    bank = oracle.slice_fp8_bank(pieces)
+    e = 2
+    dense = _dense_fp8(bank["gu"][e], bank["gu_scale"][e])
+    one = synth.bf16_bits_from_f32(np.array([1.0], np.float32))[0]
+    for k in (0, 5, 127, 128, 200, 255):
+        x = np.zeros(FP8.hidden, np.uint16)
+        x[k] = one
+        assert np.array_equal(oracle.expert_gate_up(bank, 128, e, x), dense[:, k]), k
+    dd = _dense_fp8(bank["dn"][e], bank["dn_scale"][e])
+    for i in (3, 130):
+        h = np.zeros(FP8.intermediate)
+        h[i] = 1.0
+        assert np.array_equal(oracle.expert_down(bank, 128, e, h), dd[:, i]), i
+
+
+def pin_fp8_dense_mlp_and_partials():
+    """E=1, k=1, weight 1: a dense SwiGLU MLP (torch fp64 on test-side weights); and the
+    tp=2 partials of a routed layer with a shared expert sum to the full output."""
+    shape = synth.LayerShape(hidden=256, intermediate=256, num_experts=1, top_k=1, group=128, fmt="fp8_block")
+    pieces = synth.make_fp8_pieces(shape, seed=33)
+    x = synth.make_activations(4, 256, seed=33)
+    out = oracle.moe_forward(oracle.slice_fp8_bank(pieces), None, 128, x, np.zeros((4, 1), np.int32), np.ones((4, 1)))
+    Wg, Wu, Wd = (torch.from_numpy(_dense_fp8(pieces[n][0], pieces[n + "_scale"][0])) for n in ("gate", "up", "down"))
+    xt = torch.from_numpy(_bf16_to_f64(x))
+    ref = (torch.nn.functional.silu(xt @ Wg.T) * (xt @ Wu.T)) @ Wd.T
+    assert torch.allclose(torch.from_numpy(out), ref, rtol=1e-12, atol=1e-9 * ref.abs().max().item())
+    pieces = synth.make_fp8_pieces(FP8, seed=34)
+    sp = synth.make_fp8_pieces(FP8, seed=34, shared=True)
+    T = 6
+    x = synth.make_activations(T, 256, seed=34)
+    ids, w = oracle.route(synth.make_logits(T, FP8.num_experts, seed=34), 2)
+    full = oracle.moe_forward(oracle.slice_fp8_bank(pieces), oracle.slice_fp8_bank(sp), 128, x, ids, w)
+    parts = [oracle.moe_forward(oracle.slice_fp8_bank(pieces, r, 2), oracle.slice_fp8_bank(sp, r, 2), 128, x, ids, w)
+             for r in range(2)]
+    rel = np.abs(np.sum(parts, axis=0) - full).max() / np.abs(full).max()
+    assert rel < 1e-12, rel
+    assert np.abs(parts[0] - full).max() / np.abs(full).max() > 1e-3
+
+
 PINS = [pin_e2m1, pin_e4m3, pin_dequant_bf16, pin_route_worked_example, pin_route_brute_force,
         pin_route_library, pin_route_ties_and_shift, pin_align, pin_slice_identity_and_tiling,
         pin_one_hot_columns, pin_linear_parts_exact, pin_dense_mlp_special_case,
         pin_routed_combination, pin_untouched_experts_and_tokens, pin_tp_partial_sum,
-        pin_router_logits_exact, pin_router_one_hot, pin_asymmetric_partition]
+        pin_router_logits_exact, pin_router_one_hot, pin_asymmetric_partition,
+        pin_fp8_slice_identity_and_tiling, pin_fp8_one_hot_columns, pin_fp8_dense_mlp_and_partials]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
