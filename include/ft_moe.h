@@ -95,7 +95,17 @@ typedef struct {
     int32_t shard_size;
     int32_t shared_shard_begin;
     int32_t shared_shard_size;
+    /* Expert weight format (FT_FORMAT_*). FT_FORMAT_FP8_BLOCK is the fp8-block expert
+     * format the sharding pages carry beside NVFP4 ("feat(qwen3_5_moe): tensor-parallel
+     * weight sharding", Summary and Implementation notes; the dsv4 PR, Checkpoint
+     * loading: FP8 128x128 blocks): one e4m3 code byte per weight and an fp32
+     * weight_scale_inv per 128 x 128 block, W = code * scale_inv, no per-row global.
+     * It needs group = 128, and H, the rank's intermediate share (and any explicit
+     * range) multiples of 128 (the same issue's item 2: "128 for fp8_block"). */
+    int32_t format;
 } ft_moe_config;
+
+enum { FT_FORMAT_NVFP4 = 0, FT_FORMAT_FP8_BLOCK = 1 };
 
 enum { FT_DTYPE_U8 = 0, FT_DTYPE_E4M3 = 1, FT_DTYPE_F32 = 2, FT_DTYPE_BF16 = 3 };
 
@@ -116,6 +126,12 @@ typedef struct {
  *   p[FT_DN]        u8   [E, H, I_l/2]
  *   p[FT_DN_SCALE]  e4m3 [E, H, I_l/group]
  *   p[FT_DN_GLOBAL] f32  [E, H]
+ * FT_FORMAT_FP8_BLOCK instead:
+ *   p[FT_GU]        u8 (e4m3 codes) [E, 2*I_l, H]
+ *   p[FT_GU_SCALE]  f32 [E, 2*I_l/128, H/128]   scale_inv, gate block rows first
+ *   p[FT_DN]        u8 (e4m3 codes) [E, H, I_l]
+ *   p[FT_DN_SCALE]  f32 [E, H/128, I_l/128]
+ *   p[FT_GU_GLOBAL], p[FT_DN_GLOBAL]: none (0 bytes; the pointers may be NULL).
  * Device pointers, caller-owned, each 16-byte aligned. */
 typedef struct { void *p[FT_NBANKS]; } ft_moe_banks;
 
@@ -125,7 +141,10 @@ typedef struct { void *p[FT_NBANKS]; } ft_moe_banks;
  *   gate, up          u8 [E, I, H/2];  gate_scale, up_scale  e4m3 [E, I, H/group];
  *   gate_global, up_global f32 [E, I]
  *   down u8 [E, H, I/2];  down_scale e4m3 [E, H, I/group];  down_global f32 [E, H]
- * on_device = 1: all nine are device pointers; 0: all nine are host pointers. */
+ * FT_FORMAT_FP8_BLOCK: gate, up u8 [E, I, H] with gate_scale, up_scale f32 scale_inv
+ * [E, I/128, H/128]; down u8 [E, H, I] with down_scale f32 [E, H/128, I/128]; the
+ * three _global pointers are ignored (may be NULL).
+ * on_device = 1: all are device pointers; 0: all are host pointers. */
 typedef struct {
     const void *gate, *gate_scale, *gate_global;
     const void *up, *up_scale, *up_global;

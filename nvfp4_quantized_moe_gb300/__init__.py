@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libftmoe.so
 
 FT_GU, FT_GU_SCALE, FT_GU_GLOBAL, FT_DN, FT_DN_SCALE, FT_DN_GLOBAL, FT_NBANKS = range(7)
 FT_DTYPE_U8, FT_DTYPE_E4M3, FT_DTYPE_F32, FT_DTYPE_BF16 = range(4)
+FT_FORMAT_NVFP4, FT_FORMAT_FP8_BLOCK = range(2)
 STATUS = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_INDIVISIBLE", 3: "FT_ERR_UNSUPPORTED",
           4: "FT_ERR_WORKSPACE", 5: "FT_ERR_CUDA", 6: "FT_ERR_INVALID_ROUTING", 7: "FT_ERR_TIMEOUT"}
 BANK_NAMES = ("gate_up", "gate_up_scale", "gate_up_global", "down", "down_scale", "down_global")
@@ -49,15 +50,16 @@ class MoEConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("group", ctypes.c_int32), ("shared_intermediate", ctypes.c_int32),
                 ("tp_rank", ctypes.c_int32), ("tp_size", ctypes.c_int32), ("shard_begin", ctypes.c_int32),
                 ("shard_size", ctypes.c_int32), ("shared_shard_begin", ctypes.c_int32),
-                ("shared_shard_size", ctypes.c_int32)]
+                ("shared_shard_size", ctypes.c_int32), ("format", ctypes.c_int32)]
 
     @classmethod
     def of(cls, shape, tp_rank: int = 0, tp_size: int = 1, shard=None, shared_shard=None) -> "MoEConfig":
         """Even split (tp_rank of tp_size) or explicit (begin, size) ranges of the intermediate."""
         sb, ss = shard if shard else (0, 0)
         hb, hs = shared_shard if shared_shard else (0, 0)
+        fmt = FT_FORMAT_FP8_BLOCK if getattr(shape, "fmt", "nvfp4") == "fp8_block" else FT_FORMAT_NVFP4
         return cls(shape.hidden, shape.intermediate, shape.num_experts, shape.top_k, shape.group,
-                   shape.shared_intermediate, tp_rank, tp_size, sb, ss, hb, hs)
+                   shape.shared_intermediate, tp_rank, tp_size, sb, ss, hb, hs, fmt)
 
 
 class _BankSpec(ctypes.Structure):
@@ -164,15 +166,16 @@ def _banks(tensors):
 
 def ft_moe_pack(cfg: MoEConfig, shared: int, pieces: dict, banks, stream=None):
     """Slice full checkpoint-shaped pieces (all host numpy/CPU tensors or all CUDA tensors) into banks."""
-    vals = [pieces[n] for n in ("gate", "gate_scale", "gate_global", "up", "up_scale", "up_global", "down",
-                                "down_scale", "down_global")]
-    on_dev = all(isinstance(v, torch.Tensor) and v.is_cuda for v in vals)
+    names = ("gate", "gate_scale", "gate_global", "up", "up_scale", "up_global", "down", "down_scale", "down_global")
+    vals = [pieces.get(n) for n in names]  # fp8_block pieces have no globals
+    given = [v for v in vals if v is not None]
+    on_dev = all(isinstance(v, torch.Tensor) and v.is_cuda for v in given)
     if not on_dev:
         vals = [v.numpy() if isinstance(v, torch.Tensor) else v for v in vals]
     for v in vals:
-        if not (v.is_contiguous() if isinstance(v, torch.Tensor) else v.flags.c_contiguous):
+        if v is not None and not (v.is_contiguous() if isinstance(v, torch.Tensor) else v.flags.c_contiguous):
             raise ValueError("pieces must be contiguous")
-    p = _Pieces(*[_ptr(v).value for v in vals], 1 if on_dev else 0)
+    p = _Pieces(*[_ptr(v).value if v is not None else None for v in vals], 1 if on_dev else 0)
     _check(load().ft_moe_pack(ctypes.byref(cfg), shared, ctypes.byref(p), ctypes.byref(_banks(banks)),
                               _stream(stream, *banks)))
 

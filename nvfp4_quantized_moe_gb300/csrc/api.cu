@@ -75,6 +75,7 @@ static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 
 struct Geometry {
     int H, I, E, k, g, Is, r, tp;
+    int fmt;         // FT_FORMAT_*
     int Il, Isl;     // rank-local intermediate sizes (routed, shared)
     int rb, sb;      // first intermediate column of the rank's range (routed, shared)
 };
@@ -88,7 +89,13 @@ static ft_status check_config(const ft_moe_config *cfg, Geometry &G)
         return fail(FT_ERR_INVALID_ARG, "config fields must be positive and 0 <= tp_rank < tp_size");
     if (cfg->shard_size < 0 || cfg->shared_shard_size < 0)
         return fail(FT_ERR_INVALID_ARG, "shard sizes must be >= 0 (0 = even split by tp_rank/tp_size)");
-    if (G.g != 16 && G.g != 32) return fail(FT_ERR_UNSUPPORTED, "group must be 16 or 32 (got %d)", G.g);
+    G.fmt = cfg->format;
+    if (G.fmt != FT_FORMAT_NVFP4 && G.fmt != FT_FORMAT_FP8_BLOCK)
+        return fail(FT_ERR_INVALID_ARG, "unknown weight format %d", G.fmt);
+    if (G.fmt == FT_FORMAT_FP8_BLOCK && G.g != 128)
+        return fail(FT_ERR_UNSUPPORTED, "fp8_block needs group = 128 (its scale block; got %d)", G.g);
+    if (G.fmt == FT_FORMAT_NVFP4 && G.g != 16 && G.g != 32)
+        return fail(FT_ERR_UNSUPPORTED, "group must be 16 or 32 (got %d)", G.g);
     if (G.E > 1024 || G.k > 32 || G.k > G.E)
         return fail(FT_ERR_UNSUPPORTED, "need top_k <= 32, top_k <= num_experts <= 1024");
     if (G.H % G.g || G.H % 2)
@@ -139,6 +146,15 @@ static void spec(ft_bank_spec &s, int dtype, int64_t a, int64_t b, int64_t c, in
 static void bank_specs(const Geometry &G, int shared, ft_bank_spec out[FT_NBANKS])
 {
     const int64_t E = shared ? 1 : G.E, Il = shared ? G.Isl : G.Il;
+    if (G.fmt == FT_FORMAT_FP8_BLOCK) {
+        spec(out[FT_GU], FT_DTYPE_U8, E, 2 * Il, G.H, 3);
+        spec(out[FT_GU_SCALE], FT_DTYPE_F32, E, 2 * Il / 128, G.H / 128, 3);
+        spec(out[FT_GU_GLOBAL], FT_DTYPE_F32, 0, 0, 0, 2);
+        spec(out[FT_DN], FT_DTYPE_U8, E, G.H, Il, 3);
+        spec(out[FT_DN_SCALE], FT_DTYPE_F32, E, G.H / 128, Il / 128, 3);
+        spec(out[FT_DN_GLOBAL], FT_DTYPE_F32, 0, 0, 0, 2);
+        return;
+    }
     spec(out[FT_GU], FT_DTYPE_U8, E, 2 * Il, G.H / 2, 3);
     spec(out[FT_GU_SCALE], FT_DTYPE_E4M3, E, 2 * Il, G.H / G.g, 3);
     spec(out[FT_GU_GLOBAL], FT_DTYPE_F32, E, 2 * Il, 0, 2);
@@ -244,11 +260,14 @@ static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, 
                  : launch_gemv_down(p, ks2, max_blocks * p.n_tiles, s);
 }
 
-static bool banks_ok(const ft_moe_banks *b)
+static bool banks_ok(const ft_moe_banks *b, int fmt = FT_FORMAT_NVFP4)
 {
     if (!b) return false;
-    for (int i = 0; i < FT_NBANKS; ++i)
+    for (int i = 0; i < FT_NBANKS; ++i) {
+        const bool none = fmt == FT_FORMAT_FP8_BLOCK && (i == FT_GU_GLOBAL || i == FT_DN_GLOBAL);
+        if (none) continue;  // fp8_block has no globals: the pointer is not read
         if (!b->p[i] || !aligned(b->p[i], 16)) return false;
+    }
     return true;
 }
 
@@ -313,18 +332,23 @@ ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pie
     if (st) return st;
     if (shared != 0 && shared != 1) return fail(FT_ERR_INVALID_ARG, "shared must be 0 or 1");
     if (shared && G.Is == 0) return fail(FT_ERR_UNSUPPORTED, "layer has no shared expert");
-    if (!src || !src->gate || !src->gate_scale || !src->gate_global || !src->up || !src->up_scale ||
-        !src->up_global || !src->down || !src->down_scale || !src->down_global)
+    const bool fp8 = G.fmt == FT_FORMAT_FP8_BLOCK;
+    if (!src || !src->gate || !src->gate_scale || !src->up || !src->up_scale || !src->down || !src->down_scale ||
+        (!fp8 && (!src->gate_global || !src->up_global || !src->down_global)))
         return fail(FT_ERR_INVALID_ARG, "a source piece is NULL");
-    if (!banks_ok(dst)) return fail(FT_ERR_INVALID_ARG, "destination banks must be non-NULL and 16-byte aligned");
+    if (!banks_ok(dst, G.fmt))
+        return fail(FT_ERR_INVALID_ARG, "destination banks must be non-NULL and 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the rank's range [b0, b0 + Il) of the intermediate dimension (even or explicit split)
     const size_t E = shared ? 1 : G.E, I = shared ? G.Is : G.I, Il = shared ? G.Isl : G.Il, H = G.H, g = G.g;
     const size_t b0 = shared ? G.sb : G.rb;
     ft_bank_spec specs[FT_NBANKS];
     bank_specs(G, shared, specs);
-    const size_t src_bytes[9] = {E * I * H / 2, E * I * H / g, E * I * 4, E * I * H / 2, E * I * H / g, E * I * 4,
-                                 E * H * I / 2, E * H * I / g, E * H * 4};
+    // fp8_block: one code byte per weight, fp32 scale_inv per 128 x 128 block, no globals
+    const size_t sblk = (I / 128) * (H / 128) * 4;
+    const size_t src_bytes[9] = {fp8 ? E * I * H : E * I * H / 2, fp8 ? E * sblk : E * I * H / g, fp8 ? 0 : E * I * 4,
+                                 fp8 ? E * I * H : E * I * H / 2, fp8 ? E * sblk : E * I * H / g, fp8 ? 0 : E * I * 4,
+                                 fp8 ? E * H * I : E * H * I / 2, fp8 ? E * sblk : E * H * I / g, fp8 ? 0 : E * H * 4};
     const void *srcs[9] = {src->gate, src->gate_scale, src->gate_global, src->up, src->up_scale,
                            src->up_global, src->down, src->down_scale, src->down_global};
     if (src->on_device) {
@@ -336,6 +360,17 @@ ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pie
     struct Copy { const void *s; size_t sp; void *d; size_t dp; size_t w; size_t h; };
     auto u8 = [](const void *p, size_t off) { return static_cast<const uint8_t *>(p) + off; };
     auto w8 = [](void *p, size_t off) { return static_cast<uint8_t *>(p) + off; };
+    const size_t hb = H / 128, lb = Il / 128, ib = I / 128;
+    const Copy copies_fp8[6] = {
+        {u8(src->gate, b0 * H), I * H, w8(dst->p[FT_GU], 0), 2 * Il * H, Il * H, E},
+        {u8(src->up, b0 * H), I * H, w8(dst->p[FT_GU], Il * H), 2 * Il * H, Il * H, E},
+        {u8(src->gate_scale, (b0 / 128) * hb * 4), ib * hb * 4, w8(dst->p[FT_GU_SCALE], 0), 2 * lb * hb * 4,
+         lb * hb * 4, E},
+        {u8(src->up_scale, (b0 / 128) * hb * 4), ib * hb * 4, w8(dst->p[FT_GU_SCALE], lb * hb * 4), 2 * lb * hb * 4,
+         lb * hb * 4, E},
+        {u8(src->down, b0), I, w8(dst->p[FT_DN], 0), Il, Il, E * H},
+        {u8(src->down_scale, (b0 / 128) * 4), ib * 4, w8(dst->p[FT_DN_SCALE], 0), lb * 4, lb * 4, E * hb},
+    };
     const Copy copies[9] = {
         {u8(src->gate, b0 * H / 2), I * H / 2, w8(dst->p[FT_GU], 0), 2 * Il * H / 2, Il * H / 2, E},
         {u8(src->up, b0 * H / 2), I * H / 2, w8(dst->p[FT_GU], Il * H / 2), 2 * Il * H / 2, Il * H / 2, E},
@@ -348,7 +383,10 @@ ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pie
         {u8(src->down_scale, b0 / g), I / g, w8(dst->p[FT_DN_SCALE], 0), Il / g, Il / g, E * H},
         {u8(src->down_global, 0), E * H * 4, w8(dst->p[FT_DN_GLOBAL], 0), E * H * 4, E * H * 4, 1},
     };
-    for (const Copy &c : copies) {
+    const Copy *list = fp8 ? copies_fp8 : copies;
+    const int n_copies = fp8 ? 6 : 9;
+    for (int ci = 0; ci < n_copies; ++ci) {
+        const Copy &c = list[ci];
         cudaError_t e;
         if (src->on_device)
             e = launch_pack_copy2d(static_cast<const uint8_t *>(c.s), c.sp, static_cast<uint8_t *>(c.d), c.dp, c.w,
@@ -432,8 +470,9 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     if (T < 0 || T > (1 << 20)) return fail(FT_ERR_UNSUPPORTED, "T must be in [0, 2^20]");
     if (out_dtype != FT_DTYPE_BF16 && out_dtype != FT_DTYPE_F32)
         return fail(FT_ERR_INVALID_ARG, "out_dtype must be FT_DTYPE_BF16 or FT_DTYPE_F32");
-    if (!banks_ok(routed)) return fail(FT_ERR_INVALID_ARG, "routed banks must be non-NULL and 16-byte aligned");
-    if (G.Is > 0 && !banks_ok(shared))
+    if (!banks_ok(routed, G.fmt))
+        return fail(FT_ERR_INVALID_ARG, "routed banks must be non-NULL and 16-byte aligned");
+    if (G.Is > 0 && !banks_ok(shared, G.fmt))
         return fail(FT_ERR_INVALID_ARG, "shared banks required (shared_intermediate > 0), 16-byte aligned");
     if (G.Is == 0 && shared) return fail(FT_ERR_INVALID_ARG, "shared banks given but shared_intermediate is 0");
     if (T == 0) return ok();
@@ -463,6 +502,87 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
 
     auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
+    if (G.fmt == FT_FORMAT_FP8_BLOCK) {
+        // ---------------------------------------------------------------- fp8_block experts
+        // register-fed grouped GEMV for every batch size: align, gate_up (+ shared), down
+        // (+ shared) with the routing weight and the fused ordered combine
+        e = launch_align(topk_ids, T, G.k, G.E, kGemvBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s,
+                         status, L.zero_bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "align launch");
+        const int max_blocks = (int)(((int64_t)n_slots + (n_slots < G.E ? n_slots : G.E) * (kGemvBlock - 1)) /
+                                     kGemvBlock);
+        const int tpad = cdiv(T, kGemvBlock);
+        auto problem = [&](const ft_moe_banks *b, bool gated, int E, int Il) {
+            GemvParams p = {};
+            p.codes = static_cast<const uint8_t *>(b->p[gated ? FT_GU : FT_DN]);
+            p.sinv = static_cast<const float *>(b->p[gated ? FT_GU_SCALE : FT_DN_SCALE]);
+            p.R = gated ? 2 * Il : G.H;
+            p.K = gated ? G.H : Il;
+            p.e_codes = (int64_t)p.R * p.K;
+            p.e_sinv = (int64_t)(p.R / 128) * (p.K / 128);
+            p.group = 128;
+            p.up_off = gated ? Il : 0;
+            p.num_experts = E;
+            p.status = status;
+            return p;
+        };
+        GemvParams gu = problem(routed, true, G.E, G.Il), dn = problem(routed, false, G.E, G.Il);
+        gu.act = static_cast<const uint16_t *>(x);
+        gu.h_out = h; gu.h_ld = G.Il;
+        dn.act = h; dn.y_out = y; dn.route_w = topk_w;
+        for (GemvParams *p : {&gu, &dn}) {
+            p->n_pos_dev = npad; p->sorted_slot = sorted; p->block_expert = bexp;
+            p->n_slots = n_slots; p->top_k = G.k;
+        }
+        GemvParams gu_sh = {}, dn_sh = {};
+        if (G.Is) {
+            gu_sh = problem(shared, true, 1, G.Isl);
+            dn_sh = problem(shared, false, 1, G.Isl);
+            gu_sh.act = static_cast<const uint16_t *>(x);
+            gu_sh.h_out = h_sh; gu_sh.h_ld = G.Isl;
+            dn_sh.act = h_sh; dn_sh.y_out = y_sh;
+            for (GemvParams *p : {&gu_sh, &dn_sh}) {
+                p->n_pos_static = T; p->n_slots = T; p->top_k = 1;
+            }
+        }
+        const int kmax_l = G.Il > G.Isl ? G.Il : G.Isl;
+        int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(kmax_l, 16 * 8), G.H);
+        int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
+        if (!gemv_fp8_ok(G.H, ks_gu)) ks_gu = 1;
+        if (!gemv_fp8_ok(G.Il, ks_dn) || (G.Is && !gemv_fp8_ok(G.Isl, ks_dn))) ks_dn = 1;
+        FastLaunch F = {};
+        F.prob[0] = gu;
+        F.prob[0].n_tiles = cdiv(G.Il, 16 * (8 / ks_gu));
+        F.nprob = 1;
+        if (G.Is) {
+            F.prob[1] = gu_sh;
+            F.prob[1].n_tiles = cdiv(G.Isl, 16 * (8 / ks_gu));
+            F.nprob = 2;
+        }
+        if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        int max_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
+        if ((e = launch_gemv_fp8(F, true, ks_gu, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
+        if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        FastLaunch D = {};
+        D.prob[0] = dn;
+        D.prob[0].n_tiles = cdiv(G.H, 32 * (8 / ks_dn));
+        D.nprob = 1;
+        if (G.Is) {
+            D.prob[1] = dn_sh;
+            D.prob[1].n_tiles = D.prob[0].n_tiles;
+            D.nprob = 2;
+        }
+        D.counters = reinterpret_cast<int *>(ws + L.counters);
+        D.combine_target = G.k + (G.Is ? 1 : 0);
+        D.y = y; D.y_sh = G.Is ? y_sh : nullptr; D.out = out; D.out_dtype = out_dtype;
+        D.T = T; D.H = G.H; D.k = G.k;
+        if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
+        if ((e = launch_gemv_fp8(D, false, ks_dn, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
+        for (int st = FT_STAGE_SHARED_DOWN; st <= FT_NSTAGES; ++st)
+            if ((e = stage_mark(st, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        return ok();
+    }
     if (use_tc(G, T)) {
         // ---------------------------------------------------------------- tensor-core path
         e = launch_align(topk_ids, T, G.k, G.E, kTcBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s,
@@ -739,6 +859,7 @@ ft_status ft_moe_dequant(const ft_moe_config *cfg, int32_t shared, const ft_moe_
     if (st) return st;
     if (shared != 0 && shared != 1) return fail(FT_ERR_INVALID_ARG, "shared must be 0 or 1");
     if (shared && G.Is == 0) return fail(FT_ERR_UNSUPPORTED, "layer has no shared expert");
+    if (G.fmt != FT_FORMAT_NVFP4) return fail(FT_ERR_UNSUPPORTED, "dequant export is for NVFP4 banks");
     if (!banks_ok(banks) || !out_bf16 || !aligned(out_bf16, 16))
         return fail(FT_ERR_INVALID_ARG, "banks and out must be non-NULL and 16-byte aligned");
     const int E = shared ? 1 : G.E, Il = shared ? G.Isl : G.Il;

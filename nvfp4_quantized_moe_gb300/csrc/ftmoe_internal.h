@@ -42,6 +42,8 @@ struct GemvParams {
     float *y_out;            // down: f32 [n_slots][R]
     const float *route_w;    // down, routed: [T*k]; nullptr = weight 1
     int *status;
+    const float *sinv;       // fp8_block: scale_inv [E][R/128][K/128] (codes are then [E][R][K])
+    int64_t e_sinv;          // fp8_block: per-expert stride of sinv (elements)
 };
 
 // Positions per block (the MMA N side) of the tensor-core prefill path.
@@ -154,6 +156,11 @@ struct FastLaunch {
     int out_dtype, T, H, k;
 };
 cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
+
+// fp8_block grouped GEMV (register-fed, any batch size): K a whole number of 128-element
+// scale blocks per warp's share.
+bool gemv_fp8_ok(int K, int ks);
+cudaError_t launch_gemv_fp8(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
 
 // Tensor-core decode GEMV (A operand dequantised into tensor memory, one persistent CTA
 // per SM). Units per block: prob[i].n_tiles = ceil(I/128) for gate_up, ceil(H/256) for down.

@@ -1,0 +1,311 @@
+// Grouped GEMV for fp8_block experts (every batch size): W[n][k] = e4m3(code[n][k]) *
+// scale_inv[n/128][k/128], one code byte per weight ("feat(qwen3_5_moe): tensor-parallel
+// weight sharding", Implementation notes: an fp8-block weight carries a 128-block
+// weight_scale_inv; the dsv4 PR, Checkpoint loading: FP8 128x128 blocks).
+//
+// Structure of the register-fed NVFP4 decode kernel: weights as M, a block of 8
+// expert-sorted positions as N, m16n8k16 f16 MMAs with fp32 accumulation, each warp
+// owning two 16-row tiles (gate rows i and up rows I_l + i for gate_up, so SwiGLU fuses;
+// rows n and n + 16 for down), loads running two steps ahead through a 4-slot register
+// ring, routed and shared expert in one launch, fused ordered combine in the down stage.
+// What differs:
+//  * a step is 64 K elements: lane (g, c) loads 16 code bytes of rows g and g + 8 of
+//    each tile (K elements 16c .. 16c + 15 of the step); e4m3 converts to f16 exactly
+//    (cvt.rn.f16x2.e4m3x2), two codes per instruction, with no scale multiply;
+//  * the 16 K elements of a lane are spread over the step's four MMAs (MMA j takes
+//    16c + 4j .. 16c + 4j + 3 of every lane c), the same permutation of K for both
+//    operands, so the activations are read as two contiguous 16-byte pieces per lane;
+//  * a 16-row tile lies inside one 128-row scale block and two steps make one 128-K
+//    block, so each tile accumulates a block's MMAs into a fresh fp32 partial that is
+//    added to the running sum times the block's scale_inv (exact fp32 arithmetic; no
+//    global, and nothing folded into the f16 operands);
+//  * activation rows are staged (f16, scaled by a power of two per row, as in the
+//    NVFP4 kernels) with a 16-byte row padding that makes the reads conflict-free.
+#include <cuda_runtime.h>
+
+#include "ftmoe_device.cuh"
+#include "ftmoe_internal.h"
+#include "gemv_common.cuh"
+
+namespace ftmoe {
+
+using namespace gemv;
+
+namespace {
+
+constexpr int kStep8 = 64;  // K elements per warp step
+
+struct Fp8Frag {
+    uint4 a_lo, a_hi, b_lo, b_hi;  // codes: tile 0 rows g / g+8, tile 1 rows g / g+8
+};
+
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_bytes)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(two_bytes));
+    return h2;
+}
+
+// The four MMAs of one step for one tile: word j of each row's 16 code bytes holds the
+// K elements 4j .. 4j + 3 of the lane's range; the activations of token g for the same
+// elements are words 2j, 2j + 1 of b.
+__device__ __forceinline__ void fp8_tile_step(const uint4 &lo, const uint4 &hi, const uint32_t (&b)[8],
+                                              float (&acc)[4])
+{
+    const uint32_t cl[4] = {lo.x, lo.y, lo.z, lo.w};
+    const uint32_t ch[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t a0 = e4m3x2_f16x2(cl[j]), a2 = e4m3x2_f16x2(cl[j] >> 16);
+        const uint32_t a1 = e4m3x2_f16x2(ch[j]), a3 = e4m3x2_f16x2(ch[j] >> 16);
+        mma_f16_16816(acc, a0, a1, a2, a3, b[2 * j], b[2 * j + 1]);
+    }
+}
+
+// Stage the block's 8 activation rows: f16 of x * 2^-e_r (row maximum in [2^14, 2^15)),
+// row pitch K + 8 elements; inv[r] = 2^e_r (0 for padding rows, which are zero).
+__device__ __forceinline__ void fp8_stage(const GemvParams &p, int blk, int n_pos, bool gated, int *rows,
+                                          uint4 *sm, float *inv)
+{
+    __syncthreads();
+    if (threadIdx.x < kGemvBlock) rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, gated);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, K = p.K, pitch = K / 8 + 1;
+    for (int r = threadIdx.x >> 5; r < kGemvBlock; r += blockDim.x >> 5) {
+        const int row = rows[r];
+        uint4 *dst = sm + (size_t)r * pitch;
+        if (row < 0) {
+            for (int q = lane; q < K / 8; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
+            if (lane == 0) inv[r] = 0.f;
+            continue;
+        }
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(p.act + (size_t)row * K);
+        float m = 0.f;
+        for (int q = lane; q < K / 8; q += 32) {
+            const uint4 v = __ldg(s4 + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        const int e = row_scale_exp(m);
+        const float down = pow2f(-e);
+        for (int q = lane; q < K / 8; q += 32) {
+            const uint4 v = __ldg(s4 + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half2 hh = __floats2half2_rn(__uint_as_float(w[i] << 16) * down,
+                                                     __uint_as_float(w[i] & 0xFFFF0000u) * down);
+                h[i] = *reinterpret_cast<const uint32_t *>(&hh);
+            }
+            dst[q] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        if (lane == 0) inv[r] = pow2f(e);
+    }
+    __syncthreads();
+}
+
+// One unit: block `blk` of problem p, pair tiles (group `grp` of TPW per CTA) over the
+// warp's K range (K split KS ways across the CTA's warps, partials added in warp order).
+template <bool GATED, int KS>
+__device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &L, int lu, int n_pos,
+                                         const uint4 *smem_b, const float *inv,
+                                         float (&red)[KS > 1 ? 8 : 1][32][8])
+{
+    constexpr int TPW = 8 / KS;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ks = warp % KS, tp = warp / KS;
+    const int g = lane >> 2, c = lane & 3;
+    const int K = p.K, kb_n = K / 128;
+    const int blk = lu / p.n_tiles, grp = lu - blk * p.n_tiles;
+    const int Kw = K / KS, k0 = ks * Kw, nstep = Kw / kStep8;
+    const int pair_rows = GATED ? 16 : 32;
+    const int rows_limit = GATED ? p.up_off : p.R;
+    const int r0 = (grp * TPW + tp) * pair_rows;
+    const bool ok = r0 < rows_limit;
+    const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+        const int row_a = r0 + g, row_b = GATED ? p.up_off + r0 + g : r0 + 16 + g;
+        const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
+        const uint8_t *ca = codes_e + (size_t)row_a * K + k0 + 16 * c;
+        const uint8_t *cb = codes_e + (size_t)row_b * K + k0 + 16 * c;
+        const size_t row8 = (size_t)8 * K;
+        // scale_inv rows of the two tiles (each tile lies inside one 128-row block)
+        const float *sinv_e = p.sinv + (size_t)e * p.e_sinv;
+        const float *sa = sinv_e + (size_t)((r0) / 128) * kb_n + k0 / 128;
+        const float *sb = sinv_e + (size_t)((GATED ? p.up_off + r0 : r0 + 16) / 128) * kb_n + k0 / 128;
+        const uint4 *bb = smem_b + (size_t)g * (K / 8 + 1) + k0 / 8 + 2 * c;
+        auto load = [&](int s, Fp8Frag &f) {
+            const int off = s * kStep8;
+            f.a_lo = ldg_nc_v4(ca + off);
+            f.a_hi = ldg_nc_v4(ca + row8 + off);
+            f.b_lo = ldg_nc_v4(cb + off);
+            f.b_hi = ldg_nc_v4(cb + row8 + off);
+        };
+        float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};  // current 128-K block
+        Fp8Frag ring[4];
+        load(0, ring[0]);
+        if (nstep > 1) load(1, ring[1]);
+        for (int s0 = 0; s0 < nstep; s0 += 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int s = s0 + q;
+                if (s + 2 < nstep) load(s + 2, ring[(q + 2) & 3]);
+                if (s < nstep) {
+                    const uint4 x0 = bb[8 * s], x1 = bb[8 * s + 1];
+                    const uint32_t b[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    fp8_tile_step(ring[q].a_lo, ring[q].a_hi, b, t0);
+                    fp8_tile_step(ring[q].b_lo, ring[q].b_hi, b, t1);
+                    if (q & 1) {  // end of a 128-K block (steps are 64 K; the warp range is block-aligned)
+                        const float fa = __ldg(sa + (s >> 1)), fb = __ldg(sb + (s >> 1));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc0[i] = fmaf(fa, t0[i], acc0[i]);
+                            acc1[i] = fmaf(fb, t1[i], acc1[i]);
+                            t0[i] = 0.f;
+                            t1[i] = 0.f;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (KS > 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            red[warp][lane][i] = acc0[i];
+            red[warp][lane][4 + i] = acc1[i];
+        }
+        __syncthreads();
+    }
+    if (ks == 0 && ok) {
+        if (KS > 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float a = 0.f, b2 = 0.f;
+                for (int w = 0; w < KS; ++w) {
+                    a += red[tp * KS + w][lane][i];
+                    b2 += red[tp * KS + w][lane][4 + i];
+                }
+                acc0[i] = a;
+                acc1[i] = b2;
+            }
+        }
+        if (GATED) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int i = r0 + g + 8 * half;
+#pragma unroll
+                for (int col = 0; col < 2; ++col) {
+                    const int pos = blk * kGemvBlock + 2 * c + col;
+                    const float scl = inv[2 * c + col];
+                    const float gate = acc0[2 * half + col] * scl, up = acc1[2 * half + col] * scl;
+                    __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
+                    p.h_out[(size_t)pos * p.h_ld + i] = *reinterpret_cast<uint16_t *>(&hv);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int col = 0; col < 2; ++col) {
+                const int pos = blk * kGemvBlock + 2 * c + col;
+                if (pos >= n_pos) continue;
+                int dst;
+                float wgt = inv[2 * c + col];
+                if (p.sorted_slot) {
+                    dst = __ldg(p.sorted_slot + pos);
+                    if (dst >= p.n_slots) continue;
+                    if (p.route_w) wgt *= __ldg(p.route_w + dst);
+                } else {
+                    dst = pos;
+                    if (dst >= p.n_pos_static) continue;
+                }
+                float *yrow = p.y_out + (size_t)dst * p.R;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int n = r0 + g + 8 * half;
+                    yrow[n] = acc0[2 * half + col] * wgt;
+                    yrow[n + 16] = acc1[2 * half + col] * wgt;
+                }
+            }
+            if (L.counters) fused_combine(p, L, blk, n_pos, r0, 0xFFu);
+        }
+    }
+    if (KS > 1) __syncthreads();
+}
+
+template <bool GATED, int KS>
+__global__ void __launch_bounds__(kThreads, 2) gemv_fp8_kernel(const __grid_constant__ FastLaunch L)
+{
+    pdl_enter();
+    extern __shared__ uint4 smem_b[];
+    __shared__ float inv[kGemvBlock];
+    __shared__ int rows[kGemvBlock];
+    __shared__ float red[KS > 1 ? 8 : 1][32][8];
+    const int n_pos0 = load_n_pos(L.prob[0]);
+    const int n_pos1 = L.nprob > 1 ? load_n_pos(L.prob[1]) : 0;
+    const int units0 = (n_pos0 / kGemvBlock) * L.prob[0].n_tiles;
+    const int units1 = L.nprob > 1 ? (n_pos1 / kGemvBlock) * L.prob[1].n_tiles : 0;
+    const int n_units = units0 + units1;
+    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    int staged = -1;
+    for (int u = u_lo; u < u_hi; ++u) {
+        const int pi = u < units0 ? 0 : 1;
+        const GemvParams &p = L.prob[pi];
+        const int lu = pi ? u - units0 : u;
+        const int n_pos = pi ? n_pos1 : n_pos0;
+        const int blk = lu / p.n_tiles;
+        const int key = pi * (1 << 30) + blk;
+        if (key != staged) {
+            fp8_stage(p, blk, n_pos, GATED, rows, smem_b, inv);
+            staged = key;
+        }
+        fp8_unit<GATED, KS>(p, L, lu, n_pos, smem_b, inv, red);
+    }
+}
+
+template <bool GATED, int KS>
+static cudaError_t launch_fp8_t(const FastLaunch &L, int max_units, cudaStream_t s)
+{
+    auto kern = gemv_fp8_kernel<GATED, KS>;
+    const int Kmax = L.nprob > 1 && L.prob[1].K > L.prob[0].K ? L.prob[1].K : L.prob[0].K;
+    const size_t smem = (size_t)kGemvBlock * (Kmax + 8) * 2;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int grid = sm_count() * 2;
+    if (max_units < grid) grid = max_units;
+    if (grid < 1) grid = 1;
+    FT_LAUNCH(kern, dim3(grid), dim3(kThreads), smem, s, L);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// K a multiple of 128 (one scale block) and each warp's share of K a whole number of blocks.
+bool gemv_fp8_ok(int K, int ks) { return K % 128 == 0 && (K / ks) % 128 == 0; }
+
+cudaError_t launch_gemv_fp8(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s)
+{
+    if (gated) {
+        switch (ks) {
+        case 1: return launch_fp8_t<true, 1>(L, max_units, s);
+        case 2: return launch_fp8_t<true, 2>(L, max_units, s);
+        case 4: return launch_fp8_t<true, 4>(L, max_units, s);
+        default: return launch_fp8_t<true, 8>(L, max_units, s);
+        }
+    }
+    switch (ks) {
+    case 1: return launch_fp8_t<false, 1>(L, max_units, s);
+    case 2: return launch_fp8_t<false, 2>(L, max_units, s);
+    case 4: return launch_fp8_t<false, 4>(L, max_units, s);
+    default: return launch_fp8_t<false, 8>(L, max_units, s);
+    }
+}
+
+}  // namespace ftmoe

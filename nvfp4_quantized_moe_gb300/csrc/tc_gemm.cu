@@ -10,9 +10,10 @@
 //               reads them from the expert-sorted f16 copy of x, down from the f16 copy
 //               of h; each activation row carries a power-of-two scale (see
 //               rows_to_f16_kernel) that the epilogue multiplies back;
-//   warp 1      allocates tensor memory and from one thread issues tcgen05.mma
+//   warps 1, 14 warp 1 allocates tensor memory; one thread of each issues tcgen05.mma
 //               (kind::f16, f16 x f16 -> fp32, M = 128, N = 128, K = 16 per
-//               instruction, two per K step) and commits to the stage barriers;
+//               instruction) for one of the two tiles (the issue cost is per issuing
+//               thread) and commits to the stage barriers, which count both issuers;
 //   warps 2..9  dequantise the raw codes to the exact f16 code*scale (each thread reads
 //               its row's block scales from global memory, 16 bytes a group ahead), written in the
 //               128-byte swizzled K-major layout the MMA descriptors describe (warp
@@ -45,7 +46,9 @@ constexpr int MT = 128;       // weight rows per tile (MMA M)
 constexpr int KC = 64;        // K elements per chunk (128 bytes of f16)
 constexpr int NSMAX = 4;      // TMA stages (at most)
 constexpr int NA = 4;         // dequantised A buffers
-constexpr int kThreadsTc = 448;  // producer, MMA, 8 dequant warps, 4 epilogue warps
+constexpr int kThreadsTc = 480;  // producer, MMA (tile 0), 8 dequant, 4 epilogue, MMA (tile 1)
+constexpr int kMmaWarp1 = 14;    // issuer of tile 1: the issue cost of a tcgen05.mma is per
+                                 // issuing thread, so one issuer per tile doubles the rate
 constexpr int kDq = 256;         // dequantising threads
 constexpr int kEp = 128;         // epilogue threads (one TMEM lane each)
 constexpr int kEpWarp0 = 10;     // first epilogue warp
@@ -113,10 +116,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t tmem_cols = 4 * NT;  // two accumulators of two 128-column tiles
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSMAX; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 1); }
+        // a stage and an A buffer are released by both issuers' commits
+        for (int i = 0; i < NSMAX; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 2); }
         // consumer barriers count warps: each warp arrives once, from lane 0 after __syncwarp
-        for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq / 32); mbar_init(a_empty + i, 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEp / 32); }
+        for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq / 32); mbar_init(a_empty + i, 2); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 2); mbar_init(acc_empty + i, kEp / 32); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -164,16 +168,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 mbar_wait_timed(full + last % ns, (last / ns) & 1, nullptr);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == kMmaWarp1) {
+        // ------------------------------------------------------------ MMA issuers
         if (lane == 0) {
+            const uint32_t tile = warp == 1 ? 0u : 1u;  // this issuer's tile and accumulator half
             const uint32_t idesc = tc::idesc_f16_f32(MT, NT);
             int it = 0, ia = 0, uc = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
                 const int ab2 = uc & 1;  // accumulator of this unit
                 if (!wait_bar(acc_empty + ab2, ((uc >> 1) & 1) ^ 1, abort_flag)) { dead = true; break; }
                 tc::fence_after_sync();
-                const uint32_t acc = tmem + (uint32_t)(ab2 * 2 * NT);
+                const uint32_t acc = tmem + (uint32_t)(ab2 * 2 * NT) + tile * NT;
                 for (int c = 0; c < nk; ++c, ++it, ++ia) {
                     const int slot = it % ns, ab = ia % NA;
                     if (!wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
@@ -187,8 +192,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
                     for (int kk = 0; kk < KC / 16; ++kk) {
                         const uint64_t bd = tc::sw128_desc(b0 + kk * 32);
-                        tc::mma_f16(acc, tc::sw128_desc(a0 + kk * 32), bd, idesc, (c | kk) != 0);
-                        tc::mma_f16(acc + NT, tc::sw128_desc(a0 + MT * 128 + kk * 32), bd, idesc, (c | kk) != 0);
+                        tc::mma_f16(acc, tc::sw128_desc(a0 + tile * MT * 128 + kk * 32), bd, idesc, (c | kk) != 0);
                     }
                     tc::commit(empty + slot);
                     tc::commit(a_empty + ab);

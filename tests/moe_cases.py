@@ -21,8 +21,9 @@ ROUTE_W_RTOL = 1e-6   # routing weights (fp32 on the GPU vs fp64 oracle)
 @functools.lru_cache(maxsize=4)
 def pieces(shape_name: str, seed: int = 0):
     shape = synth.SHAPES[shape_name]
-    routed = synth.make_pieces(shape, seed)
-    shared = synth.make_pieces(shape, seed, shared=True) if shape.shared_intermediate else None
+    make = synth.make_fp8_pieces if shape.fmt == "fp8_block" else synth.make_pieces
+    routed = make(shape, seed)
+    shared = make(shape, seed, shared=True) if shape.shared_intermediate else None
     return routed, shared
 
 
@@ -36,6 +37,10 @@ def oracle_banks(shape_name: str, tp_rank: int = 0, tp_size: int = 1, seed: int 
     """Rank-local banks: even split (tp_rank of tp_size) or explicit (begin, size) ranges."""
     shape = synth.SHAPES[shape_name]
     routed, shared = pieces(shape_name, seed)
+    if shape.fmt == "fp8_block":
+        rb = oracle.slice_fp8_bank(routed, tp_rank, tp_size, shard=shard)
+        sb = oracle.slice_fp8_bank(shared, tp_rank, tp_size, shard=shared_shard) if shared is not None else None
+        return rb, sb
     rb = oracle.slice_bank(routed, shape.group, tp_rank, tp_size, shard=shard)
     sb = (oracle.slice_bank(shared, shape.group, tp_rank, tp_size, shard=shared_shard)
           if shared is not None else None)

@@ -70,6 +70,39 @@ def test_layout_follows_explicit_shard(ft):
     assert sa["gate_up"] == (1, 384, 1024) and sb["gate_up"] == (1, 640, 1024)
 
 
+def test_layout_fp8_block(ft):
+    """fp8_block banks: one code byte per weight, fp32 scale_inv per 128 x 128 block, no globals."""
+    c = ft.MoEConfig.of(synth.SHAPES["qwen36_fp8"], 1, 2)
+    got = {n: (tuple(sh), b) for n, sh, _, b in ft.ft_moe_layout(c, 0)}
+    assert got["gate_up"] == ((256, 512, 2048), 256 * 512 * 2048)
+    assert got["gate_up_scale"] == ((256, 4, 16), 256 * 4 * 16 * 4)
+    assert got["down"] == ((256, 2048, 256), 256 * 2048 * 256)
+    assert got["down_scale"] == ((256, 16, 2), 256 * 16 * 2 * 4)
+    assert got["gate_up_global"][1] == 0 and got["down_global"][1] == 0
+
+
+@pytest.mark.parametrize("fields,code", [
+    (dict(format=1), 3),                                   # fp8_block needs group 128
+    (dict(format=1, group=128, tp_size=4), 2),             # 512 / 4 = 128 is fine ...
+    (dict(format=1, group=128, intermediate=384, tp_size=2), 2),  # ... 192 is not whole 128-blocks
+    (dict(format=1, group=128, shard_begin=64, shard_size=128), 2),
+    (dict(format=7), 1),
+])
+def test_layout_rejects_bad_fp8_geometry(ft, fields, code):
+    base = dict(hidden=2048, intermediate=512, num_experts=256, top_k=8, group=16, shared_intermediate=512,
+                tp_rank=0, tp_size=1, shard_begin=0, shard_size=0, shared_shard_begin=0, shared_shard_size=0,
+                format=0)
+    base.update(fields)
+    cfg = ft.MoEConfig(*[base[n] for n, _ in ft.MoEConfig._fields_])
+    if fields.get("tp_size") == 4 and fields.get("intermediate") is None:
+        # shared 512 / 4 = 128 as well: valid
+        assert len(ft.ft_moe_layout(cfg, 0)) == 6
+        return
+    with pytest.raises(ft.FtMoeError) as ei:
+        ft.ft_moe_layout(cfg, 0)
+    assert ei.value.status == code
+
+
 @pytest.mark.parametrize("fields,code", [
     (dict(tp_size=3), 2),                      # 512 % 3
     (dict(tp_size=64), 2),                     # 512/64 = 8 not a multiple of 16
@@ -88,7 +121,8 @@ def test_layout_follows_explicit_shard(ft):
 ])
 def test_layout_rejects_bad_geometry(ft, fields, code):
     base = dict(hidden=2048, intermediate=512, num_experts=256, top_k=8, group=16, shared_intermediate=512,
-                tp_rank=0, tp_size=1, shard_begin=0, shard_size=0, shared_shard_begin=0, shared_shard_size=0)
+                tp_rank=0, tp_size=1, shard_begin=0, shard_size=0, shared_shard_begin=0, shared_shard_size=0,
+                format=0)
     base.update(fields)
     cfg = ft.MoEConfig(*[base[n] for n, _ in ft.MoEConfig._fields_])
     with pytest.raises(ft.FtMoeError) as ei:
