@@ -265,6 +265,93 @@ def measure_router(ft, dev, T, E=256, H=2048, reps=6):
             "tflops": 2.0 * T * E * H / (us * 1e-6) / 1e12, "l2": "512 MB written before every repetition"}
 
 
+def measure_fp8(ft, dev, T=64, L=16, reps=20, T_prefill=2048):
+    """fp8_block experts (the Qwen3.6-FP8 geometry): decode layer time over L distinct layer
+    copies (captured in a CUDA graph, inputs larger than L2) and one prefill layer."""
+    import torch
+    shape = synth.SHAPES["qwen36_fp8"]
+    cfg = ft.MoEConfig.of(shape)
+    H, E, k = shape.hidden, shape.num_experts, shape.top_k
+    routed = {n: torch.from_numpy(v).to(dev) for n, v in synth.make_fp8_pieces(shape, 0).items()}
+    shared = {n: torch.from_numpy(v).to(dev) for n, v in synth.make_fp8_pieces(shape, 0, shared=True).items()}
+    layers = []
+    for _ in range(L):
+        rb, sb = ft.alloc_banks(cfg, 0, dev), ft.alloc_banks(cfg, 1, dev)
+        ft.ft_moe_pack(cfg, 0, routed, rb)
+        ft.ft_moe_pack(cfg, 1, shared, sb)
+        layers.append((rb, sb))
+    del routed, shared
+    x = torch.from_numpy(np.stack([synth.make_activations(T, H, seed=l) for l in range(L)]).view(np.int16)).to(dev)
+    x = x.view(torch.bfloat16)
+    lg = torch.from_numpy(np.stack([synth.make_logits(T, E, seed=l) for l in range(L)])).to(dev)
+    ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
+    out = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(ft.ft_moe_workspace_size(cfg, T_prefill), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        for l in range(L):
+            ft.ft_moe_route(lg[l], k, ids[l], w[l])
+            ft.ft_moe_forward(cfg, layers[l][0], layers[l][1], x[l], ids[l], w[l], out[l], ws)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize(dev)
+    assert ft.ft_moe_read_status(ws) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for _ in range(3):
+            g.replay()
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        stop.record(stream)
+    torch.cuda.synchronize(dev)
+    us_layer = start.elapsed_time(stop) * 1e3 / (reps * L)
+    ids_np = ids.cpu().numpy()
+    per_expert = 2 * 512 * 2048 + 8 * 16 * 4 + 2048 * 512 + 16 * 4 * 4
+    layer_bytes = float(np.mean([(len(np.unique(ids_np[l])) + 1) * per_expert for l in range(L)]))
+    hbm, _, kind = _peaks()
+    decode = {"T": T, "layers": L, "us_per_layer": us_layer, "tokens_per_s": T / (us_layer * 1e-6),
+              "weight_gbs": layer_bytes / (us_layer * 1e-6) / 1e9,
+              "frac_of_hbm": layer_bytes / (us_layer * 1e-6) / 1e9 / hbm,
+              "weight_bytes_per_layer": layer_bytes, "bytes_per_expert": per_expert,
+              "peak_source": f"{kind} HBM copy bandwidth"}
+    # one prefill layer, L2 flushed before every repetition
+    xp = torch.from_numpy(synth.make_activations(T_prefill, H, seed=7).view(np.int16)).to(dev).view(torch.bfloat16)
+    lgp = torch.from_numpy(synth.zipf_logits(T_prefill, E, seed=7)).to(dev)
+    idp = torch.empty((T_prefill, k), dtype=torch.int32, device=dev)
+    wp = torch.empty((T_prefill, k), dtype=torch.float32, device=dev)
+    outp = torch.empty((T_prefill, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    cur = torch.cuda.current_stream(dev)
+    for r in range(6):
+        flush.fill_(r & 0xFF)
+        start.record(cur)
+        ft.ft_moe_route(lgp, k, idp, wp)
+        ft.ft_moe_forward(cfg, layers[0][0], layers[0][1], xp, idp, wp, outp, ws)
+        stop.record(cur)
+        torch.cuda.synchronize(dev)
+        if r >= 2:
+            times.append(start.elapsed_time(stop))
+    assert ft.ft_moe_read_status(ws) == 0
+    ms = float(np.median(times))
+    _, tfl, _ = _peaks()
+    flops = 56623104.0 * T_prefill
+    prefill = {"T": T_prefill, "routing": "zipf(1.1)", "us": ms * 1e3, "tokens_per_s": T_prefill / (ms / 1e3),
+               "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tfl,
+               "kernel": "register-fed grouped GEMV (no tensor-core fp8 prefill kernel yet)"}
+    del layers, flush
+    torch.cuda.empty_cache()
+    return {"format": "fp8_block (e4m3 weights, fp32 scale_inv per 128x128 block)", "decode": decode,
+            "prefill": prefill}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import nvfp4_quantized_moe_gb300 as ft
@@ -297,6 +384,7 @@ def run_ours(args, world, rank, local):
     if not args.no_prefill:
         prefill = [measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T_) for T_ in (2048, 8192)]
     router = [measure_router(ft, dev, T_) for T_ in (T, 2048)]
+    fp8 = None if args.no_fp8 else measure_fp8(ft, dev)
     del routed_d, shared_d
     x_host = [synth.make_activations(T, H, seed=l) for l in range(L)]
     lg_host = [synth.make_logits(T, E, seed=l) for l in range(L)]
@@ -432,7 +520,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline, "layer": {"us": layer_us, "touched_experts_mean": float(np.mean(touched)),
                                         "weight_bytes_mean": float(np.mean(layer_bytes)), "gbs": layer_gbs,
                                         "frac_of_hbm": layer_gbs / hbm},
-        "stage_us": stage_mean_us, "prefill": prefill, "router_gemm": router, "e2e": e2e,
+        "stage_us": stage_mean_us, "prefill": prefill, "router_gemm": router, "fp8_block": fp8, "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk.summary(),
     }
@@ -452,6 +540,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the fp8_block expert measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
