@@ -345,7 +345,7 @@ def measure_fp8(ft, dev, T=64, L=16, reps=20, T_prefill=2048):
     flops = 56623104.0 * T_prefill
     prefill = {"T": T_prefill, "routing": "zipf(1.1)", "us": ms * 1e3, "tokens_per_s": T_prefill / (ms / 1e3),
                "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tfl,
-               "kernel": "register-fed grouped GEMV (no tensor-core fp8 prefill kernel yet)"}
+               "kernel": "tcgen05 grouped GEMM (f16 operands, block scale folded into A per 128-row tile)"}
     del layers, flush
     torch.cuda.empty_cache()
     return {"format": "fp8_block (e4m3 weights, fp32 scale_inv per 128x128 block)", "decode": decode,

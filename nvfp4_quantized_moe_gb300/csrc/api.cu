@@ -173,6 +173,15 @@ static bool use_tc(const Geometry &G, int T)
     return true;
 }
 
+// The same for fp8_block banks (whole 128-row tiles, K a whole number of 128-blocks).
+static bool use_tc_fp8(const Geometry &G, int T)
+{
+    if ((int64_t)T * G.k < (int64_t)32 * G.E || G.H % 256) return false;
+    if (!tc_shape_ok_fp8(G.H, G.Il) || !tc_shape_ok_fp8(G.Il, G.H)) return false;
+    if (G.Is && (!tc_shape_ok_fp8(G.H, G.Isl) || !tc_shape_ok_fp8(G.Isl, G.H))) return false;
+    return true;
+}
+
 // Workspace regions of ft_moe_forward, each 256-byte aligned.
 struct WsLayout {
     size_t status, counters, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
@@ -203,7 +212,7 @@ static WsLayout ws_layout(const Geometry &G, int T)
     L.h_sh = take(G.Is ? 2 * (size_t)tpad * G.Isl : 0);
     L.y = take(4 * (size_t)n * G.H);
     L.y_sh = take(G.Is ? 4 * (size_t)T * G.H : 0);
-    const bool tc = use_tc(G, T);
+    const bool tc = G.fmt == FT_FORMAT_FP8_BLOCK ? use_tc_fp8(G, T) : use_tc(G, T);
     L.xs = take(tc ? 2 * (size_t)pmax * G.H : 0);
     L.xs_scale = take(tc ? 4 * (size_t)pmax : 0);
     L.x16 = take(tc && G.Is ? 2 * (size_t)tpad * G.H : 0);
@@ -502,7 +511,9 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
 
     auto cdiv = [](int a, int b) { return (a + b - 1) / b; };
-    if (G.fmt == FT_FORMAT_FP8_BLOCK) {
+    const bool fp8 = G.fmt == FT_FORMAT_FP8_BLOCK;
+    const bool tc_path = fp8 ? use_tc_fp8(G, T) : use_tc(G, T);
+    if (fp8 && !tc_path) {
         // ---------------------------------------------------------------- fp8_block experts
         // register-fed grouped GEMV for every batch size: align, gate_up (+ shared), down
         // (+ shared) with the routing weight and the fused ordered combine
@@ -583,8 +594,17 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             if ((e = stage_mark(st, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         return ok();
     }
-    if (use_tc(G, T)) {
+    if (tc_path) {
         // ---------------------------------------------------------------- tensor-core path
+        // fp8_block banks: codes of one byte, scale_inv per 128 x 128 block, no globals
+        auto fp8_fields = [&](TcParams &t, const ft_moe_banks *b, bool gate_up, int il) {
+            if (!fp8) return;
+            t.fp8 = 1;
+            t.sinv = static_cast<const float *>(b->p[gate_up ? FT_GU_SCALE : FT_DN_SCALE]);
+            t.e_sinv = gate_up ? (int64_t)(2 * il / 128) * (G.H / 128) : (int64_t)(G.H / 128) * (il / 128);
+            t.scales = nullptr;
+            t.glob = nullptr;
+        };
         e = launch_align(topk_ids, T, G.k, G.E, kTcBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s,
                          status, L.zero_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "align launch");
@@ -596,6 +616,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il; gp.n_mtiles = G.Il / 128;
         gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp; gp.n_slots = n_slots; gp.top_k = G.k;
         gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
+        fp8_fields(gp, routed, true, G.Il);
         if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         auto f16buf = [&](size_t off) { return reinterpret_cast<uint16_t *>(ws + off); };
         auto f32buf = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
@@ -615,6 +636,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
             sp.n_slots = T; sp.top_k = 1; sp.h_out = h_sh; sp.h_ld = G.Isl;
             sp.act_scale = f32buf(L.x16_scale);
+            fp8_fields(sp, shared, true, G.Isl);
             const int tp = tpad_tc * kTcBlock;
             e = launch_rows_to_f16(xb, G.H, nullptr, nullptr, tp, T, 1, tp, f16buf(L.x16), f32buf(L.x16_scale), s);
             if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
@@ -630,6 +652,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp; dp.n_slots = n_slots; dp.top_k = G.k;
         dp.y_out = yb; dp.y_ld = G.H; dp.route_w = topk_w; dp.status = status;
         dp.act_scale = f32buf(L.h16_scale);
+        fp8_fields(dp, routed, false, G.Il);
         // h rows are already in sorted-position order: convert them in place of a gather
         e = launch_rows_to_f16(h, G.Il, nullptr, npad, 0, L.pmax, 1, L.pmax, f16buf(L.h16), f32buf(L.h16_scale), s);
         if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
@@ -644,6 +667,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sd.K = G.Isl; sd.n_pos_dev = nullptr; sd.n_pos_static = T; sd.sorted_slot = nullptr;
             sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.y_out = yb_sh; sd.route_w = nullptr;
             sd.act_scale = f32buf(L.hsh16_scale);
+            fp8_fields(sd, shared, false, G.Isl);
             const int tp = tpad_tc * kTcBlock;
             e = launch_rows_to_f16(h_sh, G.Isl, nullptr, nullptr, tp, T, 1, tp, f16buf(L.hsh16),
                                    f32buf(L.hsh16_scale), s);

@@ -68,8 +68,12 @@ struct TcParams {
     const float *route_w;    // down, routed: [T*k]
     const float *act_scale;  // per position: factor that undoes the B rows' f16 scaling (or null)
     int *status;
+    int fp8;                 // fp8_block banks: codes [E][R][K] bytes, sinv below, no globals
+    const float *sinv;       // fp8_block: scale_inv [E][R/128][K/128]
+    int64_t e_sinv;          // fp8_block: per-expert stride of sinv (elements)
 };
 bool tc_shape_ok(int K, int group, int rows_per_expert);
+bool tc_shape_ok_fp8(int K, int rows_per_expert);
 size_t tc_smem_bytes(bool gated, int K, int group);
 // codes: the bank's packed codes (rows_total rows of K/2 bytes); act: the activation
 // matrix the B operand comes from (gate_up: x, act_rows = T; down: h, act_rows = its rows).

@@ -74,12 +74,16 @@ struct TcSmem {
     int ns;
 };
 
-__host__ __device__ inline TcSmem tc_smem(int K, int group, int ns)
+// Raw code bytes per weight row and 64-element K chunk: 32 (NVFP4, two codes a byte) or
+// 64 (fp8_block, one code a byte).
+__host__ __device__ constexpr uint32_t raw_row_bytes(bool fp8) { return fp8 ? 64u : 32u; }
+
+__host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8 = false)
 {
     TcSmem s;
     s.a_bytes = 2u * MT * 128;
     s.b_bytes = (uint32_t)NT * 128;
-    s.raw_bytes = 2u * MT * 32;
+    s.raw_bytes = 2u * MT * raw_row_bytes(fp8);
     (void)K;
     (void)group;
     s.ns = ns;
@@ -94,7 +98,12 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns)
 
 }  // namespace
 
-template <bool GATED>
+// FP8: fp8_block banks (one e4m3 code byte per weight, an fp32 scale_inv per 128 x 128
+// block, no globals). The dequantising warps then convert codes exactly to f16 and
+// multiply by f16(scale_inv * 2^-e_t), where 2^e_t is a power of two per 128-row tile
+// chosen from the tile's largest scale_inv so that every product stays below 2^15; the
+// epilogue multiplies 2^e_t back in place of the row global.
+template <bool GATED, bool FP8>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ TcParams p, int ns)
@@ -105,7 +114,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // compiler keeps every access derived from it in the shared state space
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int K = p.K;
-    const TcSmem L = tc_smem(K, p.group, ns);
+    const TcSmem L = tc_smem(K, p.group, ns, FP8);
+    constexpr int RB = (int)raw_row_bytes(FP8);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
     uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + 2;  // two accumulators
@@ -154,8 +164,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     if (!wait_bar(empty + slot, ((it / ns) & 1) ^ 1, abort_flag)) { dead = true; break; }
                     unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
                     mbar_arrive_expect_tx(full + slot, L.raw_bytes + L.b_bytes);
-                    tc::tma_load_2d(raw, &codes_map, c * 32, row_a, full + slot);
-                    tc::tma_load_2d(raw + MT * 32, &codes_map, c * 32, row_b, full + slot);
+                    tc::tma_load_2d(raw, &codes_map, c * RB, row_a, full + slot);
+                    tc::tma_load_2d(raw + MT * RB, &codes_map, c * RB, row_b, full + slot);
                     tc::tma_load_2d(smem + L.b_off + slot * L.b_bytes, &b_map, c * KC, b * NT, full + slot);
                 }
             }
@@ -202,6 +212,63 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             if (dead) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
         }
+    } else if (FP8 && warp < kEpWarp0) {
+        // ------------------------------------------------------------ dequantisation (fp8_block)
+        // warp (quarter, half): rows 32*quarter .. +32 of tile `half`; per chunk each thread
+        // converts the 64 code bytes of its row (read in the 64-byte swizzle of the TMA box:
+        // 16-byte piece j of row r sits at j ^ ((r >> 1) & 3), so 8 consecutive rows hit 8
+        // different bank quads) and writes 128 bytes of A.
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        const int r = 32 * quarter + lane;
+        const int kbn = K / 128;
+        int it = 0, ia = 0;
+        for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
+            const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
+            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+            const int nb = GATED ? (half ? p.up_off / MT : 0) + m : 2 * m + half;  // the tile's scale block row
+            const float *srow = p.sinv + (size_t)e * p.e_sinv + (size_t)nb * kbn;
+            float smax = 0.f;
+            for (int q = 0; q < kbn; ++q) smax = fmaxf(smax, __ldg(srow + q));
+            const float down = pow2f(-row_scale_exp(448.f * smax));
+            for (int c = 0; c < nk; ++c, ++it, ++ia) {
+                const int slot = it % ns, ab = ia % NA;
+                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
+                    !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag)) {
+                    dead = true;
+                    break;
+                }
+                const __half2 s2 = __float2half2_rn(__ldg(srow + (c >> 1)) * down);
+                const uint32_t sv = *reinterpret_cast<const uint32_t *>(&s2);
+                const unsigned char *rw = smem + L.raw_off + slot * L.raw_bytes + half * MT * RB + r * RB;
+                const int x = (r >> 1) & 3;
+                uint4 q[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4 *>(rw + ((j ^ x) << 4));
+                const uint32_t words[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
+                                            q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
+                unsigned char *arow = smem + L.a_off + ab * L.a_bytes + half * MT * 128 + r * 128;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {  // 16-byte piece w of the A row = code words 2w, 2w + 1
+                    uint32_t o[4];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint32_t cw = words[2 * w + h2];
+                        uint32_t lo, hi;
+                        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+                            : "=r"(lo) : "r"(cw));
+                        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+                            : "=r"(hi) : "r"(cw >> 16));
+                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * h2]) : "r"(lo), "r"(sv));
+                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * h2 + 1]) : "r"(hi), "r"(sv));
+                    }
+                    *reinterpret_cast<uint4 *>(arow + ((w ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) arrive(a_full + ab);
+            }
+        }
+        if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else if (warp < kEpWarp0) {
         // ------------------------------------------------------------ dequantisation
         // warp (quarter, half): rows 32*quarter .. +32 of tile `half`.
@@ -311,8 +378,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
             const float *glob_e = p.glob + (size_t)e * p.R;
             const int row0 = GATED ? m * MT + r : m * 2 * MT + r;
-            const float g0 = __ldg(glob_e + row0);
-            const float g1 = __ldg(glob_e + (GATED ? p.up_off + row0 : row0 + MT));
+            float g0, g1;
+            if constexpr (FP8) {
+                // 2^e_t of each tile, the inverse of the dequantising warps' factor
+                const int kbn = p.K / 128;
+                const int nb0 = GATED ? m : 2 * m, nb1 = GATED ? p.up_off / MT + m : 2 * m + 1;
+                const float *s0 = p.sinv + (size_t)e * p.e_sinv + (size_t)nb0 * kbn;
+                const float *s1 = p.sinv + (size_t)e * p.e_sinv + (size_t)nb1 * kbn;
+                float m0 = 0.f, m1 = 0.f;
+                for (int q = 0; q < kbn; ++q) {
+                    m0 = fmaxf(m0, __ldg(s0 + q));
+                    m1 = fmaxf(m1, __ldg(s1 + q));
+                }
+                g0 = pow2f(row_scale_exp(448.f * m0));
+                g1 = pow2f(row_scale_exp(448.f * m1));
+            } else {
+                g0 = __ldg(glob_e + row0);
+                g1 = __ldg(glob_e + (GATED ? p.up_off + row0 : row0 + MT));
+            }
             const int ab2 = uc & 1;
             if (!warp_wait_bar(acc_full + ab2, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
             tc::fence_after_sync();
@@ -444,19 +527,21 @@ bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ba
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tc_shape_ok_fp8(int K, int rows_per_expert) { return K % 128 == 0 && K >= 128 && rows_per_expert % MT == 0; }
+
 bool tc_shape_ok(int K, int group, int rows_per_expert)
 {
     return K % KC == 0 && K >= KC && rows_per_expert % MT == 0 && (K / group) % 16 == 0 && K / group <= 256;
 }
 
 // Deepest TMA ring (4, 3 or 2 stages) that fits the opt-in shared memory.
-static int tc_stages(int K, int group)
+static int tc_stages(int K, int group, bool fp8 = false)
 {
     int optin = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     for (int ns : {4, 3, 2})
-        if (tc_smem(K, group, ns).total + 1024 <= (uint32_t)optin) return ns;
+        if (tc_smem(K, group, ns, fp8).total + 1024 <= (uint32_t)optin) return ns;
     return 0;
 }
 
@@ -488,19 +573,24 @@ cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slo
 cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total,
                            const void *act, int64_t act_rows, int max_units, cudaStream_t s)
 {
-    const int ns = tc_stages(p.K, p.group);
+    const bool fp8 = p.fp8 != 0;
+    const int ns = tc_stages(p.K, p.group, fp8);
     if (!ns) return cudaErrorInvalidValue;
     CUtensorMap cmap, bmap;
-    if (!make_tensor_map_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)p.K / 2, (uint64_t)rows_total,
-                            (uint64_t)p.K / 2, 32, MT, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    // codes: NVFP4 rows of K/2 bytes in boxes of 32 bytes (no swizzle); fp8_block rows of K
+    // bytes in boxes of 64 bytes with the 64-byte swizzle the dequantising warps undo
+    const uint64_t row_bytes = fp8 ? (uint64_t)p.K : (uint64_t)p.K / 2;
+    if (!make_tensor_map_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, row_bytes, (uint64_t)rows_total, row_bytes,
+                            raw_row_bytes(fp8), MT, fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tensor_map_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, (uint64_t)p.K, (uint64_t)act_rows,
                             (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const size_t smem = tc_smem(p.K, p.group, ns).total + 1024;
+    const size_t smem = tc_smem(p.K, p.group, ns, fp8).total + 1024;
     int grid = sm_count();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
-    auto kern = gated ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    auto kern = fp8 ? (gated ? tc_gemm_kernel<true, true> : tc_gemm_kernel<false, true>)
+                    : (gated ? tc_gemm_kernel<true, false> : tc_gemm_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     FT_LAUNCH(kern, dim3(grid), dim3(kThreadsTc), smem, s, cmap, bmap, p, ns);
