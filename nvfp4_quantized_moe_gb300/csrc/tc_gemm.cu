@@ -1,28 +1,32 @@
-// Prefill-regime grouped GEMM for the NVFP4 experts on the 5th-generation tensor cores.
+// Prefill-regime grouped GEMM for the NVFP4 (and fp8_block) experts on the 5th-generation
+// tensor cores.
 //
 // A work unit is (block of NT = 128 expert-sorted positions, two tiles of 128 weight
 // rows): for gate_up the gate rows [i0, i0+128) and the matching up rows I_l + i0 + ..,
 // whose accumulators sit side by side in tensor memory so SwiGLU fuses into the
 // epilogue; for down the rows [n0, n0+256) as two tiles. Warp roles, persistent CTA:
 //   warp 0      one thread issues every TMA: per 64-element K chunk the raw packed
-//               codes of both tiles (box 32 bytes x 128 rows) and the block's
-//               activations (f16 box 64 x 128, 128-byte swizzled, K-major) -- gate_up
-//               reads them from the expert-sorted f16 copy of x, down from the f16 copy
-//               of h; each activation row carries a power-of-two scale (see
-//               rows_to_f16_kernel) that the epilogue multiplies back;
+//               codes of both tiles (box 32 bytes x 128 rows; fp8_block 64 bytes with the
+//               64-byte swizzle) and the block's activations (f16 box 64 x 128, 128-byte
+//               swizzled, K-major) -- gate_up reads them from the expert-sorted f16 copy of
+//               x, down from the f16 copy of h; each activation row carries a power-of-two
+//               scale (see rows_to_f16_kernel) that the epilogue multiplies back;
 //   warps 1, 14 warp 1 allocates tensor memory; one thread of each issues tcgen05.mma
-//               (kind::f16, f16 x f16 -> fp32, M = 128, N = 128, K = 16 per
-//               instruction) for one of the two tiles (the issue cost is per issuing
-//               thread) and commits to the stage barriers, which count both issuers;
+//               (kind::f16, A from tensor memory, B from shared memory, f16 x f16 -> fp32,
+//               M = 128, N = 128, K = 16) for one of the two tiles (the issue cost is per
+//               issuing thread) and commits to the barriers, which count both issuers;
 //   warps 2..9  dequantise the raw codes to the exact f16 code*scale (each thread reads
-//               its row's block scales from global memory, 16 bytes a group ahead), written in the
-//               128-byte swizzled K-major layout the MMA descriptors describe (warp
-//               half 0 tile 0, half 1 tile 1);
-//   warps 10-13 the epilogue: read an accumulator with tcgen05.ld (one TMEM lane = one
-//               weight row per thread), apply globals, row scales and SwiGLU or the
-//               routing weight, store. Tensor memory holds two accumulators (512
-//               columns), so the MMAs of the next unit run while the epilogue drains
-//               the previous one.
+//               its row's block scales from global memory, 16 bytes a group ahead) and
+//               write them straight into tensor memory with tcgen05.st (warp (quarter,
+//               half): TMEM lanes of its quarter, tile `half`) -- the A operand makes no
+//               round trip through shared memory;
+//   warps 10-13 the epilogue: read the accumulator with tcgen05.ld (one TMEM lane = one
+//               weight row per thread), apply globals, row scales and SwiGLU (h) or the
+//               routing weight (y: each 32-position chunk is transposed through shared
+//               memory so that every position's 256 contiguous outputs leave in 512-byte
+//               warp stores). Tensor memory: the accumulator (256 columns) and four A
+//               buffers (256 columns); the accumulator is released as soon as its last
+//               chunk is loaded.
 // f16 operands instead of bf16: code*scale is exact in both; a bf16 activation row
 // scaled by its power of two (maximum in [2^14, 2^15)) converts to f16 exactly except
 // for elements below 2^-31 of the row maximum, which move by less than 2^-38 of it;
@@ -44,8 +48,9 @@ namespace {
 constexpr int NT = kTcBlock;  // positions per unit (MMA N)
 constexpr int MT = 128;       // weight rows per tile (MMA M)
 constexpr int KC = 64;        // K elements per chunk (128 bytes of f16)
-constexpr int NSMAX = 4;      // TMA stages (at most)
-constexpr int NA = 4;         // dequantised A buffers
+constexpr int NSMAX = 6;      // TMA stages (at most)
+constexpr int NA = 4;         // dequantised A buffers (tensor memory)
+constexpr uint32_t kColA = 2 * NT;  // A buffer ab, tile t at columns kColA + 64 ab + 32 t
 constexpr int kThreadsTc = 480;  // producer, MMA (tile 0), 8 dequant, 4 epilogue, MMA (tile 1)
 constexpr int kMmaWarp1 = 14;    // issuer of tile 1: the issue cost of a tcgen05.mma is per
                                  // issuing thread, so one issuer per tile doubles the rate
@@ -70,7 +75,7 @@ __device__ __forceinline__ void arrive(uint64_t *bar) { mbar_arrive(bar); }
 
 struct TcSmem {
     uint32_t a_bytes, b_bytes, raw_bytes;
-    uint32_t a_off, b_off, raw_off, tbl_off, bar_off, total;
+    uint32_t a_off, b_off, raw_off, tp_off, tbl_off, bar_off, total;
     int ns;
 };
 
@@ -81,7 +86,7 @@ __host__ __device__ constexpr uint32_t raw_row_bytes(bool fp8) { return fp8 ? 64
 __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8 = false)
 {
     TcSmem s;
-    s.a_bytes = 2u * MT * 128;
+    s.a_bytes = 0;  // the dequantised A operand lives in tensor memory
     s.b_bytes = (uint32_t)NT * 128;
     s.raw_bytes = 2u * MT * raw_row_bytes(fp8);
     (void)K;
@@ -90,7 +95,8 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8 = f
     s.a_off = 0;
     s.b_off = s.a_off + NA * s.a_bytes;
     s.raw_off = s.b_off + ns * s.b_bytes;
-    s.tbl_off = s.raw_off + ns * s.raw_bytes;
+    s.tp_off = s.raw_off + ns * s.raw_bytes;      // down epilogue: two 32-position x 256-row bf16 tiles
+    s.tbl_off = s.tp_off + 2 * 32 * 2 * MT * 2;
     s.bar_off = s.tbl_off + 4 * NT * 8;           // per epilogue warp: [NT] slots + [NT] factors
     s.total = s.bar_off + 512;
     return s;
@@ -118,19 +124,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     constexpr int RB = (int)raw_row_bytes(FP8);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
-    uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + 2;  // two accumulators
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + 2;  // one accumulator (index 0)
+    uint64_t *tp_bar = acc_empty + 2;  // down epilogue: transpose tile written by all 4 warps
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tp_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tmem_cols = 4 * NT;  // two accumulators of two 128-column tiles
+    // columns [0, 256): the accumulator (two 128-column tiles); [256, 512): NA A buffers
+    const uint32_t tmem_cols = 512;
 
     if (threadIdx.x == 0) {
         // a stage and an A buffer are released by both issuers' commits
         for (int i = 0; i < NSMAX; ++i) { mbar_init(full + i, 1); mbar_init(empty + i, 2); }
         // consumer barriers count warps: each warp arrives once, from lane 0 after __syncwarp
         for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq / 32); mbar_init(a_empty + i, 2); }
-        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 2); mbar_init(acc_empty + i, kEp / 32); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full + i, 2);
+            mbar_init(acc_empty + i, kEp / 32);
+            mbar_init(tp_bar + i, kEp / 32);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -148,6 +160,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int n_units = (n_pos / NT) * p.n_mtiles;
     const int nk = K / KC;
     const int tile_rows = GATED ? MT : 2 * MT;  // row stride of the unit index m
+    // units are strided over the CTAs: at any moment the GPU works on consecutive units,
+    // which share their block's B tiles in L2
     bool dead = false;
 
     if (warp == 0) {
@@ -185,10 +199,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint32_t idesc = tc::idesc_f16_f32(MT, NT);
             int it = 0, ia = 0, uc = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
-                const int ab2 = uc & 1;  // accumulator of this unit
-                if (!wait_bar(acc_empty + ab2, ((uc >> 1) & 1) ^ 1, abort_flag)) { dead = true; break; }
+                // one accumulator: the epilogue of the previous unit has read it out
+                if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag)) { dead = true; break; }
                 tc::fence_after_sync();
-                const uint32_t acc = tmem + (uint32_t)(ab2 * 2 * NT) + tile * NT;
+                const uint32_t acc = tmem + tile * NT;
                 for (int c = 0; c < nk; ++c, ++it, ++ia) {
                     const int slot = it % ns, ab = ia % NA;
                     if (!wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
@@ -197,18 +211,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t a0 = smem_u32(smem + L.a_off + ab * L.a_bytes);
+                    const uint32_t a0 = tmem + kColA + (uint32_t)ab * 64u + tile * 32u;  // A in tensor memory
                     const uint32_t b0 = smem_u32(smem + L.b_off + slot * L.b_bytes);
 #pragma unroll
                     for (int kk = 0; kk < KC / 16; ++kk) {
                         const uint64_t bd = tc::sw128_desc(b0 + kk * 32);
-                        tc::mma_f16(acc, tc::sw128_desc(a0 + tile * MT * 128 + kk * 32), bd, idesc, (c | kk) != 0);
+                        tc::mma_f16_ts(acc, a0 + kk * 8u, bd, idesc, (c | kk) != 0);
                     }
                     tc::commit(empty + slot);
                     tc::commit(a_empty + ab);
                 }
                 if (dead) break;
-                tc::commit(acc_full + ab2);
+                tc::commit(acc_full);
             }
             if (dead) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
         }
@@ -246,10 +260,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4 *>(rw + ((j ^ x) << 4));
                 const uint32_t words[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
                                             q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
-                unsigned char *arow = smem + L.a_off + ab * L.a_bytes + half * MT * 128 + r * 128;
+                uint32_t o[32];  // the row's 64 f16 values, TMEM columns in K order
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {  // 16-byte piece w of the A row = code words 2w, 2w + 1
-                    uint32_t o[4];
+                for (int w = 0; w < 8; ++w) {  // columns 4w .. 4w + 3 = code words 2w, 2w + 1
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const uint32_t cw = words[2 * w + h2];
@@ -258,12 +271,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             : "=r"(lo) : "r"(cw));
                         asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
                             : "=r"(hi) : "r"(cw >> 16));
-                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * h2]) : "r"(lo), "r"(sv));
-                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * h2 + 1]) : "r"(hi), "r"(sv));
+                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * w + 2 * h2]) : "r"(lo), "r"(sv));
+                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * w + 2 * h2 + 1]) : "r"(hi), "r"(sv));
                     }
-                    *reinterpret_cast<uint4 *>(arow + ((w ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
-                fence_proxy_async_smem();
+                tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
+                tc::wait_st();
+                tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) arrive(a_full + ab);
             }
@@ -326,16 +340,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 const uint4 qb = *reinterpret_cast<const uint4 *>(rw + 16 * (j0 ^ 1));
                 const uint4 q0 = j0 ? qb : qa, q1 = j0 ? qa : qb;
                 const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                unsigned char *arow = smem + L.a_off + ab * L.a_bytes + half * MT * 128 + r * 128;
+                uint32_t o[32];  // the row's 64 f16 values, TMEM columns in K order
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
-                    uint32_t o[4];
-                    dequant8_f16(words[w], sv[w >> 1], o);
-                    *reinterpret_cast<uint4 *>(arow + ((w ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    uint32_t t4[4];
+                    dequant8_f16(words[w], sv[w >> 1], t4);
+                    o[4 * w] = t4[0]; o[4 * w + 1] = t4[1]; o[4 * w + 2] = t4[2]; o[4 * w + 3] = t4[3];
                 }
-                // every thread orders its A writes before the tensor core's reads, then
-                // the warp arrives once
-                fence_proxy_async_smem();
+                // the row goes to this warp's TMEM lane quarter; every thread's stores complete
+                // before the warp arrives once
+                tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
+                tc::wait_st();
+                tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) arrive(a_full + ab);
             }
@@ -354,27 +370,31 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int r = 32 * quarter + lane;
         int *tbl_slot = reinterpret_cast<int *>(smem + L.tbl_off) + (warp - kEpWarp0) * 2 * NT;
         float *tbl_w = reinterpret_cast<float *>(tbl_slot + NT);
-        int uc = 0;
+        int uc = 0, gc = 0;  // units, and down-epilogue chunks (transpose tile use count)
+        int tbl_block = -1;  // block whose positions the table holds
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
             const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
-            __syncwarp();
-            for (int t = lane; t < NT; t += 32) {
-                const int pos = b * NT + t;
-                float w = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
-                int dst = pos;
-                if (!GATED) {
-                    if (p.sorted_slot) {
-                        dst = __ldg(p.sorted_slot + pos);
-                        if (dst >= p.n_slots) dst = -1;
-                        else if (p.route_w) w *= __ldg(p.route_w + dst);
-                    } else if (dst >= p.n_pos_static) {
-                        dst = -1;
+            if (b != tbl_block) {
+                tbl_block = b;
+                __syncwarp();
+                for (int t = lane; t < NT; t += 32) {
+                    const int pos = b * NT + t;
+                    float w = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
+                    int dst = pos;
+                    if (!GATED) {
+                        if (p.sorted_slot) {
+                            dst = __ldg(p.sorted_slot + pos);
+                            if (dst >= p.n_slots) dst = -1;
+                            else if (p.route_w) w *= __ldg(p.route_w + dst);
+                        } else if (dst >= p.n_pos_static) {
+                            dst = -1;
+                        }
                     }
+                    tbl_slot[t] = dst;
+                    tbl_w[t] = w;
                 }
-                tbl_slot[t] = dst;
-                tbl_w[t] = w;
+                __syncwarp();
             }
-            __syncwarp();
             const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
             const float *glob_e = p.glob + (size_t)e * p.R;
             const int row0 = GATED ? m * MT + r : m * 2 * MT + r;
@@ -396,38 +416,61 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 g0 = __ldg(glob_e + row0);
                 g1 = __ldg(glob_e + (GATED ? p.up_off + row0 : row0 + MT));
             }
-            const int ab2 = uc & 1;
-            if (!warp_wait_bar(acc_full + ab2, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
+            if (!warp_wait_bar(acc_full, uc & 1, abort_flag)) { dead = true; break; }
             tc::fence_after_sync();
-            const uint32_t lane_addr = tmem + (uint32_t)(ab2 * 2 * NT) + ((uint32_t)(32 * quarter) << 16);
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
             for (int cb = 0; cb < NT / 32; ++cb) {
                 uint32_t v0[32], v1[32];
                 tc::ld32(lane_addr + cb * 32, v0);
                 tc::ld32(lane_addr + NT + cb * 32, v1);
                 tc::wait_ld();
+                if (cb == NT / 32 - 1) {  // accumulator read out: the next unit's MMAs may start
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) arrive(acc_empty);
+                }
+                if (GATED) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = cb * 32 + j;
-                    const float w = tbl_w[t];
-                    if (GATED) {
+                    for (int j = 0; j < 32; ++j) {
+                        const int t = cb * 32 + j;
+                        const float w = tbl_w[t];
                         const float gate = __uint_as_float(v0[j]) * w * g0;
                         const float up = __uint_as_float(v1[j]) * w * g1;
                         __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
                         p.h_out[(size_t)(b * NT + t) * p.h_ld + row0] = *reinterpret_cast<uint16_t *>(&hv);
-                    } else {
-                        const int dst = tbl_slot[t];
-                        if (dst < 0) continue;
-                        uint16_t *yrow = p.y_out + (size_t)dst * p.y_ld;
+                    }
+                } else {
+                    // y rows of the chunk's 32 positions, each 256 contiguous values (both tiles):
+                    // every thread writes its row of the two tiles into a shared [32][256] bf16
+                    // tile, then each warp stores 8 whole position rows with 16-byte stores
+                    // (512 contiguous bytes per warp instruction instead of 64).
+                    const int X = gc & 1;
+                    uint16_t *tb = reinterpret_cast<uint16_t *>(smem + L.tp_off + X * (32 * 2 * MT * 2));
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float w = tbl_w[cb * 32 + j];
                         __nv_bfloat16 y0 = __float2bfloat16_rn(__uint_as_float(v0[j]) * g0 * w);
                         __nv_bfloat16 y1 = __float2bfloat16_rn(__uint_as_float(v1[j]) * g1 * w);
-                        yrow[row0] = *reinterpret_cast<uint16_t *>(&y0);
-                        yrow[row0 + MT] = *reinterpret_cast<uint16_t *>(&y1);
+                        tb[j * 2 * MT + r] = *reinterpret_cast<uint16_t *>(&y0);
+                        tb[j * 2 * MT + MT + r] = *reinterpret_cast<uint16_t *>(&y1);
                     }
+                    // all four warps have written the tile (the barrier of this buffer's previous
+                    // use also ordered every warp's reads of it before these writes)
+                    __syncwarp();
+                    if (lane == 0) arrive(tp_bar + X);
+                    if (!warp_wait_bar(tp_bar + X, (gc >> 1) & 1, abort_flag)) { dead = true; break; }
+                    const int n0 = m * 2 * MT;  // first y column of the unit's two tiles
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = 8 * quarter + jj;
+                        const int dst = tbl_slot[cb * 32 + j];
+                        if (dst < 0) continue;  // padding position (uniform across the warp)
+                        const uint4 v = *reinterpret_cast<const uint4 *>(tb + j * 2 * MT + lane * 8);
+                        *reinterpret_cast<uint4 *>(p.y_out + (size_t)dst * p.y_ld + n0 + lane * 8) = v;
+                    }
+                    ++gc;
                 }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) arrive(acc_empty + ab2);
         }
         if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     }
@@ -540,7 +583,7 @@ static int tc_stages(int K, int group, bool fp8 = false)
     int optin = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    for (int ns : {4, 3, 2})
+    for (int ns = NSMAX; ns >= 2; --ns)
         if (tc_smem(K, group, ns, fp8).total + 1024 <= (uint32_t)optin) return ns;
     return 0;
 }
