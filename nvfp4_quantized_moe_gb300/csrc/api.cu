@@ -184,7 +184,8 @@ static bool use_tc_fp8(const Geometry &G, int T)
 
 // Workspace regions of ft_moe_forward, each 256-byte aligned.
 struct WsLayout {
-    size_t status, counters, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    size_t status, counters, split_cnt, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    size_t split_part;  // register-fed decode kernels: partial sums of units split between CTAs
     // tensor-core path only: f16 copies of the B operands and their per-row scales
     size_t xs, xs_scale, x16, x16_scale, h16, h16_scale, hsh16, hsh16_scale;
     size_t zero_bytes;  // [status, counters) cleared at the start of every forward
@@ -202,6 +203,7 @@ static WsLayout ws_layout(const Geometry &G, int T)
     auto take = [&](size_t bytes) { size_t at = o; o = round_up(o + bytes, 256); return at; };
     L.status = take(256);
     L.counters = take(sizeof(int) * (size_t)T * (G.H / 32));
+    L.split_cnt = take(sizeof(int) * 2 * (size_t)kMaxSplitSlots);  // gate_up, down
     L.zero_bytes = o;
     L.sorted = take(sizeof(int) * (size_t)pmax);
     L.block_expert = take(sizeof(int) * (size_t)(pmax / kGemvBlock + 1));
@@ -212,6 +214,7 @@ static WsLayout ws_layout(const Geometry &G, int T)
     L.h_sh = take(G.Is ? 2 * (size_t)tpad * G.Isl : 0);
     L.y = take(4 * (size_t)n * G.H);
     L.y_sh = take(G.Is ? 4 * (size_t)T * G.H : 0);
+    L.split_part = take(sizeof(float) * (size_t)kMaxSplitSlots * kSplitPartFloats);
     const bool tc = G.fmt == FT_FORMAT_FP8_BLOCK ? use_tc_fp8(G, T) : use_tc(G, T);
     L.xs = take(tc ? 2 * (size_t)pmax * G.H : 0);
     L.xs_scale = take(tc ? 4 * (size_t)pmax : 0);
@@ -836,6 +839,8 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             F.prob[1].n_tiles = cdiv(G.Isl, 16 * (8 / ks_gu));
             F.nprob = 2;
         }
+        F.split_part = reinterpret_cast<float *>(ws + L.split_part);
+        F.split_cnt = reinterpret_cast<int *>(ws + L.split_cnt);
         if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         int max_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
         if ((e = launch_gemv_fast(F, true, ks_gu, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
@@ -851,6 +856,9 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             D.nprob = 2;
         }
         set_combine(D);
+        // down units are short (I_l / 128 steps): splitting them costs more than it balances
+        D.split_part = nullptr;
+        D.split_cnt = nullptr;
         if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
         if ((e = launch_gemv_fast(D, false, ks_dn, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");

@@ -158,7 +158,15 @@ struct FastLaunch {
     const float *y, *y_sh;
     void *out;
     int out_dtype, T, H, k;
+    // Even split of the K steps over the CTAs (register-fed kernel, no in-CTA K split): a
+    // unit shared by CTAs c and c + 1 leaves each piece's partial sums in
+    // split_part[c][piece] and the second arrival on split_cnt[c] finishes it. Null: each
+    // CTA takes whole units. split_cnt is zero at launch; at most kMaxSplitSlots CTAs.
+    float *split_part;
+    int *split_cnt;
 };
+constexpr int kMaxSplitSlots = 512;
+constexpr size_t kSplitPartFloats = 2 * 256 * 8;  // two pieces x 256 threads x 8 partial sums
 cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
 
 // fp8_block grouped GEMV (register-fed, any batch size): K a whole number of 128-element

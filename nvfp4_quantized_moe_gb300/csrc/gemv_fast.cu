@@ -60,12 +60,37 @@ __device__ __forceinline__ void fast_compute(const FastFrag &f, const uint4 *bb,
     mma_step(f.b_lo, f.b_hi, f.sb & 0xFFFFu, f.sb >> 16, b, acc1);
 }
 
+// Lane bases of a warp's pair tile (first row r0) of expert e over the K range from k0.
+template <bool GATED>
+__device__ __forceinline__ FastPtrs fast_ptrs(const GemvParams &p, int e, int r0, int g, int c, int k0)
+{
+    const int K = p.K;
+    const int row_a = r0 + g, row_b = GATED ? p.up_off + r0 + g : r0 + 16 + g;
+    const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
+    const uint8_t *scales_e = p.scales + (size_t)e * p.e_scales;
+    FastPtrs P;
+    P.ca = codes_e + (size_t)row_a * (K / 2) + k0 / 2 + 16 * c;
+    P.cb = codes_e + (size_t)row_b * (K / 2) + k0 / 2 + 16 * c;
+    P.sa = scales_e + (size_t)row_a * (K / p.group) + (k0 + 32 * c) / p.group;
+    P.sb = scales_e + (size_t)row_b * (K / p.group) + (k0 + 32 * c) / p.group;
+    P.crow8 = (size_t)8 * (K / 2);
+    P.srow8 = (size_t)8 * (K / p.group);
+    P.group = p.group;
+    return P;
+}
+
 }  // namespace
 
-// One unit of work: a block of 8 positions of problem `p` and one pair-tile per warp.
+// One unit of work: a block of 8 positions of problem `p` and one pair-tile per warp,
+// over the warp's 128-element steps [s_lo, s_hi) (all of them unless the unit is split
+// between CTAs c - 1 and c (piece 1, this CTA is c) or c and c + 1 (piece 0): the pair's
+// partials meet in split slot c - piece and only the second of the two CTAs to finish
+// adds the other piece and runs the epilogue; a sum of two fp32 terms does not depend on
+// their order).
 template <bool GATED, int KS>
 __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch &L, int lu, int n_pos, uint4 *smem_b,
-                                          const float *inv, float (&red)[KS > 1 ? 8 : 1][32][8])
+                                          const float *inv, float (&red)[KS > 1 ? 8 : 1][32][8], int s_lo = 0,
+                                          int s_hi = -1, int piece = -1)
 {
     constexpr int TPW = 8 / KS;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -73,7 +98,9 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     const int g = lane >> 2, c = lane & 3;
     const int K = p.K;
     const int blk = lu / p.n_tiles, grp = lu - blk * p.n_tiles;
-    const int Kw = K / KS, k0 = ks * Kw, nstep = Kw / kStep;
+    const int Kw = K / KS, k0 = ks * Kw;
+    if (s_hi < 0) s_hi = Kw / kStep;
+    const int nstep = s_hi - s_lo;
     const int pair_rows = GATED ? 16 : 32;
     const int rows_limit = GATED ? p.up_off : p.R;
     const int m = ((c >> 1) << 1) ^ (g & 1);
@@ -83,28 +110,41 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
-        const int row_a = r0 + g, row_b = GATED ? p.up_off + r0 + g : r0 + 16 + g;
-        const uint8_t *codes_e = p.codes + (size_t)e * p.e_codes;
-        const uint8_t *scales_e = p.scales + (size_t)e * p.e_scales;
-        FastPtrs P;
-        P.ca = codes_e + (size_t)row_a * (K / 2) + k0 / 2 + 16 * c;
-        P.cb = codes_e + (size_t)row_b * (K / 2) + k0 / 2 + 16 * c;
-        P.sa = scales_e + (size_t)row_a * (K / p.group) + (k0 + 32 * c) / p.group;
-        P.sb = scales_e + (size_t)row_b * (K / p.group) + (k0 + 32 * c) / p.group;
-        P.crow8 = (size_t)8 * (K / 2);
-        P.srow8 = (size_t)8 * (K / p.group);
-        P.group = p.group;
+        const FastPtrs P = fast_ptrs<GATED>(p, e, r0, g, c, k0);
         const uint4 *bb = smem_b + (size_t)g * (K / 8) + k0 / 8;
         FastFrag ring[4];
-        fast_load(P, 0, ring[0]);
-        if (nstep > 1) fast_load(P, 1, ring[1]);
+        fast_load(P, s_lo, ring[0]);
+        if (nstep > 1) fast_load(P, s_lo + 1, ring[1]);
         for (int s0 = 0; s0 < nstep; s0 += 4) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int s = s0 + q;
-                if (s + 2 < nstep) fast_load(P, s + 2, ring[(q + 2) & 3]);
-                if (s < nstep) fast_compute(ring[q], bb, boff, s, acc0, acc1);
+                if (s + 2 < nstep) fast_load(P, s_lo + s + 2, ring[(q + 2) & 3]);
+                if (s < nstep) fast_compute(ring[q], bb, boff, s_lo + s, acc0, acc1);
             }
+        }
+    }
+    if constexpr (KS == 1) {
+        if (piece >= 0) {
+            __shared__ int s_flag;
+            const int slot = (int)blockIdx.x - piece;
+            float *part = L.split_part + (size_t)slot * kSplitPartFloats;
+            float4 *mine = reinterpret_cast<float4 *>(part + ((size_t)piece * kThreads + threadIdx.x) * 8);
+            __stcg(mine, make_float4(acc0[0], acc0[1], acc0[2], acc0[3]));
+            __stcg(mine + 1, make_float4(acc1[0], acc1[1], acc1[2], acc1[3]));
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();  // every thread's partials before the count
+                s_flag = atomicAdd(L.split_cnt + slot, 1) == 1;
+            }
+            __syncthreads();
+            if (!s_flag) return;  // the other piece finishes the unit
+            __threadfence();
+            const float4 *other =
+                reinterpret_cast<const float4 *>(part + ((size_t)(1 - piece) * kThreads + threadIdx.x) * 8);
+            const float4 o0 = __ldcg(other), o1 = __ldcg(other + 1);
+            acc0[0] += o0.x; acc0[1] += o0.y; acc0[2] += o0.z; acc0[3] += o0.w;
+            acc1[0] += o1.x; acc1[1] += o1.y; acc1[2] += o1.z; acc1[3] += o1.w;
         }
     }
     if (KS > 1) {
@@ -200,21 +240,52 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const int units0 = (n_pos0 / kGemvBlock) * L.prob[0].n_tiles;
     const int units1 = L.nprob > 1 ? (n_pos1 / kGemvBlock) * L.prob[1].n_tiles : 0;
     const int n_units = units0 + units1;
-    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
-    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
     int staged = -1;
-    for (int u = u_lo; u < u_hi; ++u) {
+    auto stage_for = [&](int u) -> int {  // stage the unit's block if needed; returns its local index
         const int pi = u < units0 ? 0 : 1;
         const GemvParams &p = L.prob[pi];
         const int lu = pi ? u - units0 : u;
-        const int n_pos = pi ? n_pos1 : n_pos0;
         const int blk = lu / p.n_tiles;
         const int key = pi * (1 << 30) + blk;
         if (key != staged) {
-            fast_stage<GATED>(p, blk, n_pos, rows, smem_b, inv);
+            fast_stage<GATED>(p, blk, pi ? n_pos1 : n_pos0, rows, smem_b, inv);
             staged = key;
         }
-        fast_unit<GATED, KS>(p, L, lu, n_pos, smem_b, inv, red);
+        return lu;
+    };
+    if constexpr (KS == 1) {
+        // Even split of all K steps: W = units0 * S0 + units1 * S1 steps, CTA c takes
+        // [c W / G, (c + 1) W / G). Needs every CTA's share to be at least one unit, so
+        // that a unit is cut at most once.
+        const int S0 = L.prob[0].K / kStep, S1 = L.nprob > 1 ? L.prob[1].K / kStep : S0;
+        const int64_t W = (int64_t)units0 * S0 + (int64_t)units1 * S1;
+        const int Smax = S0 > S1 ? S0 : S1;
+        if (L.split_part && gridDim.x <= kMaxSplitSlots && W >= (int64_t)gridDim.x * Smax) {
+            const int w_hi = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x), W0 = units0 * S0;
+            for (int w = (int)((int64_t)blockIdx.x * W / gridDim.x); w < w_hi;) {
+                int u, s, S;
+                if (w < W0) {
+                    u = w / S0; s = w - u * S0; S = S0;
+                } else {
+                    u = units0 + (w - W0) / S1; s = (w - W0) - (u - units0) * S1; S = S1;
+                }
+                const int s_end = w_hi - w < S - s ? s + (w_hi - w) : S;
+                const int pi = u < units0 ? 0 : 1;
+                const int lu = stage_for(u);
+                // piece 1: tail of the unit begun by CTA c - 1; piece 0: head of one CTA c + 1 ends
+                const int piece = s > 0 ? 1 : (s_end < S ? 0 : -1);
+                fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, red, s, s_end, piece);
+                w += s_end - s;
+            }
+            return;
+        }
+    }
+    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    for (int u = u_lo; u < u_hi; ++u) {
+        const int pi = u < units0 ? 0 : 1;
+        const int lu = stage_for(u);
+        fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, red);
     }
 }
 
