@@ -105,6 +105,23 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(value: float, dev=None) -> float:
+    """Largest value over the ranks of the default process group (the value itself when
+    there is none): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev if dev is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_value(tokens_per_step_per_rank: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput under weak scaling: all ranks' tokens over the slowest rank's time."""
+    return world * tokens_per_step_per_rank * steps / (max_ms / 1e3)
+
+
 def run_reference(args, world, rank):
     """CPU oracle on a bounded sample of the workload (the reference arm)."""
     import oracle
@@ -442,13 +459,9 @@ def run_ours(args, world, rank, local):
                 g_plain.replay()
             stop.record(stream)
         torch.cuda.synchronize(dev)
-    elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = _max_over_ranks(start.elapsed_time(stop), dev)
     ms_step = elapsed_ms / args.steps
-    value = world * T * L * args.steps / (elapsed_ms / 1e3)
+    value = _job_value(T * L, world, args.steps, elapsed_ms)
 
     # per-stage durations from the profiled graph
     g_prof = graphs[True][0]
