@@ -97,7 +97,7 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8 = f
     s.raw_off = s.b_off + ns * s.b_bytes;
     s.tp_off = s.raw_off + ns * s.raw_bytes;      // down epilogue: two 32-position x 256-row bf16 tiles
     s.tbl_off = s.tp_off + 2 * 32 * 2 * MT * 2;
-    s.bar_off = s.tbl_off + 4 * NT * 8;           // per epilogue warp: [NT] slots + [NT] factors
+    s.bar_off = s.tbl_off + 2 * NT * 8;           // two position tables (unit parity): [NT] slots + [NT] factors
     s.total = s.bar_off + 512;
     return s;
 }
@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
     uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + 2;  // one accumulator (index 0)
     uint64_t *tp_bar = acc_empty + 2;  // down epilogue: transpose tile written by all 4 warps
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tp_bar + 2);
+    uint64_t *tbl_bar = tp_bar + 2;    // epilogue: a unit's position table written by all 4 warps
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tbl_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             mbar_init(acc_full + i, 2);
             mbar_init(acc_empty + i, kEp / 32);
             mbar_init(tp_bar + i, kEp / 32);
+            mbar_init(tbl_bar + i, kEp / 32);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -363,37 +365,37 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // ------------------------------------------------------------ epilogue
         // Thread = TMEM lane = tile row r (warp w may read lanes 32 (w % 4) ..); every
         // thread handles all NT positions of its row in both tiles of the accumulator.
-        // Per unit the warp first builds its own table of the block's positions (slot and
-        // routing weight x activation row scale, or the row scale alone) in shared memory,
-        // while the MMAs of the unit are still running.
+        // Per unit the warps first build a table of the block's positions (slot and routing
+        // weight x activation row scale, or the row scale alone) in shared memory, and load
+        // their rows' globals, while the MMAs of the unit are still running.
         const int quarter = warp & 3;
         const int r = 32 * quarter + lane;
-        int *tbl_slot = reinterpret_cast<int *>(smem + L.tbl_off) + (warp - kEpWarp0) * 2 * NT;
-        float *tbl_w = reinterpret_cast<float *>(tbl_slot + NT);
+        // One position table per unit, built by the four warps together (lane = position,
+        // 32 per warp) and double-buffered by unit parity: a warp writes table X for unit u
+        // only after passing the table barrier of unit u - 1, which every warp reaches after
+        // finishing unit u - 2, the last reader of table X.
+        const int ew = warp - kEpWarp0;
         int uc = 0, gc = 0;  // units, and down-epilogue chunks (transpose tile use count)
-        int tbl_block = -1;  // block whose positions the table holds
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
             const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
-            if (b != tbl_block) {
-                tbl_block = b;
-                __syncwarp();
-                for (int t = lane; t < NT; t += 32) {
-                    const int pos = b * NT + t;
-                    float w = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
-                    int dst = pos;
-                    if (!GATED) {
-                        if (p.sorted_slot) {
-                            dst = __ldg(p.sorted_slot + pos);
-                            if (dst >= p.n_slots) dst = -1;
-                            else if (p.route_w) w *= __ldg(p.route_w + dst);
-                        } else if (dst >= p.n_pos_static) {
-                            dst = -1;
-                        }
+            const int X = uc & 1;
+            int *tbl_slot = reinterpret_cast<int *>(smem + L.tbl_off) + X * 2 * NT;
+            float *tbl_w = reinterpret_cast<float *>(tbl_slot + NT);
+            {
+                const int t = 32 * ew + lane, pos = b * NT + t;
+                float w = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
+                int dst = pos;
+                if (!GATED) {
+                    if (p.sorted_slot) {
+                        dst = __ldg(p.sorted_slot + pos);
+                        if (dst >= p.n_slots) dst = -1;
+                        else if (p.route_w) w *= __ldg(p.route_w + dst);
+                    } else if (dst >= p.n_pos_static) {
+                        dst = -1;
                     }
-                    tbl_slot[t] = dst;
-                    tbl_w[t] = w;
                 }
-                __syncwarp();
+                tbl_slot[t] = dst;
+                tbl_w[t] = w;
             }
             const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
             const float *glob_e = p.glob + (size_t)e * p.R;
@@ -416,6 +418,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 g0 = __ldg(glob_e + row0);
                 g1 = __ldg(glob_e + (GATED ? p.up_off + row0 : row0 + MT));
             }
+            __syncwarp();
+            if (lane == 0) arrive(tbl_bar + X);
+            if (!warp_wait_bar(tbl_bar + X, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
             if (!warp_wait_bar(acc_full, uc & 1, abort_flag)) { dead = true; break; }
             tc::fence_after_sync();
             const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
