@@ -828,8 +828,8 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     // Lean register-fed kernels, same launch structure.
     const int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H);
     const int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
-    if (gemv_fast_ok(G.H, G.g, ks_gu) && gemv_fast_ok(G.Il, G.g, ks_dn) &&
-        (!G.Is || gemv_fast_ok(G.Isl, G.g, ks_dn))) {
+    if (gemv_fast_ok(G.H, G.g, ks_gu, 2 * (G.Il > G.Isl ? G.Il : G.Isl)) && gemv_fast_ok(G.Il, G.g, ks_dn, G.H) &&
+        (!G.Is || gemv_fast_ok(G.Isl, G.g, ks_dn, G.H))) {
         FastLaunch F = {};
         F.prob[0] = gu;
         F.prob[0].n_tiles = cdiv(G.Il, 16 * (8 / ks_gu));

@@ -145,8 +145,9 @@ int gemv_ksplit(int max_blocks, int units_per_block_ks1, int K);
 cudaError_t launch_gemv_gated(const GemvParams &p, int ks, int max_units, cudaStream_t s);
 cudaError_t launch_gemv_down(const GemvParams &p, int ks, int max_units, cudaStream_t s);
 // Lean register-fed GEMV (two 16-row tiles per warp): usable when K % 32 == 0 and
-// (K / ks) % 128 == 0. p.n_tiles = ceil(rows / (pair_rows * 8 / ks)).
-bool gemv_fast_ok(int K, int group, int ks);
+// (K / ks) % 128 == 0 and one expert's R x K codes take under 2 GB. p.n_tiles =
+// ceil(rows / (pair_rows * 8 / ks)).
+bool gemv_fast_ok(int K, int group, int ks, int R);
 
 // One lean-GEMV launch over up to two problems (routed experts, shared expert). For
 // the down stage, non-null `counters` ([T][H/32] ints, zero on entry) fuse the combine.

@@ -38,6 +38,17 @@ __device__ __forceinline__ uint32_t scale_pair(const uint8_t *p, int group)
     return b | (b << 8);
 }
 
+// Step weights at byte offsets co (codes) and so (scales) from the lane bases.
+__device__ __forceinline__ void fast_load_at(const FastPtrs &P, uint32_t co, uint32_t so, FastFrag &f)
+{
+    f.a_lo = ldg_nc_v4(P.ca + co);
+    f.a_hi = ldg_nc_v4(P.ca + P.crow8 + co);
+    f.b_lo = ldg_nc_v4(P.cb + co);
+    f.b_hi = ldg_nc_v4(P.cb + P.crow8 + co);
+    f.sa = scale_pair(P.sa + so, P.group) | (scale_pair(P.sa + P.srow8 + so, P.group) << 16);
+    f.sb = scale_pair(P.sb + so, P.group) | (scale_pair(P.sb + P.srow8 + so, P.group) << 16);
+}
+
 __device__ __forceinline__ void fast_load(const FastPtrs &P, int s, FastFrag &f)
 {
     const int co = 64 * s;                     // 128 elements = 64 code bytes per step
@@ -225,6 +236,116 @@ __device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_p
     __syncthreads();
 }
 
+// Down stage over the CTA's unit range [u_lo, u_hi), whole units of a multiple of 4 steps
+// (K a multiple of 512). Consecutive units of
+// one block share the expert and the staged activations, and warp w's rows in them are
+// 256 apart, so each warp streams a run of them through one register ring as a single
+// sequence of steps (no refill between units) and writes y and counts the combine at
+// each unit's last step.
+__device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int u_lo,
+                                          int u_hi, uint4 *smem_b, float *inv, int *rows, int *tbl_dst,
+                                          float *tbl_w)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int m = ((c >> 1) << 1) ^ (g & 1);
+    const int boff[4] = {4 * c + (0 ^ m), 4 * c + (1 ^ m), 4 * c + (2 ^ m), 4 * c + (3 ^ m)};
+    for (int u = u_lo; u < u_hi;) {
+        const int pi = u < units0 ? 0 : 1;
+        const GemvParams &p = L.prob[pi];
+        const int n_pos = pi ? n_pos1 : n_pos0;
+        const int lu = pi ? u - units0 : u;
+        const int blk = lu / p.n_tiles, grp0 = lu - blk * p.n_tiles;
+        const int nu = min(p.n_tiles - grp0, u_hi - u);  // the run: this block's units in range
+        u += nu;
+        fast_stage<false>(p, blk, n_pos, rows, smem_b, inv);
+        if (threadIdx.x < kGemvBlock) {  // per block position: y row (slot) or -1, and its factor
+            const int pos = blk * kGemvBlock + threadIdx.x;
+            int dst = -1;
+            float w = inv[threadIdx.x];
+            if (pos < n_pos) {
+                if (p.sorted_slot) {
+                    const int sl = __ldg(p.sorted_slot + pos);
+                    if (sl < p.n_slots) {
+                        dst = sl;
+                        if (p.route_w) w *= __ldg(p.route_w + sl);
+                    }
+                } else if (pos < p.n_pos_static) {
+                    dst = pos;
+                }
+            }
+            tbl_dst[threadIdx.x] = dst;
+            tbl_w[threadIdx.x] = w;
+        }
+        __syncthreads();
+        const int r0a = (grp0 * 8 + warp) * 32;  // the warp's first row in the run's first unit
+        // units with rows in range form a prefix of the run
+        const int nok = r0a < p.R ? min(nu, (p.R - r0a + 255) / 256) : 0;
+        const int S = p.K / kStep, tot = nok * S;
+        if (tot == 0) continue;
+        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const FastPtrs P = fast_ptrs<false>(p, e, r0a, g, c, 0);
+        const uint32_t spb = (p.group == 16) ? 8u : 4u;  // scale bytes per step and row pair
+        // from a unit's last step to the next unit's first: 256 rows on, back to K = 0
+        const uint32_t jump_c = 256u * (uint32_t)(p.K / 2) - 64u * (uint32_t)(S - 1);
+        const uint32_t jump_s = 256u * (uint32_t)(p.K / p.group) - spb * (uint32_t)(S - 1);
+        const uint4 *bb = smem_b + (size_t)g * (p.K / 8);
+        const float *glob_e = p.glob + (size_t)e * p.e_glob;
+        uint32_t lco = 0, lso = 0;
+        int ls = 0;  // load cursor: byte offsets and step within its unit
+        auto advance_load = [&]() {
+            if (++ls == S) {
+                ls = 0;
+                lco += jump_c;
+                lso += jump_s;
+            } else {
+                lco += 64u;
+                lso += spb;
+            }
+        };
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        FastFrag ring[4];
+        fast_load_at(P, lco, lso, ring[0]);
+        advance_load();
+        if (tot > 1) {
+            fast_load_at(P, lco, lso, ring[1]);
+            advance_load();
+        }
+        int cs = 0, r0 = r0a;  // compute cursor: step within the unit, the unit's first row
+        for (int t0 = 0; t0 < tot; t0 += 4) {  // S, and so tot, is a multiple of 4
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (t0 + q + 2 < tot) {
+                    fast_load_at(P, lco, lso, ring[(q + 2) & 3]);
+                    advance_load();
+                }
+                fast_compute(ring[q], bb, boff, cs + q, acc0, acc1);
+            }
+            cs += 4;
+            if (cs == S) {  // the unit's last step: y rows r0 .. r0 + 31 of its positions
+#pragma unroll
+                for (int col = 0; col < 2; ++col) {
+                    const int dst = tbl_dst[2 * c + col];
+                    if (dst < 0) continue;
+                    const float w = tbl_w[2 * c + col];
+                    float *yrow = p.y_out + (size_t)dst * p.R;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int n = r0 + g + 8 * half;
+                        yrow[n] = acc0[2 * half + col] * __ldg(glob_e + n) * w;
+                        yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * w;
+                    }
+                }
+                if (L.counters) fused_combine(p, L, blk, n_pos, r0, 0xFFu);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc0[i] = acc1[i] = 0.f;
+                cs = 0;
+                r0 += 256;
+            }
+        }
+    }
+}
+
 // Grid-strided over the concatenated unit lists of up to two problems (the routed
 // experts and the shared expert); each CTA takes a contiguous range of units.
 template <bool GATED, int KS>
@@ -282,6 +403,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     }
     const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
     const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    if constexpr (!GATED && KS == 1) {  // (the host keeps each expert's bank below 2 GB here)
+        if (L.prob[0].K % (4 * kStep) == 0 && (L.nprob < 2 || L.prob[1].K % (4 * kStep) == 0)) {
+            __shared__ int tbl_dst[kGemvBlock];
+            __shared__ float tbl_w[kGemvBlock];
+            down_runs(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, inv, rows, tbl_dst, tbl_w);
+            return;
+        }
+    }
     for (int u = u_lo; u < u_hi; ++u) {
         const int pi = u < units0 ? 0 : 1;
         const int lu = stage_for(u);
@@ -289,10 +418,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     }
 }
 
-// Usable for this shape and K-split?
-bool gemv_fast_ok(int K, int group, int ks)
+// Usable for this shape and K-split? (R = the matrix's rows: the down path addresses an
+// expert's codes with 32-bit offsets.)
+bool gemv_fast_ok(int K, int group, int ks, int R)
 {
-    return K % 32 == 0 && (K / ks) % kStep == 0 && (group == 16 || group == 32);
+    return K % 32 == 0 && (K / ks) % kStep == 0 && (group == 16 || group == 32) &&
+           (int64_t)R * (K / 2) < ((int64_t)1 << 31);
 }
 
 template <bool GATED, int KS>
