@@ -184,11 +184,11 @@ static bool use_tc_fp8(const Geometry &G, int T)
 
 // Workspace regions of ft_moe_forward, each 256-byte aligned.
 struct WsLayout {
-    size_t status, counters, split_cnt, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    size_t status, split_cnt, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
     size_t split_part;  // register-fed decode kernels: partial sums of units split between CTAs
     // tensor-core path only: f16 copies of the B operands and their per-row scales
     size_t xs, xs_scale, x16, x16_scale, h16, h16_scale, hsh16, hsh16_scale;
-    size_t zero_bytes;  // [status, counters) cleared at the start of every forward
+    size_t zero_bytes;  // [0, zero_bytes): status and split counts, cleared at the start of every forward
     int pmax;
 };
 
@@ -202,7 +202,6 @@ static WsLayout ws_layout(const Geometry &G, int T)
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = round_up(o + bytes, 256); return at; };
     L.status = take(256);
-    L.counters = take(sizeof(int) * (size_t)T * (G.H / 32));
     L.split_cnt = take(sizeof(int) * 2 * (size_t)kMaxSplitSlots);  // gate_up, down
     L.zero_bytes = o;
     L.sorted = take(sizeof(int) * (size_t)pmax);
@@ -586,15 +585,14 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             D.prob[1].n_tiles = D.prob[0].n_tiles;
             D.nprob = 2;
         }
-        D.counters = reinterpret_cast<int *>(ws + L.counters);
-        D.combine_target = G.k + (G.Is ? 1 : 0);
-        D.y = y; D.y_sh = G.Is ? y_sh : nullptr; D.out = out; D.out_dtype = out_dtype;
-        D.T = T; D.H = G.H; D.k = G.k;
         if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
         if ((e = launch_gemv_fp8(D, false, ks_dn, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
-        for (int st = FT_STAGE_SHARED_DOWN; st <= FT_NSTAGES; ++st)
-            if ((e = stage_mark(st, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+        if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         return ok();
     }
     if (tc_path) {
@@ -732,19 +730,13 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         dn_sh.block_expert = nullptr; dn_sh.n_slots = T; dn_sh.top_k = 1; dn_sh.num_experts = 1;
         dn_sh.y_out = y_sh; dn_sh.route_w = nullptr;
     }
-    int *counters = reinterpret_cast<int *>(ws + L.counters);
-    auto set_combine = [&](auto &D) {
-        D.counters = counters;
-        D.combine_target = G.k + (G.Is ? 1 : 0);
-        D.y = y; D.y_sh = G.Is ? y_sh : nullptr; D.out = out; D.out_dtype = out_dtype;
-        D.T = T; D.H = G.H; D.k = G.k;
-    };
-    auto trailing_marks = [&]() -> cudaError_t {
-        for (int st = FT_STAGE_SHARED_DOWN; st <= FT_NSTAGES; ++st) {
-            cudaError_t err = stage_mark(st, s);
-            if (err != cudaSuccess) return err;
-        }
-        return cudaSuccess;
+    // after the down stage: the combine, out[t] = sum_j y[t k + j] (+ y_sh[t]), in that order
+    auto combine = [&]() -> cudaError_t {
+        cudaError_t err;
+        if ((err = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return err;
+        if ((err = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return err;
+        if ((err = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s)) != cudaSuccess) return err;
+        return stage_mark(FT_NSTAGES, s);
     };
 
     // TMA-streamed kernels, routed and shared expert in one launch per stage, combine
@@ -765,8 +757,6 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
                 SG.prob[1].p = gu_sh; SD.prob[1].p = dn_sh;
                 SG.nprob = SD.nprob = 2;
             }
-            set_combine(SD);
-            SD.counters = nullptr;  // combine in its own launch (below)
             auto units = [&](const StreamLaunch &S) {
                 return max_blocks * S.prob[0].n_ptiles + (G.Is ? tpad * S.prob[1].n_ptiles : 0);
             };
@@ -775,11 +765,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
             if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
             if ((e = launch_gemv_stream(SD, false, units(SD), s)) != cudaSuccess) return cuda_fail(e, "down launch");
-            if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
-            if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-            if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            if ((e = combine()) != cudaSuccess) return cuda_fail(e, "combine launch");
             return ok();
         }
     }
@@ -811,16 +797,10 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
                 D.prob[1].n_tiles = D.prob[0].n_tiles;
                 D.nprob = 2;
             }
-            set_combine(D);
-            D.counters = nullptr;  // combine in its own launch (below): no atomics in the epilogue
             if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
             max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
             if ((e = launch_tc_gemv(D, false, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
-            if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
-            if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-            if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            if ((e = combine()) != cudaSuccess) return cuda_fail(e, "combine launch");
             return ok();
         }
     }
@@ -855,14 +835,13 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             D.prob[1].n_tiles = D.prob[0].n_tiles;
             D.nprob = 2;
         }
-        set_combine(D);
         // down units are short (I_l / 128 steps): splitting them costs more than it balances
         D.split_part = nullptr;
         D.split_cnt = nullptr;
         if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
         if ((e = launch_gemv_fast(D, false, ks_dn, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
-        if ((e = trailing_marks()) != cudaSuccess) return cuda_fail(e, "stage event");
+        if ((e = combine()) != cudaSuccess) return cuda_fail(e, "combine launch");
         return ok();
     }
 

@@ -149,16 +149,11 @@ cudaError_t launch_gemv_down(const GemvParams &p, int ks, int max_units, cudaStr
 // ceil(rows / (pair_rows * 8 / ks)).
 bool gemv_fast_ok(int K, int group, int ks, int R);
 
-// One lean-GEMV launch over up to two problems (routed experts, shared expert). For
-// the down stage, non-null `counters` ([T][H/32] ints, zero on entry) fuse the combine.
+// One lean-GEMV launch over up to two problems (routed experts, shared expert); the
+// down stage writes the slot-major y rows, and the combine runs as its own launch.
 struct FastLaunch {
     GemvParams prob[2];
     int nprob;
-    int *counters;
-    int combine_target;  // k, or k + 1 with a shared expert
-    const float *y, *y_sh;
-    void *out;
-    int out_dtype, T, H, k;
     // Even split of the K steps over the CTAs (register-fed kernel, no in-CTA K split): a
     // unit shared by CTAs c and c + 1 leaves each piece's partial sums in
     // split_part[c][piece] and the second arrival on split_cnt[c] finishes it. Null: each
@@ -192,11 +187,6 @@ struct StreamLaunch {
     CUtensorMap cmap[2], smap[2];  // per problem: packed codes, block scales (set by the launch)
     StreamProb prob[2];
     int nprob;
-    int *counters;                 // down: fused combine as in FastLaunch
-    int combine_target;
-    const float *y, *y_sh;
-    void *out;
-    int out_dtype, T, H, k;
     int ns, act_bytes;             // stages, activation bytes (set by the launch)
 };
 // Geometry for a problem of K columns and `rows` rows (I_l for gate_up, H for down);

@@ -119,59 +119,5 @@ __device__ __forceinline__ void load_b(const uint4 *sm_row, int q0, int r, uint4
     for (int j = 0; j < 4; ++j) b[j] = sm_row[swz(q0 + j, r)];
 }
 
-// Fused combine: after a warp stores y for rows [r0, r0+32) of the block positions in
-// `pos_mask` (bit i = position i of the block), it counts one contribution per token
-// for that row range; the warp that brings a counter to k (+1 with a shared expert)
-// sums that token's k routed rows in order j = 0..k-1 and then the shared row, and
-// writes the output. Only the identity of the summing warp depends on timing, not the
-// order of the sum.
-template <class Launch>
-__device__ __forceinline__ void fused_combine(const GemvParams &p, const Launch &L, int blk, int n_pos, int r0,
-                                              uint32_t pos_mask)
-{
-    const int lane = threadIdx.x & 31;
-    // The warp's y stores are ordered before the counting atomics by the warp barrier;
-    // the acq_rel atomic releases them (cumulatively) and acquires the other writers'.
-    __syncwarp();
-    int t = -1;
-    if (lane < kGemvBlock && ((pos_mask >> lane) & 1u)) {
-        const int pos = blk * kGemvBlock + lane;
-        if (pos < n_pos) {
-            if (p.sorted_slot) {
-                const int sl = __ldg(p.sorted_slot + pos);
-                if (sl < p.n_slots) t = sl / p.top_k;
-            } else if (pos < p.n_pos_static) {
-                t = pos;
-            }
-        }
-    }
-    bool last = false;
-    if (t >= 0) {
-        int old;
-        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
-                     : "=r"(old)
-                     : "l"(L.counters + (size_t)t * (L.H / 32) + r0 / 32)
-                     : "memory");
-        last = old == L.combine_target - 1;
-    }
-    uint32_t mask = __ballot_sync(0xFFFFFFFFu, last);
-    if (!mask) return;
-    const int n = r0 + lane;
-    while (mask) {
-        const int src = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int tt = __shfl_sync(0xFFFFFFFFu, t, src);
-        float acc = 0.f;
-        for (int j = 0; j < L.k; ++j) acc += __ldcg(L.y + ((size_t)tt * L.k + j) * L.H + n);
-        if (L.y_sh) acc += __ldcg(L.y_sh + (size_t)tt * L.H + n);
-        if (L.out_dtype == FT_DTYPE_F32) {
-            static_cast<float *>(L.out)[(size_t)tt * L.H + n] = acc;
-        } else {
-            __nv_bfloat16 b = __float2bfloat16_rn(acc);
-            static_cast<uint16_t *>(L.out)[(size_t)tt * L.H + n] = *reinterpret_cast<uint16_t *>(&b);
-        }
-    }
-}
-
 }  // namespace gemv
 }  // namespace ftmoe

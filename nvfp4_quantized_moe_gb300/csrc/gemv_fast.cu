@@ -31,11 +31,18 @@ struct FastPtrs {
     int group;
 };
 
+// The lane's two scale bytes of a row and step (group 16), or its one byte twice (group
+// 32). Issued in program order with the code loads (volatile), so that they too run two
+// steps ahead of their use.
 __device__ __forceinline__ uint32_t scale_pair(const uint8_t *p, int group)
 {
-    if (group == 16) return __ldg(reinterpret_cast<const uint16_t *>(p));
-    const uint32_t b = __ldg(p);
-    return b | (b << 8);
+    uint32_t v;
+    if (group == 16) {
+        asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(v) : "l"(p));
+        return v;
+    }
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+    return v | (v << 8);
 }
 
 // Step weights at byte offsets co (codes) and so (scales) from the lane bases.
@@ -218,7 +225,6 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
                     yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * wgt;
                 }
             }
-            if (L.counters) fused_combine(p, L, blk, n_pos, r0, 0xFFu);
         }
     }
     if (KS > 1) __syncthreads();
@@ -240,8 +246,7 @@ __device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_p
 // (K a multiple of 512). Consecutive units of
 // one block share the expert and the staged activations, and warp w's rows in them are
 // 256 apart, so each warp streams a run of them through one register ring as a single
-// sequence of steps (no refill between units) and writes y and counts the combine at
-// each unit's last step.
+// sequence of steps (no refill between units) and writes y at each unit's last step.
 __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int u_lo,
                                           int u_hi, uint4 *smem_b, float *inv, int *rows, int *tbl_dst,
                                           float *tbl_w)
@@ -336,7 +341,6 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
                         yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * w;
                     }
                 }
-                if (L.counters) fused_combine(p, L, blk, n_pos, r0, 0xFFu);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc0[i] = acc1[i] = 0.f;
                 cs = 0;

@@ -7,7 +7,7 @@
 // expert-sorted positions as N, m16n8k16 f16 MMAs with fp32 accumulation, each warp
 // owning two 16-row tiles (gate rows i and up rows I_l + i for gate_up, so SwiGLU fuses;
 // rows n and n + 16 for down), loads running two steps ahead through a 4-slot register
-// ring, routed and shared expert in one launch, fused ordered combine in the down stage.
+// ring, routed and shared expert in one launch; the ordered combine runs as its own launch.
 // What differs:
 //  * a step is 64 K elements: lane (g, c) loads 16 code bytes of rows g and g + 8 of
 //    each tile (K elements 16c .. 16c + 15 of the step); e4m3 converts to f16 exactly
@@ -232,7 +232,6 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
                     yrow[n + 16] = acc1[2 * half + col] * wgt;
                 }
             }
-            if (L.counters) fused_combine(p, L, blk, n_pos, r0, 0xFFu);
         }
     }
     if (KS > 1) __syncthreads();

@@ -15,8 +15,8 @@
 // TPS pair tiles) over the whole K, i.e. K/(256 LPS) stages. The math warps only
 // multiply: at the end of a unit each drops its partial sums into one of 4 buffers;
 // 4 epilogue warps add the partials of each pair tile, apply globals, row scales and
-// SwiGLU or routing weights and run the fused combine, with their global operands
-// fetched before they wait -- so the weight stream never waits for an epilogue.
+// SwiGLU or routing weights, with their global operands fetched before they wait --
+// so the weight stream never waits for an epilogue. The combine is its own launch.
 //
 // Shared-memory layouts (every read is free of bank conflicts):
 //   codes    per stage line: TMA boxes of 128 bytes x 16*TPS rows (gate and up boxes)
@@ -372,7 +372,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const __
                             yrow[r0 + 16 + g + 8 * h2] = bb * gl[sp * 32 + 16 + g + 8 * h2] * wgt;
                         }
                     }
-                    if (L.counters) fused_combine(p, L, q.blk, n_pos, r0, par ? 0xAAu : 0x55u);
                 }
             }
             __syncwarp();

@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(1024) align_fused_kernel(const int32_t *__rest
                                                            int *zero, int zero_words)
 {
     pdl_enter();
-    // the forward's status word and combine counters start at zero (cleared here instead
+    // the forward's status word and split counts start at zero (cleared here instead
     // of by a separate memset); the __syncthreads below orders this before any error report
     for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero[i] = 0;
     extern __shared__ int smem[];

@@ -15,8 +15,8 @@
 //               commits to the buffer barriers (each counts both issuers);
 //   warps 4..7  stage the block's activation rows into shared memory (f16, K-major,
 //               128-byte swizzled) ahead of use, and run the epilogue: one TMEM lane =
-//               one weight row per thread, globals, row scales, SwiGLU or routing weight,
-//               and the fused ordered combine of the down stage;
+//               one weight row per thread, globals, row scales, SwiGLU or routing weight
+//               (the combine follows as its own launch);
 //   warps 8..23 dequantise: warp (quarter q, operand, half) owns rows 32q .. 32q+31 of its
 //               tile; per 128-element sub-stage each thread converts 64 codes of its row
 //               (its half) with their block scales (read from global memory, two stages
@@ -510,7 +510,6 @@ __global__ void __launch_bounds__(kThreadsTg, 1)
                         if (dst < 0) continue;
                         p.y_out[(size_t)dst * p.R + n] = (opx ? vb[j] : va[j]) * g * inv[j];
                     }
-                    if (L.counters) fused_combine(p, L, I.blk, n_pos, n0 + 32 * q, 0xFFu);
                 }
             }
             // the last unit of a block frees its staging buffer for the block after next
