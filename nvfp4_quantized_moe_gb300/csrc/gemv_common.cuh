@@ -82,6 +82,53 @@ __device__ __forceinline__ void stage_row(const uint16_t *__restrict__ src, int 
     if (lane == 0) inv[r] = pow2f(e);
 }
 
+// The same with Kp = K and a single pass over global memory: the raw bf16 pieces go to
+// their final shared-memory places while the maximum is taken, then each lane converts
+// its own pieces in place.
+__device__ __forceinline__ void stage_row_1pass(const uint16_t *__restrict__ src, int K, const int *rows, uint4 *sm,
+                                                float *inv, int r)
+{
+    const int lane = threadIdx.x & 31;
+    const int row = rows[r];
+    uint4 *dst = sm + (size_t)r * (K / 8);
+    const int nq = K / 8;
+    if (row < 0) {
+        for (int q = lane; q < nq; q += 32) dst[swz(q, r)] = make_uint4(0, 0, 0, 0);
+        if (lane == 0) inv[r] = 0.f;
+        return;
+    }
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)row * K);
+    float m = 0.f;
+#pragma unroll 4
+    for (int q = lane; q < nq; q += 32) {
+        const uint4 v = __ldg(s4 + q);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+            m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+        }
+        dst[swz(q, r)] = v;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    const int e = row_scale_exp(m);
+    const float down = pow2f(-e);
+    for (int q = lane; q < nq; q += 32) {
+        const uint4 v = dst[swz(q, r)];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 hh = __floats2half2_rn(__uint_as_float(w[j] << 16) * down,
+                                                 __uint_as_float(w[j] & 0xFFFF0000u) * down);
+            h[j] = *reinterpret_cast<const uint32_t *>(&hh);
+        }
+        dst[swz(q, r)] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    if (lane == 0) inv[r] = pow2f(e);
+}
+
 // Stage all 8 rows of the block: warp w handles rows w, w + nwarps, ...
 __device__ __forceinline__ void stage_block(const uint16_t *__restrict__ src, int K, int Kp, const int *rows,
                                             uint4 *sm, float *inv)

@@ -107,8 +107,8 @@ __device__ __forceinline__ FastPtrs fast_ptrs(const GemvParams &p, int e, int r0
 // their order).
 template <bool GATED, int KS>
 __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch &L, int lu, int n_pos, uint4 *smem_b,
-                                          const float *inv, float (&red)[KS > 1 ? 8 : 1][32][8], int s_lo = 0,
-                                          int s_hi = -1, int piece = -1)
+                                          const float *inv, const int *s_e, float (&red)[KS > 1 ? 8 : 1][32][8],
+                                          int s_lo = 0, int s_hi = -1, int piece = -1)
 {
     constexpr int TPW = 8 / KS;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -125,7 +125,7 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     const int boff[4] = {4 * c + (0 ^ m), 4 * c + (1 ^ m), 4 * c + (2 ^ m), 4 * c + (3 ^ m)};
     const int r0 = (grp * TPW + tp) * pair_rows;
     const bool ok = r0 < rows_limit;
-    const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+    const int e = *s_e;
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
         const FastPtrs P = fast_ptrs<GATED>(p, e, r0, g, c, k0);
@@ -230,15 +230,17 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     if (KS > 1) __syncthreads();
 }
 
-// Stage the activation rows of block `blk` of problem `p` (CTA-wide, with barriers).
+// Stage the activation rows of block `blk` of problem `p` and the block's expert id
+// (CTA-wide, with barriers).
 template <bool GATED>
 __device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_pos, int *rows, uint4 *smem_b,
-                                           float *inv)
+                                           float *inv, int *s_e)
 {
     __syncthreads();
     if (threadIdx.x < kGemvBlock) rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, GATED);
+    if (threadIdx.x == kGemvBlock) *s_e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
     __syncthreads();
-    stage_block(p.act, p.K, p.K, rows, smem_b, inv);
+    for (int r = threadIdx.x >> 5; r < kGemvBlock; r += kThreads / 32) stage_row_1pass(p.act, p.K, rows, smem_b, inv, r);
     __syncthreads();
 }
 
@@ -248,7 +250,7 @@ __device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_p
 // 256 apart, so each warp streams a run of them through one register ring as a single
 // sequence of steps (no refill between units) and writes y at each unit's last step.
 __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int u_lo,
-                                          int u_hi, uint4 *smem_b, float *inv, int *rows, int *tbl_dst,
+                                          int u_hi, uint4 *smem_b, float *inv, int *rows, int *s_e, int *tbl_dst,
                                           float *tbl_w)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -263,7 +265,7 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
         const int blk = lu / p.n_tiles, grp0 = lu - blk * p.n_tiles;
         const int nu = min(p.n_tiles - grp0, u_hi - u);  // the run: this block's units in range
         u += nu;
-        fast_stage<false>(p, blk, n_pos, rows, smem_b, inv);
+        fast_stage<false>(p, blk, n_pos, rows, smem_b, inv, s_e);
         if (threadIdx.x < kGemvBlock) {  // per block position: y row (slot) or -1, and its factor
             const int pos = blk * kGemvBlock + threadIdx.x;
             int dst = -1;
@@ -288,7 +290,7 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
         const int nok = r0a < p.R ? min(nu, (p.R - r0a + 255) / 256) : 0;
         const int S = p.K / kStep, tot = nok * S;
         if (tot == 0) continue;
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int e = *s_e;
         const FastPtrs P = fast_ptrs<false>(p, e, r0a, g, c, 0);
         const uint32_t spb = (p.group == 16) ? 8u : 4u;  // scale bytes per step and row pair
         // from a unit's last step to the next unit's first: 256 rows on, back to K = 0
@@ -359,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     extern __shared__ uint4 smem_b[];
     __shared__ float inv[kGemvBlock];
     __shared__ int rows[kGemvBlock];
+    __shared__ int s_e;  // expert of the staged block
     __shared__ float red[KS > 1 ? 8 : 1][32][8];
     const int n_pos0 = load_n_pos(L.prob[0]);
     const int n_pos1 = L.nprob > 1 ? load_n_pos(L.prob[1]) : 0;
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         const int blk = lu / p.n_tiles;
         const int key = pi * (1 << 30) + blk;
         if (key != staged) {
-            fast_stage<GATED>(p, blk, pi ? n_pos1 : n_pos0, rows, smem_b, inv);
+            fast_stage<GATED>(p, blk, pi ? n_pos1 : n_pos0, rows, smem_b, inv, &s_e);
             staged = key;
         }
         return lu;
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
                 const int lu = stage_for(u);
                 // piece 1: tail of the unit begun by CTA c - 1; piece 0: head of one CTA c + 1 ends
                 const int piece = s > 0 ? 1 : (s_end < S ? 0 : -1);
-                fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, red, s, s_end, piece);
+                fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, &s_e, red, s, s_end, piece);
                 w += s_end - s;
             }
             return;
@@ -411,14 +414,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         if (L.prob[0].K % (4 * kStep) == 0 && (L.nprob < 2 || L.prob[1].K % (4 * kStep) == 0)) {
             __shared__ int tbl_dst[kGemvBlock];
             __shared__ float tbl_w[kGemvBlock];
-            down_runs(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, inv, rows, tbl_dst, tbl_w);
+            down_runs(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, inv, rows, &s_e, tbl_dst, tbl_w);
             return;
         }
     }
     for (int u = u_lo; u < u_hi; ++u) {
         const int pi = u < units0 ? 0 : 1;
         const int lu = stage_for(u);
-        fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, red);
+        fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, &s_e, red);
     }
 }
 

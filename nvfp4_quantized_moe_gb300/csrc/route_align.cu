@@ -86,30 +86,33 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
 
 // ---------------------------------------------------------------- align
 
-// Expert id of slot s, or -1 when it is out of range (flagged, then skipped).
-// A repeated id inside a token's row is flagged but still placed.
-__device__ __forceinline__ int checked_expert(const int32_t *ids, int s, int k, int E, int *status)
-{
-    int e = __ldg(ids + s);
-    if (e < 0 || e >= E) {
-        raise_status(status, FT_ERR_INVALID_ROUTING);
-        return -1;
-    }
-    int base = s - s % k;
-    for (int j = base; j < s; ++j)
-        if (__ldg(ids + j) == e) raise_status(status, FT_ERR_INVALID_ROUTING);
-    return e;
-}
-
 // Rank of each slot among the slots of the same expert inside a warp's contiguous
-// range [lo, hi), in slot order; per-warp expert counts accumulate in cnt[E].
+// range [lo, hi), in slot order; per-warp expert counts accumulate in cnt[E]. An id
+// out of range is flagged and the slot skipped; an id repeated inside a token's row is
+// flagged but still placed. The row's earlier slots inside the warp's 32-slot window
+// are compared through shuffles, the rest (a row that began before the window) loaded.
 __device__ __forceinline__ void warp_rank_range(const int32_t *ids, int lo, int hi, int k, int E, int *cnt,
                                                 int *rank_out, int rank_base, int *status)
 {
     const int lane = threadIdx.x & 31;
     for (int s0 = lo; s0 < hi; s0 += 32) {
-        int s = s0 + lane;
-        int e = (s < hi) ? checked_expert(ids, s, k, E, status) : -1;
+        const int s = s0 + lane;
+        const int raw = (s < hi) ? __ldg(ids + s) : -1;
+        int e = raw;
+        if (s < hi && (raw < 0 || raw >= E)) {
+            raise_status(status, FT_ERR_INVALID_ROUTING);
+            e = -1;
+        }
+        const int base = s - s % k;  // first slot of the token's row
+        bool dup = false;
+        for (int d = 1; d < k && d < 32; ++d) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, raw, d);
+            if (e >= 0 && lane >= d && s - d >= base && v == e) dup = true;
+        }
+        if (e >= 0)
+            for (int j = base; j < s0; ++j)
+                if (__ldg(ids + j) == e) dup = true;
+        if (dup) raise_status(status, FT_ERR_INVALID_ROUTING);
         uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
         int rank = __popc(peers & lanemask_lt());
         int leader = __ffs(peers) - 1;
