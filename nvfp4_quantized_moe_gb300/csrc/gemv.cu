@@ -307,16 +307,17 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
     if (idx >= (size_t)T * H4) return;
     const int t = (int)(idx / H4), n4 = (int)(idx % H4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // unrolled so that the loads of a group of rows are in flight together; the
-    // additions stay in the order j = 0 .. k-1
+    // the shared row first and the routed rows unrolled, so that the loads are in flight
+    // together; the additions stay in the order j = 0 .. k-1, then the shared row
+    const float4 sh = ysh ? __ldg(reinterpret_cast<const float4 *>(ysh + (size_t)t * H) + n4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
         float4 v = __ldg(reinterpret_cast<const float4 *>(y + ((size_t)t * k + j) * H) + n4);
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     if (ysh) {
-        float4 v = __ldg(reinterpret_cast<const float4 *>(ysh + (size_t)t * H) + n4);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        acc.x += sh.x; acc.y += sh.y; acc.z += sh.z; acc.w += sh.w;
     }
     if (out_dtype == FT_DTYPE_F32) {
         reinterpret_cast<float4 *>(static_cast<float *>(out) + (size_t)t * H)[n4] = acc;

@@ -92,7 +92,7 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
 // flagged but still placed. The row's earlier slots inside the warp's 32-slot window
 // are compared through shuffles, the rest (a row that began before the window) loaded.
 __device__ __forceinline__ void warp_rank_range(const int32_t *ids, int lo, int hi, int k, int E, int *cnt,
-                                                int *rank_out, int rank_base, int *status)
+                                                int *rank_out, int rank_base, int *status, int *e_out = nullptr)
 {
     const int lane = threadIdx.x & 31;
     for (int s0 = lo; s0 < hi; s0 += 32) {
@@ -118,6 +118,7 @@ __device__ __forceinline__ void warp_rank_range(const int32_t *ids, int lo, int 
         int leader = __ffs(peers) - 1;
         int before = (e >= 0) ? cnt[e] : 0;
         if (e >= 0) rank_out[s - rank_base] = before + rank;
+        if (e_out && s < hi) e_out[s - rank_base] = e;  // the slot's expert, or -1
         __syncwarp();
         if (e >= 0 && lane == leader) cnt[e] = before + __popc(peers);
         __syncwarp();
@@ -192,12 +193,13 @@ __global__ void __launch_bounds__(1024) align_fused_kernel(const int32_t *__rest
     int *off = rank + n;                // [E+1]
     int *count = off + E + 1;           // [E]
     int *wt = count + E;                // [33]
+    int *ex = wt + 33;                  // [n] expert of each slot (-1: out of range)
     const int tid = threadIdx.x, wid = tid >> 5;
     for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
     const int per = (n + 31) / 32;
     int lo = min(n, wid * per), hi = min(n, lo + per);
-    warp_rank_range(ids, lo, hi, k, E, cnt + wid * E, rank, 0, status);
+    warp_rank_range(ids, lo, hi, k, E, cnt + wid * E, rank, 0, status, ex);
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) {
         int run = 0;
@@ -216,8 +218,8 @@ __global__ void __launch_bounds__(1024) align_fused_kernel(const int32_t *__rest
     if (tid == 0) off[E] = total;
     __syncthreads();
     for (int s = tid; s < n; s += blockDim.x) {
-        int e = __ldg(ids + s);
-        if (e < 0 || e >= E) continue;
+        const int e = ex[s];
+        if (e < 0) continue;
         int w = s / per;
         sorted_slot[off[e] + cnt[w * E + e] + rank[s]] = s;
     }
@@ -316,7 +318,7 @@ cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t
 {
     const int n = T * k;
     if (n <= kAlignFusedMax) {
-        size_t smem = sizeof(int) * ((size_t)32 * E + n + (E + 1) + E + 33);
+        size_t smem = sizeof(int) * ((size_t)32 * E + n + (E + 1) + E + 33 + n);
         cudaError_t err = cudaFuncSetAttribute(align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)smem);
         if (err != cudaSuccess) return err;
