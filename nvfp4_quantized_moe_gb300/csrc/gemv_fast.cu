@@ -250,8 +250,8 @@ __device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_p
 // 256 apart, so each warp streams a run of them through one register ring as a single
 // sequence of steps (no refill between units) and writes y at each unit's last step.
 __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int u_lo,
-                                          int u_hi, uint4 *smem_b, float *inv, int *rows, int *s_e, int *tbl_dst,
-                                          float *tbl_w)
+                                          int u_hi, uint4 *smem_b, float *inv, int *rows, int *s_e, float *s_glob,
+                                          int *tbl_dst, float *tbl_w)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -319,7 +319,16 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
             advance_load();
         }
         int cs = 0, r0 = r0a;  // compute cursor: step within the unit, the unit's first row
+        float *gs = s_glob + threadIdx.x * 4;
         for (int t0 = 0; t0 < tot; t0 += 4) {  // S, and so tot, is a multiple of 4
+            if (cs == 0) {  // a unit's first steps: copy its rows' globals to shared memory
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    cp_async_4(gs + 2 * half, glob_e + r0 + g + 8 * half);
+                    cp_async_4(gs + 2 * half + 1, glob_e + r0 + g + 8 * half + 16);
+                }
+                cp_async_commit();
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (t0 + q + 2 < tot) {
@@ -330,6 +339,7 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
             }
             cs += 4;
             if (cs == S) {  // the unit's last step: y rows r0 .. r0 + 31 of its positions
+                cp_async_wait<0>();
 #pragma unroll
                 for (int col = 0; col < 2; ++col) {
                     const int dst = tbl_dst[2 * c + col];
@@ -339,8 +349,8 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int n = r0 + g + 8 * half;
-                        yrow[n] = acc0[2 * half + col] * __ldg(glob_e + n) * w;
-                        yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * w;
+                        yrow[n] = acc0[2 * half + col] * gs[2 * half] * w;
+                        yrow[n + 16] = acc1[2 * half + col] * gs[2 * half + 1] * w;
                     }
                 }
 #pragma unroll
@@ -362,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     __shared__ float inv[kGemvBlock];
     __shared__ int rows[kGemvBlock];
     __shared__ int s_e;  // expert of the staged block
+    __shared__ float s_glob[GATED ? 1 : kThreads * 4];  // down: each thread's row globals of its current unit
     __shared__ float red[KS > 1 ? 8 : 1][32][8];
     const int n_pos0 = load_n_pos(L.prob[0]);
     const int n_pos1 = L.nprob > 1 ? load_n_pos(L.prob[1]) : 0;
@@ -414,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         if (L.prob[0].K % (4 * kStep) == 0 && (L.nprob < 2 || L.prob[1].K % (4 * kStep) == 0)) {
             __shared__ int tbl_dst[kGemvBlock];
             __shared__ float tbl_w[kGemvBlock];
-            down_runs(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, inv, rows, &s_e, tbl_dst, tbl_w);
+            down_runs(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, inv, rows, &s_e, s_glob, tbl_dst, tbl_w);
             return;
         }
     }
