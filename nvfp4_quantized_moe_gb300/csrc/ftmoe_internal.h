@@ -13,8 +13,9 @@ namespace ftmoe {
 // Slots are grouped into blocks of this many rows for the warp-MMA (decode) path:
 // one block is the N=8 side of an m16n8k16 MMA.
 constexpr int kGemvBlock = 8;
-// Align: slot counts up to this size are sorted by one CTA; larger ones by three
-// grid-wide passes over chunks of kAlignChunk slots.
+// Align: slot counts up to this size are sorted by one CTA when its shared memory
+// (32 E + 2 n + 2 E + 34 ints) fits; larger ones by three grid-wide passes over chunks of
+// kAlignChunk slots.
 constexpr int kAlignFusedMax = 8192;
 constexpr int kAlignChunk = 2048;
 

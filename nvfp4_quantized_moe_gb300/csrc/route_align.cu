@@ -95,9 +95,20 @@ __device__ __forceinline__ void warp_rank_range(const int32_t *ids, int lo, int 
                                                 int *rank_out, int rank_base, int *status, int *e_out = nullptr)
 {
     const int lane = threadIdx.x & 31;
-    for (int s0 = lo; s0 < hi; s0 += 32) {
+    constexpr int kAhead = 8;  // windows of 32 slots whose ids are loaded together
+    for (int s00 = lo; s00 < hi; s00 += 32 * kAhead) {
+    int raws[kAhead];
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) {
+        const int s = s00 + 32 * i + lane;
+        raws[i] = (s < hi) ? __ldg(ids + s) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) {
+        const int s0 = s00 + 32 * i;
+        if (s0 >= hi) continue;  // (uniform over the warp)
         const int s = s0 + lane;
-        const int raw = (s < hi) ? __ldg(ids + s) : -1;
+        const int raw = raws[i];
         int e = raw;
         if (s < hi && (raw < 0 || raw >= E)) {
             raise_status(status, FT_ERR_INVALID_ROUTING);
@@ -122,6 +133,7 @@ __device__ __forceinline__ void warp_rank_range(const int32_t *ids, int lo, int 
         __syncwarp();
         if (e >= 0 && lane == leader) cnt[e] = before + __popc(peers);
         __syncwarp();
+    }
     }
 }
 
@@ -176,7 +188,7 @@ __device__ void fill_blocks(const int *off, const int *count, int E, int B, int 
     }
 }
 
-// One CTA sorts up to kAlignFusedMax slots: 32 warps each rank a contiguous range,
+// One CTA sorts up to kAlignFusedMax slots (shared memory permitting): 32 warps each rank a contiguous range,
 // then per-expert prefixes over warps, padded offsets, placement.
 __global__ void __launch_bounds__(1024) align_fused_kernel(const int32_t *__restrict__ ids, int n, int k, int E,
                                                            int B, int32_t *sorted_slot, int32_t *block_expert,
@@ -273,10 +285,15 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int *chunk_cnt, int n_
     const int tid = threadIdx.x;
     for (int e = tid; e < E; e += blockDim.x) {
         int run = 0;
-        for (int c = 0; c < n_chunks; ++c) {
-            int v = chunk_cnt[(size_t)c * E + e];
-            chunk_cnt[(size_t)c * E + e] = run;
-            run += v;
+        for (int c0 = 0; c0 < n_chunks; c0 += 8) {  // 8 chunks' counts loaded together
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = c0 + i < n_chunks ? chunk_cnt[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (c0 + i < n_chunks) chunk_cnt[(size_t)(c0 + i) * E + e] = run;
+                run += v[i];
+            }
         }
         count[e] = run;
         off[e] = (run + B - 1) / B * B;
@@ -305,9 +322,13 @@ __global__ void align_place_kernel(const int32_t *__restrict__ ids, int n, int E
 
 static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Shared memory of the one-CTA align, and whether it fits the per-block opt-in limit.
+static size_t align_fused_smem(int n, int E) { return sizeof(int) * ((size_t)32 * E + n + (E + 1) + E + 33 + n); }
+static bool align_fused_ok(int n, int E) { return n <= kAlignFusedMax && align_fused_smem(n, E) <= 227 * 1024; }
+
 size_t align_scratch_bytes(int n_slots, int E)
 {
-    if (n_slots <= kAlignFusedMax) return 0;
+    if (align_fused_ok(n_slots, E)) return 0;
     size_t chunks = (size_t)(n_slots + kAlignChunk - 1) / kAlignChunk;
     return round_up(chunks * E * sizeof(int), 256) + round_up((size_t)n_slots * sizeof(int), 256);
 }
@@ -317,8 +338,8 @@ cudaError_t launch_align(const int32_t *ids, int T, int k, int E, int B, int32_t
                          void *scratch, cudaStream_t s, int *zero, size_t zero_bytes)
 {
     const int n = T * k;
-    if (n <= kAlignFusedMax) {
-        size_t smem = sizeof(int) * ((size_t)32 * E + n + (E + 1) + E + 33 + n);
+    if (align_fused_ok(n, E)) {
+        const size_t smem = align_fused_smem(n, E);
         cudaError_t err = cudaFuncSetAttribute(align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)smem);
         if (err != cudaSuccess) return err;
