@@ -51,12 +51,16 @@ constexpr int KC = 64;        // K elements per chunk (128 bytes of f16)
 constexpr int NSMAX = 6;      // TMA stages (at most)
 constexpr int NA = 4;         // dequantised A buffers (tensor memory)
 constexpr uint32_t kColA = 2 * NT;  // A buffer ab, tile t at columns kColA + 64 ab + 32 t
-constexpr int kThreadsTc = 480;  // producer, MMA (tile 0), 8 dequant, 4 epilogue, MMA (tile 1)
+// Warps: 0 producer, 1 MMA (tile 0), 2..9 dequantise, 10..13 epilogue, 14 MMA (tile 1),
+// and for the down stage 15..18 a second epilogue group: the down epilogue (transpose and
+// 512-byte row stores) is that stage's limit, so two warps per TMEM quadrant take
+// alternate 32-position chunks of the accumulator.
+__host__ __device__ constexpr int tc_epi_groups(bool gated) { return gated ? 1 : 2; }
+__host__ __device__ constexpr int tc_threads(bool gated) { return gated ? 480 : 608; }
 constexpr int kMmaWarp1 = 14;    // issuer of tile 1: the issue cost of a tcgen05.mma is per
                                  // issuing thread, so one issuer per tile doubles the rate
 constexpr int kDq = 256;         // dequantising threads
-constexpr int kEp = 128;         // epilogue threads (one TMEM lane each)
-constexpr int kEpWarp0 = 10;     // first epilogue warp
+constexpr int kEpWarp0 = 10;     // first epilogue warp (group 0: 10..13, group 1: 15..18)
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
@@ -83,7 +87,7 @@ struct TcSmem {
 // 64 (fp8_block, one code a byte).
 __host__ __device__ constexpr uint32_t raw_row_bytes(bool fp8) { return fp8 ? 64u : 32u; }
 
-__host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8 = false)
+__host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8, bool gated)
 {
     TcSmem s;
     s.a_bytes = 0;  // the dequantised A operand lives in tensor memory
@@ -95,8 +99,9 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8 = f
     s.a_off = 0;
     s.b_off = s.a_off + NA * s.a_bytes;
     s.raw_off = s.b_off + ns * s.b_bytes;
-    s.tp_off = s.raw_off + ns * s.raw_bytes;      // down epilogue: two 32-position x 256-row bf16 tiles
-    s.tbl_off = s.tp_off + 2 * 32 * 2 * MT * 2;
+    // down epilogue: per group two 32-position x 256-row bf16 tiles
+    s.tp_off = s.raw_off + ns * s.raw_bytes;
+    s.tbl_off = s.tp_off + (gated ? 0 : tc_epi_groups(false) * 2 * 32 * 2 * MT * 2);
     s.bar_off = s.tbl_off + 2 * NT * 8;           // two position tables (unit parity): [NT] slots + [NT] factors
     s.total = s.bar_off + 512;
     return s;
@@ -110,7 +115,7 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8 = f
 // chosen from the tile's largest scale_inv so that every product stays below 2^15; the
 // epilogue multiplies 2^e_t back in place of the row global.
 template <bool GATED, bool FP8>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+__global__ void __launch_bounds__(tc_threads(GATED), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap b_map,
                    const __grid_constant__ TcParams p, int ns)
 {
@@ -120,13 +125,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // compiler keeps every access derived from it in the shared state space
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int K = p.K;
-    const TcSmem L = tc_smem(K, p.group, ns, FP8);
+    const TcSmem L = tc_smem(K, p.group, ns, FP8, GATED);
+    constexpr int NG = tc_epi_groups(GATED);  // epilogue groups of 4 warps
     constexpr int RB = (int)raw_row_bytes(FP8);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
     uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + 2;  // one accumulator (index 0)
-    uint64_t *tp_bar = acc_empty + 2;  // down epilogue: transpose tile written by all 4 warps
-    uint64_t *tbl_bar = tp_bar + 2;    // epilogue: a unit's position table written by all 4 warps
+    uint64_t *tp_bar = acc_empty + 2;  // down epilogue, per group: transpose tile written by its 4 warps
+    uint64_t *tbl_bar = tp_bar + 4;    // epilogue: a unit's position table (written by group 0)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tbl_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -141,10 +147,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int i = 0; i < NA; ++i) { mbar_init(a_full + i, kDq / 32); mbar_init(a_empty + i, 2); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full + i, 2);
-            mbar_init(acc_empty + i, kEp / 32);
-            mbar_init(tp_bar + i, kEp / 32);
-            mbar_init(tbl_bar + i, kEp / 32);
+            mbar_init(acc_empty + i, 4 * NG);  // every epilogue warp, after its last TMEM read
+            mbar_init(tbl_bar + i, 4 * NG);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(tp_bar + i, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -364,24 +370,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         // Thread = TMEM lane = tile row r (warp w may read lanes 32 (w % 4) ..); every
-        // thread handles all NT positions of its row in both tiles of the accumulator.
+        // thread handles its row in both tiles of the accumulator, for the 32-position
+        // chunks cb = eg, eg + NG, ... of its group eg.
         // Per unit the warps first build a table of the block's positions (slot and routing
         // weight x activation row scale, or the row scale alone) in shared memory, and load
         // their rows' globals, while the MMAs of the unit are still running.
         const int quarter = warp & 3;
         const int r = 32 * quarter + lane;
-        // One position table per unit, built by the four warps together (lane = position,
-        // 32 per warp) and double-buffered by unit parity: a warp writes table X for unit u
-        // only after passing the table barrier of unit u - 1, which every warp reaches after
+        const int eg = warp < kMmaWarp1 ? 0 : 1;               // epilogue group
+        const int ew = warp - (eg ? kMmaWarp1 + 1 : kEpWarp0);  // warp within the group
+        // One position table per unit, built by group 0 (lane = position, 32 per warp) and
+        // double-buffered by unit parity: a warp writes table X for unit u only after
+        // passing the table barrier of unit u - 1, which every epilogue warp reaches after
         // finishing unit u - 2, the last reader of table X.
-        const int ew = warp - kEpWarp0;
         int uc = 0, gc = 0;  // units, and down-epilogue chunks (transpose tile use count)
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
             const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
             const int X = uc & 1;
             int *tbl_slot = reinterpret_cast<int *>(smem + L.tbl_off) + X * 2 * NT;
             float *tbl_w = reinterpret_cast<float *>(tbl_slot + NT);
-            {
+            if (eg == 0) {
                 const int t = 32 * ew + lane, pos = b * NT + t;
                 float w = p.act_scale ? __ldg(p.act_scale + pos) : 1.f;
                 int dst = pos;
@@ -424,12 +432,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (!warp_wait_bar(acc_full, uc & 1, abort_flag)) { dead = true; break; }
             tc::fence_after_sync();
             const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-            for (int cb = 0; cb < NT / 32; ++cb) {
+            for (int cb = eg; cb < NT / 32; cb += NG) {
                 uint32_t v0[32], v1[32];
                 tc::ld32(lane_addr + cb * 32, v0);
                 tc::ld32(lane_addr + NT + cb * 32, v1);
                 tc::wait_ld();
-                if (cb == NT / 32 - 1) {  // accumulator read out: the next unit's MMAs may start
+                if (cb + NG >= NT / 32) {  // this warp's share read out: the next unit's MMAs may start
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) arrive(acc_empty);
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     // every thread writes its row of the two tiles into a shared [32][256] bf16
                     // tile, then each warp stores 8 whole position rows with 16-byte stores
                     // (512 contiguous bytes per warp instruction instead of 64).
-                    const int X = gc & 1;
+                    const int X = eg * 2 + (gc & 1);  // the group's tile, by chunk parity
                     uint16_t *tb = reinterpret_cast<uint16_t *>(smem + L.tp_off + X * (32 * 2 * MT * 2));
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -582,22 +590,21 @@ bool tc_shape_ok(int K, int group, int rows_per_expert)
     return K % KC == 0 && K >= KC && rows_per_expert % MT == 0 && (K / group) % 16 == 0 && K / group <= 256;
 }
 
-// Deepest TMA ring (4, 3 or 2 stages) that fits the opt-in shared memory.
-static int tc_stages(int K, int group, bool fp8 = false)
+// Deepest TMA ring (NSMAX down to 2 stages) that fits the opt-in shared memory.
+static int tc_stages(int K, int group, bool fp8, bool gated)
 {
     int optin = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     for (int ns = NSMAX; ns >= 2; --ns)
-        if (tc_smem(K, group, ns, fp8).total + 1024 <= (uint32_t)optin) return ns;
+        if (tc_smem(K, group, ns, fp8, gated).total + 1024 <= (uint32_t)optin) return ns;
     return 0;
 }
 
 size_t tc_smem_bytes(bool gated, int K, int group)
 {
-    (void)gated;
-    const int ns = tc_stages(K, group);
-    return ns ? tc_smem(K, group, ns).total + 1024 : 0;
+    const int ns = tc_stages(K, group, false, gated);
+    return ns ? tc_smem(K, group, ns, false, gated).total + 1024 : 0;
 }
 
 cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
@@ -622,7 +629,7 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
                            const void *act, int64_t act_rows, int max_units, cudaStream_t s)
 {
     const bool fp8 = p.fp8 != 0;
-    const int ns = tc_stages(p.K, p.group, fp8);
+    const int ns = tc_stages(p.K, p.group, fp8, gated);
     if (!ns) return cudaErrorInvalidValue;
     CUtensorMap cmap, bmap;
     // codes: NVFP4 rows of K/2 bytes in boxes of 32 bytes (no swizzle); fp8_block rows of K
@@ -633,7 +640,7 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
         !make_tensor_map_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, (uint64_t)p.K, (uint64_t)act_rows,
                             (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const size_t smem = tc_smem(p.K, p.group, ns, fp8).total + 1024;
+    const size_t smem = tc_smem(p.K, p.group, ns, fp8, gated).total + 1024;
     int grid = sm_count();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
@@ -641,7 +648,7 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
                     : (gated ? tc_gemm_kernel<true, false> : tc_gemm_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    FT_LAUNCH(kern, dim3(grid), dim3(kThreadsTc), smem, s, cmap, bmap, p, ns);
+    FT_LAUNCH(kern, dim3(grid), dim3(tc_threads(gated)), smem, s, cmap, bmap, p, ns);
     count_launches(1);
     return cudaGetLastError();
 }
