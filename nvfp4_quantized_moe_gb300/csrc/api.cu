@@ -625,10 +625,11 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         e = launch_rows_to_f16(xb, G.H, sorted, npad, 0, n_slots, G.k, L.pmax, f16buf(L.xs), f32buf(L.xs_scale), s);
         if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
         gp.act_scale = f32buf(L.xs_scale);
-        e = launch_tc_gemm(gp, true, routed->p[FT_GU], (int64_t)G.E * 2 * G.Il, f16buf(L.xs), L.pmax,
-                           max_blocks_tc * gp.n_mtiles, s);
-        if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
-        if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        // routed and shared expert in one launch (units of the routed experts first)
+        TcParams gprob[2] = {gp, gp};
+        TcOperands gops[2] = {{routed->p[FT_GU], (int64_t)G.E * 2 * G.Il, f16buf(L.xs), L.pmax}, {}};
+        int n_gprob = 1, gunits = max_blocks_tc * gp.n_mtiles;
+        const int tp = tpad_tc * kTcBlock;
         if (G.Is) {
             TcParams sp = gp;
             sp.scales = static_cast<const uint8_t *>(shared->p[FT_GU_SCALE]);
@@ -638,13 +639,16 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sp.n_slots = T; sp.top_k = 1; sp.h_out = h_sh; sp.h_ld = G.Isl;
             sp.act_scale = f32buf(L.x16_scale);
             fp8_fields(sp, shared, true, G.Isl);
-            const int tp = tpad_tc * kTcBlock;
             e = launch_rows_to_f16(xb, G.H, nullptr, nullptr, tp, T, 1, tp, f16buf(L.x16), f32buf(L.x16_scale), s);
             if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
-            e = launch_tc_gemm(sp, true, shared->p[FT_GU], 2 * (int64_t)G.Isl, f16buf(L.x16), tp,
-                               tpad_tc * sp.n_mtiles, s);
-            if (e != cudaSuccess) return cuda_fail(e, "shared gate_up launch");
+            gprob[1] = sp;
+            gops[1] = {shared->p[FT_GU], 2 * (int64_t)G.Isl, f16buf(L.x16), tp};
+            n_gprob = 2;
+            gunits += tpad_tc * sp.n_mtiles;
         }
+        if ((e = launch_tc_gemm(gprob, gops, n_gprob, true, gunits, s)) != cudaSuccess)
+            return cuda_fail(e, "gate_up launch");
+        if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         TcParams dp = {};
         dp.scales = static_cast<const uint8_t *>(routed->p[FT_DN_SCALE]);
@@ -657,10 +661,9 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         // h rows are already in sorted-position order: convert them in place of a gather
         e = launch_rows_to_f16(h, G.Il, nullptr, npad, 0, L.pmax, 1, L.pmax, f16buf(L.h16), f32buf(L.h16_scale), s);
         if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
-        e = launch_tc_gemm(dp, false, routed->p[FT_DN], (int64_t)G.E * G.H, f16buf(L.h16), L.pmax,
-                           max_blocks_tc * dp.n_mtiles, s);
-        if (e != cudaSuccess) return cuda_fail(e, "down launch");
-        if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        TcParams dprob[2] = {dp, dp};
+        TcOperands dops[2] = {{routed->p[FT_DN], (int64_t)G.E * G.H, f16buf(L.h16), L.pmax}, {}};
+        int n_dprob = 1, dunits = max_blocks_tc * dp.n_mtiles;
         if (G.Is) {
             TcParams sd = dp;
             sd.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
@@ -669,14 +672,17 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.y_out = yb_sh; sd.route_w = nullptr;
             sd.act_scale = f32buf(L.hsh16_scale);
             fp8_fields(sd, shared, false, G.Isl);
-            const int tp = tpad_tc * kTcBlock;
             e = launch_rows_to_f16(h_sh, G.Isl, nullptr, nullptr, tp, T, 1, tp, f16buf(L.hsh16),
                                    f32buf(L.hsh16_scale), s);
             if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
-            e = launch_tc_gemm(sd, false, shared->p[FT_DN], G.H, f16buf(L.hsh16), (int64_t)tpad_tc * kTcBlock,
-                               tpad_tc * sd.n_mtiles, s);
-            if (e != cudaSuccess) return cuda_fail(e, "shared down launch");
+            dprob[1] = sd;
+            dops[1] = {shared->p[FT_DN], G.H, f16buf(L.hsh16), tp};
+            n_dprob = 2;
+            dunits += tpad_tc * sd.n_mtiles;
         }
+        if ((e = launch_tc_gemm(dprob, dops, n_dprob, false, dunits, s)) != cudaSuccess)
+            return cuda_fail(e, "down launch");
+        if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         e = launch_combine_bf16(yb, G.Is ? yb_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
         if (e != cudaSuccess) return cuda_fail(e, "combine launch");

@@ -73,13 +73,27 @@ struct TcParams {
     const float *sinv;       // fp8_block: scale_inv [E][R/128][K/128]
     int64_t e_sinv;          // fp8_block: per-expert stride of sinv (elements)
 };
+// One tensor-core grouped GEMM launch over up to two problems of the same stage, format
+// and group (the routed experts, then the shared expert): units of problem 0, then of
+// problem 1; K may differ between them.
+struct TcLaunch {
+    TcParams prob[2];
+    int nprob;
+};
+// The operands of one problem: its bank's packed codes (rows_total rows) and the f16
+// matrix its B operand comes from (act_rows rows of K).
+struct TcOperands {
+    const void *codes;
+    int64_t rows_total;
+    const void *act;
+    int64_t act_rows;
+};
 bool tc_shape_ok(int K, int group, int rows_per_expert);
 bool tc_shape_ok_fp8(int K, int rows_per_expert);
 size_t tc_smem_bytes(bool gated, int K, int group);
-// codes: the bank's packed codes (rows_total rows of K/2 bytes); act: the activation
-// matrix the B operand comes from (gate_up: x, act_rows = T; down: h, act_rows = its rows).
-cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total,
-                           const void *act, int64_t act_rows, int max_units, cudaStream_t s);
+// nprob (1 or 2) problems in one launch; max_units bounds their total unit count.
+cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int nprob, bool gated, int max_units,
+                           cudaStream_t s);
 // B rows for the f16 tensor-core path: out[pos] = f16(src[row] * 2^-e), scale[pos] = 2^e,
 // row = token of sorted_slot[pos] (or pos when sorted_slot is null; rows >= n_slots and
 // padding slots give zero rows). pos < *n_pos_dev, or < n_pos_static when that is null.

@@ -116,16 +116,17 @@ __host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8, bo
 // epilogue multiplies 2^e_t back in place of the row global.
 template <bool GATED, bool FP8>
 __global__ void __launch_bounds__(tc_threads(GATED), 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap b_map,
-                   const __grid_constant__ TcParams p, int ns)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap codes_map0, const __grid_constant__ CUtensorMap b_map0,
+                   const __grid_constant__ CUtensorMap codes_map1, const __grid_constant__ CUtensorMap b_map1,
+                   const __grid_constant__ TcLaunch TL, int ns)
 {
     pdl_enter();
+    const TcParams &p0 = TL.prob[0];  // what both problems share: group, format, status
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base by pointer arithmetic on the shared array itself, so that the
     // compiler keeps every access derived from it in the shared state space
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int K = p.K;
-    const TcSmem L = tc_smem(K, p.group, ns, FP8, GATED);
+    const TcSmem L = tc_smem(p0.K, p0.group, ns, FP8, GATED);
     constexpr int NG = tc_epi_groups(GATED);  // epilogue groups of 4 warps
     constexpr int RB = (int)raw_row_bytes(FP8);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -156,17 +157,30 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
     }
     if (warp == 1) tc::tmem_alloc(tmem_slot, tmem_cols);
     if (warp == 0 && lane == 0) {
-        tc::prefetch_map(&codes_map);
-        tc::prefetch_map(&b_map);
+        tc::prefetch_map(&codes_map0);
+        tc::prefetch_map(&b_map0);
+        if (TL.nprob > 1) {
+            tc::prefetch_map(&codes_map1);
+            tc::prefetch_map(&b_map1);
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    const int n_pos = p.n_pos_dev ? *p.n_pos_dev : (p.n_pos_static + NT - 1) / NT * NT;
-    const int n_units = (n_pos / NT) * p.n_mtiles;
-    const int nk = K / KC;
+    // units: problem 0's (blocks x row tiles), then problem 1's
+    auto n_units_of = [&](const TcParams &q) {
+        const int n_pos = q.n_pos_dev ? *q.n_pos_dev : (q.n_pos_static + NT - 1) / NT * NT;
+        return (n_pos / NT) * q.n_mtiles;
+    };
+    const int units0 = n_units_of(p0);
+    const int n_units = units0 + (TL.nprob > 1 ? n_units_of(TL.prob[1]) : 0);
+    // the problem of unit u and u's index within it
+    auto prob_of = [&](int u, int &lu) -> const TcParams & {
+        lu = u < units0 ? u : u - units0;
+        return TL.prob[u < units0 ? 0 : 1];
+    };
     const int tile_rows = GATED ? MT : 2 * MT;  // row stride of the unit index m
     // units are strided over the CTAs: at any moment the GPU works on consecutive units,
     // which share their block's B tiles in L2
@@ -177,21 +191,26 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         if (lane == 0) {
             int it = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
-                const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
+                int lu;
+                const TcParams &p = prob_of(u, lu);
+                const CUtensorMap *codes_map = u < units0 ? &codes_map0 : &codes_map1;
+                const CUtensorMap *b_map = u < units0 ? &b_map0 : &b_map1;
+                const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
                 const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
                 const int row_a = e * p.R + m * tile_rows;
                 const int row_b = GATED ? row_a + p.up_off : row_a + MT;
+                const int nk = p.K / KC;
                 for (int c = 0; c < nk; ++c, ++it) {
                     const int slot = it % ns;
                     if (!wait_bar(empty + slot, ((it / ns) & 1) ^ 1, abort_flag)) { dead = true; break; }
                     unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
                     mbar_arrive_expect_tx(full + slot, L.raw_bytes + L.b_bytes);
-                    tc::tma_load_2d(raw, &codes_map, c * RB, row_a, full + slot);
-                    tc::tma_load_2d(raw + MT * RB, &codes_map, c * RB, row_b, full + slot);
-                    tc::tma_load_2d(smem + L.b_off + slot * L.b_bytes, &b_map, c * KC, b * NT, full + slot);
+                    tc::tma_load_2d(raw, codes_map, c * RB, row_a, full + slot);
+                    tc::tma_load_2d(raw + MT * RB, codes_map, c * RB, row_b, full + slot);
+                    tc::tma_load_2d(smem + L.b_off + slot * L.b_bytes, b_map, c * KC, b * NT, full + slot);
                 }
             }
-            if (dead) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
+            if (dead) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
             // let every issued copy land before the CTA's shared memory can be released:
             // wait for the last issued phase of each stage (already complete unless a
             // consumer gave up)
@@ -207,6 +226,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             const uint32_t idesc = tc::idesc_f16_f32(MT, NT);
             int it = 0, ia = 0, uc = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
+                int lu;
+                const int nk = prob_of(u, lu).K / KC;
                 // one accumulator: the epilogue of the previous unit has read it out
                 if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag)) { dead = true; break; }
                 tc::fence_after_sync();
@@ -232,7 +253,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 if (dead) break;
                 tc::commit(acc_full);
             }
-            if (dead) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
+            if (dead) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
         }
     } else if (FP8 && warp < kEpWarp0) {
         // ------------------------------------------------------------ dequantisation (fp8_block)
@@ -242,10 +263,12 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         // different bank quads) and writes 128 bytes of A.
         const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;
-        const int kbn = K / 128;
         int it = 0, ia = 0;
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
-            const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
+            int lu;
+            const TcParams &p = prob_of(u, lu);
+            const int kbn = p.K / 128, nk = p.K / KC;
+            const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
             const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
             const int nb = GATED ? (half ? p.up_off / MT : 0) + m : 2 * m + half;  // the tile's scale block row
             const float *srow = p.sinv + (size_t)e * p.e_sinv + (size_t)nb * kbn;
@@ -290,7 +313,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 if (lane == 0) arrive(a_full + ab);
             }
         }
-        if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
+        if (dead && lane == 0) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else if (warp < kEpWarp0) {
         // ------------------------------------------------------------ dequantisation
         // warp (quarter, half): rows 32*quarter .. +32 of tile `half`.
@@ -298,19 +321,22 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         // 16-byte groups (one group covers cpl chunks), one group ahead, across units.
         const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;
-        const int cpl = 16 * p.group / KC;  // K chunks covered by 16 scale bytes
-        const int ngroups = nk / cpl;
-        const size_t srow_bytes = (size_t)(K / p.group);
+        const int cpl = 16 * p0.group / KC;  // K chunks covered by 16 scale bytes
         auto scale_row = [&](int uu) {
-            const int bb = uu / p.n_mtiles, mm = uu - bb * p.n_mtiles;
-            const int ee = p.block_expert ? __ldg(p.block_expert + bb) : 0;
-            const int row = ee * p.R + mm * tile_rows + (half ? (GATED ? p.up_off : MT) : 0) + r;
-            return p.scales + (size_t)row * srow_bytes;
+            int lu;
+            const TcParams &q = prob_of(uu, lu);
+            const int bb = lu / q.n_mtiles, mm = lu - bb * q.n_mtiles;
+            const int ee = q.block_expert ? __ldg(q.block_expert + bb) : 0;
+            const int row = ee * q.R + mm * tile_rows + (half ? (GATED ? q.up_off : MT) : 0) + r;
+            return q.scales + (size_t)row * (size_t)(q.K / q.group);
         };
         int it = 0, ia = 0;
-        const uint8_t *srow = blockIdx.x < n_units ? scale_row(blockIdx.x) : p.scales;
+        const uint8_t *srow = blockIdx.x < n_units ? scale_row(blockIdx.x) : p0.scales;
         uint4 s_next = blockIdx.x < n_units ? __ldg(reinterpret_cast<const uint4 *>(srow)) : make_uint4(0, 0, 0, 0);
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
+            int lu;
+            const int nk = prob_of(u, lu).K / KC;
+            const int ngroups = nk / cpl;
             const int u_next = u + gridDim.x;
             const uint8_t *srow_next = u_next < n_units ? scale_row(u_next) : nullptr;
             uint4 s16 = make_uint4(0, 0, 0, 0);
@@ -329,7 +355,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 }
                 const int ci = c % cpl;
                 uint32_t sw;
-                if (p.group == 16) {
+                if (p0.group == 16) {
                     sw = ci == 0 ? s16.x : ci == 1 ? s16.y : ci == 2 ? s16.z : s16.w;
                 } else {
                     const int wi = ci >> 1;
@@ -366,7 +392,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             if (dead) break;
             srow = srow_next;
         }
-        if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
+        if (dead && lane == 0) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else {
         // ------------------------------------------------------------ epilogue
         // Thread = TMEM lane = tile row r (warp w may read lanes 32 (w % 4) ..); every
@@ -385,7 +411,9 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         // finishing unit u - 2, the last reader of table X.
         int uc = 0, gc = 0;  // units, and down-epilogue chunks (transpose tile use count)
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
-            const int b = u / p.n_mtiles, m = u - b * p.n_mtiles;
+            int lu;
+            const TcParams &p = prob_of(u, lu);
+            const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
             const int X = uc & 1;
             int *tbl_slot = reinterpret_cast<int *>(smem + L.tbl_off) + X * 2 * NT;
             float *tbl_w = reinterpret_cast<float *>(tbl_slot + NT);
@@ -485,7 +513,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 }
             }
         }
-        if (dead && lane == 0) { raise_status(p.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
+        if (dead && lane == 0) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     }
 
     // wind down (the producer has let its copies land before reaching this barrier)
@@ -621,26 +649,39 @@ cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slo
     return cudaGetLastError();
 }
 
-// codes: the bank's packed codes (rows_total rows of K/2 bytes); act: the B operand
-// rows (gate_up: the f16 expert-sorted copy of x or, for the shared expert, the f16 copy
-// of x; down: the f16 copy of h), act_rows rows of K f16, read in blocks of 128
-// consecutive rows.
-cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int64_t rows_total,
-                           const void *act, int64_t act_rows, int max_units, cudaStream_t s)
+// Per problem: codes = the bank's packed codes (rows_total rows of K/2 bytes, or K bytes
+// for fp8_block); act = the B operand rows (gate_up: the f16 expert-sorted copy of x or,
+// for the shared expert, the f16 copy of x; down: the f16 copy of h), act_rows rows of K
+// f16, read in blocks of 128 consecutive rows. The problems share group and format.
+cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int nprob, bool gated, int max_units,
+                           cudaStream_t s)
 {
-    const bool fp8 = p.fp8 != 0;
-    const int ns = tc_stages(p.K, p.group, fp8, gated);
+    if (nprob < 1 || nprob > 2) return cudaErrorInvalidValue;
+    if (nprob == 2 && (probs[1].group != probs[0].group || probs[1].fp8 != probs[0].fp8)) return cudaErrorInvalidValue;
+    const bool fp8 = probs[0].fp8 != 0;
+    const int ns = tc_stages(probs[0].K, probs[0].group, fp8, gated);
     if (!ns) return cudaErrorInvalidValue;
-    CUtensorMap cmap, bmap;
-    // codes: NVFP4 rows of K/2 bytes in boxes of 32 bytes (no swizzle); fp8_block rows of K
-    // bytes in boxes of 64 bytes with the 64-byte swizzle the dequantising warps undo
-    const uint64_t row_bytes = fp8 ? (uint64_t)p.K : (uint64_t)p.K / 2;
-    if (!make_tensor_map_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, row_bytes, (uint64_t)rows_total, row_bytes,
-                            raw_row_bytes(fp8), MT, fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_tensor_map_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, act, (uint64_t)p.K, (uint64_t)act_rows,
-                            (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    const size_t smem = tc_smem(p.K, p.group, ns, fp8, gated).total + 1024;
+    CUtensorMap cmap[2], bmap[2];
+    TcLaunch TL = {};
+    TL.nprob = nprob;
+    for (int i = 0; i < nprob; ++i) {
+        const TcParams &p = probs[i];
+        TL.prob[i] = p;
+        // codes: NVFP4 rows of K/2 bytes in boxes of 32 bytes (no swizzle); fp8_block rows of
+        // K bytes in boxes of 64 bytes with the 64-byte swizzle the dequantising warps undo
+        const uint64_t row_bytes = fp8 ? (uint64_t)p.K : (uint64_t)p.K / 2;
+        if (!make_tensor_map_2d(&cmap[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, ops[i].codes, row_bytes,
+                                (uint64_t)ops[i].rows_total, row_bytes, raw_row_bytes(fp8), MT,
+                                fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_tensor_map_2d(&bmap[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ops[i].act, (uint64_t)p.K,
+                                (uint64_t)ops[i].act_rows, (uint64_t)p.K * 2, KC, NT, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    if (nprob == 1) {  // (never read)
+        cmap[1] = cmap[0];
+        bmap[1] = bmap[0];
+    }
+    const size_t smem = tc_smem(probs[0].K, probs[0].group, ns, fp8, gated).total + 1024;
     int grid = sm_count();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
@@ -648,7 +689,7 @@ cudaError_t launch_tc_gemm(const TcParams &p, bool gated, const void *codes, int
                     : (gated ? tc_gemm_kernel<true, false> : tc_gemm_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    FT_LAUNCH(kern, dim3(grid), dim3(tc_threads(gated)), smem, s, cmap, bmap, p, ns);
+    FT_LAUNCH(kern, dim3(grid), dim3(tc_threads(gated)), smem, s, cmap[0], bmap[0], cmap[1], bmap[1], TL, ns);
     count_launches(1);
     return cudaGetLastError();
 }
