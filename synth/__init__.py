@@ -65,6 +65,10 @@ SHAPES = {
     # DeepSeek-V4-Flash-like routed FP4 layer, 32-element scale blocks
     "dsv4": LayerShape(hidden=4096, intermediate=2048, num_experts=256, top_k=8,
                        group=32, shared_intermediate=2048),
+    # hidden width not a multiple of 256 (the decode down stage's last row tile of a block
+    # is partly out of range), small enough for full-oracle parity
+    "odd_h": LayerShape(hidden=640, intermediate=512, num_experts=128, top_k=8, group=16,
+                        shared_intermediate=512),
     # fp8_block experts: a small layer (full-oracle parity) and the Qwen3.6-FP8 layer
     "mini_fp8": LayerShape(hidden=256, intermediate=256, num_experts=8, top_k=2, group=128,
                            shared_intermediate=128, fmt="fp8_block"),

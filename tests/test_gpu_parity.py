@@ -241,6 +241,14 @@ def test_forward_qwen36_decode(T):
     assert_close(got, ref, f"qwen36 decode T={T}")
 
 
+@pytest.mark.parametrize("T", [1, 64, 200])
+def test_forward_odd_hidden_decode(T):
+    """H = 640: the down stage's 256-row units of a block end half out of range (at T=64 and
+    200 the down launch streams block runs of units, whose warps then stop early)."""
+    got, ref = _run_and_compare("odd_h", T, False)
+    assert_close(got, ref, f"odd_h decode T={T}")
+
+
 def test_forward_bf16_output():
     got, ref = _run_and_compare("qwen36", 8, False, out_dtype=torch.bfloat16)
     assert_close(got, ref, "bf16 out")
