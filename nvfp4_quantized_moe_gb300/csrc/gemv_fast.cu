@@ -8,6 +8,9 @@
 // its K range. Loads run two 128-element steps ahead through a 4-slot register ring;
 // every address is a per-lane base plus a step offset; scales arrive as one 16-bit load
 // per row and step; the activation swizzle reduces to a per-lane XOR, precomputed.
+// gate_up splits all K steps evenly over the CTAs (a unit cut between two CTAs is
+// finished by the second); the down stage streams each CTA's consecutive units of one
+// block through a single ring (down_runs). The combine is a separate launch.
 #include <cuda_runtime.h>
 
 #include "ftmoe_device.cuh"

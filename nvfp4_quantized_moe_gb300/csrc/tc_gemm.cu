@@ -4,7 +4,9 @@
 // A work unit is (block of NT = 128 expert-sorted positions, two tiles of 128 weight
 // rows): for gate_up the gate rows [i0, i0+128) and the matching up rows I_l + i0 + ..,
 // whose accumulators sit side by side in tensor memory so SwiGLU fuses into the
-// epilogue; for down the rows [n0, n0+256) as two tiles. Warp roles, persistent CTA:
+// epilogue; for down the rows [n0, n0+256) as two tiles. One launch covers the routed
+// experts' units and then the shared expert's (each role looks up its unit's problem;
+// K may differ between the two), strided over persistent CTAs. Warp roles:
 //   warp 0      one thread issues every TMA: per 64-element K chunk the raw packed
 //               codes of both tiles (box 32 bytes x 128 rows; fp8_block 64 bytes with the
 //               64-byte swizzle) and the block's activations (f16 box 64 x 128, 128-byte
@@ -20,13 +22,14 @@
 //               write them straight into tensor memory with tcgen05.st (warp (quarter,
 //               half): TMEM lanes of its quarter, tile `half`) -- the A operand makes no
 //               round trip through shared memory;
-//   warps 10-13 the epilogue: read the accumulator with tcgen05.ld (one TMEM lane = one
-//               weight row per thread), apply globals, row scales and SwiGLU (h) or the
-//               routing weight (y: each 32-position chunk is transposed through shared
-//               memory so that every position's 256 contiguous outputs leave in 512-byte
-//               warp stores). Tensor memory: the accumulator (256 columns) and four A
-//               buffers (256 columns); the accumulator is released as soon as its last
-//               chunk is loaded.
+//   warps 10-13 the epilogue (and, for down, warps 15-18 as a second group taking the
+//               other half of the 32-position chunks): read the accumulator with tcgen05.ld
+//               (one TMEM lane = one weight row per thread), apply globals, row scales and
+//               SwiGLU (h) or the routing weight (y: each 32-position chunk is transposed
+//               through shared memory so that every position's 256 contiguous outputs leave
+//               in 512-byte warp stores). Tensor memory: the accumulator (256 columns) and
+//               four A buffers (256 columns); the accumulator is released once every
+//               epilogue warp has loaded its last chunk.
 // f16 operands instead of bf16: code*scale is exact in both; a bf16 activation row
 // scaled by its power of two (maximum in [2^14, 2^15)) converts to f16 exactly except
 // for elements below 2^-31 of the row maximum, which move by less than 2^-38 of it;
