@@ -22,8 +22,8 @@
 //               write them straight into tensor memory with tcgen05.st (warp (quarter,
 //               half): TMEM lanes of its quarter, tile `half`) -- the A operand makes no
 //               round trip through shared memory;
-//   warps 10-13 the epilogue (and, for down, warps 15-18 as a second group taking the
-//               other half of the 32-position chunks): read the accumulator with tcgen05.ld
+//   warps 10-13 the epilogue (and warps 15-18 as a second group taking the other half
+//               of the 32-position chunks): read the accumulator with tcgen05.ld
 //               (one TMEM lane = one weight row per thread), apply globals, row scales and
 //               SwiGLU (h) or the routing weight (y: each 32-position chunk is transposed
 //               through shared memory so that every position's 256 contiguous outputs leave
@@ -55,11 +55,11 @@ constexpr int NSMAX = 6;      // TMA stages (at most)
 constexpr int NA = 4;         // dequantised A buffers (tensor memory)
 constexpr uint32_t kColA = 2 * NT;  // A buffer ab, tile t at columns kColA + 64 ab + 32 t
 // Warps: 0 producer, 1 MMA (tile 0), 2..9 dequantise, 10..13 epilogue, 14 MMA (tile 1),
-// and for the down stage 15..18 a second epilogue group: the down epilogue (transpose and
-// 512-byte row stores) is that stage's limit, so two warps per TMEM quadrant take
-// alternate 32-position chunks of the accumulator.
-__host__ __device__ constexpr int tc_epi_groups(bool gated) { return gated ? 1 : 2; }
-__host__ __device__ constexpr int tc_threads(bool gated) { return gated ? 480 : 608; }
+// 15..18 a second epilogue group: two warps per TMEM quadrant take alternate 32-position
+// chunks of the accumulator, so it is read out (and released to the next unit's MMAs) in
+// half the time.
+__host__ __device__ constexpr int tc_epi_groups(bool gated) { return (void)gated, 2; }
+__host__ __device__ constexpr int tc_threads(bool gated) { return (void)gated, 608; }
 constexpr int kMmaWarp1 = 14;    // issuer of tile 1: the issue cost of a tcgen05.mma is per
                                  // issuing thread, so one issuer per tile doubles the rate
 constexpr int kDq = 256;         // dequantising threads
