@@ -518,7 +518,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     if (fp8 && !tc_path) {
         // ---------------------------------------------------------------- fp8_block experts
         // register-fed grouped GEMV for every batch size: align, gate_up (+ shared), down
-        // (+ shared) with the routing weight and the fused ordered combine
+        // (+ shared) with the routing weight, then the ordered combine
         e = launch_align(topk_ids, T, G.k, G.E, kGemvBlock, sorted, bexp, eoff, npad, status, ws + L.scratch, s,
                          status, L.zero_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "align launch");
@@ -572,6 +572,9 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             F.prob[1].n_tiles = cdiv(G.Isl, 16 * (8 / ks_gu));
             F.nprob = 2;
         }
+        // K split evenly over the CTAs (whole 128-K blocks; with ks_gu = 1)
+        F.split_part = reinterpret_cast<float *>(ws + L.split_part);
+        F.split_cnt = reinterpret_cast<int *>(ws + L.split_cnt);
         if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         int max_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
         if ((e = launch_gemv_fp8(F, true, ks_gu, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");

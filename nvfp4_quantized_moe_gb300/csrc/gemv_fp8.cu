@@ -110,11 +110,17 @@ __device__ __forceinline__ void fp8_stage(const GemvParams &p, int blk, int n_po
 }
 
 // One unit: block `blk` of problem p, pair tiles (group `grp` of TPW per CTA) over the
-// warp's K range (K split KS ways across the CTA's warps, partials added in warp order).
+// warp's K range (K split KS ways across the CTA's warps, partials added in warp order),
+// or, with KS = 1, over its 64-K steps [s_lo, s_hi) only (both even: whole scale blocks)
+// when the unit is split between CTAs c - 1 and c (piece 1, this CTA is c) or c and c + 1
+// (piece 0): the pieces' partial sums meet in split slot c - piece and the second of the
+// two CTAs to finish adds the other piece (a sum of two fp32 terms does not depend on
+// their order) and runs the epilogue.
 template <bool GATED, int KS>
 __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &L, int lu, int n_pos,
                                          const uint4 *smem_b, const float *inv,
-                                         float (&red)[KS > 1 ? 8 : 1][32][8])
+                                         float (&red)[KS > 1 ? 8 : 1][32][8], int s_lo = 0, int s_hi = -1,
+                                         int piece = -1)
 {
     constexpr int TPW = 8 / KS;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -122,7 +128,9 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
     const int g = lane >> 2, c = lane & 3;
     const int K = p.K, kb_n = K / 128;
     const int blk = lu / p.n_tiles, grp = lu - blk * p.n_tiles;
-    const int Kw = K / KS, k0 = ks * Kw, nstep = Kw / kStep8;
+    const int Kw = K / KS, k0 = ks * Kw;
+    if (s_hi < 0) s_hi = Kw / kStep8;
+    const int nstep = s_hi - s_lo;
     const int pair_rows = GATED ? 16 : 32;
     const int rows_limit = GATED ? p.up_off : p.R;
     const int r0 = (grp * TPW + tp) * pair_rows;
@@ -141,7 +149,7 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
         const float *sb = sinv_e + (size_t)((GATED ? p.up_off + r0 : r0 + 16) / 128) * kb_n + k0 / 128;
         const uint4 *bb = smem_b + (size_t)g * (K / 8 + 1) + k0 / 8 + 2 * c;
         auto load = [&](int s, Fp8Frag &f) {
-            const int off = s * kStep8;
+            const int off = (s_lo + s) * kStep8;
             f.a_lo = ldg_nc_v4(ca + off);
             f.a_hi = ldg_nc_v4(ca + row8 + off);
             f.b_lo = ldg_nc_v4(cb + off);
@@ -157,12 +165,12 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
                 const int s = s0 + q;
                 if (s + 2 < nstep) load(s + 2, ring[(q + 2) & 3]);
                 if (s < nstep) {
-                    const uint4 x0 = bb[8 * s], x1 = bb[8 * s + 1];
+                    const uint4 x0 = bb[8 * (s_lo + s)], x1 = bb[8 * (s_lo + s) + 1];
                     const uint32_t b[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                     fp8_tile_step(ring[q].a_lo, ring[q].a_hi, b, t0);
                     fp8_tile_step(ring[q].b_lo, ring[q].b_hi, b, t1);
-                    if (q & 1) {  // end of a 128-K block (steps are 64 K; the warp range is block-aligned)
-                        const float fa = __ldg(sa + (s >> 1)), fb = __ldg(sb + (s >> 1));
+                    if (q & 1) {  // end of a 128-K block (steps are 64 K; ranges start on a block)
+                        const float fa = __ldg(sa + ((s_lo + s) >> 1)), fb = __ldg(sb + ((s_lo + s) >> 1));
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             acc0[i] = fmaf(fa, t0[i], acc0[i]);
@@ -173,6 +181,29 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
                     }
                 }
             }
+        }
+    }
+    if constexpr (KS == 1) {
+        if (piece >= 0) {
+            __shared__ int s_flag;
+            const int slot = (int)blockIdx.x - piece;
+            float *part = L.split_part + (size_t)slot * kSplitPartFloats;
+            float4 *mine = reinterpret_cast<float4 *>(part + ((size_t)piece * kThreads + threadIdx.x) * 8);
+            __stcg(mine, make_float4(acc0[0], acc0[1], acc0[2], acc0[3]));
+            __stcg(mine + 1, make_float4(acc1[0], acc1[1], acc1[2], acc1[3]));
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();  // every thread's partials before the count
+                s_flag = atomicAdd(L.split_cnt + slot, 1) == 1;
+            }
+            __syncthreads();
+            if (!s_flag) return;  // the other piece finishes the unit
+            __threadfence();
+            const float4 *other =
+                reinterpret_cast<const float4 *>(part + ((size_t)(1 - piece) * kThreads + threadIdx.x) * 8);
+            const float4 o0 = __ldcg(other), o1 = __ldcg(other + 1);
+            acc0[0] += o0.x; acc0[1] += o0.y; acc0[2] += o0.z; acc0[3] += o0.w;
+            acc1[0] += o1.x; acc1[1] += o1.y; acc1[2] += o1.z; acc1[3] += o1.w;
         }
     }
     if (KS > 1) {
@@ -250,21 +281,53 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fp8_kernel(const __grid_cons
     const int units0 = (n_pos0 / kGemvBlock) * L.prob[0].n_tiles;
     const int units1 = L.nprob > 1 ? (n_pos1 / kGemvBlock) * L.prob[1].n_tiles : 0;
     const int n_units = units0 + units1;
-    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
-    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
     int staged = -1;
-    for (int u = u_lo; u < u_hi; ++u) {
+    auto stage_for = [&](int u) -> int {  // stage the unit's block if needed; returns its local index
         const int pi = u < units0 ? 0 : 1;
         const GemvParams &p = L.prob[pi];
         const int lu = pi ? u - units0 : u;
-        const int n_pos = pi ? n_pos1 : n_pos0;
         const int blk = lu / p.n_tiles;
         const int key = pi * (1 << 30) + blk;
         if (key != staged) {
-            fp8_stage(p, blk, n_pos, GATED, rows, smem_b, inv);
+            fp8_stage(p, blk, pi ? n_pos1 : n_pos0, GATED, rows, smem_b, inv);
             staged = key;
         }
-        fp8_unit<GATED, KS>(p, L, lu, n_pos, smem_b, inv, red);
+        return lu;
+    };
+    if constexpr (KS == 1) {
+        // Even split of all K, in 128-K scale blocks (two steps): W = units0 * B0 + units1 * B1
+        // blocks, CTA c takes [c W / G, (c + 1) W / G). Needs every CTA's share to be at least
+        // one unit, so that a unit is cut at most once.
+        const int B0 = L.prob[0].K / 128, B1 = L.nprob > 1 ? L.prob[1].K / 128 : B0;
+        const int64_t W = (int64_t)units0 * B0 + (int64_t)units1 * B1;
+        const int Bmax = B0 > B1 ? B0 : B1;
+        if (L.split_part && gridDim.x <= kMaxSplitSlots && W >= (int64_t)gridDim.x * Bmax) {
+            const int w_hi = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x), W0 = units0 * B0;
+            for (int w = (int)((int64_t)blockIdx.x * W / gridDim.x); w < w_hi;) {
+                int u, q, Bq;
+                if (w < W0) {
+                    u = w / B0; q = w - u * B0; Bq = B0;
+                } else {
+                    u = units0 + (w - W0) / B1; q = (w - W0) - (u - units0) * B1; Bq = B1;
+                }
+                const int q_end = w_hi - w < Bq - q ? q + (w_hi - w) : Bq;
+                const int pi = u < units0 ? 0 : 1;
+                const int lu = stage_for(u);
+                // piece 1: tail of the unit begun by CTA c - 1; piece 0: head of one CTA c + 1 ends
+                const int piece = q > 0 ? 1 : (q_end < Bq ? 0 : -1);
+                fp8_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, red, 2 * q, 2 * q_end,
+                                    piece);
+                w += q_end - q;
+            }
+            return;
+        }
+    }
+    const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    for (int u = u_lo; u < u_hi; ++u) {
+        const int pi = u < units0 ? 0 : 1;
+        const int lu = stage_for(u);
+        fp8_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, red);
     }
 }
 
