@@ -268,6 +268,121 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
     if (KS > 1) __syncthreads();
 }
 
+// Down stage with KS = 1 and K a multiple of 256 (units of a multiple of 4 steps), whole
+// units: the CTA's consecutive units of one block (same expert and staged activations,
+// the warp's rows 256 apart, so its scale-block rows two apart) stream through one
+// register ring as a single sequence of steps, y written at each unit's last step.
+__device__ __forceinline__ void fp8_down_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int u_lo,
+                                              int u_hi, uint4 *smem_b, float *inv, int *rows, int *tbl_dst,
+                                              float *tbl_w)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    for (int u = u_lo; u < u_hi;) {
+        const int pi = u < units0 ? 0 : 1;
+        const GemvParams &p = L.prob[pi];
+        const int n_pos = pi ? n_pos1 : n_pos0;
+        const int lu = pi ? u - units0 : u;
+        const int blk = lu / p.n_tiles, grp0 = lu - blk * p.n_tiles;
+        const int nu = min(p.n_tiles - grp0, u_hi - u);  // the run: this block's units in range
+        u += nu;
+        fp8_stage(p, blk, n_pos, false, rows, smem_b, inv);
+        if (threadIdx.x < kGemvBlock) {  // per block position: y row (slot) or -1, and its factor
+            const int pos = blk * kGemvBlock + threadIdx.x;
+            int dst = -1;
+            float w = inv[threadIdx.x];
+            if (pos < n_pos) {
+                if (p.sorted_slot) {
+                    const int sl = __ldg(p.sorted_slot + pos);
+                    if (sl < p.n_slots) {
+                        dst = sl;
+                        if (p.route_w) w *= __ldg(p.route_w + sl);
+                    }
+                } else if (pos < p.n_pos_static) {
+                    dst = pos;
+                }
+            }
+            tbl_dst[threadIdx.x] = dst;
+            tbl_w[threadIdx.x] = w;
+        }
+        __syncthreads();
+        const int K = p.K, kb_n = K / 128, S = K / kStep8;
+        const int r0a = (grp0 * 8 + warp) * 32;  // the warp's first row in the run's first unit
+        const int nok = r0a < p.R ? min(nu, (p.R - r0a + 255) / 256) : 0;  // units with rows in range
+        const int tot = nok * S;
+        if (tot == 0) continue;
+        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const uint8_t *ca = p.codes + (size_t)e * p.e_codes + (size_t)(r0a + g) * K + 16 * c;
+        const uint8_t *cb = ca + (size_t)16 * K;  // rows r0 + 16 + g
+        const size_t row8 = (size_t)8 * K;
+        const uint4 *bb = smem_b + (size_t)g * (K / 8 + 1) + 2 * c;
+        // scale_inv rows of the warp's two tiles (both inside one 128-row block)
+        const float *sa = p.sinv + (size_t)e * p.e_sinv + (size_t)(r0a / 128) * kb_n;
+        uint32_t loff = 0;  // load cursor: byte offset from the lane bases
+        int ls = 0;         // and the step within its unit
+        const uint32_t jump = 256u * (uint32_t)K - (uint32_t)kStep8 * (S - 1);  // to the next unit's first step
+        auto load = [&](Fp8Frag &f) {
+            f.a_lo = ldg_nc_v4(ca + loff);
+            f.a_hi = ldg_nc_v4(ca + row8 + loff);
+            f.b_lo = ldg_nc_v4(cb + loff);
+            f.b_hi = ldg_nc_v4(cb + row8 + loff);
+            if (++ls == S) {
+                ls = 0;
+                loff += jump;
+            } else {
+                loff += kStep8;
+            }
+        };
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};  // current 128-K block
+        Fp8Frag ring[4];
+        load(ring[0]);
+        if (tot > 1) load(ring[1]);
+        int cs = 0, r0 = r0a;  // compute cursor: step within the unit, the unit's first row
+        for (int t = 0; t < tot; t += 4) {  // S, and so tot, is a multiple of 4
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (t + q + 2 < tot) load(ring[(q + 2) & 3]);
+                const uint4 x0 = bb[8 * (cs + q)], x1 = bb[8 * (cs + q) + 1];
+                const uint32_t b[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                fp8_tile_step(ring[q].a_lo, ring[q].a_hi, b, t0);
+                fp8_tile_step(ring[q].b_lo, ring[q].b_hi, b, t1);
+                if (q & 1) {  // end of a 128-K block: both tiles share its scale row
+                    const float f = __ldg(sa + ((cs + q) >> 1));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc0[i] = fmaf(f, t0[i], acc0[i]);
+                        acc1[i] = fmaf(f, t1[i], acc1[i]);
+                        t0[i] = 0.f;
+                        t1[i] = 0.f;
+                    }
+                }
+            }
+            cs += 4;
+            if (cs == S) {  // the unit's last step: y rows r0 .. r0 + 31 of its positions
+#pragma unroll
+                for (int col = 0; col < 2; ++col) {
+                    const int dst = tbl_dst[2 * c + col];
+                    if (dst < 0) continue;
+                    const float w = tbl_w[2 * c + col];
+                    float *yrow = p.y_out + (size_t)dst * p.R;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int n = r0 + g + 8 * half;
+                        yrow[n] = acc0[2 * half + col] * w;
+                        yrow[n + 16] = acc1[2 * half + col] * w;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc0[i] = acc1[i] = 0.f;
+                cs = 0;
+                r0 += 256;
+                sa += 2 * kb_n;  // 256 rows on: two scale-block rows
+            }
+        }
+    }
+}
+
 template <bool GATED, int KS>
 __global__ void __launch_bounds__(kThreads, 2) gemv_fp8_kernel(const __grid_constant__ FastLaunch L)
 {
@@ -324,6 +439,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fp8_kernel(const __grid_cons
     }
     const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
     const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    if constexpr (!GATED && KS == 1) {
+        auto runs_ok = [](const GemvParams &q) {  // whole units of 4k steps; 32-bit code offsets
+            return q.K % 256 == 0 && (int64_t)q.R * q.K < ((int64_t)1 << 32);
+        };
+        if (runs_ok(L.prob[0]) && (L.nprob < 2 || runs_ok(L.prob[1]))) {
+            __shared__ int tbl_dst[kGemvBlock];
+            __shared__ float tbl_w[kGemvBlock];
+            fp8_down_runs(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, inv, rows, tbl_dst, tbl_w);
+            return;
+        }
+    }
     for (int u = u_lo; u < u_hi; ++u) {
         const int pi = u < units0 ? 0 : 1;
         const int lu = stage_for(u);
