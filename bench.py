@@ -128,7 +128,7 @@ def run_reference(args, world, rank):
     oracle.build()
     if rank != 0:
         return
-    shape = synth.SHAPES["qwen36"]
+    shape = synth.SHAPES[args.shape]
     routed = synth.make_pieces(shape, 0)
     shared = synth.make_pieces(shape, 0, shared=True)
     rb, sb = oracle.slice_bank(routed, shape.group), oracle.slice_bank(shared, shape.group)
@@ -158,6 +158,15 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def _expert_bytes(shape, inter):
+    """Algorithmic bytes of one NVFP4 expert of intermediate width `inter` (tp=1): gate_up and
+    down codes, e4m3 block scales and fp32 row globals."""
+    H, g = shape.hidden, shape.group
+    gate_up = 2 * inter * H // 2 + 2 * inter * H // g + 2 * inter * 4
+    down = H * inter // 2 + H * inter // g + H * 4
+    return gate_up, down
+
+
 def _sources_sha256(paths):
     import hashlib
     h = hashlib.sha256()
@@ -182,16 +191,17 @@ def _traffic(stage):
 
 
 def _config(args):
-    return {"workload": f"qwen36-moe-decode-T{args.T}", "T": args.T, "layers": args.layers, "hidden": 2048,
-            "num_experts": 256, "top_k": 8, "intermediate": 512, "shared_intermediate": 512, "group": 16,
+    sh = synth.SHAPES[args.shape]
+    return {"workload": f"{args.shape}-moe-decode-T{args.T}", "T": args.T, "layers": args.layers,
+            "hidden": sh.hidden, "num_experts": sh.num_experts, "top_k": sh.top_k, "intermediate": sh.intermediate,
+            "shared_intermediate": sh.shared_intermediate, "group": sh.group,
             "tp": 1, "seed": 0, "routing": "N(0,1) logits",
             "l2": f"inputs larger than L2: {args.layers} distinct layer copies per step"}
 
 
-def cpu_baseline(T, budget_s=10.0):
+def cpu_baseline(T, shape, budget_s=10.0):
     import oracle
     oracle.build()
-    shape = synth.SHAPES["qwen36"]
     routed = synth.make_pieces(shape, 0)
     shared = synth.make_pieces(shape, 0, shared=True)
     rb, sb = oracle.slice_bank(routed, shape.group), oracle.slice_bank(shared, shape.group)
@@ -211,7 +221,7 @@ def cpu_baseline(T, budget_s=10.0):
 
 
 def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
-    """One qwen36 layer at T tokens (Zipf routing), L2 flushed before every repetition."""
+    """One layer of `shape` at T tokens (Zipf routing), L2 flushed before every repetition."""
     import torch
     rb, sb = ft.alloc_banks(cfg, 0, dev), ft.alloc_banks(cfg, 1, dev)
     ft.ft_moe_pack(cfg, 0, routed_d, rb)
@@ -244,7 +254,8 @@ def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
             stages.append([ev[i].elapsed_time(ev[i + 1]) for i in range(ft.FT_NSTAGES)])
     assert ft.ft_moe_read_status(ws) == 0
     ms = float(np.median(times))
-    flops = 56623104.0 * T   # 2 * 3 * H * I per routed expert x 8 + shared, per token
+    # 2 * 3 * H * I per routed expert x k, plus the shared expert's 2 * 3 * H * I_s, per token
+    flops = 6.0 * H * (k * shape.intermediate + shape.shared_intermediate) * T
     _, tfl, peak_kind = _peaks()
     st = np.median(np.array(stages), axis=0)
     counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=E)
@@ -384,7 +395,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ft.load()
-    shape = synth.SHAPES["qwen36"]
+    shape = synth.SHAPES[args.shape]
     cfg = ft.MoEConfig.of(shape)
     T, L, H, E, k = args.T, args.layers, shape.hidden, shape.num_experts, shape.top_k
     routed_np = synth.make_pieces(shape, 0)
@@ -399,8 +410,9 @@ def run_ours(args, world, rank, local):
         layers.append((rb, sb))
     prefill = None
     if not args.no_prefill:
-        prefill = [measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T_) for T_ in (2048, 8192)]
-    router = [measure_router(ft, dev, T_) for T_ in (T, 2048)]
+        prefill = [measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, int(T_))
+                   for T_ in args.prefill_T.split(",")]
+    router = [measure_router(ft, dev, T_, E=E, H=H) for T_ in (T, 2048)]
     fp8 = None if args.no_fp8 else measure_fp8(ft, dev)
     del routed_d, shared_d
     x_host = [synth.make_activations(T, H, seed=l) for l in range(L)]
@@ -441,9 +453,10 @@ def run_ours(args, world, rank, local):
     # touched experts per layer (algorithmic bytes)
     ids_np = ids.cpu().numpy()
     touched = [len(np.unique(ids_np[l])) for l in range(L)]
-    per_expert = 1781760
-    gu_bytes_per_expert = 1024 * 1024 + 1024 * 128 + 1024 * 4
-    layer_bytes = [(t + 1) * per_expert for t in touched]
+    gu_bytes_per_expert, dn_bytes_per_expert = _expert_bytes(shape, shape.intermediate)
+    gu_sh, dn_sh = _expert_bytes(shape, shape.shared_intermediate) if shape.shared_intermediate else (0, 0)
+    per_expert = gu_bytes_per_expert + dn_bytes_per_expert
+    layer_bytes = [t * per_expert + gu_sh + dn_sh for t in touched]
 
     for _ in range(args.warmup):
         g_plain.replay()
@@ -477,10 +490,9 @@ def run_ours(args, world, rank, local):
     dominant = max(stage_mean_us, key=stage_mean_us.get)
     hbm, tfl, peak_kind = _peaks()
     # the routed and the shared expert run in the same launch per stage (decode regime)
-    gu_alg = float(np.mean([(t + 1) * gu_bytes_per_expert for t in touched]))
-    dn_alg = float(np.mean([(t + 1) * (2048 * 256 + 2048 * 32 + 2048 * 4) for t in touched]))
-    alg = {"gate_up": gu_alg, "down": dn_alg, "shared_gate_up": float(gu_bytes_per_expert),
-           "shared_down": float(2048 * 256 + 2048 * 32 + 2048 * 4)}
+    gu_alg = float(np.mean([t * gu_bytes_per_expert + gu_sh for t in touched]))
+    dn_alg = float(np.mean([t * dn_bytes_per_expert + dn_sh for t in touched]))
+    alg = {"gate_up": gu_alg, "down": dn_alg, "shared_gate_up": float(gu_sh), "shared_down": float(dn_sh)}
     dom_bytes = alg.get(dominant, 0.0)
     dom_s = stage_mean_us[dominant] * 1e-6
     achieved = dom_bytes / dom_s / 1e9 if dom_bytes else None
@@ -538,7 +550,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(T)
+        line["cpu_baseline"] = cpu_baseline(T, shape)
     print(json.dumps(line), flush=True)
 
 
@@ -554,6 +566,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8_block expert measurement")
+    ap.add_argument("--shape", choices=["qwen36", "dsv4"], default="qwen36",
+                    help="NVFP4 layer family of the decode and prefill measurements")
+    ap.add_argument("--prefill-T", default="2048,8192", help="comma-separated prefill token counts")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
