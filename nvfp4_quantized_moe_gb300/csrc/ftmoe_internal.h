@@ -90,7 +90,6 @@ struct TcOperands {
 };
 bool tc_shape_ok(int K, int group, int rows_per_expert);
 bool tc_shape_ok_fp8(int K, int rows_per_expert);
-size_t tc_smem_bytes(bool gated, int K, int group);
 // nprob (1 or 2) problems in one launch; max_units bounds their total unit count.
 cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int nprob, bool gated, int max_units,
                            cudaStream_t s);

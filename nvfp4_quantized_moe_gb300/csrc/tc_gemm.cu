@@ -90,14 +90,12 @@ struct TcSmem {
 // 64 (fp8_block, one code a byte).
 __host__ __device__ constexpr uint32_t raw_row_bytes(bool fp8) { return fp8 ? 64u : 32u; }
 
-__host__ __device__ inline TcSmem tc_smem(int K, int group, int ns, bool fp8, bool gated)
+__host__ __device__ inline TcSmem tc_smem(int ns, bool fp8, bool gated)
 {
     TcSmem s;
     s.a_bytes = 0;  // the dequantised A operand lives in tensor memory
     s.b_bytes = (uint32_t)NT * 128;
     s.raw_bytes = 2u * MT * raw_row_bytes(fp8);
-    (void)K;
-    (void)group;
     s.ns = ns;
     s.a_off = 0;
     s.b_off = s.a_off + NA * s.a_bytes;
@@ -129,7 +127,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
     // 1024-byte aligned base by pointer arithmetic on the shared array itself, so that the
     // compiler keeps every access derived from it in the shared state space
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const TcSmem L = tc_smem(p0.K, p0.group, ns, FP8, GATED);
+    const TcSmem L = tc_smem(ns, FP8, GATED);
     constexpr int NG = tc_epi_groups(GATED);  // epilogue groups of 4 warps
     constexpr int RB = (int)raw_row_bytes(FP8);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -622,20 +620,14 @@ bool tc_shape_ok(int K, int group, int rows_per_expert)
 }
 
 // Deepest TMA ring (NSMAX down to 2 stages) that fits the opt-in shared memory.
-static int tc_stages(int K, int group, bool fp8, bool gated)
+static int tc_stages(bool fp8, bool gated)
 {
     int optin = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     for (int ns = NSMAX; ns >= 2; --ns)
-        if (tc_smem(K, group, ns, fp8, gated).total + 1024 <= (uint32_t)optin) return ns;
+        if (tc_smem(ns, fp8, gated).total + 1024 <= (uint32_t)optin) return ns;
     return 0;
-}
-
-size_t tc_smem_bytes(bool gated, int K, int group)
-{
-    const int ns = tc_stages(K, group, false, gated);
-    return ns ? tc_smem(K, group, ns, false, gated).total + 1024 : 0;
 }
 
 cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
@@ -662,7 +654,7 @@ cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int npr
     if (nprob < 1 || nprob > 2) return cudaErrorInvalidValue;
     if (nprob == 2 && (probs[1].group != probs[0].group || probs[1].fp8 != probs[0].fp8)) return cudaErrorInvalidValue;
     const bool fp8 = probs[0].fp8 != 0;
-    const int ns = tc_stages(probs[0].K, probs[0].group, fp8, gated);
+    const int ns = tc_stages(fp8, gated);
     if (!ns) return cudaErrorInvalidValue;
     CUtensorMap cmap[2], bmap[2];
     TcLaunch TL = {};
@@ -684,7 +676,7 @@ cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int npr
         cmap[1] = cmap[0];
         bmap[1] = bmap[0];
     }
-    const size_t smem = tc_smem(probs[0].K, probs[0].group, ns, fp8, gated).total + 1024;
+    const size_t smem = tc_smem(ns, fp8, gated).total + 1024;
     int grid = sm_count();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
