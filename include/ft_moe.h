@@ -69,9 +69,9 @@ typedef enum {
 
 /* Geometry of one MoE layer as seen by one tp rank. `intermediate` and
  * `shared_intermediate` are the FULL (unsliced) sizes; the rank-local sizes are
- * I_l = intermediate / tp_size and I_sl = shared_intermediate / tp_size
- * ("MoEConfig ... local_intermediate = intermediate // tp_size", NVFP4 port
- * section 3a), or the explicit shard sizes below. shared_intermediate = 0 means the
+ * I_l = intermediate / tp_size and I_sl = shared_intermediate / tp_size (the rank's
+ * share of the intermediate axis that the NVFP4 port's MoE config derives from the full
+ * size and tp_size, NVFP4 port section 3a), or the explicit shard sizes below. shared_intermediate = 0 means the
  * layer has no shared expert. A shard range that is negative, empty, not a multiple
  * of group or past the full size is FT_ERR_INDIVISIBLE. */
 typedef struct {
@@ -208,7 +208,12 @@ ft_status ft_moe_route_gemm(const void *x, int32_t T, int32_t H, const void *w_r
                             float *logits, int32_t *topk_ids, float *topk_w, void *stream);
 
 /* Bytes of workspace ft_moe_forward needs for this config and token count
- * (256-byte aligned buffer). Host-only. */
+ * (256-byte aligned buffer). Host-only. The pages keep the layer's intermediates
+ * (sorted token order, the SwiGLU activations h, the per-slot down outputs) as
+ * framework-owned buffers ("feat(qwen3_5_moe): tensor-parallel weight sharding", Notes:
+ * the moe_align step feeding the grouped GEMMs); here the caller owns them, sized by
+ * this call, since the library allocates nothing. Errors: as ft_moe_layout, plus
+ * FT_ERR_INVALID_ARG (bytes NULL) and FT_ERR_UNSUPPORTED (T outside [0, 2^20]). */
 ft_status ft_moe_workspace_size(const ft_moe_config *cfg, int32_t T, size_t *bytes);
 
 /* Rank-local MoE partial for T tokens:
@@ -251,17 +256,20 @@ ft_status ft_moe_align(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
                        int32_t *sorted_slot, int32_t *block_expert, int32_t *expert_off,
                        int32_t *n_padded, void *workspace, size_t workspace_bytes, void *stream);
 
-/* ft_moe_align without a workspace, for callers that cannot allocate device memory
- * (for instance code running in a host callback on a stream, where CUDA calls are not
- * allowed, or an engine that fixes every device allocation at start-up). The pages
- * have no counterpart: it is the same sort as ft_moe_align, with the scratch and the
- * status word in a static array of 393,472 bytes that the library holds on every GPU
- * that loads it, until the process exits.
+/* ft_moe_align without a workspace, for callers that cannot allocate device memory:
+ * an engine that fixes every device allocation at start-up and may not allocate
+ * afterwards, or a caller that only owns the buffers handed to it. The pages have no
+ * counterpart: it is the same sort as ft_moe_align, with the scratch and the status
+ * word in a static array of 393,472 bytes that the library holds on every GPU that
+ * loads it, until the process exits. It still issues CUDA calls on `stream` (a memset,
+ * kernel launches, a device-to-device copy of the status), so it must not be called
+ * from a stream host callback or anywhere else the CUDA API may not be used.
  *   Limits: T*k <= 65536 slots, E <= 1024, k <= 32; larger inputs return
  *   FT_ERR_UNSUPPORTED (use ft_moe_align with a workspace).
  *   status  device i32 [1] (out, may be NULL): FT_OK or FT_ERR_INVALID_ROUTING.
- * Other arguments as ft_moe_align. The first call on each device looks up the array's
- * device address; make that first call before any stream capture on that device.
+ * Other arguments as ft_moe_align. The first call on each device (and again after a
+ * cudaDeviceReset, in the new context) looks up the array's device address with that
+ * device current; make that first call before any stream capture on that device.
  * All calls share the one array: calls that overlap on the GPU (other streams, other
  * threads) race and must be ordered by the caller. Allocates nothing. */
 ft_status ft_moe_align_static(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E, int32_t block,
@@ -269,7 +277,11 @@ ft_status ft_moe_align_static(const int32_t *topk_ids, int32_t T, int32_t k, int
                               int32_t *n_padded, int32_t *status, void *stream);
 
 /* Dequantised weights of one expert without the per-row global:
- * out[n, k] = bf16(e2m1(code[n][k]) * e4m3(scale[n][k/group])), exact in bf16.
+ * out[n, k] = bf16(e2m1(code[n][k]) * e4m3(scale[n][k/group])), exact in bf16 -- the
+ * weight value the NVFP4 port's dequantiser produces before its fp16 matmul, less the
+ * per-row global that this library applies to each row's fp32 sum instead ("[TP=2]
+ * Quantized MoE expert parallelism ... NVFP4 port", section 4, the _dequant_nvfp4
+ * routine of the weight.py diff, packed NVFP4 to bf16).
  * which = FT_GU (rows 2*I_l, K = H) or FT_DN (rows H, K = I_l); `banks` are
  * routed banks when shared = 0, else the shared expert's. out: device bf16 [rows, K].
  * It runs the same device routine the fused kernels use. */
@@ -278,7 +290,13 @@ ft_status ft_moe_dequant(const ft_moe_config *cfg, int32_t shared, const ft_moe_
 
 /* Synchronise `stream` and return the status word at the start of `workspace`
  * (FT_OK, FT_ERR_INVALID_ROUTING or FT_ERR_TIMEOUT). Returns FT_ERR_CUDA if the
- * stream itself failed. */
+ * stream itself failed. The pages want bad geometry to fail with an error rather
+ * than run ("[1/3] feat(dsv4): add tensor-parallel DeepSeek-V4 runtime", Checkpoint
+ * loading and memory correctness: incompatible sizes fail before any layer is built)
+ * and count a stage that hangs instead of erroring as a defect ("Offloaded MoE ignores
+ * tensor parallelism", follow-up comment: the rank-0 relay race that wedges the
+ * server); kernels cannot return an error code, so they record the first one here for
+ * the host to read. */
 ft_status ft_moe_read_status(const void *workspace, void *stream);
 
 /* Thread-local description of the last error returned on this thread ("" if none). */

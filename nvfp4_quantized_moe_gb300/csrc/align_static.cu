@@ -1,10 +1,13 @@
 // ft_moe_align_static: moe_align with library-owned scratch, for callers that must not
-// allocate device memory. Examples: code running inside a host callback enqueued on a
-// stream (the CUDA API may not be called there at all), and engines that plan every
-// device byte at start-up and forbid allocation afterwards. Their only device memory
-// is the inputs and outputs they already own. The scratch that the multi-pass sort needs
-// (per-chunk expert counts, per-slot ranks) and the status word live in one
-// file-scope array that every GPU loading this library keeps until the process exits.
+// allocate device memory: an engine that plans every device byte at start-up and forbids
+// allocation afterwards, or a caller whose device memory is fixed by someone else (a
+// shared arena it may not grow). Their only device memory is the inputs and outputs they
+// already own. The scratch that the multi-pass sort needs (per-chunk expert counts,
+// per-slot ranks) and the status word live in one file-scope array that every GPU
+// loading this library keeps until the process exits. The entry point still issues CUDA
+// calls (a memset, kernel launches, a device-to-device copy), so it cannot be called
+// where the CUDA API is off limits, such as inside a stream host callback.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,25 +30,56 @@ constexpr size_t kScratchBytes = kStatusBytes + kChunkCountBytes + kRankBytes;  
 // Status word at offset 0, then the align scratch.
 static __device__ __align__(256) unsigned char g_align_scratch[kScratchBytes];
 
-std::mutex g_scratch_mu;
-void *g_scratch_addr[64];
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
 
-// Device address of g_align_scratch on the current device. Looked up once per device
-// (the host-side symbol is only a stand-in and must never reach a kernel).
+// cuCtxGetCurrent through the runtime's driver entry point (no link against libcuda).
+CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    });
+    return fn;
+}
+
+std::mutex g_scratch_mu;
+struct ScratchEntry {
+    CUcontext ctx;
+    void *addr;
+};
+ScratchEntry g_scratch_addr[64];  // per device ordinal: the context it was looked up in
+
+// Device address of g_align_scratch in the current device's context. Looked up once per
+// device and context with that device current (the host-side symbol is only a stand-in
+// and must never reach a kernel); a new context on the device (after cudaDeviceReset)
+// looks it up again, since the module and its array may then sit elsewhere.
 cudaError_t scratch_address(void **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get) return cudaErrorInitializationError;
+    CUcontext ctx = nullptr;  // null until the runtime has bound a context to this thread
+    if (get(&ctx) != CUDA_SUCCESS) return cudaErrorInitializationError;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchEntry &slot = g_scratch_addr[dev];
+    if (!ctx || !slot.addr || slot.ctx != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_align_scratch);
+        e = cudaGetSymbolAddress(&p, g_align_scratch);  // binds the device's primary context
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorInitializationError;
+        slot.ctx = ctx;
+        slot.addr = p;
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return cudaSuccess;
 }
 

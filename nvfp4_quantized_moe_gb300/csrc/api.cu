@@ -240,26 +240,6 @@ static int fast_ksplit(int blocks, int units_per_block_ks1, int K0, int K1 = 0)
     return ks;
 }
 
-// Decode kernel family: the lean register-fed kernels (default) or, with the
-// environment variable FTMOE_DECODE=stream, the TMA-streamed ones. Read once per process.
-static bool decode_mode_is(const char *name)
-{
-    const char *e = getenv("FTMOE_DECODE");
-    return e && strcmp(e, name) == 0;
-}
-
-static bool decode_streamed()
-{
-    static const bool v = decode_mode_is("stream");
-    return v;
-}
-
-static bool decode_tensor_core()
-{
-    static const bool v = decode_mode_is("tc");
-    return v;
-}
-
 // Generic register-fed launch for one problem (shapes the lean kernels do not cover).
 // `rows` = I_l (gated) or H (down); max_blocks bounds the blocks.
 static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, cudaStream_t s)
@@ -748,73 +728,8 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         return stage_mark(FT_NSTAGES, s);
     };
 
-    // TMA-streamed kernels, routed and shared expert in one launch per stage, combine
-    // fused into the down stage.
-    {
-        StreamLaunch SG = {}, SD = {};
-        const int kmax = G.H > G.Il ? (G.H > G.Isl ? G.H : G.Isl) : (G.Il > G.Isl ? G.Il : G.Isl);
-        bool use = decode_streamed() && gemv_stream_fits(kmax) &&
-                   gemv_stream_geom(G.H, G.g, G.Il, true, SG.prob[0]) &&
-                   gemv_stream_geom(G.Il, G.g, G.H, false, SD.prob[0]);
-        if (use && G.Is)
-            use = gemv_stream_geom(G.H, G.g, G.Isl, true, SG.prob[1]) &&
-                  gemv_stream_geom(G.Isl, G.g, G.H, false, SD.prob[1]);
-        if (use) {
-            SG.prob[0].p = gu; SD.prob[0].p = dn;
-            SG.nprob = SD.nprob = 1;
-            if (G.Is) {
-                SG.prob[1].p = gu_sh; SD.prob[1].p = dn_sh;
-                SG.nprob = SD.nprob = 2;
-            }
-            auto units = [&](const StreamLaunch &S) {
-                return max_blocks * S.prob[0].n_ptiles + (G.Is ? tpad * S.prob[1].n_ptiles : 0);
-            };
-            if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            if ((e = launch_gemv_stream(SG, true, units(SG), s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
-            if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            if ((e = launch_gemv_stream(SD, false, units(SD), s)) != cudaSuccess) return cuda_fail(e, "down launch");
-            if ((e = combine()) != cudaSuccess) return cuda_fail(e, "combine launch");
-            return ok();
-        }
-    }
-
-    // Tensor-core kernels (A operand dequantised into tensor memory), same launch structure.
-    {
-        const int kmax = G.H > G.Il ? (G.H > G.Isl ? G.H : G.Isl) : (G.Il > G.Isl ? G.Il : G.Isl);
-        if (decode_tensor_core() && tc_gemv_ok(G.H, G.g) && tc_gemv_ok(G.Il, G.g) &&
-            (!G.Is || tc_gemv_ok(G.Isl, G.g)) && tc_gemv_fits(kmax)) {
-            FastLaunch F = {};
-            F.prob[0] = gu;
-            F.prob[0].n_tiles = cdiv(G.Il, 128);
-            F.nprob = 1;
-            if (G.Is) {
-                F.prob[1] = gu_sh;
-                F.prob[1].n_tiles = cdiv(G.Isl, 128);
-                F.nprob = 2;
-            }
-            if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            int max_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
-            if ((e = launch_tc_gemv(F, true, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
-            if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            FastLaunch D = {};
-            D.prob[0] = dn;
-            D.prob[0].n_tiles = cdiv(G.H, 256);
-            D.nprob = 1;
-            if (G.Is) {
-                D.prob[1] = dn_sh;
-                D.prob[1].n_tiles = D.prob[0].n_tiles;
-                D.nprob = 2;
-            }
-            if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-            max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
-            if ((e = launch_tc_gemv(D, false, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
-            if ((e = combine()) != cudaSuccess) return cuda_fail(e, "combine launch");
-            return ok();
-        }
-    }
-
-    // Lean register-fed kernels, same launch structure.
+    // Lean register-fed kernels: routed and shared expert in one launch per stage, then the
+    // ordered combine as its own launch.
     const int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H);
     const int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
     if (gemv_fast_ok(G.H, G.g, ks_gu, 2 * (G.Il > G.Isl ? G.Il : G.Isl)) && gemv_fast_ok(G.Il, G.g, ks_dn, G.H) &&

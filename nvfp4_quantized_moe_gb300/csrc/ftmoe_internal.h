@@ -184,31 +184,6 @@ cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_un
 bool gemv_fp8_ok(int K, int ks);
 cudaError_t launch_gemv_fp8(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
 
-// Tensor-core decode GEMV (A operand dequantised into tensor memory, one persistent CTA
-// per SM). Units per block: prob[i].n_tiles = ceil(I/128) for gate_up, ceil(H/256) for down.
-bool tc_gemv_ok(int K, int group);
-bool tc_gemv_fits(int kmax);
-cudaError_t launch_tc_gemv(const FastLaunch &L, bool gated, int max_units, cudaStream_t s);
-
-// TMA-streamed decode GEMV (one persistent CTA per SM). Per problem: lps lines of 256 K
-// elements x tps pair tiles per stage, nst stages per unit, n_ptiles units per block of
-// positions, sbytes scale bytes per row and stage (gemv_stream_geom fills these).
-struct StreamProb {
-    GemvParams p;
-    int lps, tps, nst, n_ptiles, sbytes;
-};
-struct StreamLaunch {
-    CUtensorMap cmap[2], smap[2];  // per problem: packed codes, block scales (set by the launch)
-    StreamProb prob[2];
-    int nprob;
-    int ns, act_bytes;             // stages, activation bytes (set by the launch)
-};
-// Geometry for a problem of K columns and `rows` rows (I_l for gate_up, H for down);
-// false when the shape is outside the kernel's coverage.
-bool gemv_stream_geom(int K, int group, int rows, bool gated, StreamProb &P);
-// Enough shared memory for at least two stages next to Kmax-long activations?
-bool gemv_stream_fits(int Kmax);
-cudaError_t launch_gemv_stream(StreamLaunch &L, bool gated, int max_units, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *y_shared, int T, int k, int H, void *out, int out_dtype,
                            cudaStream_t s);
 

@@ -25,7 +25,7 @@
  *    ownership and collectives" (shared SwiGLU expert on the same split, added to
  *    the routed partial before the one reduction).
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *  - element 2m of a packed row sits in the LOW nibble of byte m, 2m+1 in the high;
  *  - e2m1 nibble = S.EE.M (bit 3 sign) valued sign * {0,.5,1,1.5,2,3,4,6}[bits 0-2];
  *  - block scales are OCP E4M3 "fn" (bias 7, no infinities, S.1111.111 = NaN);

@@ -191,3 +191,18 @@ def test_pack_rejects_overlap(ft):
         banks.p[i] = 1 << 20 + i
     pieces = ft._Pieces(*([1 << 20] * 9), 1)
     assert lib.ft_moe_pack(ctypes.byref(cfg), 0, ctypes.byref(pieces), ctypes.byref(banks), None) == 1
+
+
+def test_align_static_rejects_sizes_beyond_its_array(ft):
+    """The static entry point's limits (slots, experts, top_k) are checked on the host,
+    before any CUDA call: sizes its fixed array cannot hold return FT_ERR_UNSUPPORTED."""
+    lib = ctypes.CDLL(ft.LIB_PATH)
+    P, I32 = ctypes.c_void_p, ctypes.c_int32
+    lib.ft_moe_align_static.argtypes = [P, I32, I32, I32, I32, P, P, P, P, P, P]
+    lib.ft_moe_align_static.restype = ctypes.c_int
+    dummy = ctypes.c_void_p(16)  # never dereferenced: the call returns before using it
+    bufs = [dummy] * 4
+    for T, k, E in ((1, 8, 1025), (1, 33, 64), (8193, 8, 256), (65537, 1, 8)):
+        assert lib.ft_moe_align_static(dummy, T, k, E, 8, *bufs, None, None) == 3, (T, k, E)
+    assert lib.ft_moe_align_static(dummy, -1, 8, 256, 8, *bufs, None, None) == 1
+    assert lib.ft_moe_align_static(dummy, 4, 8, 256, 0, *bufs, None, None) == 1
