@@ -93,6 +93,7 @@ MUTATIONS = {
     "nibble_order": 1, "swap_gate_up": 2, "drop_global": 3, "scale_index": 4, "e2m1_sign": 5,
     "no_renorm": 6, "tie_high": 7, "down_rows": 8, "drop_shared": 9, "drop_route_w": 10,
     "e4m3_bias": 11, "up_slice": 12, "router_transposed": 13, "fp8_block_transposed": 14,
+    "dequant_transposed": 15,
 }
 
 

@@ -73,6 +73,7 @@ enum {
     ORC_MUT_UP_SLICE = 12,      /* up rows taken from the gate half */
     ORC_MUT_ROUTER_T = 13,      /* router weight read transposed (square shapes only) */
     ORC_MUT_FP8_BLOCK_T = 14,   /* fp8_block: scale block indexed [k/128][n/128] */
+    ORC_MUT_DEQUANT_T = 15,     /* dense matrices written column-major ([K][rows]) */
 };
 
 /* ---------------------------------------------------------------- formats */
@@ -175,7 +176,10 @@ void orc_dequant_fp8_matrix(const uint8_t *codes, const float *sinv, int rows, i
 {
     fill_tables();
     for (int n = 0; n < rows; ++n)
-        for (int k = 0; k < K; ++k) out[(size_t)n * K + k] = fp8_weight_at(codes, sinv, n, k, K);
+        for (int k = 0; k < K; ++k) {
+            size_t at = (orc_mutation == ORC_MUT_DEQUANT_T) ? (size_t)k * rows + n : (size_t)n * K + k;
+            out[at] = fp8_weight_at(codes, sinv, n, k, K);
+        }
 }
 
 /* Dense dequantised matrix of one expert, W as above, row-major [rows][K]. */
@@ -184,7 +188,10 @@ void orc_dequant_matrix(const uint8_t *codes, const uint8_t *scales, const float
 {
     fill_tables();
     for (int n = 0; n < rows; ++n)
-        for (int k = 0; k < K; ++k) out[(size_t)n * K + k] = weight_at(codes, scales, glob, n, k, K, g);
+        for (int k = 0; k < K; ++k) {
+            size_t at = (orc_mutation == ORC_MUT_DEQUANT_T) ? (size_t)k * rows + n : (size_t)n * K + k;
+            out[at] = weight_at(codes, scales, glob, n, k, K, g);
+        }
 }
 
 /* ---------------------------------------------------------------- routing */

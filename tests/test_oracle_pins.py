@@ -460,12 +460,33 @@ def pin_fp8_dense_mlp_and_partials():
     assert np.abs(parts[0] - full).max() / np.abs(full).max() > 1e-3
 
 
+def pin_dequant_matrices():
+    """The oracle's dense matrix routines against the test-side dequantisers on
+    non-square matrices (a row-stride or transposition slip changes the result): NVFP4
+    with groups 16 and 32, its per-row global included, and fp8_block with three row
+    blocks and two K blocks."""
+    rng = np.random.default_rng(41)
+    for rows, K, g in ((48, 96, 16), (40, 128, 32), (3, 256, 16)):
+        codes = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+        scales = synth.e4m3_rne_bytes(rng.uniform(0.25, 2.0, (rows, K // g)))
+        glob = rng.uniform(0.5, 1.5, rows).astype(np.float32)
+        got = oracle.dequant_matrix(codes, scales, glob, g)
+        assert got.shape == (rows, K)
+        assert np.array_equal(got, _dense(codes, scales, glob, g)), (rows, K, g)
+    codes = rng.integers(0, 256, (384, 256), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3F  # no NaN codes
+    sinv = rng.uniform(0.5, 1.5, (3, 2)).astype(np.float32)
+    got = oracle.dequant_fp8_matrix(codes, sinv)
+    assert np.array_equal(got, _dense_fp8(codes, sinv))
+
+
 PINS = [pin_e2m1, pin_e4m3, pin_dequant_bf16, pin_route_worked_example, pin_route_brute_force,
         pin_route_library, pin_route_ties_and_shift, pin_align, pin_slice_identity_and_tiling,
         pin_one_hot_columns, pin_linear_parts_exact, pin_dense_mlp_special_case,
         pin_routed_combination, pin_untouched_experts_and_tokens, pin_tp_partial_sum,
         pin_router_logits_exact, pin_router_one_hot, pin_asymmetric_partition,
-        pin_fp8_slice_identity_and_tiling, pin_fp8_one_hot_columns, pin_fp8_dense_mlp_and_partials]
+        pin_fp8_slice_identity_and_tiling, pin_fp8_one_hot_columns, pin_fp8_dense_mlp_and_partials,
+        pin_dequant_matrices]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
