@@ -380,6 +380,159 @@ def measure_fp8(ft, dev, T=64, L=16, reps=20, T_prefill=2048):
             "prefill": prefill}
 
 
+def _rank_bytes(ft, cfg):
+    """Algorithmic weight bytes of one routed expert and of the shared expert for this
+    rank's banks (codes, block scales and row globals, from the library's own layout)."""
+    E = cfg.num_experts
+    routed = sum(b for *_, b in ft.ft_moe_layout(cfg, 0)) / E
+    shared = sum(b for *_, b in ft.ft_moe_layout(cfg, 1)) if cfg.shared_intermediate else 0
+    return float(routed), float(shared)
+
+
+def _ranks(ft, dev, shape, tp, pieces_d):
+    """Packed banks of every tp rank of one layer copy: [(cfg, routed, shared)]."""
+    out = []
+    for r in range(tp):
+        cfg = ft.MoEConfig.of(shape, r, tp)
+        rb, sb = ft.alloc_banks(cfg, 0, dev), ft.alloc_banks(cfg, 1, dev)
+        ft.ft_moe_pack(cfg, 0, pieces_d[0], rb)
+        ft.ft_moe_pack(cfg, 1, pieces_d[1], sb)
+        out.append((cfg, rb, sb))
+    return out
+
+
+def measure_decode_row(ft, dev, shape, copies, T, zipf, reps=20, seed=100):
+    """Decode regime: one step = for every layer copy, route once (the router is
+    replicated) and run every tp rank's forward in sequence. Inputs larger than L2: the
+    copies are distinct allocations of the full layer. Returns per-layer time (summed over
+    ranks), touched-expert bytes and the fraction of the measured HBM bandwidth."""
+    import torch
+    L, tp = len(copies), len(copies[0])
+    H, E, k = shape.hidden, shape.num_experts, shape.top_k
+    mk = synth.zipf_logits if zipf else synth.make_logits
+    x = torch.from_numpy(np.stack([synth.make_activations(T, H, seed=seed + l) for l in range(L)]).view(np.int16))
+    x = x.to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(np.stack([mk(T, E, seed=seed + l) for l in range(L)])).to(dev)
+    ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
+    out = torch.empty((L, tp, T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(ft.ft_moe_workspace_size(c[0], T) for c in copies[0]), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        for l in range(L):
+            ft.ft_moe_route(lg[l], k, ids[l], w[l])
+            for r, (cfg, rb, sb) in enumerate(copies[l]):
+                ft.ft_moe_forward(cfg, rb, sb, x[l], ids[l], w[l], out[l, r], ws)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize(dev)
+    assert ft.ft_moe_read_status(ws) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        stop.record(stream)
+    torch.cuda.synchronize(dev)
+    us_layer = start.elapsed_time(stop) * 1e3 / (reps * L)
+    ids_np = ids.cpu().numpy()
+    per_rank = [_rank_bytes(ft, c[0]) for c in copies[0]]
+    layer_bytes = float(np.mean([sum(len(np.unique(ids_np[l])) * re + se for re, se in per_rank)
+                                 for l in range(L)]))
+    hbm, _, kind = _peaks()
+    gbs = layer_bytes / (us_layer * 1e-6) / 1e9
+    del x, lg, ids, w, out, ws, g
+    return {"T": T, "tp": tp, "layers": L, "routing": "zipf(1.1)" if zipf else "N(0,1)",
+            "us_per_layer": us_layer, "tokens_per_s": T / (us_layer * 1e-6), "weight_bytes_per_layer": layer_bytes,
+            "gbs": gbs, "frac_of_hbm": gbs / hbm, "peak_source": f"{kind} HBM copy bandwidth",
+            "timing": "CUDA graph of all layer copies, CUDA events, inputs larger than L2"}
+
+
+def measure_prefill_row(ft, dev, shape, ranks, T, reps=5, seed=7):
+    """Prefill regime, one layer: route once, then every tp rank's forward in sequence, L2
+    flushed (512 MB written) before the route and before each rank; the layer time is the
+    sum of the route and rank times (CUDA events on the launch stream)."""
+    import torch
+    H, E, k = shape.hidden, shape.num_experts, shape.top_k
+    x = torch.from_numpy(synth.make_activations(T, H, seed=seed).view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(synth.zipf_logits(T, E, seed=seed)).to(dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(ft.ft_moe_workspace_size(c, T) for c, _, _ in ranks), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * (len(ranks) + 1))]
+    totals = []
+    for rep in range(reps + 2):
+        parts = []
+        flush.fill_(rep & 0xFF)
+        evs[0].record(stream)
+        ft.ft_moe_route(lg, k, ids, w)
+        evs[1].record(stream)
+        for r, (cfg, rb, sb) in enumerate(ranks):
+            flush.fill_((rep + r + 1) & 0xFF)
+            evs[2 * r + 2].record(stream)
+            ft.ft_moe_forward(cfg, rb, sb, x, ids, w, out, ws)
+            evs[2 * r + 3].record(stream)
+        torch.cuda.synchronize(dev)
+        assert ft.ft_moe_read_status(ws) == 0
+        parts = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(len(ranks) + 1)]
+        if rep >= 2:
+            totals.append(parts)
+    med = np.median(np.array(totals), axis=0)
+    ms = float(med.sum())
+    flops = 6.0 * H * (k * shape.intermediate + shape.shared_intermediate) * T
+    _, tfl, kind = _peaks()
+    del x, lg, ids, w, out, ws, flush
+    return {"T": T, "tp": len(ranks), "routing": "zipf(1.1)", "us": ms * 1e3, "route_us": float(med[0] * 1e3),
+            "rank_us": [float(v * 1e3) for v in med[1:]], "tokens_per_s": T / (ms / 1e3),
+            "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tfl,
+            "peak_source": f"{kind} bf16 dense", "l2": "512 MB written before the route and before each rank"}
+
+
+def measure_configs(ft, dev, qwen_pieces_d, qwen_copies, args):
+    """The benchmark's other configurations, each with its roofline fraction: qwen36 decode
+    at T = 1, 8, 32 (N(0,1) routing); the rank-local tp slices (tp = 2, 4) at decode T = 32
+    and prefill T = 2048; and the DeepSeek-V4-like layer (H = 4096, I = I_s = 2048, g = 32)
+    at T = 1, 16 (decode) and 4096 (prefill), tp = 1 and 4."""
+    import torch
+    qwen = synth.SHAPES["qwen36"]
+    rows = {"qwen36_decode": [measure_decode_row(ft, dev, qwen, qwen_copies, T, False) for T in (1, 8, 32)]}
+    tp_rows = []
+    for tp in (2, 4):
+        copies = [_ranks(ft, dev, qwen, tp, qwen_pieces_d) for _ in range(16)]
+        tp_rows.append(measure_decode_row(ft, dev, qwen, copies, 32, False))
+        tp_rows.append(measure_prefill_row(ft, dev, qwen, copies[0], 2048))
+        del copies
+        torch.cuda.empty_cache()
+    rows["qwen36_tp_slices"] = tp_rows
+    if not args.no_dsv4:
+        ds = synth.SHAPES["dsv4"]
+        pieces = synth.make_pieces(ds, 0), synth.make_pieces(ds, 0, shared=True)
+        pieces_d = tuple({n: torch.from_numpy(v).to(dev) for n, v in p.items()} for p in pieces)
+        del pieces
+        ds_rows = []
+        for tp in (1, 4):
+            copies = [_ranks(ft, dev, ds, tp, pieces_d) for _ in range(8)]
+            for T in (1, 16):
+                ds_rows.append(measure_decode_row(ft, dev, ds, copies, T, True))
+            ds_rows.append(measure_prefill_row(ft, dev, ds, copies[0], 4096))
+            del copies
+            torch.cuda.empty_cache()
+        rows["dsv4"] = ds_rows
+        del pieces_d
+        torch.cuda.empty_cache()
+    return rows
+
+
 def run_ours(args, world, rank, local):
     import torch
     import nvfp4_quantized_moe_gb300 as ft
@@ -414,6 +567,9 @@ def run_ours(args, world, rank, local):
                    for T_ in args.prefill_T.split(",")]
     router = [measure_router(ft, dev, T_, E=E, H=H) for T_ in (T, 2048)]
     fp8 = None if args.no_fp8 else measure_fp8(ft, dev)
+    configs = None
+    if not args.no_configs:
+        configs = measure_configs(ft, dev, (routed_d, shared_d), [[(cfg, rb, sb)] for rb, sb in layers], args)
     del routed_d, shared_d
     x_host = [synth.make_activations(T, H, seed=l) for l in range(L)]
     lg_host = [synth.make_logits(T, E, seed=l) for l in range(L)]
@@ -487,12 +643,17 @@ def run_ours(args, world, rank, local):
             for s in range(ft.FT_NSTAGES):
                 stage_ms[r, l, s] = ev[l][s].elapsed_time(ev[l][s + 1])
     stage_mean_us = {name: float(stage_ms[:, :, i].mean() * 1e3) for i, name in enumerate(ft.STAGES)}
-    dominant = max(stage_mean_us, key=stage_mean_us.get)
     hbm, tfl, peak_kind = _peaks()
     # the routed and the shared expert run in the same launch per stage (decode regime)
     gu_alg = float(np.mean([t * gu_bytes_per_expert + gu_sh for t in touched]))
     dn_alg = float(np.mean([t * dn_bytes_per_expert + dn_sh for t in touched]))
     alg = {"gate_up": gu_alg, "down": dn_alg, "shared_gate_up": float(gu_sh), "shared_down": float(dn_sh)}
+    if stage_mean_us["down"] < 0.5 and stage_mean_us["combine"] < 0.5:
+        # one fused launch (gate_up, down, combine) between the gate_up and the next stage
+        # marks: it streams every touched expert's gate_up and down bytes
+        stage_mean_us = {"align": stage_mean_us["align"], "decode_fused": stage_mean_us["gate_up"]}
+        alg = {"decode_fused": gu_alg + dn_alg}
+    dominant = max(stage_mean_us, key=stage_mean_us.get)
     dom_bytes = alg.get(dominant, 0.0)
     dom_s = stage_mean_us[dominant] * 1e-6
     achieved = dom_bytes / dom_s / 1e9 if dom_bytes else None
@@ -545,7 +706,8 @@ def run_ours(args, world, rank, local):
         "roofline": roofline, "layer": {"us": layer_us, "touched_experts_mean": float(np.mean(touched)),
                                         "weight_bytes_mean": float(np.mean(layer_bytes)), "gbs": layer_gbs,
                                         "frac_of_hbm": layer_gbs / hbm},
-        "stage_us": stage_mean_us, "prefill": prefill, "router_gemm": router, "fp8_block": fp8, "e2e": e2e,
+        "stage_us": stage_mean_us, "prefill": prefill, "configs": configs, "router_gemm": router,
+        "fp8_block": fp8, "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk.summary(),
     }
@@ -566,6 +728,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the fp8_block expert measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (decode T=1/8/32, tp slices, the DeepSeek-V4-like layer)")
+    ap.add_argument("--no-dsv4", action="store_true", help="skip the DeepSeek-V4-like layer among the configurations")
     ap.add_argument("--shape", choices=["qwen36", "dsv4"], default="qwen36",
                     help="NVFP4 layer family of the decode and prefill measurements")
     ap.add_argument("--prefill-T", default="2048,8192", help="comma-separated prefill token counts")

@@ -316,6 +316,20 @@ enum { FT_STAGE_ALIGN = 0, FT_STAGE_GATE_UP, FT_STAGE_SHARED_GATE_UP, FT_STAGE_D
  * itself after one forward call; events = NULL disarms it explicitly. */
 ft_status ft_moe_set_stage_events(void *const *events);
 
+/* Fault injection for tests of the error path, armed for the next ft_moe_forward call
+ * on this thread that launches kernels (then disarmed). wait_limit_ns replaces the
+ * pipelined kernels' limit on every barrier wait (0 = the default, about two seconds;
+ * otherwise 1 ms to 2 s); skip_producer = 1 makes the tensor-core (prefill) kernels issue
+ * no copies, so that their consumers' bounded waits run out: each CTA then records
+ * FT_ERR_TIMEOUT in the status word, stops, frees its tensor memory and returns, and
+ * the stream and the context stay usable. In the fused decode kernel skip_producer = 1
+ * makes the gate_up stage publish no finished block, so that every down unit's bounded
+ * wait for its block runs out, with the same outcome. The pages count a distributed stage that wedges instead of failing as a
+ * defect ("Offloaded MoE ignores tensor parallelism", follow-up comment: the rank-0
+ * relay race); this hook shows that a stalled pipeline here ends with an error status.
+ * Errors: FT_ERR_INVALID_ARG (skip_producer not 0/1, limit out of range). Host-only. */
+ft_status ft_moe_debug_inject_stall(uint64_t wait_limit_ns, int32_t skip_producer);
+
 /* Number of kernels this library has launched (or captured into a graph) from the
  * calling thread since it was loaded. */
 int64_t ft_moe_launch_count(void);

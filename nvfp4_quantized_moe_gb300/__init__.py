@@ -19,7 +19,7 @@ __all__ = [
     "ft_moe_dequant", "ft_moe_read_status", "ft_last_error", "alloc_banks", "EXPORTS",
     "FT_GU", "FT_GU_SCALE", "FT_GU_GLOBAL", "FT_DN", "FT_DN_SCALE", "FT_DN_GLOBAL",
     "FT_DTYPE_BF16", "FT_DTYPE_F32", "STATUS", "ft_moe_set_stage_events", "ft_moe_launch_count",
-    "FT_NSTAGES", "STAGES",
+    "FT_NSTAGES", "STAGES", "ft_moe_debug_inject_stall",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libftmoe.so")
@@ -34,7 +34,8 @@ BANK_NAMES = ("gate_up", "gate_up_scale", "gate_up_global", "down", "down_scale"
 # Every symbol include/ft_moe.h declares.
 EXPORTS = ("ft_moe_layout", "ft_moe_pack", "ft_moe_route", "ft_moe_route_gemm", "ft_moe_workspace_size",
            "ft_moe_forward", "ft_moe_align_workspace_size", "ft_moe_align", "ft_moe_dequant", "ft_moe_read_status",
-           "ft_last_error", "ft_moe_set_stage_events", "ft_moe_launch_count", "ft_moe_align_static")
+           "ft_last_error", "ft_moe_set_stage_events", "ft_moe_launch_count", "ft_moe_align_static",
+           "ft_moe_debug_inject_stall")
 FT_NSTAGES = 6
 STAGES = ("align", "gate_up", "shared_gate_up", "down", "shared_down", "combine")
 
@@ -99,6 +100,7 @@ def load():
             "ft_moe_dequant": [P, I32, P, I32, I32, P, P],
             "ft_moe_read_status": [P, P],
             "ft_moe_set_stage_events": [P],
+            "ft_moe_debug_inject_stall": [ctypes.c_uint64, I32],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -237,6 +239,11 @@ def ft_moe_set_stage_events(events):
         return
     arr = (ctypes.c_void_p * (FT_NSTAGES + 1))(*[ev.cuda_event for ev in events])
     _check(load().ft_moe_set_stage_events(arr))
+
+
+def ft_moe_debug_inject_stall(wait_limit_ns: int, skip_producer: int):
+    """Arm fault injection for the next ft_moe_forward on this thread (see ft_moe.h)."""
+    _check(load().ft_moe_debug_inject_stall(wait_limit_ns, skip_producer))
 
 
 def ft_moe_launch_count() -> int:

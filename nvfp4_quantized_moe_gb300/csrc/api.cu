@@ -17,6 +17,19 @@ static thread_local int64_t g_launches = 0;
 
 void count_launches(int n) { g_launches += n; }
 
+// Fault injection (ft_moe_debug_inject_stall): armed on the host for one forward call.
+static thread_local bool g_stall_armed = false;
+static thread_local bool g_stall_active = false;  // inside the forward call it was armed for
+static thread_local uint64_t g_stall_wait_ns = 0;
+static constexpr uint64_t kWaitNsMax = 2000000000ull;  // the kernels' default limit
+static thread_local int g_stall_skip = 0;
+
+void injected_stall(uint64_t *wait_ns, int *skip_producer)
+{
+    *wait_ns = g_stall_active ? g_stall_wait_ns : 0;
+    *skip_producer = g_stall_active ? g_stall_skip : 0;
+}
+
 // Record the stage boundary event i, if timing is armed.
 static cudaError_t stage_mark(int i, cudaStream_t s)
 {
@@ -184,7 +197,7 @@ static bool use_tc_fp8(const Geometry &G, int T)
 
 // Workspace regions of ft_moe_forward, each 256-byte aligned.
 struct WsLayout {
-    size_t status, split_cnt, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
+    size_t status, split_cnt, gu_done, sorted, block_expert, expert_off, npad, scratch, h, h_sh, y, y_sh, total;
     size_t split_part;  // register-fed decode kernels: partial sums of units split between CTAs
     // tensor-core path only: f16 copies of the B operands and their per-row scales
     size_t xs, xs_scale, x16, x16_scale, h16, h16_scale, hsh16, hsh16_scale;
@@ -203,6 +216,9 @@ static WsLayout ws_layout(const Geometry &G, int T)
     auto take = [&](size_t bytes) { size_t at = o; o = round_up(o + bytes, 256); return at; };
     L.status = take(256);
     L.split_cnt = take(sizeof(int) * 2 * (size_t)kMaxSplitSlots);  // gate_up, down
+    // fused decode kernel: per block (routed, then shared) finished gate_up units, and the
+    // count of CTAs done with the down stage (the last int)
+    L.gu_done = take(sizeof(int) * (size_t)(pmax / kGemvBlock + 1 + (T + kGemvBlock - 1) / kGemvBlock + 1));
     L.zero_bytes = o;
     L.sorted = take(sizeof(int) * (size_t)pmax);
     L.block_expert = take(sizeof(int) * (size_t)(pmax / kGemvBlock + 1));
@@ -285,6 +301,17 @@ ft_status ft_moe_set_stage_events(void *const *events)
 }
 
 int64_t ft_moe_launch_count(void) { return g_launches; }
+
+ft_status ft_moe_debug_inject_stall(uint64_t wait_limit_ns, int32_t skip_producer)
+{
+    if (skip_producer != 0 && skip_producer != 1) return fail(FT_ERR_INVALID_ARG, "skip_producer must be 0 or 1");
+    if (wait_limit_ns != 0 && (wait_limit_ns < 1000000ull || wait_limit_ns > kWaitNsMax))
+        return fail(FT_ERR_INVALID_ARG, "wait limit must be 0 (default) or within [1 ms, 2 s]");
+    g_stall_wait_ns = wait_limit_ns;
+    g_stall_skip = skip_producer;
+    g_stall_armed = true;
+    return ok();
+}
 
 ft_status ft_moe_layout(const ft_moe_config *cfg, int32_t shared, ft_bank_spec out[FT_NBANKS])
 {
@@ -488,7 +515,14 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     float *y_sh = reinterpret_cast<float *>(ws + L.y_sh);
     const int n_slots = T * G.k;
 
-    struct Disarm { ~Disarm() { g_stage_armed = false; } } disarm_on_return;
+    struct Disarm {
+        ~Disarm()
+        {
+            g_stage_armed = false;
+            g_stall_armed = g_stall_active = false;
+        }
+    } disarm_on_return;
+    g_stall_active = g_stall_armed;
     cudaError_t e;
     if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
 
@@ -593,7 +627,6 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
                          status, L.zero_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "align launch");
         const int max_blocks_tc = L.pmax / kTcBlock, tpad_tc = cdiv(T, kTcBlock);
-        uint16_t *yb = reinterpret_cast<uint16_t *>(y), *yb_sh = reinterpret_cast<uint16_t *>(y_sh);
         TcParams gp = {};
         gp.scales = static_cast<const uint8_t *>(routed->p[FT_GU_SCALE]);
         gp.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
@@ -638,7 +671,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
         dp.R = G.H; dp.K = G.Il; dp.group = G.g; dp.up_off = 0; dp.n_mtiles = G.H / 256;
         dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp; dp.n_slots = n_slots; dp.top_k = G.k;
-        dp.y_out = yb; dp.y_ld = G.H; dp.route_w = topk_w; dp.status = status;
+        dp.y_out = y; dp.y_ld = G.H; dp.route_w = topk_w; dp.status = status;
         dp.act_scale = f32buf(L.h16_scale);
         fp8_fields(dp, routed, false, G.Il);
         // h rows are already in sorted-position order: convert them in place of a gather
@@ -652,7 +685,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sd.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
             sd.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
             sd.K = G.Isl; sd.n_pos_dev = nullptr; sd.n_pos_static = T; sd.sorted_slot = nullptr;
-            sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.y_out = yb_sh; sd.route_w = nullptr;
+            sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.y_out = y_sh; sd.route_w = nullptr;
             sd.act_scale = f32buf(L.hsh16_scale);
             fp8_fields(sd, shared, false, G.Isl);
             e = launch_rows_to_f16(h_sh, G.Isl, nullptr, nullptr, tp, T, 1, tp, f16buf(L.hsh16),
@@ -667,7 +700,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             return cuda_fail(e, "down launch");
         if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-        e = launch_combine_bf16(yb, G.Is ? yb_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
+        e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
         if (e != cudaSuccess) return cuda_fail(e, "combine launch");
         if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         return ok();
@@ -728,13 +761,15 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         return stage_mark(FT_NSTAGES, s);
     };
 
-    // Lean register-fed kernels: routed and shared expert in one launch per stage, then the
-    // ordered combine as its own launch.
+    // Lean register-fed kernels, fused: gate_up (+ shared expert), down (+ shared expert) and
+    // the ordered combine in one persistent launch.
     const int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H);
-    const int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
+    int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
+    if (ks_dn > 4) ks_dn = 4;
     if (gemv_fast_ok(G.H, G.g, ks_gu, 2 * (G.Il > G.Isl ? G.Il : G.Isl)) && gemv_fast_ok(G.Il, G.g, ks_dn, G.H) &&
         (!G.Is || gemv_fast_ok(G.Isl, G.g, ks_dn, G.H))) {
-        FastLaunch F = {};
+        FusedLaunch FL = {};
+        FastLaunch &F = FL.gu;
         F.prob[0] = gu;
         F.prob[0].n_tiles = cdiv(G.Il, 16 * (8 / ks_gu));
         F.nprob = 1;
@@ -745,12 +780,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         }
         F.split_part = reinterpret_cast<float *>(ws + L.split_part);
         F.split_cnt = reinterpret_cast<int *>(ws + L.split_cnt);
-        if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-        int max_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
-        if ((e = launch_gemv_fast(F, true, ks_gu, max_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
-        if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-
-        FastLaunch D = {};
+        FastLaunch &D = FL.dn;
         D.prob[0] = dn;
         D.prob[0].n_tiles = cdiv(G.H, 32 * (8 / ks_dn));
         D.nprob = 1;
@@ -762,10 +792,25 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         // down units are short (I_l / 128 steps): splitting them costs more than it balances
         D.split_part = nullptr;
         D.split_cnt = nullptr;
-        if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-        max_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
-        if ((e = launch_gemv_fast(D, false, ks_dn, max_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
-        if ((e = combine()) != cudaSuccess) return cuda_fail(e, "combine launch");
+        FL.gu_done = reinterpret_cast<int *>(ws + L.gu_done);
+        FL.shared_base = max_blocks;
+        FL.done = FL.gu_done + max_blocks + tpad;
+        FL.y = y;
+        FL.y_sh = G.Is ? y_sh : nullptr;
+        FL.out = out;
+        FL.out_dtype = out_dtype;
+        FL.T = T;
+        FL.k = G.k;
+        FL.H = G.H;
+        FL.status = status;
+        injected_stall(&FL.wait_ns, &FL.skip_publish);
+        const int gu_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
+        const int dn_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
+        if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if ((e = launch_gemv_fused(FL, ks_gu, ks_dn, gu_units > dn_units ? gu_units : dn_units, s)) != cudaSuccess)
+            return cuda_fail(e, "fused decode launch");
+        for (int st_ = FT_STAGE_SHARED_GATE_UP; st_ <= FT_NSTAGES; ++st_)
+            if ((e = stage_mark(st_, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         return ok();
     }
 

@@ -284,7 +284,8 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
-// Limit of every mbarrier wait in the pipelined kernels: about two seconds.
+// Default limit of every mbarrier wait in the pipelined kernels: about two seconds (a
+// launch may pass a shorter one, see ft_moe_debug_inject_stall).
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // try_wait that lets the hardware suspend the thread for up to `hint_ns` nanoseconds
@@ -303,12 +304,14 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
     return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`: false after about two seconds, or as soon as
-// another role of the CTA has set *abort_flag (non-null) after giving up itself.
+// Wait for phase `parity` of `bar`: false after limit_ns nanoseconds (about two seconds
+// by default), or as soon as another role of the CTA has set *abort_flag (non-null)
+// after giving up itself.
 // The first 2048 polls spin (the pipelines' waits are short and latency-critical); after
 // that the thread sleeps between polls (32 ns doubling to 256 ns), so that a warp left
 // waiting for long leaves the issue slots of its scheduler to the warps that have work.
-__device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                uint64_t limit_ns = kWaitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -321,7 +324,7 @@ __device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, 
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (abort_flag && *abort_flag) return false;
-            if (globaltimer() - t0 > kWaitNs) return false;
+            if (globaltimer() - t0 > limit_ns) return false;
         }
     }
 }

@@ -64,7 +64,7 @@ struct TcParams {
     int n_slots, top_k;
     uint16_t *h_out;         // gate_up: bf16 [positions][h_ld]
     int h_ld;
-    uint16_t *y_out;         // down: bf16 [slots][y_ld]
+    float *y_out;            // down: fp32 [slots][y_ld]
     int y_ld;
     const float *route_w;    // down, routed: [T*k]
     const float *act_scale;  // per position: factor that undoes the B rows' f16 scaling (or null)
@@ -79,7 +79,14 @@ struct TcParams {
 struct TcLaunch {
     TcParams prob[2];
     int nprob;
+    uint64_t wait_ns;   // limit of every barrier wait (0: the default, about two seconds)
+    int skip_producer;  // fault injection: issue no copies, so the consumers' waits run out
+    int scale_load_bytes;  // NVFP4 block scales read 16 (or 8, when some K/group is 8 mod 16) bytes at a time
 };
+// Fault injection armed by ft_moe_debug_inject_stall for the current ft_moe_forward call
+// on this thread: the wait limit (0 = default) and whether the pipelined kernels skip
+// their producer role.
+void injected_stall(uint64_t *wait_ns, int *skip_producer);
 // The operands of one problem: its bank's packed codes (rows_total rows) and the f16
 // matrix its B operand comes from (act_rows rows of K).
 struct TcOperands {
@@ -99,9 +106,6 @@ cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int npr
 cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
                                int n_pos_static, int n_slots, int top_k, int max_rows, uint16_t *out, float *scale,
                                cudaStream_t s);
-cudaError_t launch_combine_bf16(const uint16_t *y, const uint16_t *y_shared, int T, int k, int H, void *out,
-                                int out_dtype, cudaStream_t s);
-
 // 2D tiled tensor map (rows of `row_bytes` bytes, `inner` elements used per row) through
 // the driver's cuTensorMapEncodeTiled; false when the driver refuses the shape.
 bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
@@ -178,6 +182,25 @@ struct FastLaunch {
 constexpr int kMaxSplitSlots = 512;
 constexpr size_t kSplitPartFloats = 2 * 256 * 8;  // two pieces x 256 threads x 8 partial sums
 cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_units, cudaStream_t s);
+
+// The fused decode launch: the gate_up stage (gu, as for launch_gemv_fast with gated =
+// true, its split buffers included), the down stage (dn) and the ordered combine in one
+// persistent kernel. gu_done (one counter per block: the routed expert's blocks, then the
+// shared expert's from shared_base) and done are zero at launch.
+struct FusedLaunch {
+    FastLaunch gu, dn;
+    int *gu_done;
+    int shared_base;
+    int *done;
+    const float *y, *y_sh;  // the down stage's outputs (dn.prob[0/1].y_out), combined in order
+    void *out;
+    int out_dtype, T, k, H;
+    int *status;
+    uint64_t wait_ns;       // limit of every cross-CTA wait (0: the default, about two seconds)
+    int skip_publish;       // fault injection: gate_up publishes no finished units, so down's waits run out
+};
+// ks_gu in {1, 2, 4, 8}, ks_dn in {1, 2, 4}; max_units bounds the larger stage's unit count.
+cudaError_t launch_gemv_fused(const FusedLaunch &F, int ks_gu, int ks_dn, int max_units, cudaStream_t s);
 
 // fp8_block grouped GEMV (register-fed, any batch size): K a whole number of 128-element
 // scale blocks per warp's share.

@@ -330,54 +330,6 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
     }
 }
 
-// Same order of summation for bf16 partial rows (tensor-core path).
-__global__ void combine_bf16_kernel(const uint16_t *__restrict__ y, const uint16_t *__restrict__ ysh, int T, int k,
-                                    int H, void *out, int out_dtype)
-{
-    pdl_enter();
-    const int H8 = H / 8;
-    size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (size_t)T * H8) return;
-    const int t = (int)(idx / H8), n8 = (int)(idx % H8);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    auto add = [&](const uint16_t *row) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row) + n8);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] += __uint_as_float(w[i] << 16);
-            acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-    };
-#pragma unroll 8
-    for (int j = 0; j < k; ++j) add(y + ((size_t)t * k + j) * H);
-    if (ysh) add(ysh + (size_t)t * H);
-    if (out_dtype == FT_DTYPE_F32) {
-        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + (size_t)t * H) + 2 * n8;
-        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    } else {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-            w[i] = *reinterpret_cast<uint32_t *>(&b);
-        }
-        reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + (size_t)t * H)[n8] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-
-cudaError_t launch_combine_bf16(const uint16_t *y, const uint16_t *y_shared, int T, int k, int H, void *out,
-                                int out_dtype, cudaStream_t s)
-{
-    const size_t n = (size_t)T * (H / 8);
-    const int threads = 256;
-    FT_LAUNCH(combine_bf16_kernel, dim3((unsigned)((n + threads - 1) / threads)), dim3(threads), 0, s, y,
-              y_shared, T, k, H, out, out_dtype);
-    count_launches(1);
-    return cudaGetLastError();
-}
-
 // ---------------------------------------------------------------- launchers
 
 static size_t stage_bytes(int K) { return (size_t)kGemvBlock * ((K + kStep - 1) / kStep * kStep) * 2; }

@@ -84,7 +84,9 @@ __device__ __forceinline__ void stage_row(const uint16_t *__restrict__ src, int 
 
 // The same with Kp = K and a single pass over global memory: the raw bf16 pieces go to
 // their final shared-memory places while the maximum is taken, then each lane converts
-// its own pieces in place.
+// its own pieces in place. COHERENT: the rows were written by other CTAs of the same
+// launch (after an acquire), so they are read through L2 rather than the read-only path.
+template <bool COHERENT = false>
 __device__ __forceinline__ void stage_row_1pass(const uint16_t *__restrict__ src, int K, const int *rows, uint4 *sm,
                                                 float *inv, int r)
 {
@@ -101,7 +103,7 @@ __device__ __forceinline__ void stage_row_1pass(const uint16_t *__restrict__ src
     float m = 0.f;
 #pragma unroll 4
     for (int q = lane; q < nq; q += 32) {
-        const uint4 v = __ldg(s4 + q);
+        const uint4 v = COHERENT ? __ldcg(s4 + q) : __ldg(s4 + q);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

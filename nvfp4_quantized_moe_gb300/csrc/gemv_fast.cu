@@ -100,18 +100,87 @@ __device__ __forceinline__ FastPtrs fast_ptrs(const GemvParams &p, int e, int r0
     return P;
 }
 
+// Shared-memory scratch of one CTA of the lean kernels (beside the dynamic activation rows).
+struct FastShared {
+    float inv[kGemvBlock];       // staged rows' power-of-two factors
+    int rows[kGemvBlock];        // staged rows' source rows (-1: padding)
+    int s_e;                     // expert of the staged block
+    int flag;                    // broadcast: split finisher / outcome of a wait
+    int dead;                    // fused kernel: a wait of this CTA gave up; later waits return at once
+    int tbl_dst[kGemvBlock];     // down runs: y row of each block position (or -1)
+    float tbl_w[kGemvBlock];     // down runs: its factor
+    float s_glob[kThreads * 4];  // down runs: each thread's row globals of its current unit
+    float red[8][32][8];         // in-CTA K split: the warps' partial sums
+};
+
+__device__ __forceinline__ int ld_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Thread 0 waits until *ctr >= want (acquire), sleeping between polls; false after
+// limit_ns (FT_ERR_TIMEOUT is recorded) or at once when an earlier wait of the CTA gave up.
+// The outcome reaches every thread through sm.flag (the caller synchronises).
+__device__ __forceinline__ void wait_counter_t0(const int *ctr, int want, uint64_t limit_ns, int *status,
+                                                FastShared &sm)
+{
+    int ok = !sm.dead;
+    if (ok && ld_acquire(ctr) < want) {
+        const uint64_t t0 = globaltimer();
+        uint32_t ns = 32;
+        while (ld_acquire(ctr) < want) {
+            __nanosleep(ns);
+            if (ns < 256) ns <<= 1;
+            if (globaltimer() - t0 > limit_ns) {
+                ok = 0;
+                raise_status(status, FT_ERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    if (!ok) sm.dead = 1;
+    sm.flag = ok;
+}
+
 }  // namespace
+
+// Cross-CTA ordering inside the fused decode kernel (null for the separate kernels): a
+// block's down units start once all of its gate_up CTA units have written h.
+struct DecodeSync {
+    int *gu_done;     // per block: gate_up CTA units finished (routed blocks, then the shared ones)
+    int shared_base;  // index in gu_done of the shared expert's first block
+    int target[2];    // gate_up CTA units per block of the routed / shared problem
+    int *status;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ int *gu_counter(const DecodeSync *S, int pi, int blk)
+{
+    return S->gu_done + (pi ? S->shared_base + blk : blk);
+}
+
+// CTA-wide: wait until block `blk` of problem `pi` has its h rows (fused kernel only).
+__device__ __forceinline__ void wait_block_ready(const DecodeSync *S, int pi, int blk, FastShared &sm)
+{
+    if (!S) return;
+    __syncthreads();
+    if (threadIdx.x == 0) wait_counter_t0(gu_counter(S, pi, blk), S->target[pi], S->wait_ns, S->status, sm);
+    __syncthreads();
+}
 
 // One unit of work: a block of 8 positions of problem `p` and one pair-tile per warp,
 // over the warp's 128-element steps [s_lo, s_hi) (all of them unless the unit is split
 // between CTAs c - 1 and c (piece 1, this CTA is c) or c and c + 1 (piece 0): the pair's
 // partials meet in split slot c - piece and only the second of the two CTAs to finish
 // adds the other piece and runs the epilogue; a sum of two fp32 terms does not depend on
-// their order).
+// their order). done_ctr (fused kernel, gate_up): counted once the unit's h rows are
+// written, with release semantics, by whichever CTA ran the epilogue.
 template <bool GATED, int KS>
 __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch &L, int lu, int n_pos, uint4 *smem_b,
-                                          const float *inv, const int *s_e, float (&red)[KS > 1 ? 8 : 1][32][8],
-                                          int s_lo = 0, int s_hi = -1, int piece = -1)
+                                          FastShared &sm, int s_lo = 0, int s_hi = -1, int piece = -1,
+                                          int *done_ctr = nullptr)
 {
     constexpr int TPW = 8 / KS;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -128,7 +197,8 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     const int boff[4] = {4 * c + (0 ^ m), 4 * c + (1 ^ m), 4 * c + (2 ^ m), 4 * c + (3 ^ m)};
     const int r0 = (grp * TPW + tp) * pair_rows;
     const bool ok = r0 < rows_limit;
-    const int e = *s_e;
+    const int e = sm.s_e;
+    const float *inv = sm.inv;
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
         const FastPtrs P = fast_ptrs<GATED>(p, e, r0, g, c, k0);
@@ -147,7 +217,6 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     }
     if constexpr (KS == 1) {
         if (piece >= 0) {
-            __shared__ int s_flag;
             const int slot = (int)blockIdx.x - piece;
             float *part = L.split_part + (size_t)slot * kSplitPartFloats;
             float4 *mine = reinterpret_cast<float4 *>(part + ((size_t)piece * kThreads + threadIdx.x) * 8);
@@ -156,10 +225,10 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();  // every thread's partials before the count
-                s_flag = atomicAdd(L.split_cnt + slot, 1) == 1;
+                sm.flag = atomicAdd(L.split_cnt + slot, 1) == 1;
             }
             __syncthreads();
-            if (!s_flag) return;  // the other piece finishes the unit
+            if (!sm.flag) return;  // the other piece finishes the unit
             __threadfence();
             const float4 *other =
                 reinterpret_cast<const float4 *>(part + ((size_t)(1 - piece) * kThreads + threadIdx.x) * 8);
@@ -171,8 +240,8 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     if (KS > 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            red[warp][lane][i] = acc0[i];
-            red[warp][lane][4 + i] = acc1[i];
+            sm.red[warp][lane][i] = acc0[i];
+            sm.red[warp][lane][4 + i] = acc1[i];
         }
         __syncthreads();
     }
@@ -182,8 +251,8 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
             for (int i = 0; i < 4; ++i) {
                 float a = 0.f, b2 = 0.f;
                 for (int w = 0; w < KS; ++w) {
-                    a += red[tp * KS + w][lane][i];
-                    b2 += red[tp * KS + w][lane][4 + i];
+                    a += sm.red[tp * KS + w][lane][i];
+                    b2 += sm.red[tp * KS + w][lane][4 + i];
                 }
                 acc0[i] = a;
                 acc1[i] = b2;
@@ -230,31 +299,38 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
             }
         }
     }
-    if (KS > 1) __syncthreads();
+    if (KS > 1 || done_ctr) __syncthreads();
+    if (done_ctr && threadIdx.x == 0) {
+        __threadfence();  // the unit's h rows (all warps) before the count
+        atomicAdd(done_ctr, 1);
+    }
 }
 
 // Stage the activation rows of block `blk` of problem `p` and the block's expert id
-// (CTA-wide, with barriers).
-template <bool GATED>
-__device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_pos, int *rows, uint4 *smem_b,
-                                           float *inv, int *s_e)
+// (CTA-wide, with barriers). COHERENT: rows written earlier in the same launch.
+template <bool GATED, bool COHERENT = false>
+__device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_pos, uint4 *smem_b, FastShared &sm)
 {
     __syncthreads();
-    if (threadIdx.x < kGemvBlock) rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, GATED);
-    if (threadIdx.x == kGemvBlock) *s_e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+    if (threadIdx.x < kGemvBlock)
+        sm.rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, GATED);
+    if (threadIdx.x == kGemvBlock) sm.s_e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
     __syncthreads();
-    for (int r = threadIdx.x >> 5; r < kGemvBlock; r += kThreads / 32) stage_row_1pass(p.act, p.K, rows, smem_b, inv, r);
+    for (int r = threadIdx.x >> 5; r < kGemvBlock; r += kThreads / 32)
+        stage_row_1pass<COHERENT>(p.act, p.K, sm.rows, smem_b, sm.inv, r);
     __syncthreads();
 }
 
 // Down stage over the CTA's unit range [u_lo, u_hi), whole units of a multiple of 4 steps
-// (K a multiple of 512). Consecutive units of
-// one block share the expert and the staged activations, and warp w's rows in them are
-// 256 apart, so each warp streams a run of them through one register ring as a single
-// sequence of steps (no refill between units) and writes y at each unit's last step.
-__device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int u_lo,
-                                          int u_hi, uint4 *smem_b, float *inv, int *rows, int *s_e, float *s_glob,
-                                          int *tbl_dst, float *tbl_w)
+// (K a multiple of 512). Consecutive units of one block share the expert and the staged
+// activations, and warp w's rows in them are 256 apart, so each warp streams a run of
+// them through one register ring as a single sequence of steps (no refill between units)
+// and writes y at each unit's last step. S (fused kernel): before a block's h rows are
+// staged, its gate_up units must have finished; the run's first weight loads are issued
+// before that wait.
+template <bool COHERENT>
+__device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int u_lo, int u_hi,
+                                          uint4 *smem_b, FastShared &sm, const DecodeSync *S)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -268,11 +344,44 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
         const int blk = lu / p.n_tiles, grp0 = lu - blk * p.n_tiles;
         const int nu = min(p.n_tiles - grp0, u_hi - u);  // the run: this block's units in range
         u += nu;
-        fast_stage<false>(p, blk, n_pos, rows, smem_b, inv, s_e);
+        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int r0a = (grp0 * 8 + warp) * 32;  // the warp's first row in the run's first unit
+        // units with rows in range form a prefix of the run
+        const int nok = r0a < p.R ? min(nu, (p.R - r0a + 255) / 256) : 0;
+        const int S_ = p.K / kStep, tot = nok * S_;
+        const FastPtrs P = fast_ptrs<false>(p, e, r0a < p.R ? r0a : 0, g, c, 0);
+        const uint32_t spb = (p.group == 16) ? 8u : 4u;  // scale bytes per step and row pair
+        // from a unit's last step to the next unit's first: 256 rows on, back to K = 0
+        const uint32_t jump_c = 256u * (uint32_t)(p.K / 2) - 64u * (uint32_t)(S_ - 1);
+        const uint32_t jump_s = 256u * (uint32_t)(p.K / p.group) - spb * (uint32_t)(S_ - 1);
+        uint32_t lco = 0, lso = 0;
+        int ls = 0;  // load cursor: byte offsets and step within its unit
+        auto advance_load = [&]() {
+            if (++ls == S_) {
+                ls = 0;
+                lco += jump_c;
+                lso += jump_s;
+            } else {
+                lco += 64u;
+                lso += spb;
+            }
+        };
+        // the first two steps' weights do not depend on h: load them before waiting for it
+        FastFrag ring[4];
+        if (tot > 0) {
+            fast_load_at(P, lco, lso, ring[0]);
+            advance_load();
+        }
+        if (tot > 1) {
+            fast_load_at(P, lco, lso, ring[1]);
+            advance_load();
+        }
+        wait_block_ready(S, pi, blk, sm);
+        fast_stage<false, COHERENT>(p, blk, n_pos, smem_b, sm);
         if (threadIdx.x < kGemvBlock) {  // per block position: y row (slot) or -1, and its factor
             const int pos = blk * kGemvBlock + threadIdx.x;
             int dst = -1;
-            float w = inv[threadIdx.x];
+            float w = sm.inv[threadIdx.x];
             if (pos < n_pos) {
                 if (p.sorted_slot) {
                     const int sl = __ldg(p.sorted_slot + pos);
@@ -284,46 +393,17 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
                     dst = pos;
                 }
             }
-            tbl_dst[threadIdx.x] = dst;
-            tbl_w[threadIdx.x] = w;
+            sm.tbl_dst[threadIdx.x] = dst;
+            sm.tbl_w[threadIdx.x] = w;
         }
         __syncthreads();
-        const int r0a = (grp0 * 8 + warp) * 32;  // the warp's first row in the run's first unit
-        // units with rows in range form a prefix of the run
-        const int nok = r0a < p.R ? min(nu, (p.R - r0a + 255) / 256) : 0;
-        const int S = p.K / kStep, tot = nok * S;
         if (tot == 0) continue;
-        const int e = *s_e;
-        const FastPtrs P = fast_ptrs<false>(p, e, r0a, g, c, 0);
-        const uint32_t spb = (p.group == 16) ? 8u : 4u;  // scale bytes per step and row pair
-        // from a unit's last step to the next unit's first: 256 rows on, back to K = 0
-        const uint32_t jump_c = 256u * (uint32_t)(p.K / 2) - 64u * (uint32_t)(S - 1);
-        const uint32_t jump_s = 256u * (uint32_t)(p.K / p.group) - spb * (uint32_t)(S - 1);
         const uint4 *bb = smem_b + (size_t)g * (p.K / 8);
         const float *glob_e = p.glob + (size_t)e * p.e_glob;
-        uint32_t lco = 0, lso = 0;
-        int ls = 0;  // load cursor: byte offsets and step within its unit
-        auto advance_load = [&]() {
-            if (++ls == S) {
-                ls = 0;
-                lco += jump_c;
-                lso += jump_s;
-            } else {
-                lco += 64u;
-                lso += spb;
-            }
-        };
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-        FastFrag ring[4];
-        fast_load_at(P, lco, lso, ring[0]);
-        advance_load();
-        if (tot > 1) {
-            fast_load_at(P, lco, lso, ring[1]);
-            advance_load();
-        }
         int cs = 0, r0 = r0a;  // compute cursor: step within the unit, the unit's first row
-        float *gs = s_glob + threadIdx.x * 4;
-        for (int t0 = 0; t0 < tot; t0 += 4) {  // S, and so tot, is a multiple of 4
+        float *gs = sm.s_glob + threadIdx.x * 4;
+        for (int t0 = 0; t0 < tot; t0 += 4) {  // S_, and so tot, is a multiple of 4
             if (cs == 0) {  // a unit's first steps: copy its rows' globals to shared memory
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
@@ -341,13 +421,13 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
                 fast_compute(ring[q], bb, boff, cs + q, acc0, acc1);
             }
             cs += 4;
-            if (cs == S) {  // the unit's last step: y rows r0 .. r0 + 31 of its positions
+            if (cs == S_) {  // the unit's last step: y rows r0 .. r0 + 31 of its positions
                 cp_async_wait<0>();
 #pragma unroll
                 for (int col = 0; col < 2; ++col) {
-                    const int dst = tbl_dst[2 * c + col];
+                    const int dst = sm.tbl_dst[2 * c + col];
                     if (dst < 0) continue;
-                    const float w = tbl_w[2 * c + col];
+                    const float w = sm.tbl_w[2 * c + col];
                     float *yrow = p.y_out + (size_t)dst * p.R;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
@@ -365,18 +445,14 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
     }
 }
 
-// Grid-strided over the concatenated unit lists of up to two problems (the routed
-// experts and the shared expert); each CTA takes a contiguous range of units.
-template <bool GATED, int KS>
-__global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_constant__ FastLaunch L)
+// One stage (gate_up or down) of the lean kernels over the concatenated unit lists of up
+// to two problems (the routed experts and the shared expert): the even split of all K
+// steps (gate_up, KS = 1), block runs (down, KS = 1), or contiguous unit ranges with the K
+// split inside the CTA. S: fused kernel (gate_up counts finished units per block; down
+// waits for them and reads h through L2).
+template <bool GATED, int KS, bool FUSED>
+__device__ __forceinline__ void fast_phase(const FastLaunch &L, uint4 *smem_b, FastShared &sm, const DecodeSync *S)
 {
-    pdl_enter();
-    extern __shared__ uint4 smem_b[];
-    __shared__ float inv[kGemvBlock];
-    __shared__ int rows[kGemvBlock];
-    __shared__ int s_e;  // expert of the staged block
-    __shared__ float s_glob[GATED ? 1 : kThreads * 4];  // down: each thread's row globals of its current unit
-    __shared__ float red[KS > 1 ? 8 : 1][32][8];
     const int n_pos0 = load_n_pos(L.prob[0]);
     const int n_pos1 = L.nprob > 1 ? load_n_pos(L.prob[1]) : 0;
     const int units0 = (n_pos0 / kGemvBlock) * L.prob[0].n_tiles;
@@ -390,12 +466,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         const int blk = lu / p.n_tiles;
         const int key = pi * (1 << 30) + blk;
         if (key != staged) {
-            fast_stage<GATED>(p, blk, pi ? n_pos1 : n_pos0, rows, smem_b, inv, &s_e);
+            if (!GATED) wait_block_ready(S, pi, blk, sm);
+            fast_stage<GATED, FUSED && !GATED>(p, blk, pi ? n_pos1 : n_pos0, smem_b, sm);
             staged = key;
         }
         return lu;
     };
-    if constexpr (KS == 1) {
+    auto counter = [&](int u) -> int * {  // fused gate_up: the unit's block counter
+        if (!(FUSED && GATED) || !S->gu_done) return nullptr;
+        const int pi = u < units0 ? 0 : 1;
+        const int lu = pi ? u - units0 : u;
+        return gu_counter(S, pi, lu / L.prob[pi].n_tiles);
+    };
+    if constexpr (KS == 1 && GATED) {
         // Even split of all K steps: W = units0 * S0 + units1 * S1 steps, CTA c takes
         // [c W / G, (c + 1) W / G). Needs every CTA's share to be at least one unit, so
         // that a unit is cut at most once.
@@ -405,18 +488,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         if (L.split_part && gridDim.x <= kMaxSplitSlots && W >= (int64_t)gridDim.x * Smax) {
             const int w_hi = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x), W0 = units0 * S0;
             for (int w = (int)((int64_t)blockIdx.x * W / gridDim.x); w < w_hi;) {
-                int u, s, S;
+                int u, s, Sx;
                 if (w < W0) {
-                    u = w / S0; s = w - u * S0; S = S0;
+                    u = w / S0; s = w - u * S0; Sx = S0;
                 } else {
-                    u = units0 + (w - W0) / S1; s = (w - W0) - (u - units0) * S1; S = S1;
+                    u = units0 + (w - W0) / S1; s = (w - W0) - (u - units0) * S1; Sx = S1;
                 }
-                const int s_end = w_hi - w < S - s ? s + (w_hi - w) : S;
+                const int s_end = w_hi - w < Sx - s ? s + (w_hi - w) : Sx;
                 const int pi = u < units0 ? 0 : 1;
                 const int lu = stage_for(u);
                 // piece 1: tail of the unit begun by CTA c - 1; piece 0: head of one CTA c + 1 ends
-                const int piece = s > 0 ? 1 : (s_end < S ? 0 : -1);
-                fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, &s_e, red, s, s_end, piece);
+                const int piece = s > 0 ? 1 : (s_end < Sx ? 0 : -1);
+                fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, sm, s, s_end, piece,
+                                     counter(u));
                 w += s_end - s;
             }
             return;
@@ -426,16 +510,89 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
     if constexpr (!GATED && KS == 1) {  // (the host keeps each expert's bank below 2 GB here)
         if (L.prob[0].K % (4 * kStep) == 0 && (L.nprob < 2 || L.prob[1].K % (4 * kStep) == 0)) {
-            __shared__ int tbl_dst[kGemvBlock];
-            __shared__ float tbl_w[kGemvBlock];
-            down_runs(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, inv, rows, &s_e, s_glob, tbl_dst, tbl_w);
+            down_runs<FUSED>(L, units0, n_pos0, n_pos1, u_lo, u_hi, smem_b, sm, S);
             return;
         }
     }
     for (int u = u_lo; u < u_hi; ++u) {
         const int pi = u < units0 ? 0 : 1;
         const int lu = stage_for(u);
-        fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, inv, &s_e, red);
+        fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, sm, 0, -1, -1, counter(u));
+    }
+}
+
+// A separate gate_up or down launch (its predecessor's outputs are complete on entry).
+template <bool GATED, int KS>
+__global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_constant__ FastLaunch L)
+{
+    pdl_enter();
+    extern __shared__ uint4 smem_b[];
+    __shared__ FastShared sm;
+    if (threadIdx.x == 0) sm.dead = 0;
+    fast_phase<GATED, KS, false>(L, smem_b, sm, nullptr);
+}
+
+// Fused decode forward: gate_up (+ SwiGLU into h) over every touched block, then down
+// (+ routing weight and row global into the slot-major y rows), then the ordered combine
+// out[t] = sum_{j<k} y[t k + j] (+ y_shared[t]), in one persistent launch. A block's down
+// units wait (bounded) for its gate_up units through per-block counters; the combine
+// waits (bounded) for every CTA's down units through one grid-wide count. All CTAs are
+// resident at once (the host sizes the grid by the occupancy), and the kernel lets the
+// next launch of the stream be scheduled only after its last wait, so no CTA can wait on
+// one that has no SM to run on.
+template <int KSG, int KSD>
+__global__ void __launch_bounds__(kThreads, 2) gemv_fused_kernel(const __grid_constant__ FusedLaunch F)
+{
+    pdl_wait();
+    extern __shared__ uint4 smem_b[];
+    __shared__ FastShared sm;
+    if (threadIdx.x == 0) sm.dead = 0;
+    __syncthreads();
+    DecodeSync S;
+    S.gu_done = F.gu_done;
+    S.shared_base = F.shared_base;
+    S.target[0] = F.gu.prob[0].n_tiles;
+    S.target[1] = F.gu.nprob > 1 ? F.gu.prob[1].n_tiles : 0;
+    S.status = F.status;
+    S.wait_ns = F.wait_ns ? F.wait_ns : kWaitNs;
+    DecodeSync S_gu = S;
+    if (F.skip_publish) S_gu.gu_done = nullptr;  // fault injection: nothing is published
+    fast_phase<true, KSG, true>(F.gu, smem_b, sm, &S_gu);
+    fast_phase<false, KSD, true>(F.dn, smem_b, sm, &S);
+    // every CTA's y rows before any combine
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(F.done, 1);
+        wait_counter_t0(F.done, (int)gridDim.x, S.wait_ns, F.status, sm);
+    }
+    __syncthreads();
+    pdl_trigger();  // past the last wait: the next launch may take SM slots now
+    const int H4 = F.H / 4, k = F.k;
+    const int64_t n = (int64_t)F.T * H4;
+    const int64_t lo = (int64_t)blockIdx.x * n / gridDim.x, hi = (int64_t)(blockIdx.x + 1) * n / gridDim.x;
+    for (int64_t idx = lo + threadIdx.x; idx < hi; idx += kThreads) {
+        const int t = (int)(idx / H4), n4 = (int)(idx % H4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 sh = F.y_sh ? __ldcg(reinterpret_cast<const float4 *>(F.y_sh + (size_t)t * F.H) + n4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int j = 0; j < k; ++j) {  // fixed order: j = 0 .. k - 1, then the shared row
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(F.y + ((size_t)t * k + j) * F.H) + n4);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (F.y_sh) {
+            acc.x += sh.x; acc.y += sh.y; acc.z += sh.z; acc.w += sh.w;
+        }
+        if (F.out_dtype == FT_DTYPE_F32) {
+            reinterpret_cast<float4 *>(static_cast<float *>(F.out) + (size_t)t * F.H)[n4] = acc;
+        } else {
+            __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 v;
+            v.x = *reinterpret_cast<uint32_t *>(&a);
+            v.y = *reinterpret_cast<uint32_t *>(&b);
+            reinterpret_cast<uint2 *>(static_cast<uint16_t *>(F.out) + (size_t)t * F.H)[n4] = v;
+        }
     }
 }
 
@@ -479,6 +636,46 @@ cudaError_t launch_gemv_fast(const FastLaunch &L, bool gated, int ks, int max_un
     case 4: return launch_fast_t<false, 4>(L, max_units, s);
     default: return launch_fast_t<false, 8>(L, max_units, s);
     }
+}
+
+template <int KSG, int KSD>
+static cudaError_t launch_fused_t(const FusedLaunch &F, int max_units, cudaStream_t s)
+{
+    auto kern = gemv_fused_kernel<KSG, KSD>;
+    int Kmax = 0;
+    for (const FastLaunch *L : {&F.gu, &F.dn})
+        for (int i = 0; i < L->nprob; ++i) Kmax = L->prob[i].K > Kmax ? L->prob[i].K : Kmax;
+    const size_t smem = (size_t)kGemvBlock * Kmax * 2;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // every CTA must be resident at once: the grid never exceeds what the SMs hold together
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    int grid = sm_count() * (occ < 2 ? occ : 2);
+    if (max_units < grid) grid = max_units;
+    if (grid < 1) grid = 1;
+    FT_LAUNCH(kern, dim3(grid), dim3(kThreads), smem, s, F);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_fused(const FusedLaunch &F, int ks_gu, int ks_dn, int max_units, cudaStream_t s)
+{
+#define FT_FUSED_DN(KSG)                                             \
+    switch (ks_dn) {                                                 \
+    case 1: return launch_fused_t<KSG, 1>(F, max_units, s);          \
+    case 2: return launch_fused_t<KSG, 2>(F, max_units, s);          \
+    default: return launch_fused_t<KSG, 4>(F, max_units, s);         \
+    }
+    switch (ks_gu) {
+    case 1: FT_FUSED_DN(1)
+    case 2: FT_FUSED_DN(2)
+    case 4: FT_FUSED_DN(4)
+    default: FT_FUSED_DN(8)
+    }
+#undef FT_FUSED_DN
 }
 
 }  // namespace ftmoe

@@ -25,9 +25,9 @@
 //   warps 10-13 the epilogue (and warps 15-18 as a second group taking the other half
 //               of the 32-position chunks): read the accumulator with tcgen05.ld
 //               (one TMEM lane = one weight row per thread), apply globals, row scales and
-//               SwiGLU (h) or the routing weight (y: each 32-position chunk is transposed
-//               through shared memory so that every position's 256 contiguous outputs leave
-//               in 512-byte warp stores). Tensor memory: the accumulator (256 columns) and
+//               SwiGLU (h) or the routing weight (y, fp32: each warp transposes its 32 x 32
+//               blocks through shared memory and stores 128 contiguous bytes per position with
+//               16-byte stores). Tensor memory: the accumulator (256 columns) and
 //               four A buffers (256 columns); the accumulator is released once every
 //               epilogue warp has loaded its last chunk.
 // f16 operands instead of bf16: code*scale is exact in both; a bf16 activation row
@@ -65,16 +65,17 @@ constexpr int kMmaWarp1 = 14;    // issuer of tile 1: the issue cost of a tcgen0
 constexpr int kDq = 256;         // dequantising threads
 constexpr int kEpWarp0 = 10;     // first epilogue warp (group 0: 10..13, group 1: 15..18)
 
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, uint64_t limit)
 {
-    return mbar_wait_timed(bar, parity, abort_flag);
+    return mbar_wait_timed(bar, parity, abort_flag, limit);
 }
 
 // The same, for a whole warp: every lane waits (and so acquires what the phase
 // publishes); the result is the same on all lanes, so the warp leaves its loops together.
-__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              uint64_t limit)
 {
-    const bool ok = mbar_wait_timed(bar, parity, abort_flag);
+    const bool ok = mbar_wait_timed(bar, parity, abort_flag, limit);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -100,9 +101,9 @@ __host__ __device__ inline TcSmem tc_smem(int ns, bool fp8, bool gated)
     s.a_off = 0;
     s.b_off = s.a_off + NA * s.a_bytes;
     s.raw_off = s.b_off + ns * s.b_bytes;
-    // down epilogue: per group two 32-position x 256-row bf16 tiles
+    // down epilogue: a 32 x 32 fp32 transpose block per epilogue warp
     s.tp_off = s.raw_off + ns * s.raw_bytes;
-    s.tbl_off = s.tp_off + (gated ? 0 : tc_epi_groups(false) * 2 * 32 * 2 * MT * 2);
+    s.tbl_off = s.tp_off + (gated ? 0 : 4 * tc_epi_groups(false) * 32 * 32 * 4);
     s.bar_off = s.tbl_off + 2 * NT * 8;           // two position tables (unit parity): [NT] slots + [NT] factors
     s.total = s.bar_off + 512;
     return s;
@@ -133,12 +134,12 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars, *empty = bars + NSMAX, *a_full = bars + 2 * NSMAX, *a_empty = a_full + NA;
     uint64_t *acc_full = a_empty + NA, *acc_empty = acc_full + 2;  // one accumulator (index 0)
-    uint64_t *tp_bar = acc_empty + 2;  // down epilogue, per group: transpose tile written by its 4 warps
-    uint64_t *tbl_bar = tp_bar + 4;    // epilogue: a unit's position table (written by group 0)
+    uint64_t *tbl_bar = acc_empty + 2;  // epilogue: a unit's position table (written by group 0)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tbl_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t wl = TL.wait_ns ? TL.wait_ns : kWaitNs;  // limit of every barrier wait
     // columns [0, 256): the accumulator (two 128-column tiles); [256, 512): NA A buffers
     const uint32_t tmem_cols = 512;
 
@@ -152,7 +153,6 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             mbar_init(acc_empty + i, 4 * NG);  // every epilogue warp, after its last TMEM read
             mbar_init(tbl_bar + i, 4 * NG);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(tp_bar + i, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -189,7 +189,9 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        // (fault injection: with skip_producer set on the host, no copy is ever issued, so
+        // every consumer's bounded wait runs out)
+        if (lane == 0 && !TL.skip_producer) {
             int it = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
                 int lu;
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 const int nk = p.K / KC;
                 for (int c = 0; c < nk; ++c, ++it) {
                     const int slot = it % ns;
-                    if (!wait_bar(empty + slot, ((it / ns) & 1) ^ 1, abort_flag)) { dead = true; break; }
+                    if (!wait_bar(empty + slot, ((it / ns) & 1) ^ 1, abort_flag, wl)) { dead = true; break; }
                     unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
                     mbar_arrive_expect_tx(full + slot, L.raw_bytes + L.b_bytes);
                     tc::tma_load_2d(raw, codes_map, c * RB, row_a, full + slot);
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             // consumer gave up)
             for (int i = 0; i < ns && i < it; ++i) {
                 const int last = it - 1 - i;
-                mbar_wait_timed(full + last % ns, (last / ns) & 1, nullptr);
+                mbar_wait_timed(full + last % ns, (last / ns) & 1, nullptr, wl);
             }
         }
     } else if (warp == 1 || warp == kMmaWarp1) {
@@ -230,13 +232,13 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 int lu;
                 const int nk = prob_of(u, lu).K / KC;
                 // one accumulator: the epilogue of the previous unit has read it out
-                if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag)) { dead = true; break; }
+                if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag, wl)) { dead = true; break; }
                 tc::fence_after_sync();
                 const uint32_t acc = tmem + tile * NT;
                 for (int c = 0; c < nk; ++c, ++it, ++ia) {
                     const int slot = it % ns, ab = ia % NA;
-                    if (!wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
-                        !wait_bar(a_full + ab, (ia / NA) & 1, abort_flag)) {
+                    if (!wait_bar(full + slot, (it / ns) & 1, abort_flag, wl) ||
+                        !wait_bar(a_full + ab, (ia / NA) & 1, abort_flag, wl)) {
                         dead = true;
                         break;
                     }
@@ -278,8 +280,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             const float down = pow2f(-row_scale_exp(448.f * smax));
             for (int c = 0; c < nk; ++c, ++it, ++ia) {
                 const int slot = it % ns, ab = ia % NA;
-                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
-                    !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag)) {
+                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag, wl) ||
+                    !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag, wl)) {
                     dead = true;
                     break;
                 }
@@ -319,10 +321,18 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         // ------------------------------------------------------------ dequantisation
         // warp (quarter, half): rows 32*quarter .. +32 of tile `half`.
         // Block scales come straight from global memory: each thread reads its own row's
-        // 16-byte groups (one group covers cpl chunks), one group ahead, across units.
+        // 16- (or 8-) byte groups (one group covers cpl chunks), one group ahead, across units.
         const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;
-        const int cpl = 16 * p0.group / KC;  // K chunks covered by 16 scale bytes
+        // Scale bytes per load: 16, or 8 when a problem's rows hold K/group = 8 (mod 16)
+        // scales (16-byte loads would then cross rows and lose their alignment).
+        const int sbytes = TL.scale_load_bytes;
+        const int cpl = sbytes * p0.group / KC;  // K chunks covered by one scale load
+        auto load_scales = [&](const uint8_t *ptr) -> uint4 {
+            if (sbytes == 16) return __ldg(reinterpret_cast<const uint4 *>(ptr));
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(ptr));
+            return make_uint4(v.x, v.y, 0u, 0u);
+        };
         auto scale_row = [&](int uu) {
             int lu;
             const TcParams &q = prob_of(uu, lu);
@@ -333,7 +343,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         };
         int it = 0, ia = 0;
         const uint8_t *srow = blockIdx.x < n_units ? scale_row(blockIdx.x) : p0.scales;
-        uint4 s_next = blockIdx.x < n_units ? __ldg(reinterpret_cast<const uint4 *>(srow)) : make_uint4(0, 0, 0, 0);
+        uint4 s_next = blockIdx.x < n_units ? load_scales(srow) : make_uint4(0, 0, 0, 0);
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
             int lu;
             const int nk = prob_of(u, lu).K / KC;
@@ -343,16 +353,16 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             uint4 s16 = make_uint4(0, 0, 0, 0);
             for (int c = 0; c < nk; ++c, ++it, ++ia) {
                 const int slot = it % ns, ab = ia % NA;
-                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag) ||
-                    !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag)) {
+                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag, wl) ||
+                    !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag, wl)) {
                     dead = true;
                     break;
                 }
                 if (c % cpl == 0) {
                     const int q = c / cpl;
                     s16 = s_next;
-                    if (q + 1 < ngroups) s_next = __ldg(reinterpret_cast<const uint4 *>(srow + 16 * (q + 1)));
-                    else if (srow_next) s_next = __ldg(reinterpret_cast<const uint4 *>(srow_next));
+                    if (q + 1 < ngroups) s_next = load_scales(srow + sbytes * (q + 1));
+                    else if (srow_next) s_next = load_scales(srow_next);
                 }
                 const int ci = c % cpl;
                 uint32_t sw;
@@ -410,7 +420,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         // double-buffered by unit parity: a warp writes table X for unit u only after
         // passing the table barrier of unit u - 1, which every epilogue warp reaches after
         // finishing unit u - 2, the last reader of table X.
-        int uc = 0, gc = 0;  // units, and down-epilogue chunks (transpose tile use count)
+        int uc = 0;  // units
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
             int lu;
             const TcParams &p = prob_of(u, lu);
@@ -457,8 +467,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             }
             __syncwarp();
             if (lane == 0) arrive(tbl_bar + X);
-            if (!warp_wait_bar(tbl_bar + X, (uc >> 1) & 1, abort_flag)) { dead = true; break; }
-            if (!warp_wait_bar(acc_full, uc & 1, abort_flag)) { dead = true; break; }
+            if (!warp_wait_bar(tbl_bar + X, (uc >> 1) & 1, abort_flag, wl)) { dead = true; break; }
+            if (!warp_wait_bar(acc_full, uc & 1, abort_flag, wl)) { dead = true; break; }
             tc::fence_after_sync();
             const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
             for (int cb = eg; cb < NT / 32; cb += NG) {
@@ -482,35 +492,29 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                         p.h_out[(size_t)(b * NT + t) * p.h_ld + row0] = *reinterpret_cast<uint16_t *>(&hv);
                     }
                 } else {
-                    // y rows of the chunk's 32 positions, each 256 contiguous values (both tiles):
-                    // every thread writes its row of the two tiles into a shared [32][256] bf16
-                    // tile, then each warp stores 8 whole position rows with 16-byte stores
-                    // (512 contiguous bytes per warp instruction instead of 64).
-                    const int X = eg * 2 + (gc & 1);  // the group's tile, by chunk parity
-                    uint16_t *tb = reinterpret_cast<uint16_t *>(smem + L.tp_off + X * (32 * 2 * MT * 2));
+                    // y rows in fp32 (no rounding of the slot partials before the ordered
+                    // combine). The warp holds output columns [c0, c0 + 32) (its TMEM lanes) of 32
+                    // positions; it transposes each tile's 32 x 32 block through its own 4 KB of
+                    // shared memory so that 8 lanes store one position's 128 contiguous bytes with
+                    // 16-byte stores (8 store instructions per block instead of 32).
+                    float *tb = reinterpret_cast<float *>(smem + L.tp_off) + (size_t)(eg * 4 + ew) * 32 * 32;
+                    const int jl = lane >> 3, ql = lane & 7;  // read-back: position jb + jl, columns 4 ql ..
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float w = tbl_w[cb * 32 + j];
-                        __nv_bfloat16 y0 = __float2bfloat16_rn(__uint_as_float(v0[j]) * g0 * w);
-                        __nv_bfloat16 y1 = __float2bfloat16_rn(__uint_as_float(v1[j]) * g1 * w);
-                        tb[j * 2 * MT + r] = *reinterpret_cast<uint16_t *>(&y0);
-                        tb[j * 2 * MT + MT + r] = *reinterpret_cast<uint16_t *>(&y1);
-                    }
-                    // all four warps have written the tile (the barrier of this buffer's previous
-                    // use also ordered every warp's reads of it before these writes)
-                    __syncwarp();
-                    if (lane == 0) arrive(tp_bar + X);
-                    if (!warp_wait_bar(tp_bar + X, (gc >> 1) & 1, abort_flag)) { dead = true; break; }
-                    const int n0 = m * 2 * MT;  // first y column of the unit's two tiles
+                    for (int tile = 0; tile < 2; ++tile) {
+                        const uint32_t *v = tile ? v1 : v0;
+                        const float gr = tile ? g1 : g0;
+                        __syncwarp();  // the previous block's read-back is done
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int j = 8 * quarter + jj;
-                        const int dst = tbl_slot[cb * 32 + j];
-                        if (dst < 0) continue;  // padding position (uniform across the warp)
-                        const uint4 v = *reinterpret_cast<const uint4 *>(tb + j * 2 * MT + lane * 8);
-                        *reinterpret_cast<uint4 *>(p.y_out + (size_t)dst * p.y_ld + n0 + lane * 8) = v;
+                        for (int j = 0; j < 32; ++j) tb[j * 32 + lane] = __uint_as_float(v[j]) * gr * tbl_w[cb * 32 + j];
+                        __syncwarp();
+                        const int c0 = m * 2 * MT + tile * MT + 32 * quarter + 4 * ql;
+#pragma unroll
+                        for (int jb = 0; jb < 32; jb += 4) {
+                            const int dst = tbl_slot[cb * 32 + jb + jl];
+                            const float4 o = *reinterpret_cast<const float4 *>(tb + (jb + jl) * 32 + 4 * ql);
+                            if (dst >= 0) __stcg(reinterpret_cast<float4 *>(p.y_out + (size_t)dst * p.y_ld + c0), o);
+                        }
                     }
-                    ++gc;
                 }
             }
         }
@@ -616,7 +620,7 @@ bool tc_shape_ok_fp8(int K, int rows_per_expert) { return K % 128 == 0 && K >= 1
 
 bool tc_shape_ok(int K, int group, int rows_per_expert)
 {
-    return K % KC == 0 && K >= KC && rows_per_expert % MT == 0 && (K / group) % 16 == 0 && K / group <= 256;
+    return K % KC == 0 && K >= KC && rows_per_expert % MT == 0 && (K / group) % 8 == 0 && K / group <= 256;
 }
 
 // Deepest TMA ring (NSMAX down to 2 stages) that fits the opt-in shared memory.
@@ -659,6 +663,10 @@ cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int npr
     CUtensorMap cmap[2], bmap[2];
     TcLaunch TL = {};
     TL.nprob = nprob;
+    injected_stall(&TL.wait_ns, &TL.skip_producer);
+    TL.scale_load_bytes = 16;
+    for (int i = 0; i < nprob; ++i)
+        if (!probs[i].fp8 && (probs[i].K / probs[i].group) % 16) TL.scale_load_bytes = 8;
     for (int i = 0; i < nprob; ++i) {
         const TcParams &p = probs[i];
         TL.prob[i] = p;

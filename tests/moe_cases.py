@@ -47,6 +47,24 @@ def oracle_banks(shape_name: str, tp_rank: int = 0, tp_size: int = 1, seed: int 
     return rb, sb
 
 
+def hot_block_sample(ids: np.ndarray, E: int, n: int, seed: int, block: int = 128, n_hot: int = 3):
+    """Sorted token sample of size >= n that puts at least one token in every block of
+    `block` expert-sorted positions of the n_hot most loaded experts (the blocks a
+    tensor-core unit works on), the first and last token, and random others."""
+    T, k = ids.shape
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    chosen = {0, T - 1}
+    for e in np.argsort(-counts, kind="stable")[:n_hot]:
+        slots = np.nonzero(ids.reshape(-1) == e)[0]  # slot order = the sort's order within e
+        for b in range(0, len(slots), block):
+            chosen.add(int(slots[b + (len(slots[b:b + block]) - 1) // 2]) // k)
+    rng = np.random.default_rng(seed)
+    rest = np.setdiff1d(np.arange(T), np.fromiter(chosen, int))
+    extra = max(0, n - len(chosen))
+    chosen.update(rng.choice(rest, size=min(extra, len(rest)), replace=False).tolist())
+    return np.array(sorted(chosen), dtype=np.int32)
+
+
 def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
@@ -94,7 +112,9 @@ class GpuLayer:
         T, H = x_bits.shape
         x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
         out = torch.empty((T, H), dtype=out_dtype, device="cuda")
-        ws = torch.empty(self.ft.ft_moe_workspace_size(self.cfg, T), dtype=torch.uint8, device="cuda")
+        # every byte 0xFF (a NaN in any float view): whatever the kernels read without
+        # having written it first shows up in the output
+        ws = torch.full((self.ft.ft_moe_workspace_size(self.cfg, T),), 0xFF, dtype=torch.uint8, device="cuda")
         self.ft.ft_moe_forward(self.cfg, self.routed, self.shared, x, ids, w, out, ws)
         st = self.ft.ft_moe_read_status(ws)
         if check_status:

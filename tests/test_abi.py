@@ -206,3 +206,10 @@ def test_align_static_rejects_sizes_beyond_its_array(ft):
         assert lib.ft_moe_align_static(dummy, T, k, E, 8, *bufs, None, None) == 3, (T, k, E)
     assert lib.ft_moe_align_static(dummy, -1, 8, 256, 8, *bufs, None, None) == 1
     assert lib.ft_moe_align_static(dummy, 4, 8, 256, 0, *bufs, None, None) == 1
+
+
+def test_inject_stall_rejects_bad_arguments(ft):
+    lib = ft.load()
+    assert lib.ft_moe_debug_inject_stall(0, 2) == 1
+    assert lib.ft_moe_debug_inject_stall(10, 1) == 1           # below 1 ms
+    assert lib.ft_moe_debug_inject_stall(3 * 10 ** 9, 1) == 1  # above the default limit

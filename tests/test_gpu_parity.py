@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from moe_cases import ROUTE_W_RTOL, GpuLayer, assert_close, logits_for, oracle_banks, pieces
+from moe_cases import ROUTE_W_RTOL, GpuLayer, assert_close, hot_block_sample, logits_for, oracle_banks, pieces
 
 pytestmark = pytest.mark.gpu
 
@@ -263,31 +263,58 @@ def test_forward_mini_tensor_core_path(T, tp, zipf):
         assert_close(got, ref, f"mini T={T} tp={tp} rank={r}")
 
 
-@pytest.mark.parametrize("T", [2048, 8192])
-def test_forward_qwen36_prefill_sampled(T):
-    rng = np.random.default_rng(T)
-    sample = np.sort(rng.choice(T, size=24, replace=False))
-    sample[0], sample[-1] = 0, T - 1
+_oracle_cache = {}
+
+
+def _oracle_full(name, T, zipf, tokens):
+    """The oracle's tp = 1 output for these tokens (cached: several tests sum partials
+    against it)."""
+    key = (name, T, zipf, tokens.tobytes())
+    if key not in _oracle_cache:
+        shape = synth.SHAPES[name]
+        ids, w = oracle.route(logits_for(name, T, zipf), shape.top_k)
+        rb, sb = oracle_banks(name)
+        x = synth.make_activations(T, shape.hidden)
+        _oracle_cache.clear()
+        _oracle_cache[key] = oracle.moe_forward(rb, sb, shape.group, x, ids, w, tokens=tokens,
+                                                nthreads=oracle.default_threads())
+    return _oracle_cache[key]
+
+
+def _hot_sample(name, T, n=512):
+    shape = synth.SHAPES[name]
+    ids, _ = oracle.route(logits_for(name, T, True), shape.top_k)
+    return hot_block_sample(ids, shape.num_experts, n, seed=T)
+
+
+def test_forward_qwen36_prefill_every_token():
+    """T = 2048 (tensor-core path, Zipf routing): every token against the oracle."""
+    T = 2048
+    got, ref = _run_and_compare("qwen36", T, True)
+    assert_close(got, ref, f"qwen36 prefill T={T}")
+
+
+def test_forward_qwen36_prefill_hot_blocks():
+    """T = 8192: at least 512 tokens, with one in every 128-position block of the three
+    most loaded experts (each such block is a separate tensor-core unit)."""
+    T = 8192
+    sample = _hot_sample("qwen36", T)
+    assert len(sample) >= 512
     got, ref = _run_and_compare("qwen36", T, True, sample=sample)
     assert_close(got, ref, f"qwen36 prefill T={T}")
 
 
 @pytest.mark.parametrize("tp,T,zipf", [(2, 32, False), (4, 32, False), (2, 2048, True), (4, 2048, True)])
 def test_forward_tp_partials_sum_to_full(tp, T, zipf):
-    """Each rank-local partial matches the oracle's; their host sum matches the tp=1 output."""
-    shape = synth.SHAPES["qwen36"]
-    sample = np.arange(T) if T <= 64 else np.sort(np.random.default_rng(5).choice(T, 16, replace=False))
+    """Each rank-local partial matches the oracle's on every token; their host sum
+    matches the tp=1 output."""
+    sample = np.arange(T, dtype=np.int32)
     total = 0
     for r in range(tp):
         got, ref = _run_and_compare("qwen36", T, zipf, r, tp, sample=sample)
         assert_close(got, ref, f"rank {r}/{tp}")
         total = total + got.astype(np.float64)
-    logits = logits_for("qwen36", T, zipf)
-    ids, w = oracle.route(logits, shape.top_k)
-    rb, sb = oracle_banks("qwen36")
-    x = synth.make_activations(T, shape.hidden)
-    full = oracle.moe_forward(rb, sb, shape.group, x, ids, w, tokens=sample, nthreads=oracle.default_threads())
-    assert_close(total, full, f"sum of {tp} partials vs tp=1")
+    assert_close(total, _oracle_full("qwen36", T, zipf, sample), f"sum of {tp} partials vs tp=1")
 
 
 # Two ranks with unequal shares of the intermediate dimension (routed 320 + 192 of 512,
@@ -330,10 +357,21 @@ def test_forward_dsv4_group32(T, tp):
         assert_close(got, ref, f"dsv4 T={T} tp={tp} rank={r}")
 
 
-def test_forward_dsv4_prefill_sampled():
-    sample = np.array([0, 1, 777, 2048, 4095])
-    got, ref = _run_and_compare("dsv4", 4096, True, sample=sample)
-    assert_close(got, ref, "dsv4 T=4096")
+@pytest.mark.parametrize("tp", [1, 4])
+def test_forward_dsv4_prefill_hot_blocks(tp):
+    """dsv4 T = 4096 (g = 32): at least 512 tokens covering every 128-position block of the
+    three most loaded experts; at tp = 4 every rank against the oracle and the sum of
+    the partials against the tp = 1 output."""
+    T = 4096
+    sample = _hot_sample("dsv4", T)
+    assert len(sample) >= 512
+    total = 0
+    for r in range(tp):
+        got, ref = _run_and_compare("dsv4", T, True, r, tp, sample=sample)
+        assert_close(got, ref, f"dsv4 T={T} tp={tp} rank={r}")
+        total = total + got.astype(np.float64)
+    if tp > 1:
+        assert_close(total, _oracle_full("dsv4", T, True, sample), f"dsv4 sum of {tp} partials vs tp=1")
 
 
 def _scale_rows_bf16(x_bits: np.ndarray, exps) -> np.ndarray:
@@ -420,3 +458,36 @@ def test_forward_in_cuda_graph():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+def test_tensor_core_path_deterministic_and_graph_replay():
+    """T = 2048 runs the tensor-core kernels: two eager runs are bitwise identical, and a
+    CUDA-graph replay of route + forward reproduces the eager output bit for bit."""
+    L = layer("qwen36")
+    T, H = 2048, 2048
+    x_bits = synth.make_activations(T, H, seed=13)
+    logits = torch.from_numpy(logits_for("qwen36", T, True, seed=13)).cuda()
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.empty((T, 8), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, 8), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = torch.full((L.ft.ft_moe_workspace_size(L.cfg, T),), 0xFF, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    runs = []
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            L.ft.ft_moe_route(logits, 8, ids, w)
+            L.ft.ft_moe_forward(L.cfg, L.routed, L.shared, x, ids, w, out, ws)
+            runs.append(out.clone())
+    torch.cuda.synchronize()
+    assert L.ft.ft_moe_read_status(ws) == 0
+    assert torch.equal(runs[0], runs[1])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        L.ft.ft_moe_route(logits, 8, ids, w)
+        L.ft.ft_moe_forward(L.cfg, L.routed, L.shared, x, ids, w, out, ws)
+    out.zero_()
+    ws.fill_(0xFF)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, runs[0])
