@@ -63,11 +63,20 @@ def lib():
             L.orc_expert_gate_up.restype = None
             L.orc_expert_gate_up.argtypes = [ctypes.POINTER(Bank), I, P, P]
             L.orc_swiglu.restype = None; L.orc_swiglu.argtypes = [P, I, P]
+            L.orc_expert_gate_up_f64.restype = None
+            L.orc_expert_gate_up_f64.argtypes = [ctypes.POINTER(Bank), I, P, P]
             L.orc_expert_down.restype = None
             L.orc_expert_down.argtypes = [ctypes.POINTER(Bank), I, P, P]
             L.orc_moe_forward.restype = I
             L.orc_moe_forward.argtypes = [ctypes.POINTER(Bank), ctypes.POINTER(Bank), P, I, P, P, I,
                                           P, I, P, I]
+            L.orc_moe_forward_w4a4.restype = I
+            L.orc_moe_forward_w4a4.argtypes = [ctypes.POINTER(Bank), ctypes.POINTER(Bank), P, I, P, P, I,
+                                               P, I, P, I]
+            L.orc_quant_nvfp4.restype = None
+            L.orc_quant_nvfp4.argtypes = [P, I, I, P, P, P]
+            L.orc_e4m3_code.restype = ctypes.c_uint; L.orc_e4m3_code.argtypes = [ctypes.c_float]
+            L.orc_e2m1_code.restype = ctypes.c_uint; L.orc_e2m1_code.argtypes = [ctypes.c_float]
             _lib = L
         return _lib
 
@@ -93,7 +102,7 @@ MUTATIONS = {
     "nibble_order": 1, "swap_gate_up": 2, "drop_global": 3, "scale_index": 4, "e2m1_sign": 5,
     "no_renorm": 6, "tie_high": 7, "down_rows": 8, "drop_shared": 9, "drop_route_w": 10,
     "e4m3_bias": 11, "up_slice": 12, "router_transposed": 13, "fp8_block_transposed": 14,
-    "dequant_transposed": 15,
+    "dequant_transposed": 15, "w4a4_no_h_quant": 16, "e2m1_tie_up": 17, "row_scale_448": 18,
 }
 
 
@@ -244,6 +253,14 @@ def expert_gate_up(bank: dict, group: int, e: int, x_row: np.ndarray) -> np.ndar
     return G
 
 
+def expert_gate_up_f64(bank: dict, group: int, e: int, x: np.ndarray) -> np.ndarray:
+    """gate_up pre-activations of expert e on fp64 activations (the W4A4 path's dequantized x)."""
+    x = np.ascontiguousarray(x, np.float64)
+    G = np.zeros(bank["gu"].shape[1], np.float64)
+    lib().orc_expert_gate_up_f64(ctypes.byref(_bank(bank, group)), e, _p(x), _p(G))
+    return G
+
+
 def swiglu(G: np.ndarray) -> np.ndarray:
     G = np.ascontiguousarray(G, np.float64)
     Il = G.shape[0] // 2
@@ -259,10 +276,33 @@ def expert_down(bank: dict, group: int, e: int, h: np.ndarray) -> np.ndarray:
     return y
 
 
+def e4m3_code(v: float) -> int:
+    """Nearest e4m3 code of a non-negative value (ties to even, saturating at 448)."""
+    return int(lib().orc_e4m3_code(v))
+
+
+def e2m1_code(v: float) -> int:
+    """Nearest e2m1 code (sign bit 3; ties to even, saturating at 6)."""
+    return int(lib().orc_e2m1_code(v))
+
+
+def quant_nvfp4(x: np.ndarray):
+    """NVFP4 quantization of fp32 rows [rows, K] (K % 16 == 0): (codes u8 [rows, K/2],
+    e4m3 scales u8 [rows, K/16], fp32 row scales [rows])."""
+    x = np.ascontiguousarray(x, np.float32)
+    rows, K = x.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    scales = np.zeros((rows, K // 16), np.uint8)
+    glob = np.zeros(rows, np.float32)
+    lib().orc_quant_nvfp4(_p(x), rows, K, _p(codes), _p(scales), _p(glob))
+    return codes, scales, glob
+
+
 def moe_forward(routed: dict | None, shared: dict | None, group: int, x: np.ndarray,
                 ids: np.ndarray | None = None, w: np.ndarray | None = None,
-                tokens=None, nthreads: int = 1) -> np.ndarray:
-    """Rank-local partial [len(tokens), H] in fp64 (x: bf16 bits [T, H])."""
+                tokens=None, nthreads: int = 1, w4a4: bool = False) -> np.ndarray:
+    """Rank-local partial [len(tokens), H] in fp64 (x: bf16 bits [T, H]); w4a4 = True quantizes
+    the activations (x, then each expert's h) to NVFP4 as the native FP4 variant does."""
     x = np.ascontiguousarray(x, np.uint16)
     T, H = x.shape
     tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, np.int32)
@@ -276,7 +316,8 @@ def moe_forward(routed: dict | None, shared: dict | None, group: int, x: np.ndar
         pids, pw = _p(ids), _p(w)
     else:
         k, pids, pw = 0, None, None
-    rc = lib().orc_moe_forward(ctypes.byref(rb) if rb is not None else None,
+    fwd = lib().orc_moe_forward_w4a4 if w4a4 else lib().orc_moe_forward
+    rc = fwd(ctypes.byref(rb) if rb is not None else None,
                                ctypes.byref(sb) if sb is not None else None,
                                _p(x), H, pids, pw, k, _p(tokens), len(tokens), _p(out), nthreads)
     if rc != 0:

@@ -74,6 +74,9 @@ enum {
     ORC_MUT_ROUTER_T = 13,      /* router weight read transposed (square shapes only) */
     ORC_MUT_FP8_BLOCK_T = 14,   /* fp8_block: scale block indexed [k/128][n/128] */
     ORC_MUT_DEQUANT_T = 15,     /* dense matrices written column-major ([K][rows]) */
+    ORC_MUT_W4A4_NO_H = 16,     /* W4A4: h enters down unquantized */
+    ORC_MUT_E2M1_TIE_UP = 17,   /* e2m1 rounding: ties away from zero */
+    ORC_MUT_ROW_SCALE = 18,     /* activation row scale amax / 6 (448 forgotten) */
 };
 
 /* ---------------------------------------------------------------- formats */
@@ -414,6 +417,103 @@ int orc_slice_fp8_range(int E, int H, int I, int begin, int len,
     return 0;
 }
 
+/* ---------------------------------------------------------------- W4A4: NVFP4 activations
+ *
+ * The native FP4 variant feeds the tensor cores e2m1 activations too (W4A4), which the
+ * pages' sm_86/sm_89 cards could not run ("[TP=2] Quantized MoE expert parallelism ... NVFP4
+ * port", section 2: no native FP4 tensor cores there, so NVFP4 ran as W4A16). The pages do
+ * not define how activations are quantized; the reading taken here is NVFP4's own two-level
+ * scaling applied per activation row: a row scale glob = amax / (6 * 448) in fp32, one e4m3
+ * block scale per 16 elements s = e4m3(block amax / (6 * glob)), codes q = e2m1(x / (s *
+ * glob)), both conversions rounding to nearest with ties to even and saturating; value
+ * q * s * glob. Every step is an fp32 operation in this order, the precision the kernels
+ * take these decisions in. */
+
+/* e4m3 code of a finite v >= 0: the nearest non-negative finite e4m3 value, ties to the
+ * even code, values above 448 saturating to 448 (chosen by scanning all 127 codes). */
+static unsigned e4m3_code_rne(float v)
+{
+    if (!(v > 0.0f)) return 0u;
+    unsigned best = 0;
+    double bd = INFINITY;
+    for (unsigned c = 0; c < 0x7Fu; ++c) {
+        double d = fabs(orc_e4m3(c) - (double)v);
+        if (d < bd || (d == bd && (c & 1u) == 0u)) { bd = d; best = c; }
+    }
+    return best;
+}
+
+/* e2m1 code of a finite v: sign bit 3, magnitude the nearest of {0,.5,1,1.5,2,3,4,6}
+ * (ties to the even code, above 6 saturating to 6). */
+static unsigned e2m1_code_rne(float v)
+{
+    unsigned sign = v < 0.0f ? 8u : 0u;
+    double a = fabs((double)v), bd = INFINITY;
+    unsigned best = 0;
+    for (unsigned c = 0; c < 8u; ++c) {
+        double d = fabs(E2M1_MAG[c] - a);
+        int tie_wins = (orc_mutation == ORC_MUT_E2M1_TIE_UP) ? 1 : (c & 1u) == 0u;
+        if (d < bd || (d == bd && tie_wins)) { bd = d; best = c; }
+    }
+    return sign | best;
+}
+
+unsigned orc_e4m3_code(float v) { return e4m3_code_rne(v); }
+unsigned orc_e2m1_code(float v) { return e2m1_code_rne(v); }
+
+/* NVFP4 quantization of `rows` rows of K fp32 values (K a multiple of 16): codes
+ * [rows][K/2] (element 2m in the low nibble of byte m), e4m3 block scales [rows][K/16],
+ * fp32 row scales [rows]. */
+void orc_quant_nvfp4(const float *x, int rows, int K, uint8_t *codes, uint8_t *scales, float *glob)
+{
+    for (int r = 0; r < rows; ++r) {
+        const float *xr = x + (size_t)r * K;
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) if (fabsf(xr[k]) > amax) amax = fabsf(xr[k]);
+        float g = amax / (orc_mutation == ORC_MUT_ROW_SCALE ? 6.0f : 2688.0f);
+        glob[r] = g;
+        for (int b = 0; b < K / 16; ++b) {
+            float bmax = 0.0f;
+            for (int i = 0; i < 16; ++i) if (fabsf(xr[16 * b + i]) > bmax) bmax = fabsf(xr[16 * b + i]);
+            unsigned sc = 0;
+            if (g > 0.0f) {
+                float six_g = 6.0f * g;
+                sc = e4m3_code_rne(bmax / six_g);
+            }
+            scales[(size_t)r * (K / 16) + b] = (uint8_t)sc;
+            float sv = (float)orc_e4m3(sc);
+            float d = sv * g;
+            for (int i = 0; i < 16; i += 2) {
+                unsigned lo = 0, hi = 0;
+                if (sv > 0.0f) {
+                    float q0 = xr[16 * b + i] / d, q1 = xr[16 * b + i + 1] / d;
+                    lo = e2m1_code_rne(q0);
+                    hi = e2m1_code_rne(q1);
+                }
+                codes[(size_t)r * (K / 2) + 8 * b + i / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+}
+
+/* The values of one quantized row (K elements): out[k] = e2m1 * e4m3 * glob, exact in fp64. */
+static void nvfp4_row_values(const uint8_t *codes, const uint8_t *scales, float glob, int K, double *out)
+{
+    for (int k = 0; k < K; ++k) {
+        unsigned byte = codes[k >> 1];
+        unsigned q = (k & 1) ? (byte >> 4) & 15u : byte & 15u;
+        out[k] = orc_e2m1(q) * orc_e4m3(scales[k / 16]) * (double)glob;
+    }
+}
+
+/* Quantize one fp32 row and return its values in fp64 (scratch: K/2 + K/16 bytes). */
+static void quant_dequant_row(const float *x, int K, uint8_t *scratch, double *out)
+{
+    float g;
+    orc_quant_nvfp4(x, 1, K, scratch, scratch + K / 2, &g);
+    nvfp4_row_values(scratch, scratch + K / 2, g, K, out);
+}
+
 /* ---------------------------------------------------------------- expert MLP */
 
 typedef struct {
@@ -454,6 +554,17 @@ static void expert_gate_up(const orc_bank *b, int e, const uint16_t *x_row, doub
     }
 }
 
+/* The same on fp64 activations (the dequantized NVFP4 activations of the W4A4 variant). */
+static void expert_gate_up_f64(const orc_bank *b, int e, const double *x, double *G)
+{
+    int H = b->H, rows = 2 * b->Il;
+    for (int n = 0; n < rows; ++n) {
+        double acc = 0.0;
+        for (int k = 0; k < H; ++k) acc += x[k] * bank_weight(b, 0, e, n, k);
+        G[n] = acc;
+    }
+}
+
 /* h[i] = silu(G[i]) * G[Il + i], silu(z) = z / (1 + exp(-z)). */
 void orc_swiglu(const double *G, int Il, double *h)
 {
@@ -481,6 +592,12 @@ void orc_expert_gate_up(const orc_bank *b, int e, const uint16_t *x_row, double 
     expert_gate_up(b, e, x_row, G);
 }
 
+void orc_expert_gate_up_f64(const orc_bank *b, int e, const double *x, double *G)
+{
+    fill_tables();
+    expert_gate_up_f64(b, e, x, G);
+}
+
 void orc_expert_down(const orc_bank *b, int e, const double *h, double *y)
 {
     fill_tables();
@@ -496,6 +613,7 @@ typedef struct {
     int n_tokens, k, H, first, last;
     double *out;
     int status;
+    int w4a4;  /* NVFP4 activations: x before gate_up and h (as fp32) before down are quantized */
 } fwd_job;
 
 static void *fwd_worker(void *arg)
@@ -504,33 +622,59 @@ static void *fwd_worker(void *arg)
     int H = j->H;
     int maxI = j->routed ? j->routed->Il : 0;
     if (j->shared && j->shared->Il > maxI) maxI = j->shared->Il;
+    size_t maxK = (size_t)(H > maxI ? H : maxI);
     double *G = (double *)malloc(sizeof(double) * 2 * (size_t)maxI);
     double *h = (double *)malloc(sizeof(double) * (size_t)maxI);
     double *y = (double *)malloc(sizeof(double) * (size_t)H);
-    if ((maxI && (!G || !h)) || !y) { j->status = -1; free(G); free(h); free(y); return NULL; }
+    /* W4A4 scratch: fp32 rows, their quantized values, quantizer output bytes */
+    float *rowf = (float *)malloc(sizeof(float) * maxK);
+    double *xq = (double *)malloc(sizeof(double) * (size_t)H);
+    double *hq = (double *)malloc(sizeof(double) * ((size_t)maxI + 1));
+    uint8_t *qs = (uint8_t *)malloc(maxK / 2 + maxK / 16 + 16);
+    if ((maxI && (!G || !h)) || !y || !rowf || !xq || !hq || !qs) {
+        j->status = -1;
+        free(G); free(h); free(y); free(rowf); free(xq); free(hq); free(qs);
+        return NULL;
+    }
     for (int r = j->first; r < j->last; ++r) {
         int t = j->tokens[r];
         const uint16_t *xt = j->x + (size_t)t * H;
         double *o = j->out + (size_t)r * H;
         for (int n = 0; n < H; ++n) o[n] = 0.0;
-        if (j->routed) {
-            for (int q = 0; q < j->k; ++q) {
-                int e = j->ids[(size_t)t * j->k + q];
-                double wq = (orc_mutation == ORC_MUT_DROP_ROUTE_W) ? 1.0 : j->w[(size_t)t * j->k + q];
-                expert_gate_up(j->routed, e, xt, G);
-                orc_swiglu(G, j->routed->Il, h);
-                expert_down(j->routed, e, h, y);
-                for (int n = 0; n < H; ++n) o[n] += wq * y[n];
-            }
+        if (j->w4a4) {  /* the token's activations as NVFP4 (bf16 values are exact in fp32) */
+            for (int k = 0; k < H; ++k) rowf[k] = (float)orc_bf16_to_double(xt[k]);
+            quant_dequant_row(rowf, H, qs, xq);
         }
-        if (j->shared && orc_mutation != ORC_MUT_DROP_SHARED) {
-            expert_gate_up(j->shared, 0, xt, G);
-            orc_swiglu(G, j->shared->Il, h);
-            expert_down(j->shared, 0, h, y);
-            for (int n = 0; n < H; ++n) o[n] += y[n];
+        /* one expert of `bank` with routing weight wq: gate_up, SwiGLU, (quantized h), down */
+        for (int q = 0; q <= j->k; ++q) {
+            const orc_bank *bank;
+            int e;
+            double wq;
+            if (q < j->k) {
+                if (!j->routed) continue;
+                bank = j->routed;
+                e = j->ids[(size_t)t * j->k + q];
+                wq = (orc_mutation == ORC_MUT_DROP_ROUTE_W) ? 1.0 : j->w[(size_t)t * j->k + q];
+            } else {
+                if (!j->shared || orc_mutation == ORC_MUT_DROP_SHARED) continue;
+                bank = j->shared;
+                e = 0;
+                wq = 1.0;
+            }
+            if (j->w4a4) expert_gate_up_f64(bank, e, xq, G);
+            else expert_gate_up(bank, e, xt, G);
+            orc_swiglu(G, bank->Il, h);
+            if (j->w4a4 && orc_mutation != ORC_MUT_W4A4_NO_H) {  /* h enters down as NVFP4 too, quantized from fp32 */
+                for (int i = 0; i < bank->Il; ++i) rowf[i] = (float)h[i];
+                quant_dequant_row(rowf, bank->Il, qs, hq);
+                expert_down(bank, e, hq, y);
+            } else {
+                expert_down(bank, e, h, y);
+            }
+            for (int n = 0; n < H; ++n) o[n] += wq * y[n];
         }
     }
-    free(G); free(h); free(y);
+    free(G); free(h); free(y); free(rowf); free(xq); free(hq); free(qs);
     return NULL;
 }
 
@@ -539,9 +683,34 @@ static void *fwd_worker(void *arg)
  * with e = ids[t][j], t = tokens[r]; terms added in the order j = 0..k-1, then the
  * shared expert. `routed` or `shared` may be NULL. Tokens are split statically
  * across `nthreads` POSIX threads (each token is independent). Returns 0 or -1. */
+static int moe_forward(const orc_bank *routed, const orc_bank *shared, const uint16_t *x, int H,
+                       const int32_t *ids, const double *w, int k, const int32_t *tokens, int n_tokens,
+                       double *out, int nthreads, int w4a4);
+
 int orc_moe_forward(const orc_bank *routed, const orc_bank *shared, const uint16_t *x, int H,
                     const int32_t *ids, const double *w, int k,
                     const int32_t *tokens, int n_tokens, double *out, int nthreads)
+{
+    return moe_forward(routed, shared, x, H, ids, w, k, tokens, n_tokens, out, nthreads, 0);
+}
+
+/* The W4A4 variant of the same partial: as orc_moe_forward, with the token's activations
+ * quantized to NVFP4 (orc_quant_nvfp4, one row per token over H) before gate_up, and each
+ * expert's h rounded to fp32 and quantized to NVFP4 (one row per expert and token over the
+ * rank's I_l) before down; weights as in the W4A16 layer, sums exact in fp64. Banks must be
+ * NVFP4 with H and I_l multiples of 16. */
+int orc_moe_forward_w4a4(const orc_bank *routed, const orc_bank *shared, const uint16_t *x, int H,
+                         const int32_t *ids, const double *w, int k,
+                         const int32_t *tokens, int n_tokens, double *out, int nthreads)
+{
+    if (H % 16 || (routed && (routed->fmt != 0 || routed->Il % 16)) || (shared && (shared->fmt != 0 || shared->Il % 16)))
+        return -1;
+    return moe_forward(routed, shared, x, H, ids, w, k, tokens, n_tokens, out, nthreads, 1);
+}
+
+static int moe_forward(const orc_bank *routed, const orc_bank *shared, const uint16_t *x, int H,
+                       const int32_t *ids, const double *w, int k, const int32_t *tokens, int n_tokens,
+                       double *out, int nthreads, int w4a4)
 {
     if (n_tokens < 0 || H <= 0 || (routed && (k <= 0 || !ids || !w))) return -1;
     fill_tables();
@@ -554,7 +723,7 @@ int orc_moe_forward(const orc_bank *routed, const orc_bank *shared, const uint16
     for (int i = 0; i < nthreads; ++i) {
         fwd_job *j = &jobs[i];
         j->routed = routed; j->shared = shared; j->x = x; j->ids = ids; j->w = w;
-        j->tokens = tokens; j->n_tokens = n_tokens; j->k = k; j->H = H; j->out = out;
+        j->tokens = tokens; j->n_tokens = n_tokens; j->k = k; j->H = H; j->out = out; j->w4a4 = w4a4;
         j->first = (int)((long long)n_tokens * i / nthreads);
         j->last = (int)((long long)n_tokens * (i + 1) / nthreads);
     }

@@ -480,13 +480,112 @@ def pin_dequant_matrices():
     assert np.array_equal(got, _dense_fp8(codes, sinv))
 
 
+# ------------------------------------------------------------------ W4A4 (NVFP4 activations)
+
+def pin_nvfp4_code_rounding():
+    """e2m1 codes against hand-derived round-to-nearest-even cases (golden), e4m3 codes against
+    torch's float8_e4m3fn conversion at every code and at every midpoint between neighbours."""
+    for v, want in _golden("e2m1_rounding.json")["cases"]:
+        assert oracle.e2m1_code(v) == want, (v, want, oracle.e2m1_code(v))
+    vals = _torch_e4m3(np.arange(0x7F, dtype=np.uint8))
+    probes = list(vals) + [(vals[i] + vals[i + 1]) / 2 for i in range(0x7E)] + [447.0, 449.0, 470.0]
+    ref = torch.tensor(np.minimum(np.array(probes), 448.0), dtype=torch.float32).to(torch.float8_e4m3fn)
+    ref_codes = ref.view(torch.uint8).numpy()
+    for v, want in zip(probes, ref_codes):
+        assert oracle.e4m3_code(float(v)) == int(want), (v, int(want), oracle.e4m3_code(float(v)))
+
+
+def _nvfp4_values(codes, scales, glob):
+    """Test-side decoding of quantized rows (bit-field e2m1, torch e4m3, row scale)."""
+    lut = np.array([_e2m1_bitfield(i) for i in range(16)])
+    return lut[_nibbles(codes)] * np.repeat(_torch_e4m3(scales), 16, axis=-1) * np.asarray(glob, np.float64)[:, None]
+
+
+def pin_nvfp4_exact_rows():
+    """Rows that NVFP4 represents exactly come back unchanged: row max 2688 (row scale 1),
+    each block = e2m1 magnitudes x signs x an e4m3 scale s with one element at 6 s."""
+    rng = np.random.default_rng(51)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    svals = _torch_e4m3(np.arange(0x08, 0x7F, dtype=np.uint8))  # normal scales
+    rows = []
+    for r in range(6):
+        blocks = []
+        for b in range(8):
+            # one block per row has scale 448, so that its 6 x 448 = 2688 makes the row scale 1
+            s = 448.0 if b == r % 8 else float(rng.choice(svals[svals <= 448]))
+            v = rng.choice(mags, 16) * rng.choice([-1, 1], 16) * s
+            v[rng.integers(16)] = 6 * s * rng.choice([-1, 1])
+            blocks.append(v)
+        rows.append(np.concatenate(blocks))
+    x = np.array(rows, np.float32)
+    codes, scales, glob = oracle.quant_nvfp4(x)
+    assert np.all(glob == 1.0)
+    assert np.array_equal(_nvfp4_values(codes, scales, glob), x.astype(np.float64))
+
+
+def pin_nvfp4_nearest_and_bounds():
+    """Random rows: every block scale is the e4m3 value nearest its block max / (6 x row scale),
+    every code the e2m1 value nearest x / (scale x row scale) (a brute-force search over the 15
+    values), and no element moves by more than one e2m1 step of its block."""
+    rng = np.random.default_rng(52)
+    x = (rng.standard_normal((5, 64)) * np.exp(rng.uniform(-8, 8, (5, 1)))).astype(np.float32)
+    x[2, 16:32] = 0.0  # an all-zero block
+    codes, scales, glob = oracle.quant_nvfp4(x)
+    assert np.allclose(glob, np.abs(x).max(1) / 2688.0, rtol=1e-7)
+    svals = _torch_e4m3(np.arange(0x7F, dtype=np.uint8))
+    lut = np.array([_e2m1_bitfield(i) for i in range(16)])
+    xq = _nvfp4_values(codes, scales, glob)
+    for r in range(x.shape[0]):
+        for b in range(4):
+            blk = x[r, 16 * b:16 * b + 16].astype(np.float64)
+            want = np.abs(blk).max() / (6 * float(glob[r]))
+            sv = _torch_e4m3(scales[r, b:b + 1])[0]
+            assert abs(sv - want) <= np.abs(svals - want).min() * (1 + 1e-6) + 1e-30, (r, b)
+            d = sv * float(glob[r])
+            for i in range(16):
+                if d == 0:
+                    assert xq[r, 16 * b + i] == 0
+                    continue
+                err = abs(xq[r, 16 * b + i] / d - blk[i] / d)
+                assert err <= np.abs(lut - blk[i] / d).min() * (1 + 1e-6) + 1e-12, (r, b, i)
+                assert abs(xq[r, 16 * b + i] - blk[i]) <= 2 * d * (1 + 1e-6)
+
+
+def pin_w4a4_forward_composition():
+    """The W4A4 forward is the W4A16 chain with NVFP4 activations: quantized x into gate_up,
+    SwiGLU, h rounded to fp32 and quantized into down, weighted sum then the shared expert --
+    composed here from the separately pinned pieces (quantizer, gate_up, SwiGLU, down)."""
+    shape = synth.SHAPES["mini"]
+    pieces, sp = _tiny_layer(seed=53, shared=True, shape=shape)
+    rb, sb = oracle.slice_bank(pieces, 16), oracle.slice_bank(sp, 16)
+    T = 3
+    x = synth.make_activations(T, shape.hidden, seed=53)
+    ids, w = oracle.route(synth.make_logits(T, shape.num_experts, seed=53), shape.top_k)
+    got = oracle.moe_forward(rb, sb, 16, x, ids, w, w4a4=True)
+    xf = _bf16_to_f64(x).astype(np.float32)
+    c, s_, g = oracle.quant_nvfp4(xf)
+    xq = _nvfp4_values(c, s_, g)
+    for t in range(T):
+        ref = np.zeros(shape.hidden)
+        for bank, e, wt in [(rb, int(ids[t, j]), w[t, j]) for j in range(shape.top_k)] + [(sb, 0, 1.0)]:
+            h = oracle.swiglu(oracle.expert_gate_up_f64(bank, 16, e, xq[t])).astype(np.float32)
+            hc, hs, hg = oracle.quant_nvfp4(h[None, :])
+            ref += wt * oracle.expert_down(bank, 16, e, _nvfp4_values(hc, hs, hg)[0])
+        assert np.allclose(got[t], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), t
+    # and it stays within quantization noise of the W4A16 output (a few percent)
+    full = oracle.moe_forward(rb, sb, 16, x, ids, w)
+    rel = np.linalg.norm(got - full) / np.linalg.norm(full)
+    assert 1e-3 < rel < 0.2, rel
+
+
 PINS = [pin_e2m1, pin_e4m3, pin_dequant_bf16, pin_route_worked_example, pin_route_brute_force,
         pin_route_library, pin_route_ties_and_shift, pin_align, pin_slice_identity_and_tiling,
         pin_one_hot_columns, pin_linear_parts_exact, pin_dense_mlp_special_case,
         pin_routed_combination, pin_untouched_experts_and_tokens, pin_tp_partial_sum,
         pin_router_logits_exact, pin_router_one_hot, pin_asymmetric_partition,
         pin_fp8_slice_identity_and_tiling, pin_fp8_one_hot_columns, pin_fp8_dense_mlp_and_partials,
-        pin_dequant_matrices]
+        pin_dequant_matrices, pin_nvfp4_code_rounding, pin_nvfp4_exact_rows, pin_nvfp4_nearest_and_bounds,
+        pin_w4a4_forward_composition]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
