@@ -267,6 +267,52 @@ def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
             "expert_tokens_max_over_mean": float(counts.max() / counts.mean())}
 
 
+def measure_w4a4(ft, dev, cfg, rb, sb, shape, T, reps=5):
+    """The W4A4 variant (NVFP4 activations, block-scaled FP4 tensor cores) on one prefill layer,
+    Zipf routing, L2 flushed before every repetition; TFLOP/s against the FP4 dense peak taken
+    as the measured bf16 peak times the nominal FP4 / bf16 ratio (13.5 / 2.25)."""
+    import torch
+    H, E, k = shape.hidden, shape.num_experts, shape.top_k
+    x = torch.from_numpy(synth.make_activations(T, H, seed=7).view(np.int16)).to(dev).view(torch.bfloat16)
+    lg = torch.from_numpy(synth.zipf_logits(T, E, seed=7)).to(dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(ft.ft_moe_workspace_size_w4a4(cfg, T), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    n_ev = ft.FT_NSTAGES + 1
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream(dev)
+    for e_ in ev:
+        e_.record(stream)
+    times, stages = [], []
+    for r in range(reps + 2):
+        flush.fill_(r & 0xFF)
+        start.record(stream)
+        ft.ft_moe_route(lg, k, ids, w)
+        ft.ft_moe_set_stage_events(ev)
+        ft.ft_moe_forward_w4a4(cfg, rb, sb, x, ids, w, out, ws)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if r >= 2:
+            times.append(start.elapsed_time(stop))
+            stages.append([ev[i].elapsed_time(ev[i + 1]) for i in range(ft.FT_NSTAGES)])
+    assert ft.ft_moe_read_status(ws) == 0
+    ms = float(np.median(times))
+    flops = 6.0 * H * (k * shape.intermediate + shape.shared_intermediate) * T
+    _, tfl, kind = _peaks()
+    fp4_peak = tfl * 13.5 / 2.25
+    st = np.median(np.array(stages), axis=0)
+    del ws, flush
+    return {"T": T, "routing": "zipf(1.1)", "us": ms * 1e3, "tokens_per_s": T / (ms / 1e3),
+            "tflops": flops / (ms / 1e3) / 1e12, "fp4_peak_tflops": fp4_peak,
+            "frac_of_fp4_peak": flops / (ms / 1e3) / 1e12 / fp4_peak,
+            "peak_source": f"{kind} bf16 dense x 13.5 / 2.25 (nominal FP4 / bf16)",
+            "stage_us": {n: float(v * 1e3) for n, v in zip(ft.STAGES, st)},
+            "kernel": "tcgen05 kind::mxf4nvf4 (e2m1 x e2m1, ue4m3 block scales), NVFP4 activations"}
+
+
 def measure_router(ft, dev, T, E=256, H=2048, reps=6):
     """ft_moe_route_gemm (router logit GEMM + top-8) for one layer's router, L2 flushed."""
     import torch
@@ -565,6 +611,10 @@ def run_ours(args, world, rank, local):
     if not args.no_prefill:
         prefill = [measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, int(T_))
                    for T_ in args.prefill_T.split(",")]
+    w4a4 = None
+    if not args.no_w4a4:
+        w4a4 = [measure_w4a4(ft, dev, cfg, layers[0][0], layers[0][1], shape, int(T_))
+                for T_ in args.prefill_T.split(",")]
     router = [measure_router(ft, dev, T_, E=E, H=H) for T_ in (T, 2048)]
     fp8 = None if args.no_fp8 else measure_fp8(ft, dev)
     configs = None
@@ -706,7 +756,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline, "layer": {"us": layer_us, "touched_experts_mean": float(np.mean(touched)),
                                         "weight_bytes_mean": float(np.mean(layer_bytes)), "gbs": layer_gbs,
                                         "frac_of_hbm": layer_gbs / hbm},
-        "stage_us": stage_mean_us, "prefill": prefill, "configs": configs, "router_gemm": router,
+        "stage_us": stage_mean_us, "prefill": prefill, "w4a4": w4a4, "configs": configs, "router_gemm": router,
         "fp8_block": fp8, "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk.summary(),
@@ -731,6 +781,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other configurations (decode T=1/8/32, tp slices, the DeepSeek-V4-like layer)")
     ap.add_argument("--no-dsv4", action="store_true", help="skip the DeepSeek-V4-like layer among the configurations")
+    ap.add_argument("--no-w4a4", action="store_true", help="skip the W4A4 (NVFP4 activations) prefill measurement")
     ap.add_argument("--shape", choices=["qwen36", "dsv4"], default="qwen36",
                     help="NVFP4 layer family of the decode and prefill measurements")
     ap.add_argument("--prefill-T", default="2048,8192", help="comma-separated prefill token counts")

@@ -237,6 +237,40 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
                          void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* ---- W4A4: the native block-scaled FP4 variant ------------------------------ */
+
+/* The same rank-local partial with the activations in NVFP4 as well (W4A4): the path the
+ * pages' sm_86/sm_89 cards could not take ("[TP=2] Quantized MoE expert parallelism ...
+ * NVFP4 port", section 2: without FP4 tensor cores NVFP4 ran there as W4A16). Each token's
+ * x (per expert-sorted position) and each expert's h (fp32, per position) are quantized with
+ * ft_moe_quantize_nvfp4's rule, and both GEMMs run on tcgen05 kind::mxf4nvf4 with the e4m3
+ * block scales of weights and activations as the MMA's scale factors; row globals and the
+ * activations' row scales multiply the fp32 sums. The quantization changes the numbers: the
+ * result equals the W4A16 forward only up to activation quantization error. Banks are the
+ * NVFP4 banks of ft_moe_pack (group 16 or 32). Needs hidden and the rank's intermediate
+ * sizes (routed and shared) to be multiples of 256, else FT_ERR_UNSUPPORTED. At tp_size > 1
+ * each rank quantizes its own h slice, so the sum of partials matches the tp = 1 output only
+ * up to that quantization. Arguments, errors and the status word as ft_moe_forward; the
+ * workspace size comes from ft_moe_workspace_size_w4a4. */
+ft_status ft_moe_workspace_size_w4a4(const ft_moe_config *cfg, int32_t T, size_t *bytes);
+ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *routed, const ft_moe_banks *shared,
+                              const void *x, int32_t T, const int32_t *topk_ids, const float *topk_w,
+                              void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* NVFP4 quantization of `rows` activation rows of K elements (K a multiple of 16), the rule
+ * of the W4A4 path (the pages name the format but give no activation recipe; this is NVFP4's
+ * own two-level scaling applied per row): row scale glob = amax / (6 * 448); per 16 elements
+ * the e4m3 scale s = e4m3(block max / (6 * glob)); codes q = e2m1(x / (s * glob)); every
+ * step one correctly rounded fp32 operation, both conversions to nearest with ties to even,
+ * saturating. Value of an element: e2m1(q) * e4m3(s) * glob.
+ *   src     device rows, bf16 or fp32 (src_dtype FT_DTYPE_BF16 / FT_DTYPE_F32), [rows, K]
+ *   codes   device u8 [rows, K/2] (out), element 2m in the low nibble; 8-byte aligned
+ *   scales  device u8 [rows, K/16] (out, e4m3); glob device f32 [rows] (out)
+ * Errors: FT_ERR_INVALID_ARG, FT_ERR_CUDA. */
+ft_status ft_moe_quantize_nvfp4(const void *src, int32_t src_dtype, int32_t rows, int32_t K, uint8_t *codes,
+                                uint8_t *scales, float *glob, void *stream);
+
 /* ---- test and debug exports ------------------------------------------------ */
 
 /* Expert-sorted, tile-padded slot order (the moe_align step named in "feat(qwen3_5_moe):

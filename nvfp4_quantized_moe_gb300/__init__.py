@@ -19,7 +19,8 @@ __all__ = [
     "ft_moe_dequant", "ft_moe_read_status", "ft_last_error", "alloc_banks", "EXPORTS",
     "FT_GU", "FT_GU_SCALE", "FT_GU_GLOBAL", "FT_DN", "FT_DN_SCALE", "FT_DN_GLOBAL",
     "FT_DTYPE_BF16", "FT_DTYPE_F32", "STATUS", "ft_moe_set_stage_events", "ft_moe_launch_count",
-    "FT_NSTAGES", "STAGES", "ft_moe_debug_inject_stall",
+    "FT_NSTAGES", "STAGES", "ft_moe_debug_inject_stall", "ft_moe_workspace_size_w4a4", "ft_moe_forward_w4a4",
+    "ft_moe_quantize_nvfp4",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libftmoe.so")
@@ -35,7 +36,7 @@ BANK_NAMES = ("gate_up", "gate_up_scale", "gate_up_global", "down", "down_scale"
 EXPORTS = ("ft_moe_layout", "ft_moe_pack", "ft_moe_route", "ft_moe_route_gemm", "ft_moe_workspace_size",
            "ft_moe_forward", "ft_moe_align_workspace_size", "ft_moe_align", "ft_moe_dequant", "ft_moe_read_status",
            "ft_last_error", "ft_moe_set_stage_events", "ft_moe_launch_count", "ft_moe_align_static",
-           "ft_moe_debug_inject_stall")
+           "ft_moe_debug_inject_stall", "ft_moe_workspace_size_w4a4", "ft_moe_forward_w4a4", "ft_moe_quantize_nvfp4")
 FT_NSTAGES = 6
 STAGES = ("align", "gate_up", "shared_gate_up", "down", "shared_down", "combine")
 
@@ -101,6 +102,9 @@ def load():
             "ft_moe_read_status": [P, P],
             "ft_moe_set_stage_events": [P],
             "ft_moe_debug_inject_stall": [ctypes.c_uint64, I32],
+            "ft_moe_workspace_size_w4a4": [P, I32, P],
+            "ft_moe_forward_w4a4": [P, P, P, P, I32, P, P, P, I32, P, SZ, P],
+            "ft_moe_quantize_nvfp4": [P, I32, I32, I32, P, P, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -211,6 +215,32 @@ def ft_moe_forward(cfg: MoEConfig, routed, shared, x: torch.Tensor, topk_ids: to
                                  _ptr(x), x.shape[0], _ptr(topk_ids), _ptr(topk_w), _ptr(out), out_dtype,
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream, x)))
+
+
+def ft_moe_workspace_size_w4a4(cfg: MoEConfig, T: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().ft_moe_workspace_size_w4a4(ctypes.byref(cfg), T, ctypes.byref(n)))
+    return n.value
+
+
+def ft_moe_forward_w4a4(cfg: MoEConfig, routed, shared, x: torch.Tensor, topk_ids: torch.Tensor,
+                        topk_w: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """Rank-local partial with NVFP4 activations (W4A4) into `out` (bf16 or fp32 [T, H])."""
+    out_dtype = {torch.bfloat16: FT_DTYPE_BF16, torch.float32: FT_DTYPE_F32}[out.dtype]
+    rb, sb = _banks(routed), _banks(shared)
+    _check(load().ft_moe_forward_w4a4(ctypes.byref(cfg), ctypes.byref(rb),
+                                      ctypes.byref(sb) if sb is not None else None, _ptr(x), x.shape[0],
+                                      _ptr(topk_ids), _ptr(topk_w), _ptr(out), out_dtype, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream, x)))
+
+
+def ft_moe_quantize_nvfp4(src: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, glob: torch.Tensor,
+                          stream=None):
+    """NVFP4 codes [rows, K/2], e4m3 scales [rows, K/16] and row scales [rows] of bf16 or fp32 rows."""
+    dt = {torch.bfloat16: FT_DTYPE_BF16, torch.float32: FT_DTYPE_F32}[src.dtype]
+    rows, K = src.shape
+    _check(load().ft_moe_quantize_nvfp4(_ptr(src), dt, rows, K, _ptr(codes), _ptr(scales), _ptr(glob),
+                                        _stream(stream, src)))
 
 
 def ft_moe_align_workspace_size(T: int, k: int, E: int) -> int:

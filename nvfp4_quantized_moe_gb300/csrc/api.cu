@@ -82,6 +82,9 @@ int sm_count()
 
 static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Slot counts (T * top_k) up to this many run the decode regime as one fused launch.
+constexpr int kFusedMaxSlots = 64;
+
 static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // ---------------------------------------------------------------- geometry
@@ -242,6 +245,66 @@ static WsLayout ws_layout(const Geometry &G, int T)
     L.total = o;
     L.pmax = (int)pmax;
     return L;
+}
+
+// Workspace regions of ft_moe_forward_w4a4 (NVFP4 activations), each 256-byte aligned; the
+// first regions (status word and counters, align outputs) are laid out as in ws_layout.
+struct WsW4 {
+    size_t status, split_cnt, sorted, block_expert, expert_off, npad, scratch, y, y_sh, zero_bytes;
+    size_t xq_c, xq_s, xq_g, xs_c, xs_s, xs_g, h, hs, hq_c, hq_s, hq_g, hsq_c, hsq_s, hsq_g, total;
+    int pmax, tpad;
+};
+
+static WsW4 ws_layout_w4a4(const Geometry &G, int T)
+{
+    WsW4 L;
+    const int64_t n = (int64_t)T * G.k;
+    const int64_t pmax = n + (int64_t)(n < G.E ? n : G.E) * (kTcBlock - 1);
+    const int64_t tpad = (T + kTcBlock - 1) / kTcBlock * kTcBlock;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = round_up(o + bytes, 256); return at; };
+    L.status = take(256);
+    L.split_cnt = take(sizeof(int) * 2 * (size_t)kMaxSplitSlots);
+    L.zero_bytes = o;
+    L.sorted = take(sizeof(int) * (size_t)pmax);
+    L.block_expert = take(sizeof(int) * (size_t)(pmax / kGemvBlock + 1));
+    L.expert_off = take(sizeof(int) * (size_t)(G.E + 1));
+    L.npad = take(sizeof(int));
+    L.scratch = take(align_scratch_bytes((int)n, G.E));
+    L.y = take(4 * (size_t)n * G.H);
+    L.y_sh = take(G.Is ? 4 * (size_t)T * G.H : 0);
+    const size_t sh = G.Is ? 1 : 0;
+    L.xq_c = take((size_t)pmax * G.H / 2);
+    L.xq_s = take((size_t)pmax * G.H / 16);
+    L.xq_g = take(4 * (size_t)pmax);
+    L.xs_c = take(sh * (size_t)tpad * G.H / 2);
+    L.xs_s = take(sh * (size_t)tpad * G.H / 16);
+    L.xs_g = take(sh * 4 * (size_t)tpad);
+    L.h = take(4 * (size_t)pmax * G.Il);
+    L.hs = take(sh * 4 * (size_t)tpad * G.Isl);
+    L.hq_c = take((size_t)pmax * G.Il / 2);
+    L.hq_s = take((size_t)pmax * G.Il / 16);
+    L.hq_g = take(4 * (size_t)pmax);
+    L.hsq_c = take(sh * (size_t)tpad * G.Isl / 2);
+    L.hsq_s = take(sh * (size_t)tpad * G.Isl / 16);
+    L.hsq_g = take(sh * 4 * (size_t)tpad);
+    L.total = o;
+    L.pmax = (int)pmax;
+    L.tpad = (int)tpad;
+    return L;
+}
+
+// Shapes the W4A4 kernels cover: NVFP4 banks, group 16 or 32, every K a whole number of
+// 256-element stages and every row count a whole number of 128-row tiles (down: 256).
+static ft_status check_w4a4(const Geometry &G)
+{
+    if (G.fmt != FT_FORMAT_NVFP4) return fail(FT_ERR_UNSUPPORTED, "W4A4 needs NVFP4 weight banks");
+    if (G.H % 256 || !w4a4_shape_ok(G.H, G.Il) || !w4a4_shape_ok(G.Il, G.H) ||
+        (G.Is && (!w4a4_shape_ok(G.H, G.Isl) || !w4a4_shape_ok(G.Isl, G.H))))
+        return fail(FT_ERR_UNSUPPORTED,
+                    "W4A4 needs hidden and the rank's intermediate sizes to be multiples of 256 (got H %d, I_l %d, I_sl %d)",
+                    G.H, G.Il, G.Isl);
+    return FT_OK;
 }
 
 // K-split for a merged lean launch: the smallest of 1, 2, 4, 8 that gives at least two
@@ -761,8 +824,8 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         return stage_mark(FT_NSTAGES, s);
     };
 
-    // Lean register-fed kernels, fused: gate_up (+ shared expert), down (+ shared expert) and
-    // the ordered combine in one persistent launch.
+    // Lean register-fed kernels: gate_up (+ shared expert), down (+ shared expert) and the
+    // ordered combine, fused into one persistent launch for small batches.
     const int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H);
     int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
     if (ks_dn > 4) ks_dn = 4;
@@ -807,10 +870,22 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         const int gu_units = max_blocks * F.prob[0].n_tiles + (G.Is ? tpad * F.prob[1].n_tiles : 0);
         const int dn_units = (max_blocks + (G.Is ? tpad : 0)) * D.prob[0].n_tiles;
         if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
-        if ((e = launch_gemv_fused(FL, ks_gu, ks_dn, gu_units > dn_units ? gu_units : dn_units, s)) != cudaSuccess)
-            return cuda_fail(e, "fused decode launch");
-        for (int st_ = FT_STAGE_SHARED_GATE_UP; st_ <= FT_NSTAGES; ++st_)
-            if ((e = stage_mark(st_, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if (n_slots <= kFusedMaxSlots) {
+            // small batches: one launch, the stages meeting through per-block counters
+            if ((e = launch_gemv_fused(FL, ks_gu, ks_dn, gu_units > dn_units ? gu_units : dn_units, s)) !=
+                cudaSuccess)
+                return cuda_fail(e, "fused decode launch");
+            for (int st_ = FT_STAGE_SHARED_GATE_UP; st_ <= FT_NSTAGES; ++st_)
+                if ((e = stage_mark(st_, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+            return ok();
+        }
+        // larger batches: gate_up and down as their own launches (the kernel boundary costs
+        // less than the cross-CTA waits), then the ordered combine
+        if ((e = launch_gemv_fast(F, true, ks_gu, gu_units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
+        if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+        if ((e = launch_gemv_fast(D, false, ks_dn, dn_units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
+        if ((e = combine()) != cudaSuccess) return cuda_fail(e, "combine launch");
         return ok();
     }
 
@@ -828,6 +903,148 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
     e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    return ok();
+}
+
+ft_status ft_moe_workspace_size_w4a4(const ft_moe_config *cfg, int32_t T, size_t *bytes)
+{
+    Geometry G;
+    ft_status st = check_config(cfg, G);
+    if (st) return st;
+    if ((st = check_w4a4(G))) return st;
+    if (!bytes) return fail(FT_ERR_INVALID_ARG, "bytes is NULL");
+    if (T < 0 || T > (1 << 20)) return fail(FT_ERR_UNSUPPORTED, "T must be in [0, 2^20]");
+    *bytes = ws_layout_w4a4(G, T).total;
+    return ok();
+}
+
+ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *routed, const ft_moe_banks *shared,
+                              const void *x, int32_t T, const int32_t *topk_ids, const float *topk_w, void *out,
+                              int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Geometry G;
+    ft_status st = check_config(cfg, G);
+    if (st) return st;
+    if ((st = check_w4a4(G))) return st;
+    if (T < 0 || T > (1 << 20)) return fail(FT_ERR_UNSUPPORTED, "T must be in [0, 2^20]");
+    if (out_dtype != FT_DTYPE_BF16 && out_dtype != FT_DTYPE_F32)
+        return fail(FT_ERR_INVALID_ARG, "out_dtype must be FT_DTYPE_BF16 or FT_DTYPE_F32");
+    if (!banks_ok(routed)) return fail(FT_ERR_INVALID_ARG, "routed banks must be non-NULL and 16-byte aligned");
+    if (G.Is > 0 && !banks_ok(shared))
+        return fail(FT_ERR_INVALID_ARG, "shared banks required (shared_intermediate > 0), 16-byte aligned");
+    if (G.Is == 0 && shared) return fail(FT_ERR_INVALID_ARG, "shared banks given but shared_intermediate is 0");
+    if (T == 0) return ok();
+    if (!x || !topk_ids || !topk_w || !out || !workspace)
+        return fail(FT_ERR_INVALID_ARG, "x, topk_ids, topk_w, out and workspace must be non-NULL");
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return fail(FT_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+    if (!aligned(workspace, 256)) return fail(FT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const WsW4 L = ws_layout_w4a4(G, T);
+    if (workspace_bytes < L.total) return fail(FT_ERR_WORKSPACE, "workspace needs %zu bytes", L.total);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    auto at_i = [&](size_t off) { return reinterpret_cast<int *>(ws + off); };
+    auto at_u8 = [&](size_t off) { return reinterpret_cast<uint8_t *>(ws + off); };
+    auto at_f = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+    int *status = at_i(L.status), *sorted = at_i(L.sorted), *bexp = at_i(L.block_expert), *npad = at_i(L.npad);
+    const int n_slots = T * G.k, tpad = L.tpad;
+    struct Disarm {
+        ~Disarm()
+        {
+            g_stage_armed = false;
+            g_stall_armed = g_stall_active = false;
+        }
+    } disarm_on_return;
+    g_stall_active = g_stall_armed;
+    cudaError_t e;
+    if ((e = stage_mark(FT_STAGE_ALIGN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    e = launch_align(topk_ids, T, G.k, G.E, kTcBlock, sorted, bexp, at_i(L.expert_off), npad, status,
+                     ws + L.scratch, s, status, L.zero_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "align launch");
+    if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    // NVFP4 activations: x per expert-sorted position (routed) and per token (shared)
+    e = launch_quant_nvfp4(x, false, G.H, sorted, npad, 0, n_slots, G.k, L.pmax, at_u8(L.xq_c), at_u8(L.xq_s),
+                           at_f(L.xq_g), s);
+    if (e == cudaSuccess && G.Is)
+        e = launch_quant_nvfp4(x, false, G.H, nullptr, nullptr, tpad, T, 1, tpad, at_u8(L.xs_c), at_u8(L.xs_s),
+                               at_f(L.xs_g), s);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    auto problem = [&](const ft_moe_banks *b, bool gate_up, bool is_shared) {
+        W4Params q = {};
+        const int il = is_shared ? G.Isl : G.Il;
+        q.w_scales = static_cast<const uint8_t *>(b->p[gate_up ? FT_GU_SCALE : FT_DN_SCALE]);
+        q.w_glob = static_cast<const float *>(b->p[gate_up ? FT_GU_GLOBAL : FT_DN_GLOBAL]);
+        q.R = gate_up ? 2 * il : G.H;
+        q.K = gate_up ? G.H : il;
+        q.group = G.g;
+        q.up_off = gate_up ? il : 0;
+        q.n_mtiles = gate_up ? il / 128 : G.H / 256;
+        if (is_shared) {
+            q.n_pos_static = T; q.n_slots = T; q.top_k = 1;
+        } else {
+            q.n_pos_dev = npad; q.sorted_slot = sorted; q.block_expert = bexp; q.n_slots = n_slots; q.top_k = G.k;
+        }
+        q.status = status;
+        return q;
+    };
+    W4Params gp[2] = {problem(routed, true, false), {}};
+    gp[0].a_scales = at_u8(L.xq_s); gp[0].a_glob = at_f(L.xq_g); gp[0].h_out = at_f(L.h); gp[0].h_ld = G.Il;
+    W4Operands gops[2] = {{routed->p[FT_GU], (int64_t)G.E * 2 * G.Il, at_u8(L.xq_c), L.pmax}, {}};
+    const int max_blocks = L.pmax / kTcBlock, tblocks = tpad / kTcBlock;
+    int nprob = 1, units = max_blocks * gp[0].n_mtiles;
+    if (G.Is) {
+        gp[1] = problem(shared, true, true);
+        gp[1].a_scales = at_u8(L.xs_s); gp[1].a_glob = at_f(L.xs_g); gp[1].h_out = at_f(L.hs); gp[1].h_ld = G.Isl;
+        gops[1] = {shared->p[FT_GU], 2 * (int64_t)G.Isl, at_u8(L.xs_c), tpad};
+        nprob = 2;
+        units += tblocks * gp[1].n_mtiles;
+    }
+    if ((e = launch_w4a4_gemm(gp, gops, nprob, true, units, s)) != cudaSuccess) return cuda_fail(e, "gate_up launch");
+    if ((e = stage_mark(FT_STAGE_SHARED_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    // h (fp32, position rows) as NVFP4
+    e = launch_quant_nvfp4(at_f(L.h), true, G.Il, nullptr, npad, 0, L.pmax, 1, L.pmax, at_u8(L.hq_c), at_u8(L.hq_s),
+                           at_f(L.hq_g), s);
+    if (e == cudaSuccess && G.Is)
+        e = launch_quant_nvfp4(at_f(L.hs), true, G.Isl, nullptr, nullptr, tpad, tpad, 1, tpad, at_u8(L.hsq_c),
+                               at_u8(L.hsq_s), at_f(L.hsq_g), s);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    float *y = at_f(L.y), *y_sh = at_f(L.y_sh);
+    W4Params dp[2] = {problem(routed, false, false), {}};
+    dp[0].a_scales = at_u8(L.hq_s); dp[0].a_glob = at_f(L.hq_g); dp[0].y_out = y; dp[0].y_ld = G.H;
+    dp[0].route_w = topk_w;
+    W4Operands dops[2] = {{routed->p[FT_DN], (int64_t)G.E * G.H, at_u8(L.hq_c), L.pmax}, {}};
+    nprob = 1;
+    units = max_blocks * dp[0].n_mtiles;
+    if (G.Is) {
+        dp[1] = problem(shared, false, true);
+        dp[1].a_scales = at_u8(L.hsq_s); dp[1].a_glob = at_f(L.hsq_g); dp[1].y_out = y_sh; dp[1].y_ld = G.H;
+        dops[1] = {shared->p[FT_DN], G.H, at_u8(L.hsq_c), tpad};
+        nprob = 2;
+        units += tblocks * dp[1].n_mtiles;
+    }
+    if ((e = launch_w4a4_gemm(dp, dops, nprob, false, units, s)) != cudaSuccess) return cuda_fail(e, "down launch");
+    if ((e = stage_mark(FT_STAGE_SHARED_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    if ((e = stage_mark(FT_STAGE_COMBINE, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    e = launch_combine(y, G.Is ? y_sh : nullptr, T, G.k, G.H, out, out_dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    if ((e = stage_mark(FT_NSTAGES, s)) != cudaSuccess) return cuda_fail(e, "stage event");
+    return ok();
+}
+
+ft_status ft_moe_quantize_nvfp4(const void *src, int32_t src_dtype, int32_t rows, int32_t K, uint8_t *codes,
+                                uint8_t *scales, float *glob, void *stream)
+{
+    if (src_dtype != FT_DTYPE_BF16 && src_dtype != FT_DTYPE_F32)
+        return fail(FT_ERR_INVALID_ARG, "src_dtype must be FT_DTYPE_BF16 or FT_DTYPE_F32");
+    if (rows < 0 || K <= 0 || K % 16) return fail(FT_ERR_INVALID_ARG, "need rows >= 0 and K a positive multiple of 16");
+    if (rows == 0) return ok();
+    if (!src || !codes || !scales || !glob || !aligned(codes, 8) || !aligned(src, 4) || !aligned(glob, 4))
+        return fail(FT_ERR_INVALID_ARG, "pointers must be non-NULL; codes 8-byte aligned");
+    cudaError_t e = launch_quant_nvfp4(src, src_dtype == FT_DTYPE_F32, K, nullptr, nullptr, rows, rows, 1, rows, codes,
+                                       scales, glob, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     return ok();
 }
 

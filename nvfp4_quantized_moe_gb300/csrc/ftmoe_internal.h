@@ -106,6 +106,48 @@ cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int npr
 cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
                                int n_pos_static, int n_slots, int top_k, int max_rows, uint16_t *out, float *scale,
                                cudaStream_t s);
+// One W4A4 (native FP4) grouped GEMM problem: NVFP4 weight banks against NVFP4-quantized
+// activation rows (codes, e4m3 scales per 16 elements, fp32 row scale per position).
+struct W4Params {
+    const uint8_t *w_scales;  // [E][R][K/group] e4m3
+    const float *w_glob;      // [E][R]
+    const uint8_t *a_scales;  // [positions][K/16] e4m3
+    const float *a_glob;      // [positions]
+    int R, K, group, up_off, n_mtiles;
+    const int *n_pos_dev;     // routed: device count of padded positions
+    int n_pos_static;         // shared: number of tokens
+    const int *sorted_slot;   // routed: position -> slot
+    const int *block_expert;  // routed: block -> expert
+    int n_slots, top_k;
+    float *h_out;             // gate_up: fp32 [positions][h_ld]
+    int h_ld;
+    float *y_out;             // down: fp32 [slots][y_ld]
+    int y_ld;
+    const float *route_w;     // down, routed: [T*k]
+    int *status;
+};
+struct W4Launch {
+    W4Params prob[2];
+    int nprob;
+    uint64_t wait_ns;
+    int skip_producer;
+};
+struct W4Operands {
+    const void *codes;        // the bank's packed weight codes
+    int64_t rows_total;
+    const void *act_codes;    // quantized activation codes, [act_rows][K/2]
+    int64_t act_rows;
+};
+bool w4a4_shape_ok(int K, int rows_per_expert);
+cudaError_t launch_w4a4_gemm(const W4Params *probs, const W4Operands *ops, int nprob, bool gated, int max_units,
+                             cudaStream_t s);
+// NVFP4 quantization of position rows (the token of sorted_slot[pos], or pos itself; bf16 or
+// fp32 source rows of K elements, K a multiple of 16): codes [pos][K/2], e4m3 scales
+// [pos][K/16], fp32 row scales [pos]; padding positions get zeros.
+cudaError_t launch_quant_nvfp4(const void *src, bool f32_src, int K, const int *sorted_slot, const int *n_pos_dev,
+                               int n_pos_static, int n_slots, int top_k, int max_rows, uint8_t *codes,
+                               uint8_t *scales, float *glob, cudaStream_t s);
+
 // 2D tiled tensor map (rows of `row_bytes` bytes, `inner` elements used per row) through
 // the driver's cuTensorMapEncodeTiled; false when the driver refuses the shape.
 bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,

@@ -110,8 +110,10 @@ struct FastShared {
     int tbl_dst[kGemvBlock];     // down runs: y row of each block position (or -1)
     float tbl_w[kGemvBlock];     // down runs: its factor
     float s_glob[kThreads * 4];  // down runs: each thread's row globals of its current unit
-    float red[8][32][8];         // in-CTA K split: the warps' partial sums
 };
+
+// The warps' partial sums of an in-CTA K split (declared only by kernels that split K).
+typedef float RedBuf[32][8];
 
 __device__ __forceinline__ int ld_acquire(const int *p)
 {
@@ -151,7 +153,7 @@ __device__ __forceinline__ void wait_counter_t0(const int *ctr, int want, uint64
 struct DecodeSync {
     int *gu_done;     // per block: gate_up CTA units finished (routed blocks, then the shared ones)
     int shared_base;  // index in gu_done of the shared expert's first block
-    int target[2];    // gate_up CTA units per block of the routed / shared problem
+    int target[2];    // count of a complete block of the routed / shared problem (8 per gate_up CTA unit)
     int *status;
     uint64_t wait_ns;
 };
@@ -175,11 +177,11 @@ __device__ __forceinline__ void wait_block_ready(const DecodeSync *S, int pi, in
 // between CTAs c - 1 and c (piece 1, this CTA is c) or c and c + 1 (piece 0): the pair's
 // partials meet in split slot c - piece and only the second of the two CTAs to finish
 // adds the other piece and runs the epilogue; a sum of two fp32 terms does not depend on
-// their order). done_ctr (fused kernel, gate_up): counted once the unit's h rows are
+// their order). done_ctr (fused kernel, gate_up): raised by 8 once the unit's h rows are
 // written, with release semantics, by whichever CTA ran the epilogue.
 template <bool GATED, int KS>
 __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch &L, int lu, int n_pos, uint4 *smem_b,
-                                          FastShared &sm, int s_lo = 0, int s_hi = -1, int piece = -1,
+                                          FastShared &sm, RedBuf *red, int s_lo = 0, int s_hi = -1, int piece = -1,
                                           int *done_ctr = nullptr)
 {
     constexpr int TPW = 8 / KS;
@@ -200,6 +202,19 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     const int e = sm.s_e;
     const float *inv = sm.inv;
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    // the epilogue's row globals: with the K split inside the CTA (small batches, short
+    // loops) loaded while the steps stream, otherwise after them (no registers held)
+    const float *glob_e = p.glob + (size_t)e * p.e_glob;
+    float gl[4] = {0.f, 0.f, 0.f, 0.f};
+    auto load_globals = [&]() {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int i = r0 + g + 8 * half;
+            gl[2 * half] = __ldg(glob_e + i);
+            gl[2 * half + 1] = __ldg(glob_e + (GATED ? p.up_off + i : i + 16));
+        }
+    };
+    if (KS > 1 && ok && ks == 0) load_globals();
     if (ok) {
         const FastPtrs P = fast_ptrs<GATED>(p, e, r0, g, c, k0);
         const uint4 *bb = smem_b + (size_t)g * (K / 8) + k0 / 8;
@@ -240,30 +255,30 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
     if (KS > 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            sm.red[warp][lane][i] = acc0[i];
-            sm.red[warp][lane][4 + i] = acc1[i];
+            red[warp][lane][i] = acc0[i];
+            red[warp][lane][4 + i] = acc1[i];
         }
         __syncthreads();
     }
     if (ks == 0 && ok) {
+        if (KS == 1) load_globals();
         if (KS > 1) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float a = 0.f, b2 = 0.f;
                 for (int w = 0; w < KS; ++w) {
-                    a += sm.red[tp * KS + w][lane][i];
-                    b2 += sm.red[tp * KS + w][lane][4 + i];
+                    a += red[tp * KS + w][lane][i];
+                    b2 += red[tp * KS + w][lane][4 + i];
                 }
                 acc0[i] = a;
                 acc1[i] = b2;
             }
         }
-        const float *glob_e = p.glob + (size_t)e * p.e_glob;
         if (GATED) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int i = r0 + g + 8 * half;
-                const float gg = __ldg(glob_e + i), gu = __ldg(glob_e + p.up_off + i);
+                const float gg = gl[2 * half], gu = gl[2 * half + 1];
 #pragma unroll
                 for (int col = 0; col < 2; ++col) {
                     const int pos = blk * kGemvBlock + 2 * c + col;
@@ -293,16 +308,28 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int n = r0 + g + 8 * half;
-                    yrow[n] = acc0[2 * half + col] * __ldg(glob_e + n) * wgt;
-                    yrow[n + 16] = acc1[2 * half + col] * __ldg(glob_e + n + 16) * wgt;
+                    yrow[n] = acc0[2 * half + col] * gl[2 * half] * wgt;
+                    yrow[n + 16] = acc1[2 * half + col] * gl[2 * half + 1] * wgt;
                 }
             }
         }
     }
-    if (KS > 1 || done_ctr) __syncthreads();
-    if (done_ctr && threadIdx.x == 0) {
-        __threadfence();  // the unit's h rows (all warps) before the count
-        atomicAdd(done_ctr, 1);
+    if (KS > 1) __syncthreads();
+    if (done_ctr) {
+        // publish the unit's h rows: 8 counts per unit, one per warp (each after its own rows,
+        // so that no warp waits for the others), or all 8 at once after the K-split barrier
+        if (KS > 1) {
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicAdd(done_ctr, 8);
+            }
+        } else {
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                atomicAdd(done_ctr, 1);
+            }
+        }
     }
 }
 
@@ -451,7 +478,8 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
 // split inside the CTA. S: fused kernel (gate_up counts finished units per block; down
 // waits for them and reads h through L2).
 template <bool GATED, int KS, bool FUSED>
-__device__ __forceinline__ void fast_phase(const FastLaunch &L, uint4 *smem_b, FastShared &sm, const DecodeSync *S)
+__device__ __forceinline__ void fast_phase(const FastLaunch &L, uint4 *smem_b, FastShared &sm, RedBuf *red,
+                                           const DecodeSync *S)
 {
     const int n_pos0 = load_n_pos(L.prob[0]);
     const int n_pos1 = L.nprob > 1 ? load_n_pos(L.prob[1]) : 0;
@@ -499,7 +527,7 @@ __device__ __forceinline__ void fast_phase(const FastLaunch &L, uint4 *smem_b, F
                 const int lu = stage_for(u);
                 // piece 1: tail of the unit begun by CTA c - 1; piece 0: head of one CTA c + 1 ends
                 const int piece = s > 0 ? 1 : (s_end < Sx ? 0 : -1);
-                fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, sm, s, s_end, piece,
+                fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, sm, red, s, s_end, piece,
                                      counter(u));
                 w += s_end - s;
             }
@@ -517,7 +545,7 @@ __device__ __forceinline__ void fast_phase(const FastLaunch &L, uint4 *smem_b, F
     for (int u = u_lo; u < u_hi; ++u) {
         const int pi = u < units0 ? 0 : 1;
         const int lu = stage_for(u);
-        fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, sm, 0, -1, -1, counter(u));
+        fast_unit<GATED, KS>(L.prob[pi], L, lu, pi ? n_pos1 : n_pos0, smem_b, sm, red, 0, -1, -1, counter(u));
     }
 }
 
@@ -528,8 +556,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     pdl_enter();
     extern __shared__ uint4 smem_b[];
     __shared__ FastShared sm;
+    __shared__ RedBuf red[KS > 1 ? 8 : 1];
     if (threadIdx.x == 0) sm.dead = 0;
-    fast_phase<GATED, KS, false>(L, smem_b, sm, nullptr);
+    fast_phase<GATED, KS, false>(L, smem_b, sm, red, nullptr);
 }
 
 // Fused decode forward: gate_up (+ SwiGLU into h) over every touched block, then down
@@ -546,19 +575,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fused_kernel(const __grid_co
     pdl_wait();
     extern __shared__ uint4 smem_b[];
     __shared__ FastShared sm;
+    __shared__ RedBuf red[KSG > 1 || KSD > 1 ? 8 : 1];
     if (threadIdx.x == 0) sm.dead = 0;
     __syncthreads();
     DecodeSync S;
     S.gu_done = F.gu_done;
     S.shared_base = F.shared_base;
-    S.target[0] = F.gu.prob[0].n_tiles;
-    S.target[1] = F.gu.nprob > 1 ? F.gu.prob[1].n_tiles : 0;
+    S.target[0] = 8 * F.gu.prob[0].n_tiles;  // 8 counts per gate_up CTA unit
+    S.target[1] = F.gu.nprob > 1 ? 8 * F.gu.prob[1].n_tiles : 0;
     S.status = F.status;
     S.wait_ns = F.wait_ns ? F.wait_ns : kWaitNs;
     DecodeSync S_gu = S;
     if (F.skip_publish) S_gu.gu_done = nullptr;  // fault injection: nothing is published
-    fast_phase<true, KSG, true>(F.gu, smem_b, sm, &S_gu);
-    fast_phase<false, KSD, true>(F.dn, smem_b, sm, &S);
+    fast_phase<true, KSG, true>(F.gu, smem_b, sm, red, &S_gu);
+    fast_phase<false, KSD, true>(F.dn, smem_b, sm, red, &S);
     // every CTA's y rows before any combine
     __syncthreads();
     if (threadIdx.x == 0) {

@@ -5,7 +5,8 @@
 // these logits exactly as for given logits.
 //
 // m16n8k16 bf16 MMAs with the router rows as M and tokens as N. A CTA owns 16 rows x
-// 32 tokens; its warps split K and walk it in 32-element chunks; within a chunk lane
+// 8 NJ tokens (NJ = 4, or 1 for small batches so that the grid covers the GPU); its warps
+// split K and walk it in 32-element chunks; within a chunk lane
 // (g, c) loads the 8 consecutive elements 8c .. 8c+7 of its rows (16 bytes) and of its
 // tokens, and the two MMAs of the chunk take elements 8c..8c+3 and 8c+4..8c+7: the same
 // K permutation for both operands, so every lane reads contiguous 16-byte pieces.
@@ -19,39 +20,40 @@ namespace ftmoe {
 namespace {
 
 constexpr int kRgWarps = 16;  // warps per CTA, splitting K
-constexpr int kRgTok = 32;    // tokens per CTA tile (4 MMA column tiles)
 constexpr int kGroup = 2;     // 32-element chunks whose loads are issued together
 
-// One CTA = one tile of 16 router rows x 32 tokens; its ks warps (ks a power of two up
+// One CTA = one tile of 16 router rows x 8 NJ tokens; its ks warps (ks a power of two up
 // to 16) take equal K ranges, issue the loads of two 32-element chunks at a time, and
 // the partial sums are added in warp order.
+template <int NJ>
 __global__ void __launch_bounds__(32 * kRgWarps) router_gemm_kernel(const uint16_t *__restrict__ x,
                                                                    const uint16_t *__restrict__ w, int T, int H,
                                                                    int E, int ks, float *__restrict__ logits)
 {
     pdl_enter();
-    __shared__ float red[kRgWarps][16][32];
+    constexpr int kRgTok = 8 * NJ;
+    __shared__ float red[kRgWarps][4 * NJ][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int n_rt = (E + 15) / 16;
     const int rt = blockIdx.x % n_rt, tt = blockIdx.x / n_rt;
     const int e0 = rt * 16, t0 = tt * kRgTok;
-    float acc[4][4] = {};
+    float acc[NJ][4] = {};
     {
         const int kw = H / ks, kb = warp * kw;
         // rows past E (last tile of an E not a multiple of 16) read a valid row; not stored
         const int ea = e0 + g < E ? e0 + g : E - 1, eb = e0 + g + 8 < E ? e0 + g + 8 : E - 1;
         const uint16_t *a_lo = w + (size_t)ea * H + kb + 8 * c;
         const uint16_t *a_hi = w + (size_t)eb * H + kb + 8 * c;
-        const uint16_t *b[4];
+        const uint16_t *b[NJ];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NJ; ++j) {
             int t = t0 + 8 * j + g;
             if (t > T - 1) t = T - 1;  // tail tokens read a valid row; their results are not stored
             b[j] = x + (size_t)t * H + kb + 8 * c;
         }
         // chunks in groups of kGroup: all loads of a group are issued before its MMAs
         for (int kg = 0; kg < kw; kg += kGroup * 32) {
-            uint4 lo[kGroup], hi[kGroup], bv[kGroup][4];
+            uint4 lo[kGroup], hi[kGroup], bv[kGroup][NJ];
 #pragma unroll
             for (int q = 0; q < kGroup; ++q) {
                 const int k0 = kg + 32 * q;
@@ -59,14 +61,14 @@ __global__ void __launch_bounds__(32 * kRgWarps) router_gemm_kernel(const uint16
                     lo[q] = ldg_nc_v4(a_lo + k0);
                     hi[q] = ldg_nc_v4(a_hi + k0);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) bv[q][j] = ldg_nc_v4(b[j] + k0);
+                    for (int j = 0; j < NJ; ++j) bv[q][j] = ldg_nc_v4(b[j] + k0);
                 }
             }
 #pragma unroll
             for (int q = 0; q < kGroup; ++q) {
                 if (kg + 32 * q >= kw) break;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < NJ; ++j) {
                     mma_bf16_16816(acc[j], lo[q].x, hi[q].x, lo[q].y, hi[q].y, bv[q][j].x, bv[q][j].y);
                     mma_bf16_16816(acc[j], lo[q].z, hi[q].z, lo[q].w, hi[q].w, bv[q][j].z, bv[q][j].w);
                 }
@@ -74,14 +76,14 @@ __global__ void __launch_bounds__(32 * kRgWarps) router_gemm_kernel(const uint16
         }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < NJ; ++j)
 #pragma unroll
         for (int i = 0; i < 4; ++i) red[warp][4 * j + i][lane] = acc[j][i];
     __syncthreads();
     if (warp != 0) return;
     // D fragment: rows g, g+8 (router rows), columns 2c, 2c+1 (tokens) of each tile
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NJ; ++j) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float v = 0.f;
@@ -99,10 +101,16 @@ cudaError_t launch_router_gemm(const uint16_t *x, const uint16_t *w, int T, int 
 {
     // K split: at least 8 warps per tile (their chunk loads overlap), 16 while the grid is
     // small, as long as every K range stays a multiple of 32
-    const int tiles = ((E + 15) / 16) * ((T + kRgTok - 1) / kRgTok);
+    // tokens per tile: 32, or 8 while 32-token tiles would leave most SMs idle
+    const int rows = (E + 15) / 16;
+    const int nj = rows * ((T + 31) / 32) >= sm_count() ? 4 : 1;
+    const int tiles = rows * ((T + 8 * nj - 1) / (8 * nj));
     int ks = 1;
     while (ks < kRgWarps && (ks < 8 || tiles * ks < 4 * sm_count()) && H % (64 * ks) == 0) ks <<= 1;
-    FT_LAUNCH(router_gemm_kernel, dim3(tiles), dim3(32 * ks), 0, s, x, w, T, H, E, ks, logits);
+    if (nj == 4)
+        FT_LAUNCH(router_gemm_kernel<4>, dim3(tiles), dim3(32 * ks), 0, s, x, w, T, H, E, ks, logits);
+    else
+        FT_LAUNCH(router_gemm_kernel<1>, dim3(tiles), dim3(32 * ks), 0, s, x, w, T, H, E, ks, logits);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -69,6 +69,9 @@ SHAPES = {
     # is partly out of range), small enough for full-oracle parity
     "odd_h": LayerShape(hidden=640, intermediate=512, num_experts=128, top_k=8, group=16,
                         shared_intermediate=512),
+    # small layer whose every K is a whole 256-element stage of the W4A4 kernels (full-oracle parity)
+    "mini_w4a4": LayerShape(hidden=256, intermediate=256, num_experts=8, top_k=2, group=16,
+                            shared_intermediate=256),
     # fp8_block experts: a small layer (full-oracle parity) and the Qwen3.6-FP8 layer
     "mini_fp8": LayerShape(hidden=256, intermediate=256, num_experts=8, top_k=2, group=128,
                            shared_intermediate=128, fmt="fp8_block"),

@@ -30,7 +30,7 @@ def ft():
     return ft
 
 
-@pytest.mark.parametrize("name,T", [("mini", 256), ("qwen36", 2048), ("qwen36", 8), ("qwen36", 64)])
+@pytest.mark.parametrize("name,T", [("mini", 256), ("qwen36", 2048), ("qwen36", 1), ("qwen36", 8)])
 def test_stalled_pipeline_reports_timeout_and_recovers(ft, name, T):
     L = GpuLayer(name)
     shape = synth.SHAPES[name]
