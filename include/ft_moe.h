@@ -261,10 +261,12 @@ ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *rout
 /* NVFP4 quantization of `rows` activation rows of K elements (K a multiple of 16), the rule
  * of the W4A4 path (the pages name the format but give no activation recipe; this is NVFP4's
  * own two-level scaling applied per row): row scale glob = amax / (6 * 448); per 16 elements
- * the e4m3 scale s = e4m3(block max / (6 * glob)); codes q = e2m1(x / (s * glob)); every
- * step one correctly rounded fp32 operation, both conversions to nearest with ties to even,
- * saturating. Value of an element: e2m1(q) * e4m3(s) * glob.
- *   src     device rows, bf16 or fp32 (src_dtype FT_DTYPE_BF16 / FT_DTYPE_F32), [rows, K]
+ * the e4m3 scale s = e4m3(block max / (6 * glob)); codes q = e2m1(x * r) with the block's
+ * reciprocal r = 1 / (s * glob); every step one correctly rounded fp32 operation, both
+ * conversions to nearest with ties to even, saturating. Value of an element:
+ * e2m1(q) * e4m3(s) * glob.
+ *   src     device rows, bf16 or fp32 (src_dtype FT_DTYPE_BF16 / FT_DTYPE_F32), [rows, K],
+ *           16-byte aligned
  *   codes   device u8 [rows, K/2] (out), element 2m in the low nibble; 8-byte aligned
  *   scales  device u8 [rows, K/16] (out, e4m3); glob device f32 [rows] (out)
  * Errors: FT_ERR_INVALID_ARG, FT_ERR_CUDA. */

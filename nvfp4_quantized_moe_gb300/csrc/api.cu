@@ -1040,8 +1040,8 @@ ft_status ft_moe_quantize_nvfp4(const void *src, int32_t src_dtype, int32_t rows
         return fail(FT_ERR_INVALID_ARG, "src_dtype must be FT_DTYPE_BF16 or FT_DTYPE_F32");
     if (rows < 0 || K <= 0 || K % 16) return fail(FT_ERR_INVALID_ARG, "need rows >= 0 and K a positive multiple of 16");
     if (rows == 0) return ok();
-    if (!src || !codes || !scales || !glob || !aligned(codes, 8) || !aligned(src, 4) || !aligned(glob, 4))
-        return fail(FT_ERR_INVALID_ARG, "pointers must be non-NULL; codes 8-byte aligned");
+    if (!src || !codes || !scales || !glob || !aligned(codes, 8) || !aligned(src, 16) || !aligned(glob, 4))
+        return fail(FT_ERR_INVALID_ARG, "pointers must be non-NULL; src 16-byte and codes 8-byte aligned");
     cudaError_t e = launch_quant_nvfp4(src, src_dtype == FT_DTYPE_F32, K, nullptr, nullptr, rows, rows, 1, rows, codes,
                                        scales, glob, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");

@@ -169,11 +169,13 @@ __device__ int block_exclusive_scan(int *vals, int n, int *warp_tot)
     return total;
 }
 
-// Fill padding positions with the sentinel and give every block its expert.
+// Fill padding positions with the sentinel and give every block its expert: one warp per
+// block (every lane finds the block's expert, the lanes fill its positions together).
 __device__ void fill_blocks(const int *off, const int *count, int E, int B, int n_slots, int total,
                             int32_t *sorted_slot, int32_t *block_expert)
 {
-    for (int b = threadIdx.x; b < total / B; b += blockDim.x) {
+    const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int b = threadIdx.x >> 5; b < total / B; b += nwarps) {
         int pos = b * B;
         int lo = 0, hi = E;  // largest e with off[e] <= pos and a non-empty run
         while (hi - lo > 1) {
@@ -181,9 +183,9 @@ __device__ void fill_blocks(const int *off, const int *count, int E, int B, int 
             if (off[mid] <= pos) lo = mid; else hi = mid;
         }
         while (lo + 1 < E && off[lo + 1] <= pos) ++lo;
-        block_expert[b] = lo;
+        if (lane == 0) block_expert[b] = lo;
         int run_end_real = off[lo] + count[lo];
-        for (int q = pos; q < pos + B; ++q)
+        for (int q = pos + lane; q < pos + B; q += 32)
             if (q >= run_end_real) sorted_slot[q] = n_slots;
     }
 }

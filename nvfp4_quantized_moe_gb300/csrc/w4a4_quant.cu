@@ -2,9 +2,10 @@
 // the pages' sm_86/sm_89 cards lack: "[TP=2] Quantized MoE expert parallelism ... NVFP4
 // port", section 2). The pages give no activation recipe; the reading is NVFP4's two-level
 // scaling per row: glob = amax / (6 * 448), per 16 elements the e4m3 scale
-// s = e4m3(block max / (6 * glob)), codes q = e2m1(x / (s * glob)); every step an fp32
-// operation with correct rounding (division included), both conversions rounding to
-// nearest-even with saturation, so that the codes are a function of the fp32 inputs alone.
+// s = e4m3(block max / (6 * glob)), codes q = e2m1(x * r) with the block's reciprocal
+// r = 1 / (s * glob); every step one correctly rounded fp32 operation, both conversions
+// rounding to nearest-even with saturation, so that the codes are a function of the fp32
+// inputs alone.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -41,12 +42,30 @@ __device__ __forceinline__ float e4m3_value(uint32_t b)
     return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
+// The 16 elements of block b of a row as fp32 (two or four 16-byte loads).
 template <bool F32_SRC>
-__device__ __forceinline__ float src_at(const void *row, int k)
+__device__ __forceinline__ void load_block(const void *row, int b, float (&v)[16])
 {
-    if constexpr (F32_SRC) return __ldg(static_cast<const float *>(row) + k);
-    const uint16_t v = __ldg(static_cast<const uint16_t *>(row) + k);
-    return __uint_as_float((uint32_t)v << 16);
+    if constexpr (F32_SRC) {
+        const float4 *p = reinterpret_cast<const float4 *>(row) + 4 * b;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 q = __ldg(p + i);
+            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+        }
+    } else {
+        const uint4 *p = reinterpret_cast<const uint4 *>(row) + 2 * b;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint4 q = __ldg(p + i);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+                v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+        }
+    }
 }
 
 }  // namespace
@@ -67,7 +86,7 @@ __global__ void __launch_bounds__(256) quant_nvfp4_rows_kernel(const void *__res
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     const int nb = K / 16;
-    const size_t esz = F32_SRC ? 4 : 2;
+    const size_t esz = F32_SRC ? 4 : 2;  // (rows start 16-byte aligned: K is a multiple of 16)
     for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n_pos; pos += warps) {
         int row = pos;
         if (sorted_slot) {
@@ -88,26 +107,30 @@ __global__ void __launch_bounds__(256) quant_nvfp4_rows_kernel(const void *__res
         }
         const void *xr = static_cast<const char *>(src) + (size_t)row * K * esz;
         float amax = 0.f;
-        for (int k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(src_at<F32_SRC>(xr, k)));
+        for (int b = lane; b < nb; b += 32) {
+            float v[16];
+            load_block<F32_SRC>(xr, b, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
         const float g = __fdiv_rn(amax, 2688.0f);
         for (int b = lane; b < nb; b += 32) {
             float v[16];
+            load_block<F32_SRC>(xr, b, v);  // (the row is in L1 from the first pass)
             float bmax = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                v[i] = src_at<F32_SRC>(xr, 16 * b + i);
-                bmax = fmaxf(bmax, fabsf(v[i]));
-            }
+            for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
             uint32_t sc = 0;
             if (g > 0.f) sc = e4m3_rn_sat(__fdiv_rn(bmax, __fmul_rn(6.0f, g)));
             const float d = __fmul_rn(e4m3_value(sc), g);
             uint32_t w[2] = {0u, 0u};
             if (d > 0.f) {
+                const float rcp = __fdiv_rn(1.0f, d);
 #pragma unroll
                 for (int i = 0; i < 16; i += 2)
-                    w[i >> 3] |= e2m1x2_rn_sat(__fdiv_rn(v[i], d), __fdiv_rn(v[i + 1], d)) << (8 * ((i >> 1) & 3));
+                    w[i >> 3] |= e2m1x2_rn_sat(__fmul_rn(v[i], rcp), __fmul_rn(v[i + 1], rcp)) << (8 * ((i >> 1) & 3));
             }
             *reinterpret_cast<uint2 *>(cr + 8 * b) = make_uint2(w[0], w[1]);
             sr[b] = (uint8_t)sc;

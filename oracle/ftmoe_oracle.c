@@ -424,10 +424,10 @@ int orc_slice_fp8_range(int E, int H, int I, int begin, int len,
  * port", section 2: no native FP4 tensor cores there, so NVFP4 ran as W4A16). The pages do
  * not define how activations are quantized; the reading taken here is NVFP4's own two-level
  * scaling applied per activation row: a row scale glob = amax / (6 * 448) in fp32, one e4m3
- * block scale per 16 elements s = e4m3(block amax / (6 * glob)), codes q = e2m1(x / (s *
- * glob)), both conversions rounding to nearest with ties to even and saturating; value
- * q * s * glob. Every step is an fp32 operation in this order, the precision the kernels
- * take these decisions in. */
+ * block scale per 16 elements s = e4m3(block amax / (6 * glob)), codes q = e2m1(x * r) with
+ * r = 1 / (s * glob) the block's reciprocal, both conversions rounding to nearest with ties
+ * to even and saturating; value q * s * glob. Every step is one correctly rounded fp32
+ * operation in this order, the precision the kernels take these decisions in. */
 
 /* e4m3 code of a finite v >= 0: the nearest non-negative finite e4m3 value, ties to the
  * even code, values above 448 saturating to 448 (chosen by scanning all 127 codes). */
@@ -483,10 +483,11 @@ void orc_quant_nvfp4(const float *x, int rows, int K, uint8_t *codes, uint8_t *s
             scales[(size_t)r * (K / 16) + b] = (uint8_t)sc;
             float sv = (float)orc_e4m3(sc);
             float d = sv * g;
+            float rcp = d > 0.0f ? 1.0f / d : 0.0f;
             for (int i = 0; i < 16; i += 2) {
                 unsigned lo = 0, hi = 0;
                 if (sv > 0.0f) {
-                    float q0 = xr[16 * b + i] / d, q1 = xr[16 * b + i + 1] / d;
+                    float q0 = xr[16 * b + i] * rcp, q1 = xr[16 * b + i + 1] * rcp;
                     lo = e2m1_code_rne(q0);
                     hi = e2m1_code_rne(q1);
                 }

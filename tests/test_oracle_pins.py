@@ -526,7 +526,8 @@ def pin_nvfp4_exact_rows():
 def pin_nvfp4_nearest_and_bounds():
     """Random rows: every block scale is the e4m3 value nearest its block max / (6 x row scale),
     every code the e2m1 value nearest x / (scale x row scale) (a brute-force search over the 15
-    values), and no element moves by more than one e2m1 step of its block."""
+    values; the quantizer multiplies by the rounded reciprocal, so a tie-breaking difference of
+    one fp32 rounding is tolerated), and no element moves by more than one e2m1 step."""
     rng = np.random.default_rng(52)
     x = (rng.standard_normal((5, 64)) * np.exp(rng.uniform(-8, 8, (5, 1)))).astype(np.float32)
     x[2, 16:32] = 0.0  # an all-zero block
@@ -547,7 +548,7 @@ def pin_nvfp4_nearest_and_bounds():
                     assert xq[r, 16 * b + i] == 0
                     continue
                 err = abs(xq[r, 16 * b + i] / d - blk[i] / d)
-                assert err <= np.abs(lut - blk[i] / d).min() * (1 + 1e-6) + 1e-12, (r, b, i)
+                assert err <= np.abs(lut - blk[i] / d).min() * (1 + 1e-6) + 1e-6, (r, b, i)
                 assert abs(xq[r, 16 * b + i] - blk[i]) <= 2 * d * (1 + 1e-6)
 
 
