@@ -393,18 +393,26 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
                 lso += spb;
             }
         };
-        // the first two steps' weights do not depend on h: load them before waiting for it
+        // The first two steps' weights do not depend on h. In the fused kernel they are put in
+        // flight before the wait for the block's h rows; in a separate launch h is ready, and the
+        // staging goes first (its loads then do not queue behind the weights').
         FastFrag ring[4];
-        if (tot > 0) {
-            fast_load_at(P, lco, lso, ring[0]);
-            advance_load();
+        auto prime = [&]() {
+            if (tot > 0) {
+                fast_load_at(P, lco, lso, ring[0]);
+                advance_load();
+            }
+            if (tot > 1) {
+                fast_load_at(P, lco, lso, ring[1]);
+                advance_load();
+            }
+        };
+        if (S) {
+            prime();
+            wait_block_ready(S, pi, blk, sm);
         }
-        if (tot > 1) {
-            fast_load_at(P, lco, lso, ring[1]);
-            advance_load();
-        }
-        wait_block_ready(S, pi, blk, sm);
         fast_stage<false, COHERENT>(p, blk, n_pos, smem_b, sm);
+        if (!S) prime();
         if (threadIdx.x < kGemvBlock) {  // per block position: y row (slot) or -1, and its factor
             const int pos = blk * kGemvBlock + threadIdx.x;
             int dst = -1;
@@ -472,6 +480,149 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
     }
 }
 
+// gate_up over the CTA's step range [w_lo, w_hi) of the even split (KS = 1, every K a
+// multiple of 512, I_l a multiple of 128, range ends on 4-step boundaries): consecutive
+// units of one block share the staged activations and warp w's 16 gate (and up) rows in
+// them are 128 apart, so each warp streams a run of them through one register ring as a
+// single sequence of steps and runs each unit's epilogue (SwiGLU into h, or the split
+// exchange of a unit cut between two CTAs) while the next unit's first loads are in flight.
+__device__ __forceinline__ void gate_runs(const FastLaunch &L, int units0, int n_pos0, int n_pos1, int64_t w_lo,
+                                          int64_t w_hi, uint4 *smem_b, FastShared &sm, const DecodeSync *S)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int m = ((c >> 1) << 1) ^ (g & 1);
+    const int boff[4] = {4 * c + (0 ^ m), 4 * c + (1 ^ m), 4 * c + (2 ^ m), 4 * c + (3 ^ m)};
+    const int S0 = L.prob[0].K / kStep, S1 = L.nprob > 1 ? L.prob[1].K / kStep : S0;
+    const int64_t W0 = (int64_t)units0 * S0;
+    for (int64_t w = w_lo; w < w_hi;) {
+        int u, s, Sx;
+        if (w < W0) {
+            u = (int)(w / S0); s = (int)(w - (int64_t)u * S0); Sx = S0;
+        } else {
+            u = units0 + (int)((w - W0) / S1); s = (int)((w - W0) - (int64_t)(u - units0) * S1); Sx = S1;
+        }
+        const int pi = u < units0 ? 0 : 1;
+        const GemvParams &p = L.prob[pi];
+        const int n_pos = pi ? n_pos1 : n_pos0;
+        const int lu = pi ? u - units0 : u;
+        const int blk = lu / p.n_tiles, grp0 = lu - blk * p.n_tiles;
+        // the run: this block's units from grp0 on, as far as the range reaches
+        const int64_t avail = w_hi - w;
+        const int64_t block_steps = (int64_t)(Sx - s) + (int64_t)(p.n_tiles - grp0 - 1) * Sx;
+        const int tot = (int)(avail < block_steps ? avail : block_steps);
+        const int last_end = (int)((s + tot - 1) % Sx) + 1;  // the last unit's end step
+        const int n_run = (s + tot + Sx - 1) / Sx;             // units in the run
+        w += tot;
+        fast_stage<true>(p, blk, n_pos, smem_b, sm);
+        const int e = sm.s_e;
+        const int r0a = (grp0 * 8 + warp) * 16;  // the warp's first gate row in the run's first unit
+        const FastPtrs P = fast_ptrs<true>(p, e, r0a, g, c, 0);
+        const uint32_t spb = (p.group == 16) ? 8u : 4u;
+        const uint32_t jump_c = 128u * (uint32_t)(p.K / 2) - 64u * (uint32_t)(Sx - 1);
+        const uint32_t jump_s = 128u * (uint32_t)(p.K / p.group) - spb * (uint32_t)(Sx - 1);
+        uint32_t lco = 64u * (uint32_t)s, lso = spb * (uint32_t)s;
+        int ls = s;
+        auto advance_load = [&]() {
+            if (++ls == Sx) {
+                ls = 0;
+                lco += jump_c;
+                lso += jump_s;
+            } else {
+                lco += 64u;
+                lso += spb;
+            }
+        };
+        const uint4 *bb = smem_b + (size_t)g * (p.K / 8);
+        const float *glob_e = p.glob + (size_t)e * p.e_glob;
+        int *done_ctr = S && S->gu_done ? gu_counter(S, pi, blk) : nullptr;
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        float gl[4] = {0.f, 0.f, 0.f, 0.f};
+        FastFrag ring[4];
+        fast_load_at(P, lco, lso, ring[0]);
+        advance_load();
+        if (tot > 1) {
+            fast_load_at(P, lco, lso, ring[1]);
+            advance_load();
+        }
+        int j = 0, cs = s, r0 = r0a;  // compute cursor: unit in the run, its step, its first gate row
+        for (int t0 = 0; t0 < tot; t0 += 4) {  // every piece is a whole number of 4-step groups
+            const int end_j = j == n_run - 1 ? last_end : Sx;
+            if (cs + 4 == end_j) {  // the unit's last group: its rows' globals, used by its epilogue
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int i = r0 + g + 8 * half;
+                    gl[2 * half] = __ldg(glob_e + i);
+                    gl[2 * half + 1] = __ldg(glob_e + p.up_off + i);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (t0 + q + 2 < tot) {
+                    fast_load_at(P, lco, lso, ring[(q + 2) & 3]);
+                    advance_load();
+                }
+                fast_compute(ring[q], bb, boff, cs + q, acc0, acc1);
+            }
+            cs += 4;
+            if (cs < end_j) continue;
+            // the unit's end: a piece of a unit cut between two CTAs meets its other piece
+            // first (piece 1: tail of the unit begun by CTA c - 1; piece 0: its head)
+            const int piece = (j == 0 && s > 0) ? 1 : (end_j < Sx ? 0 : -1);
+            bool finish = true;
+            if (piece >= 0) {
+                const int slot = (int)blockIdx.x - piece;
+                float *part = L.split_part + (size_t)slot * kSplitPartFloats;
+                float4 *mine = reinterpret_cast<float4 *>(part + ((size_t)piece * kThreads + threadIdx.x) * 8);
+                __stcg(mine, make_float4(acc0[0], acc0[1], acc0[2], acc0[3]));
+                __stcg(mine + 1, make_float4(acc1[0], acc1[1], acc1[2], acc1[3]));
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    __threadfence();  // every thread's partials before the count
+                    sm.flag = atomicAdd(L.split_cnt + slot, 1) == 1;
+                }
+                __syncthreads();
+                finish = sm.flag != 0;
+                if (finish) {
+                    __threadfence();
+                    const float4 *other =
+                        reinterpret_cast<const float4 *>(part + ((size_t)(1 - piece) * kThreads + threadIdx.x) * 8);
+                    const float4 o0 = __ldcg(other), o1 = __ldcg(other + 1);
+                    acc0[0] += o0.x; acc0[1] += o0.y; acc0[2] += o0.z; acc0[3] += o0.w;
+                    acc1[0] += o1.x; acc1[1] += o1.y; acc1[2] += o1.z; acc1[3] += o1.w;
+                }
+            }
+            if (finish) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int i = r0 + g + 8 * half;
+#pragma unroll
+                    for (int col = 0; col < 2; ++col) {
+                        const int pos = blk * kGemvBlock + 2 * c + col;
+                        const float scl = sm.inv[2 * c + col];
+                        const float gate = acc0[2 * half + col] * scl * gl[2 * half];
+                        const float up = acc1[2 * half + col] * scl * gl[2 * half + 1];
+                        __nv_bfloat16 hv = __float2bfloat16_rn(silu(gate) * up);
+                        p.h_out[(size_t)pos * p.h_ld + i] = *reinterpret_cast<uint16_t *>(&hv);
+                    }
+                }
+                if (done_ctr) {  // publish this warp's rows of the unit
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence();
+                        atomicAdd(done_ctr, 1);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc0[i] = acc1[i] = 0.f;
+            ++j;
+            cs = 0;
+            r0 += 128;
+        }
+    }
+}
+
 // One stage (gate_up or down) of the lean kernels over the concatenated unit lists of up
 // to two problems (the routed experts and the shared expert): the even split of all K
 // steps (gate_up, KS = 1), block runs (down, KS = 1), or contiguous unit ranges with the K
@@ -514,6 +665,16 @@ __device__ __forceinline__ void fast_phase(const FastLaunch &L, uint4 *smem_b, F
         const int64_t W = (int64_t)units0 * S0 + (int64_t)units1 * S1;
         const int Smax = S0 > S1 ? S0 : S1;
         if (L.split_part && gridDim.x <= kMaxSplitSlots && W >= (int64_t)gridDim.x * Smax) {
+            // runs of units through one ring when every K and every CTA range splits into
+            // 4-step groups and every unit's rows are all in range
+            const bool runs = S0 % 4 == 0 && S1 % 4 == 0 && L.prob[0].up_off % 128 == 0 &&
+                              (L.nprob < 2 || L.prob[1].up_off % 128 == 0);
+            if (runs) {
+                const int64_t Wq = W / 4;
+                gate_runs(L, units0, n_pos0, n_pos1, 4 * ((int64_t)blockIdx.x * Wq / gridDim.x),
+                          4 * ((int64_t)(blockIdx.x + 1) * Wq / gridDim.x), smem_b, sm, S);
+                return;
+            }
             const int w_hi = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x), W0 = units0 * S0;
             for (int w = (int)((int64_t)blockIdx.x * W / gridDim.x); w < w_hi;) {
                 int u, s, Sx;

@@ -169,13 +169,16 @@ __device__ int block_exclusive_scan(int *vals, int n, int *warp_tot)
     return total;
 }
 
-// Fill padding positions with the sentinel and give every block its expert: one warp per
-// block (every lane finds the block's expert, the lanes fill its positions together).
+// Fill padding positions with the sentinel and give every block its expert: one thread per
+// block for small blocks, one warp per block (its lanes filling the positions together) for
+// blocks of 64 positions or more.
 __device__ void fill_blocks(const int *off, const int *count, int E, int B, int n_slots, int total,
                             int32_t *sorted_slot, int32_t *block_expert)
 {
-    const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    for (int b = threadIdx.x >> 5; b < total / B; b += nwarps) {
+    const bool per_warp = B >= 64;
+    const int lane = per_warp ? (threadIdx.x & 31) : 0, step = per_warp ? 32 : 1;
+    const int nworkers = per_warp ? (int)(blockDim.x >> 5) : (int)blockDim.x;
+    for (int b = per_warp ? (int)(threadIdx.x >> 5) : (int)threadIdx.x; b < total / B; b += nworkers) {
         int pos = b * B;
         int lo = 0, hi = E;  // largest e with off[e] <= pos and a non-empty run
         while (hi - lo > 1) {
@@ -185,7 +188,7 @@ __device__ void fill_blocks(const int *off, const int *count, int E, int B, int 
         while (lo + 1 < E && off[lo + 1] <= pos) ++lo;
         if (lane == 0) block_expert[b] = lo;
         int run_end_real = off[lo] + count[lo];
-        for (int q = pos + lane; q < pos + B; q += 32)
+        for (int q = pos + lane; q < pos + B; q += step)
             if (q >= run_end_real) sorted_slot[q] = n_slots;
     }
 }
