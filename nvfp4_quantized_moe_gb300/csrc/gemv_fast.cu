@@ -395,7 +395,8 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
         };
         // The first two steps' weights do not depend on h. In the fused kernel they are put in
         // flight before the wait for the block's h rows; in a separate launch h is ready, and the
-        // staging goes first (its loads then do not queue behind the weights').
+        // staging and the position table go first (their dependent loads then do not queue
+        // behind the weights').
         FastFrag ring[4];
         auto prime = [&]() {
             if (tot > 0) {
@@ -412,7 +413,6 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
             wait_block_ready(S, pi, blk, sm);
         }
         fast_stage<false, COHERENT>(p, blk, n_pos, smem_b, sm);
-        if (!S) prime();
         if (threadIdx.x < kGemvBlock) {  // per block position: y row (slot) or -1, and its factor
             const int pos = blk * kGemvBlock + threadIdx.x;
             int dst = -1;
@@ -432,6 +432,7 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
             sm.tbl_w[threadIdx.x] = w;
         }
         __syncthreads();
+        if (!S) prime();
         if (tot == 0) continue;
         const uint4 *bb = smem_b + (size_t)g * (p.K / 8);
         const float *glob_e = p.glob + (size_t)e * p.e_glob;

@@ -267,6 +267,13 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;
         int it = 0, ia = 0;
+        int pending = -1;  // A buffer whose stores are in flight, released one chunk later
+        auto publish = [&](int buf) {  // every thread's stores complete, then the warp arrives once
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) arrive(a_full + buf);
+        };
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
             int lu;
             const TcParams &p = prob_of(u, lu);
@@ -309,13 +316,14 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                         asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * w + 2 * h2 + 1]) : "r"(hi), "r"(sv));
                     }
                 }
+                // the previous chunk's stores have had this chunk's work to land: complete them
+                // and release that buffer, then issue this chunk's stores
+                if (pending >= 0) publish(pending);
                 tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
-                tc::wait_st();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) arrive(a_full + ab);
+                pending = ab;
             }
         }
+        if (pending >= 0) publish(pending);
         if (dead && lane == 0) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else if (warp < kEpWarp0) {
         // ------------------------------------------------------------ dequantisation
@@ -342,6 +350,13 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             return q.scales + (size_t)row * (size_t)(q.K / q.group);
         };
         int it = 0, ia = 0;
+        int pending = -1;  // A buffer whose stores are in flight, released one chunk later
+        auto publish = [&](int buf) {  // every thread's stores complete, then the warp arrives once
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) arrive(a_full + buf);
+        };
         const uint8_t *srow = blockIdx.x < n_units ? scale_row(blockIdx.x) : p0.scales;
         uint4 s_next = blockIdx.x < n_units ? load_scales(srow) : make_uint4(0, 0, 0, 0);
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
@@ -392,17 +407,17 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                     dequant8_f16(words[w], sv[w >> 1], t4);
                     o[4 * w] = t4[0]; o[4 * w + 1] = t4[1]; o[4 * w + 2] = t4[2]; o[4 * w + 3] = t4[3];
                 }
-                // the row goes to this warp's TMEM lane quarter; every thread's stores complete
-                // before the warp arrives once
+                // the row goes to this warp's TMEM lane quarter
+                // the previous chunk's stores have had this chunk's work to land: complete them
+                // and release that buffer, then issue this chunk's stores
+                if (pending >= 0) publish(pending);
                 tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
-                tc::wait_st();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) arrive(a_full + ab);
+                pending = ab;
             }
             if (dead) break;
             srow = srow_next;
         }
+        if (pending >= 0) publish(pending);
         if (dead && lane == 0) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else {
         // ------------------------------------------------------------ epilogue
