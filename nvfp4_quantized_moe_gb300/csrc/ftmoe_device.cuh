@@ -307,25 +307,21 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
 // Wait for phase `parity` of `bar`: false after limit_ns nanoseconds (about two seconds
 // by default), or as soon as another role of the CTA has set *abort_flag (non-null)
 // after giving up itself.
-// The first 2048 polls spin (the pipelines' waits are short and latency-critical); after
-// that the thread sleeps between polls (32 ns doubling to 256 ns), so that a warp left
-// waiting for long leaves the issue slots of its scheduler to the warps that have work.
+// After one plain poll the thread parks in try_wait with a suspend-time hint: the hardware
+// resumes it when the phase completes (or after the hint), so a waiting warp takes no issue
+// slots from the warps that have work. (Spinning on plain polls instead, the epilogue,
+// producer and MMA warps of the tensor-core kernels starved their dequantising warps.)
+constexpr uint32_t kSuspendHintNs = 1000;
+
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                                 uint64_t limit_ns = kWaitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    uint32_t sleep_ns = 32;
-    for (uint32_t i = 1;; ++i) {
-        if (i > 2048) {
-            __nanosleep(sleep_ns);
-            if (sleep_ns < 256) sleep_ns <<= 1;
-        }
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (abort_flag && *abort_flag) return false;
-            if (globaltimer() - t0 > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 

@@ -192,7 +192,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         // (fault injection: with skip_producer set on the host, no copy is ever issued, so
         // every consumer's bounded wait runs out)
         if (lane == 0 && !TL.skip_producer) {
-            int it = 0;
+            int it = 0, slot = 0;  // chunks issued; stage slot = it % ns, with phase ph = (it / ns) & 1
+            uint32_t ph = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
                 int lu;
                 const TcParams &p = prob_of(u, lu);
@@ -204,13 +205,13 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 const int row_b = GATED ? row_a + p.up_off : row_a + MT;
                 const int nk = p.K / KC;
                 for (int c = 0; c < nk; ++c, ++it) {
-                    const int slot = it % ns;
-                    if (!wait_bar(empty + slot, ((it / ns) & 1) ^ 1, abort_flag, wl)) { dead = true; break; }
+                    if (!wait_bar(empty + slot, ph ^ 1, abort_flag, wl)) { dead = true; break; }
                     unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
                     mbar_arrive_expect_tx(full + slot, L.raw_bytes + L.b_bytes);
                     tc::tma_load_2d(raw, codes_map, c * RB, row_a, full + slot);
                     tc::tma_load_2d(raw + MT * RB, codes_map, c * RB, row_b, full + slot);
                     tc::tma_load_2d(smem + L.b_off + slot * L.b_bytes, b_map, c * KC, b * NT, full + slot);
+                    if (++slot == ns) { slot = 0; ph ^= 1; }
                 }
             }
             if (dead) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
@@ -227,7 +228,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         if (lane == 0) {
             const uint32_t tile = warp == 1 ? 0u : 1u;  // this issuer's tile and accumulator half
             const uint32_t idesc = tc::idesc_f16_f32(MT, NT);
-            int it = 0, ia = 0, uc = 0;
+            int ia = 0, uc = 0, slot = 0;  // stage slot and its phase advance incrementally
+            uint32_t ph = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
                 int lu;
                 const int nk = prob_of(u, lu).K / KC;
@@ -235,9 +237,9 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag, wl)) { dead = true; break; }
                 tc::fence_after_sync();
                 const uint32_t acc = tmem + tile * NT;
-                for (int c = 0; c < nk; ++c, ++it, ++ia) {
-                    const int slot = it % ns, ab = ia % NA;
-                    if (!wait_bar(full + slot, (it / ns) & 1, abort_flag, wl) ||
+                for (int c = 0; c < nk; ++c, ++ia) {
+                    const int ab = ia % NA;
+                    if (!wait_bar(full + slot, ph, abort_flag, wl) ||
                         !wait_bar(a_full + ab, (ia / NA) & 1, abort_flag, wl)) {
                         dead = true;
                         break;
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                     }
                     tc::commit(empty + slot);
                     tc::commit(a_empty + ab);
+                    if (++slot == ns) { slot = 0; ph ^= 1; }
                 }
                 if (dead) break;
                 tc::commit(acc_full);
@@ -266,7 +269,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         // different bank quads) and writes 128 bytes of A.
         const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int r = 32 * quarter + lane;
-        int it = 0, ia = 0;
+        int ia = 0, slot = 0;  // A buffers used; stage slot and its phase advance incrementally
+        uint32_t ph = 0;
         int pending = -1;  // A buffer whose stores are in flight, released one chunk later
         auto publish = [&](int buf) {  // every thread's stores complete, then the warp arrives once
             tc::wait_st();
@@ -285,9 +289,9 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             float smax = 0.f;
             for (int q = 0; q < kbn; ++q) smax = fmaxf(smax, __ldg(srow + q));
             const float down = pow2f(-row_scale_exp(448.f * smax));
-            for (int c = 0; c < nk; ++c, ++it, ++ia) {
-                const int slot = it % ns, ab = ia % NA;
-                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag, wl) ||
+            for (int c = 0; c < nk; ++c, ++ia) {
+                const int ab = ia % NA;
+                if (!warp_wait_bar(full + slot, ph, abort_flag, wl) ||
                     !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag, wl)) {
                     dead = true;
                     break;
@@ -321,6 +325,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 if (pending >= 0) publish(pending);
                 tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
                 pending = ab;
+                if (++slot == ns) { slot = 0; ph ^= 1; }
             }
         }
         if (pending >= 0) publish(pending);
@@ -349,7 +354,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             const int row = ee * q.R + mm * tile_rows + (half ? (GATED ? q.up_off : MT) : 0) + r;
             return q.scales + (size_t)row * (size_t)(q.K / q.group);
         };
-        int it = 0, ia = 0;
+        int ia = 0, slot = 0;  // A buffers used; stage slot and its phase advance incrementally
+        uint32_t ph = 0;
         int pending = -1;  // A buffer whose stores are in flight, released one chunk later
         auto publish = [&](int buf) {  // every thread's stores complete, then the warp arrives once
             tc::wait_st();
@@ -366,20 +372,19 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             const int u_next = u + gridDim.x;
             const uint8_t *srow_next = u_next < n_units ? scale_row(u_next) : nullptr;
             uint4 s16 = make_uint4(0, 0, 0, 0);
-            for (int c = 0; c < nk; ++c, ++it, ++ia) {
-                const int slot = it % ns, ab = ia % NA;
-                if (!warp_wait_bar(full + slot, (it / ns) & 1, abort_flag, wl) ||
+            int ci = 0, q = 0;  // chunk c = q * cpl + ci
+            for (int c = 0; c < nk; ++c, ++ia) {
+                const int ab = ia % NA;
+                if (!warp_wait_bar(full + slot, ph, abort_flag, wl) ||
                     !warp_wait_bar(a_empty + ab, ((ia / NA) & 1) ^ 1, abort_flag, wl)) {
                     dead = true;
                     break;
                 }
-                if (c % cpl == 0) {
-                    const int q = c / cpl;
+                if (ci == 0) {
                     s16 = s_next;
                     if (q + 1 < ngroups) s_next = load_scales(srow + sbytes * (q + 1));
                     else if (srow_next) s_next = load_scales(srow_next);
                 }
-                const int ci = c % cpl;
                 uint32_t sw;
                 if (p0.group == 16) {
                     sw = ci == 0 ? s16.x : ci == 1 ? s16.y : ci == 2 ? s16.z : s16.w;
@@ -413,6 +418,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 if (pending >= 0) publish(pending);
                 tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
                 pending = ab;
+                if (++slot == ns) { slot = 0; ph ^= 1; }
+                if (++ci == cpl) { ci = 0; ++q; }
             }
             if (dead) break;
             srow = srow_next;
