@@ -220,6 +220,15 @@ def cpu_baseline(T, shape, budget_s=10.0):
             "sample": f"{layers} layers x {T} tokens (route + forward, fp64), {t_total:.1f} s"}
 
 
+def _cold_l2(buf, r):
+    """Evicts L2 before a timed repetition: writes the whole 512 MB buffer, then reads its
+    first 256 MB back, so that the dirty lines the writes leave are written back here and
+    L2 holds clean lines of an unrelated buffer when the timed work starts."""
+    import torch
+    buf.fill_(r & 0xFF)
+    buf[: 256 << 20].view(torch.int32).sum()
+
+
 def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
     """One layer of `shape` at T tokens (Zipf routing), L2 flushed before every repetition."""
     import torch
@@ -242,7 +251,7 @@ def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
         e_.record(stream)
     times, stages = [], []
     for r in range(reps + 2):
-        flush.fill_(r & 0xFF)
+        _cold_l2(flush, r)
         start.record(stream)
         ft.ft_moe_route(lg, k, ids, w)
         ft.ft_moe_set_stage_events(ev)
@@ -262,7 +271,7 @@ def measure_prefill(ft, dev, cfg, shape, routed_d, shared_d, T, reps=6):
     del rb, sb, ws, flush
     return {"T": T, "routing": "zipf(1.1)", "us": ms * 1e3, "tokens_per_s": T / (ms / 1e3),
             "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tfl,
-            "peak_source": f"{peak_kind} bf16 dense", "l2": "512 MB written before every repetition",
+            "peak_source": f"{peak_kind} bf16 dense", "l2": "512 MB written, then 256 MB read back, before every repetition",
             "stage_us": {n: float(v * 1e3) for n, v in zip(ft.STAGES, st)},
             "expert_tokens_max_over_mean": float(counts.max() / counts.mean())}
 
@@ -288,7 +297,7 @@ def measure_w4a4(ft, dev, cfg, rb, sb, shape, T, reps=5):
         e_.record(stream)
     times, stages = [], []
     for r in range(reps + 2):
-        flush.fill_(r & 0xFF)
+        _cold_l2(flush, r)
         start.record(stream)
         ft.ft_moe_route(lg, k, ids, w)
         ft.ft_moe_set_stage_events(ev)
@@ -326,7 +335,7 @@ def measure_router(ft, dev, T, E=256, H=2048, reps=6):
     stream = torch.cuda.current_stream(dev)
     times = []
     for r in range(reps + 2):
-        flush.fill_(r & 0xFF)
+        _cold_l2(flush, r)
         start.record(stream)
         ft.ft_moe_route_gemm(x, wr, 8, logits, ids, w)
         stop.record(stream)
@@ -336,7 +345,7 @@ def measure_router(ft, dev, T, E=256, H=2048, reps=6):
     us = float(np.median(times)) * 1e3
     del flush
     return {"T": T, "E": E, "H": H, "us": us, "weight_gbs": E * H * 2 / (us * 1e-6) / 1e9,
-            "tflops": 2.0 * T * E * H / (us * 1e-6) / 1e12, "l2": "512 MB written before every repetition"}
+            "tflops": 2.0 * T * E * H / (us * 1e-6) / 1e12, "l2": "512 MB written, then 256 MB read back, before every repetition"}
 
 
 def measure_fp8(ft, dev, T=64, L=16, reps=20, T_prefill=2048):
@@ -405,7 +414,7 @@ def measure_fp8(ft, dev, T=64, L=16, reps=20, T_prefill=2048):
     times = []
     cur = torch.cuda.current_stream(dev)
     for r in range(6):
-        flush.fill_(r & 0xFF)
+        _cold_l2(flush, r)
         start.record(cur)
         ft.ft_moe_route(lgp, k, idp, wp)
         ft.ft_moe_forward(cfg, layers[0][0], layers[0][1], xp, idp, wp, outp, ws)
@@ -503,7 +512,7 @@ def measure_decode_row(ft, dev, shape, copies, T, zipf, reps=20, seed=100):
 
 def measure_prefill_row(ft, dev, shape, ranks, T, reps=5, seed=7):
     """Prefill regime, one layer: route once, then every tp rank's forward in sequence, L2
-    flushed (512 MB written) before the route and before each rank; the layer time is the
+    flushed (512 MB written, then 256 MB read back) before the route and before each rank; the layer time is the
     sum of the route and rank times (CUDA events on the launch stream)."""
     import torch
     H, E, k = shape.hidden, shape.num_experts, shape.top_k
@@ -519,12 +528,12 @@ def measure_prefill_row(ft, dev, shape, ranks, T, reps=5, seed=7):
     totals = []
     for rep in range(reps + 2):
         parts = []
-        flush.fill_(rep & 0xFF)
+        _cold_l2(flush, rep)
         evs[0].record(stream)
         ft.ft_moe_route(lg, k, ids, w)
         evs[1].record(stream)
         for r, (cfg, rb, sb) in enumerate(ranks):
-            flush.fill_((rep + r + 1) & 0xFF)
+            _cold_l2(flush, (rep + r + 1))
             evs[2 * r + 2].record(stream)
             ft.ft_moe_forward(cfg, rb, sb, x, ids, w, out, ws)
             evs[2 * r + 3].record(stream)
@@ -541,7 +550,7 @@ def measure_prefill_row(ft, dev, shape, ranks, T, reps=5, seed=7):
     return {"T": T, "tp": len(ranks), "routing": "zipf(1.1)", "us": ms * 1e3, "route_us": float(med[0] * 1e3),
             "rank_us": [float(v * 1e3) for v in med[1:]], "tokens_per_s": T / (ms / 1e3),
             "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tfl,
-            "peak_source": f"{kind} bf16 dense", "l2": "512 MB written before the route and before each rank"}
+            "peak_source": f"{kind} bf16 dense", "l2": "512 MB written, then 256 MB read back, before the route and before each rank"}
 
 
 def measure_configs(ft, dev, qwen_pieces_d, qwen_copies, args):
