@@ -7,10 +7,10 @@
 // epilogue; for down the rows [n0, n0+256) as two tiles. One launch covers the routed
 // experts' units and then the shared expert's (each role looks up its unit's problem;
 // K may differ between the two), strided over persistent CTAs. Warp roles:
-//   warp 0      one thread issues every TMA: per 64-element K chunk the raw packed
-//               codes of both tiles (box 32 bytes x 128 rows; fp8_block 64 bytes with the
-//               64-byte swizzle) and the block's activations (f16 box 64 x 128, 128-byte
-//               swizzled, K-major) -- gate_up reads them from the expert-sorted f16 copy of
+//   warp 0      one thread issues every TMA: per stage of 128 K elements (two 64-element
+//               sub-chunks, one barrier) the raw packed codes of both tiles (box 32 bytes x
+//               128 rows; fp8_block 64 bytes with the 64-byte swizzle) and the block's
+//               activations (f16 box 64 x 128, 128-byte swizzled, K-major), per sub-chunk -- gate_up reads them from the expert-sorted f16 copy of
 //               x, down from the f16 copy of h; each activation row carries a power-of-two
 //               scale (see rows_to_f16_kernel) that the epilogue multiplies back;
 //   warps 1, 14 warp 1 allocates tensor memory; one thread of each issues tcgen05.mma
@@ -28,8 +28,10 @@
 //               SwiGLU (h) or the routing weight (y, fp32: each warp transposes its 32 x 32
 //               blocks through shared memory and stores 128 contiguous bytes per position with
 //               16-byte stores). Tensor memory: the accumulator (256 columns) and
-//               four A buffers (256 columns); the accumulator is released once every
-//               epilogue warp has loaded its last chunk.
+//               two A buffers of one stage each (256 columns); the accumulator is released once every
+//               epilogue warp has loaded its last chunk. A stage of 128 K elements carries
+//               the per-chunk synchronisation (two barrier waits per role, a tensor-memory
+//               store wait, an arrive, two commits) over twice the work of one 64-element box.
 // f16 operands instead of bf16: code*scale is exact in both; a bf16 activation row
 // scaled by its power of two (maximum in [2^14, 2^15)) converts to f16 exactly except
 // for elements below 2^-31 of the row maximum, which move by less than 2^-38 of it;
@@ -50,10 +52,13 @@ namespace {
 
 constexpr int NT = kTcBlock;  // positions per unit (MMA N)
 constexpr int MT = 128;       // weight rows per tile (MMA M)
-constexpr int KC = 64;        // K elements per chunk (128 bytes of f16)
-constexpr int NSMAX = 6;      // TMA stages (at most)
-constexpr int NA = 4;         // dequantised A buffers (tensor memory)
-constexpr uint32_t kColA = 2 * NT;  // A buffer ab, tile t at columns kColA + 64 ab + 32 t
+constexpr int KC = 64;        // K elements per sub-chunk (128 bytes of f16: one TMA box row)
+constexpr int NSUB = 2;       // sub-chunks per stage: a stage covers KST = 128 K elements
+constexpr int KST = KC * NSUB;
+constexpr int NSMAX = 4;      // TMA stages (at most)
+constexpr int NA = 2;         // dequantised A buffers (tensor memory), one stage each
+// A buffer ab, sub-chunk j, tile t at columns kColA + 128 ab + 64 j + 32 t
+constexpr uint32_t kColA = 2 * NT;
 // Warps: 0 producer, 1 MMA (tile 0), 2..9 dequantise, 10..13 epilogue, 14 MMA (tile 1),
 // 15..18 a second epilogue group: two warps per TMEM quadrant take alternate 32-position
 // chunks of the accumulator, so it is read out (and released to the next unit's MMAs) in
@@ -87,16 +92,18 @@ struct TcSmem {
     int ns;
 };
 
-// Raw code bytes per weight row and 64-element K chunk: 32 (NVFP4, two codes a byte) or
-// 64 (fp8_block, one code a byte).
+// Raw code bytes per weight row and 64-element K sub-chunk: 32 (NVFP4, two codes a byte)
+// or 64 (fp8_block, one code a byte).
 __host__ __device__ constexpr uint32_t raw_row_bytes(bool fp8) { return fp8 ? 64u : 32u; }
 
 __host__ __device__ inline TcSmem tc_smem(int ns, bool fp8, bool gated)
 {
     TcSmem s;
     s.a_bytes = 0;  // the dequantised A operand lives in tensor memory
-    s.b_bytes = (uint32_t)NT * 128;
-    s.raw_bytes = 2u * MT * raw_row_bytes(fp8);
+    // a stage: per sub-chunk j, the B box (NT rows x 128 bytes) at b + j NT 128 and the raw
+    // code boxes of the two tiles at raw + (2 j + t) MT RB
+    s.b_bytes = (uint32_t)NSUB * NT * 128;
+    s.raw_bytes = (uint32_t)NSUB * 2u * MT * raw_row_bytes(fp8);
     s.ns = ns;
     s.a_off = 0;
     s.b_off = s.a_off + NA * s.a_bytes;
@@ -203,14 +210,19 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
                 const int row_a = e * p.R + m * tile_rows;
                 const int row_b = GATED ? row_a + p.up_off : row_a + MT;
-                const int nk = p.K / KC;
+                const int nk = p.K / KST;
                 for (int c = 0; c < nk; ++c, ++it) {
                     if (!wait_bar(empty + slot, ph ^ 1, abort_flag, wl)) { dead = true; break; }
                     unsigned char *raw = smem + L.raw_off + slot * L.raw_bytes;
+                    unsigned char *bt = smem + L.b_off + slot * L.b_bytes;
                     mbar_arrive_expect_tx(full + slot, L.raw_bytes + L.b_bytes);
-                    tc::tma_load_2d(raw, codes_map, c * RB, row_a, full + slot);
-                    tc::tma_load_2d(raw + MT * RB, codes_map, c * RB, row_b, full + slot);
-                    tc::tma_load_2d(smem + L.b_off + slot * L.b_bytes, b_map, c * KC, b * NT, full + slot);
+#pragma unroll
+                    for (int j = 0; j < NSUB; ++j) {
+                        const int kc = c * NSUB + j;  // 64-element sub-chunk index
+                        tc::tma_load_2d(raw + (2 * j) * MT * RB, codes_map, kc * RB, row_a, full + slot);
+                        tc::tma_load_2d(raw + (2 * j + 1) * MT * RB, codes_map, kc * RB, row_b, full + slot);
+                        tc::tma_load_2d(bt + j * NT * 128, b_map, kc * KC, b * NT, full + slot);
+                    }
                     if (++slot == ns) { slot = 0; ph ^= 1; }
                 }
             }
@@ -232,7 +244,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             uint32_t ph = 0;
             for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x, ++uc) {
                 int lu;
-                const int nk = prob_of(u, lu).K / KC;
+                const int nk = prob_of(u, lu).K / KST;
                 // one accumulator: the epilogue of the previous unit has read it out
                 if (!wait_bar(acc_empty, (uc & 1) ^ 1, abort_flag, wl)) { dead = true; break; }
                 tc::fence_after_sync();
@@ -245,12 +257,16 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t a0 = tmem + kColA + (uint32_t)ab * 64u + tile * 32u;  // A in tensor memory
-                    const uint32_t b0 = smem_u32(smem + L.b_off + slot * L.b_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < KC / 16; ++kk) {
-                        const uint64_t bd = tc::sw128_desc(b0 + kk * 32);
-                        tc::mma_f16_ts(acc, a0 + kk * 8u, bd, idesc, (c | kk) != 0);
+                    for (int j = 0; j < NSUB; ++j) {
+                        // A in tensor memory, B from the sub-chunk's swizzled box
+                        const uint32_t a0 = tmem + kColA + (uint32_t)ab * 128u + (uint32_t)j * 64u + tile * 32u;
+                        const uint32_t b0 = smem_u32(smem + L.b_off + slot * L.b_bytes + j * NT * 128);
+#pragma unroll
+                        for (int kk = 0; kk < KC / 16; ++kk) {
+                            const uint64_t bd = tc::sw128_desc(b0 + kk * 32);
+                            tc::mma_f16_ts(acc, a0 + kk * 8u, bd, idesc, (c | j | kk) != 0);
+                        }
                     }
                     tc::commit(empty + slot);
                     tc::commit(a_empty + ab);
@@ -263,7 +279,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         }
     } else if (FP8 && warp < kEpWarp0) {
         // ------------------------------------------------------------ dequantisation (fp8_block)
-        // warp (quarter, half): rows 32*quarter .. +32 of tile `half`; per chunk each thread
+        // warp (quarter, half): rows 32*quarter .. +32 of tile `half`; per sub-chunk each thread
         // converts the 64 code bytes of its row (read in the 64-byte swizzle of the TMA box:
         // 16-byte piece j of row r sits at j ^ ((r >> 1) & 3), so 8 consecutive rows hit 8
         // different bank quads) and writes 128 bytes of A.
@@ -271,17 +287,10 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         const int r = 32 * quarter + lane;
         int ia = 0, slot = 0;  // A buffers used; stage slot and its phase advance incrementally
         uint32_t ph = 0;
-        int pending = -1;  // A buffer whose stores are in flight, released one chunk later
-        auto publish = [&](int buf) {  // every thread's stores complete, then the warp arrives once
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) arrive(a_full + buf);
-        };
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
             int lu;
             const TcParams &p = prob_of(u, lu);
-            const int kbn = p.K / 128, nk = p.K / KC;
+            const int kbn = p.K / 128, nk = p.K / KST;
             const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
             const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
             const int nb = GATED ? (half ? p.up_off / MT : 0) + m : 2 * m + half;  // the tile's scale block row
@@ -296,39 +305,45 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                     dead = true;
                     break;
                 }
-                const __half2 s2 = __float2half2_rn(__ldg(srow + (c >> 1)) * down);
+                // a stage is one 128 x 128 scale block along K
+                const __half2 s2 = __float2half2_rn(__ldg(srow + c) * down);
                 const uint32_t sv = *reinterpret_cast<const uint32_t *>(&s2);
-                const unsigned char *rw = smem + L.raw_off + slot * L.raw_bytes + half * MT * RB + r * RB;
-                const int x = (r >> 1) & 3;
-                uint4 q[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4 *>(rw + ((j ^ x) << 4));
-                const uint32_t words[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
-                                            q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
-                uint32_t o[32];  // the row's 64 f16 values, TMEM columns in K order
+                for (int jj = 0; jj < NSUB; ++jj) {
+                    const unsigned char *rw = smem + L.raw_off + slot * L.raw_bytes + (2 * jj + half) * MT * RB + r * RB;
+                    const int x = (r >> 1) & 3;
+                    uint4 q[4];
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {  // columns 4w .. 4w + 3 = code words 2w, 2w + 1
+                    for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4 *>(rw + ((j ^ x) << 4));
+                    const uint32_t words[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
+                                                q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
+                    uint32_t o[32];  // the row's 64 f16 values, TMEM columns in K order
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const uint32_t cw = words[2 * w + h2];
-                        uint32_t lo, hi;
-                        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-                            : "=r"(lo) : "r"(cw));
-                        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-                            : "=r"(hi) : "r"(cw >> 16));
-                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * w + 2 * h2]) : "r"(lo), "r"(sv));
-                        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * w + 2 * h2 + 1]) : "r"(hi), "r"(sv));
+                    for (int w = 0; w < 8; ++w) {  // columns 4w .. 4w + 3 = code words 2w, 2w + 1
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const uint32_t cw = words[2 * w + h2];
+                            uint32_t lo, hi;
+                            asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+                                : "=r"(lo) : "r"(cw));
+                            asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+                                : "=r"(hi) : "r"(cw >> 16));
+                            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * w + 2 * h2]) : "r"(lo), "r"(sv));
+                            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * w + 2 * h2 + 1]) : "r"(hi), "r"(sv));
+                        }
                     }
+                    tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 128u + (uint32_t)jj * 64u +
+                                 (uint32_t)half * 32u,
+                             o);
                 }
-                // the previous chunk's stores have had this chunk's work to land: complete them
-                // and release that buffer, then issue this chunk's stores
-                if (pending >= 0) publish(pending);
-                tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
-                pending = ab;
+                // every thread's stores complete, then the warp releases the buffer once
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) arrive(a_full + ab);
                 if (++slot == ns) { slot = 0; ph ^= 1; }
             }
         }
-        if (pending >= 0) publish(pending);
         if (dead && lane == 0) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else if (warp < kEpWarp0) {
         // ------------------------------------------------------------ dequantisation
@@ -356,23 +371,16 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
         };
         int ia = 0, slot = 0;  // A buffers used; stage slot and its phase advance incrementally
         uint32_t ph = 0;
-        int pending = -1;  // A buffer whose stores are in flight, released one chunk later
-        auto publish = [&](int buf) {  // every thread's stores complete, then the warp arrives once
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) arrive(a_full + buf);
-        };
         const uint8_t *srow = blockIdx.x < n_units ? scale_row(blockIdx.x) : p0.scales;
         uint4 s_next = blockIdx.x < n_units ? load_scales(srow) : make_uint4(0, 0, 0, 0);
         for (int u = blockIdx.x; u < n_units && !dead; u += gridDim.x) {
             int lu;
-            const int nk = prob_of(u, lu).K / KC;
-            const int ngroups = nk / cpl;
+            const int K = prob_of(u, lu).K;
+            const int nk = K / KST, ngroups = (K / KC) / cpl;
             const int u_next = u + gridDim.x;
             const uint8_t *srow_next = u_next < n_units ? scale_row(u_next) : nullptr;
             uint4 s16 = make_uint4(0, 0, 0, 0);
-            int ci = 0, q = 0;  // chunk c = q * cpl + ci
+            int ci = 0, q = 0;  // 64-element sub-chunk = q * cpl + ci
             for (int c = 0; c < nk; ++c, ++ia) {
                 const int ab = ia % NA;
                 if (!warp_wait_bar(full + slot, ph, abort_flag, wl) ||
@@ -380,51 +388,56 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                     dead = true;
                     break;
                 }
-                if (ci == 0) {
-                    s16 = s_next;
-                    if (q + 1 < ngroups) s_next = load_scales(srow + sbytes * (q + 1));
-                    else if (srow_next) s_next = load_scales(srow_next);
-                }
-                uint32_t sw;
-                if (p0.group == 16) {
-                    sw = ci == 0 ? s16.x : ci == 1 ? s16.y : ci == 2 ? s16.z : s16.w;
-                } else {
-                    const int wi = ci >> 1;
-                    const uint32_t wv = wi == 0 ? s16.x : wi == 1 ? s16.y : wi == 2 ? s16.z : s16.w;
-                    const uint32_t two = (ci & 1) ? (wv >> 16) : (wv & 0xFFFFu);
-                    sw = (two & 0xFFu) * 0x0101u | ((two >> 8) * 0x0101u) << 16;
-                }
-                uint32_t sv[4];
-                e4m3x2_to_f16x2_bcast(sw & 0xFFFFu, sv[0], sv[1]);
-                e4m3x2_to_f16x2_bcast(sw >> 16, sv[2], sv[3]);
-                // 32 code bytes of row r; the two 16-byte reads alternate order with row
-                // bit 2 so that 8 consecutive rows hit 8 different bank quads
-                const unsigned char *rw = smem + L.raw_off + slot * L.raw_bytes + half * MT * 32 + r * 32;
-                const int j0 = (r >> 2) & 1;
-                const uint4 qa = *reinterpret_cast<const uint4 *>(rw + 16 * j0);
-                const uint4 qb = *reinterpret_cast<const uint4 *>(rw + 16 * (j0 ^ 1));
-                const uint4 q0 = j0 ? qb : qa, q1 = j0 ? qa : qb;
-                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                uint32_t o[32];  // the row's 64 f16 values, TMEM columns in K order
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    uint32_t t4[4];
-                    dequant8_f16(words[w], sv[w >> 1], t4);
-                    o[4 * w] = t4[0]; o[4 * w + 1] = t4[1]; o[4 * w + 2] = t4[2]; o[4 * w + 3] = t4[3];
+                for (int jj = 0; jj < NSUB; ++jj) {
+                    if (ci == 0) {
+                        s16 = s_next;
+                        if (q + 1 < ngroups) s_next = load_scales(srow + sbytes * (q + 1));
+                        else if (srow_next) s_next = load_scales(srow_next);
+                    }
+                    uint32_t sw;
+                    if (p0.group == 16) {
+                        sw = ci == 0 ? s16.x : ci == 1 ? s16.y : ci == 2 ? s16.z : s16.w;
+                    } else {
+                        const int wi = ci >> 1;
+                        const uint32_t wv = wi == 0 ? s16.x : wi == 1 ? s16.y : wi == 2 ? s16.z : s16.w;
+                        const uint32_t two = (ci & 1) ? (wv >> 16) : (wv & 0xFFFFu);
+                        sw = (two & 0xFFu) * 0x0101u | ((two >> 8) * 0x0101u) << 16;
+                    }
+                    uint32_t sv[4];
+                    e4m3x2_to_f16x2_bcast(sw & 0xFFFFu, sv[0], sv[1]);
+                    e4m3x2_to_f16x2_bcast(sw >> 16, sv[2], sv[3]);
+                    // 32 code bytes of row r; the two 16-byte reads alternate order with row
+                    // bit 2 so that 8 consecutive rows hit 8 different bank quads
+                    const unsigned char *rw = smem + L.raw_off + slot * L.raw_bytes + (2 * jj + half) * MT * 32 + r * 32;
+                    const int j0 = (r >> 2) & 1;
+                    const uint4 qa = *reinterpret_cast<const uint4 *>(rw + 16 * j0);
+                    const uint4 qb = *reinterpret_cast<const uint4 *>(rw + 16 * (j0 ^ 1));
+                    const uint4 q0 = j0 ? qb : qa, q1 = j0 ? qa : qb;
+                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    uint32_t o[32];  // the row's 64 f16 values, TMEM columns in K order
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        uint32_t t4[4];
+                        dequant8_f16(words[w], sv[w >> 1], t4);
+                        o[4 * w] = t4[0]; o[4 * w + 1] = t4[1]; o[4 * w + 2] = t4[2]; o[4 * w + 3] = t4[3];
+                    }
+                    // the row goes to this warp's TMEM lane quarter
+                    tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 128u + (uint32_t)jj * 64u +
+                                 (uint32_t)half * 32u,
+                             o);
+                    if (++ci == cpl) { ci = 0; ++q; }
                 }
-                // the row goes to this warp's TMEM lane quarter
-                // the previous chunk's stores have had this chunk's work to land: complete them
-                // and release that buffer, then issue this chunk's stores
-                if (pending >= 0) publish(pending);
-                tc::st32(tmem + ((uint32_t)(32 * quarter) << 16) + kColA + (uint32_t)ab * 64u + (uint32_t)half * 32u, o);
-                pending = ab;
+                // every thread's stores complete, then the warp releases the buffer once
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) arrive(a_full + ab);
                 if (++slot == ns) { slot = 0; ph ^= 1; }
-                if (++ci == cpl) { ci = 0; ++q; }
             }
             if (dead) break;
             srow = srow_next;
         }
-        if (pending >= 0) publish(pending);
         if (dead && lane == 0) { raise_status(p0.status, FT_ERR_TIMEOUT); *abort_flag = 1; }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -642,7 +655,7 @@ bool tc_shape_ok_fp8(int K, int rows_per_expert) { return K % 128 == 0 && K >= 1
 
 bool tc_shape_ok(int K, int group, int rows_per_expert)
 {
-    return K % KC == 0 && K >= KC && rows_per_expert % MT == 0 && (K / group) % 8 == 0 && K / group <= 256;
+    return K % KST == 0 && K >= KST && rows_per_expert % MT == 0 && (K / group) % 8 == 0 && K / group <= 256;
 }
 
 // Deepest TMA ring (NSMAX down to 2 stages) that fits the opt-in shared memory.
