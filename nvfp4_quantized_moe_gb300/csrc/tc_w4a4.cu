@@ -383,14 +383,18 @@ __global__ void __launch_bounds__(kThreads4, 1)
                         const uint32_t *v = tile ? v1 : v0;
                         const float gr = tile ? g1 : g0;
                         __syncwarp();
+                        // the row global (this lane's column) before the transpose, the position's
+                        // factor after it (one read per position instead of one per element)
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) tb[j * 32 + lane] = __uint_as_float(v[j]) * gr * tbl_w[cb * 32 + j];
+                        for (int j = 0; j < 32; ++j) tb[j * 32 + lane] = __uint_as_float(v[j]) * gr;
                         __syncwarp();
                         const int c0 = m * 2 * MT + tile * MT + 32 * quarter + 4 * ql;
 #pragma unroll
                         for (int jb = 0; jb < 32; jb += 4) {
                             const int dst = tbl_slot[cb * 32 + jb + jl];
-                            const float4 o = *reinterpret_cast<const float4 *>(tb + (jb + jl) * 32 + 4 * ql);
+                            const float w = tbl_w[cb * 32 + jb + jl];
+                            float4 o = *reinterpret_cast<const float4 *>(tb + (jb + jl) * 32 + 4 * ql);
+                            o.x *= w; o.y *= w; o.z *= w; o.w *= w;
                             if (dst >= 0) __stcg(reinterpret_cast<float4 *>(p.y_out + (size_t)dst * p.y_ld + c0), o);
                         }
                     }
