@@ -93,6 +93,7 @@ extern "C" ft_status ft_moe_align_static(const int32_t *topk_ids, int32_t T, int
                                          int32_t *sorted_slot, int32_t *block_expert, int32_t *expert_off,
                                          int32_t *n_padded, int32_t *status, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_align_static");
     if (T < 0 || k <= 0 || E <= 0 || block < 1 || block > 1024)
         return report_error(FT_ERR_INVALID_ARG, "need T >= 0, k > 0, E > 0, 1 <= block <= 1024");
     if (k > 32 || E > kStaticMaxExperts || (int64_t)T * k > kStaticMaxSlots)

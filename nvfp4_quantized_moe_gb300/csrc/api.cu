@@ -408,6 +408,7 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pieces *src, const ft_moe_banks *dst,
                       void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_pack");
     Geometry G;
     ft_status st = check_config(cfg, G);
     if (st) return st;
@@ -482,6 +483,7 @@ ft_status ft_moe_pack(const ft_moe_config *cfg, int32_t shared, const ft_moe_pie
 ft_status ft_moe_route(const float *logits, int32_t T, int32_t E, int32_t k, int32_t *topk_ids, float *topk_w,
                        void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_route");
     if (T < 0 || E <= 0 || k <= 0) return fail(FT_ERR_INVALID_ARG, "need T >= 0, E > 0, k > 0");
     if (E > 1024 || k > 32 || k > E) return fail(FT_ERR_UNSUPPORTED, "need k <= 32, k <= E <= 1024");
     if (T == 0) return ok();
@@ -495,6 +497,7 @@ ft_status ft_moe_route(const float *logits, int32_t T, int32_t E, int32_t k, int
 ft_status ft_moe_route_gemm(const void *x, int32_t T, int32_t H, const void *w_router, int32_t E, int32_t k,
                             float *logits, int32_t *topk_ids, float *topk_w, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_route_gemm");
     if (T < 0 || E <= 0 || k <= 0 || H <= 0) return fail(FT_ERR_INVALID_ARG, "need T >= 0, H, E, k > 0");
     if (H % 32) return fail(FT_ERR_INVALID_ARG, "need H a multiple of 32");
     if (E > 1024 || k > 32 || k > E) return fail(FT_ERR_UNSUPPORTED, "need k <= 32, k <= E <= 1024");
@@ -523,6 +526,7 @@ ft_status ft_moe_align(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
                        int32_t *block_expert, int32_t *expert_off, int32_t *n_padded, void *workspace,
                        size_t workspace_bytes, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_align");
     if (T < 0 || k <= 0 || E <= 0 || block < 1 || block > 1024)
         return fail(FT_ERR_INVALID_ARG, "need T >= 0, k > 0, E > 0, 1 <= block <= 1024");
     if (E > 1024 || T > (1 << 20) || k > 32) return fail(FT_ERR_UNSUPPORTED, "align limits exceeded");
@@ -545,6 +549,7 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
                          const void *x, int32_t T, const int32_t *topk_ids, const float *topk_w, void *out,
                          int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_forward");
     Geometry G;
     ft_status st = check_config(cfg, G);
     if (st) return st;
@@ -922,6 +927,7 @@ ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *rout
                               const void *x, int32_t T, const int32_t *topk_ids, const float *topk_w, void *out,
                               int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_forward_w4a4");
     Geometry G;
     ft_status st = check_config(cfg, G);
     if (st) return st;
@@ -1036,6 +1042,7 @@ ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *rout
 ft_status ft_moe_quantize_nvfp4(const void *src, int32_t src_dtype, int32_t rows, int32_t K, uint8_t *codes,
                                 uint8_t *scales, float *glob, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_quantize_nvfp4");
     if (src_dtype != FT_DTYPE_BF16 && src_dtype != FT_DTYPE_F32)
         return fail(FT_ERR_INVALID_ARG, "src_dtype must be FT_DTYPE_BF16 or FT_DTYPE_F32");
     if (rows < 0 || K <= 0 || K % 16) return fail(FT_ERR_INVALID_ARG, "need rows >= 0 and K a positive multiple of 16");
@@ -1051,6 +1058,7 @@ ft_status ft_moe_quantize_nvfp4(const void *src, int32_t src_dtype, int32_t rows
 ft_status ft_moe_dequant(const ft_moe_config *cfg, int32_t shared, const ft_moe_banks *banks, int32_t which,
                          int32_t expert, void *out_bf16, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_dequant");
     Geometry G;
     ft_status st = check_config(cfg, G);
     if (st) return st;
@@ -1075,6 +1083,7 @@ ft_status ft_moe_dequant(const ft_moe_config *cfg, int32_t shared, const ft_moe_
 
 ft_status ft_moe_read_status(const void *workspace, void *stream)
 {
+    FT_NVTX_RANGE("ft_moe_read_status");
     if (!workspace) return fail(FT_ERR_INVALID_ARG, "workspace is NULL");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -179,6 +180,17 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
         const cudaError_t le_ = launch_pdl(__VA_ARGS__);                                                       \
         if (le_ != cudaSuccess) return le_;                                                                    \
     } while (0)
+// An NVTX range named after the ABI call for the scope of the call (header-only NVTX 3:
+// nothing is loaded unless a profiler is attached), so that profiles group each call's
+// launches.
+struct NvtxScope {
+    explicit NvtxScope(const char *name) { nvtxRangePushA(name); }
+    ~NvtxScope() { nvtxRangePop(); }
+    NvtxScope(const NvtxScope &) = delete;
+    NvtxScope &operator=(const NvtxScope &) = delete;
+};
+#define FT_NVTX_RANGE(name) const NvtxScope ft_nvtx_scope_(name)
+
 // Sets the thread-local error message (cleared for FT_OK) and returns `code`.
 ft_status report_error(ft_status code, const char *message);
 // Adds n to the calling thread's launch counter (ft_moe_launch_count).
