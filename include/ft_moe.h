@@ -64,7 +64,9 @@ typedef enum {
     FT_ERR_WORKSPACE = 4,        /* workspace smaller than ft_moe_workspace_size */
     FT_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
     FT_ERR_INVALID_ROUTING = 6,  /* device: an expert id out of range or repeated in a row */
-    FT_ERR_TIMEOUT = 7           /* device: a bounded wait gave up */
+    FT_ERR_TIMEOUT = 7,          /* device: a bounded wait gave up */
+    FT_ERR_BOUNDS = 8            /* device, bounds-checking builds only: an index derived from the
+                                    routing (expert id, slot, padded count) was out of range */
 } ft_status;
 
 /* Geometry of one MoE layer as seen by one tp rank. `intermediate` and
@@ -325,7 +327,8 @@ ft_status ft_moe_dequant(const ft_moe_config *cfg, int32_t shared, const ft_moe_
                          int32_t which, int32_t expert, void *out_bf16, void *stream);
 
 /* Synchronise `stream` and return the status word at the start of `workspace`
- * (FT_OK, FT_ERR_INVALID_ROUTING or FT_ERR_TIMEOUT). Returns FT_ERR_CUDA if the
+ * (FT_OK, FT_ERR_INVALID_ROUTING, FT_ERR_TIMEOUT, or FT_ERR_BOUNDS from a library built
+ * with FTMOE_BOUNDS_CHECK). Returns FT_ERR_CUDA if the
  * stream itself failed. The pages want bad geometry to fail with an error rather
  * than run ("[1/3] feat(dsv4): add tensor-parallel DeepSeek-V4 runtime", Checkpoint
  * loading and memory correctness: incompatible sizes fail before any layer is built)

@@ -29,7 +29,8 @@ FT_GU, FT_GU_SCALE, FT_GU_GLOBAL, FT_DN, FT_DN_SCALE, FT_DN_GLOBAL, FT_NBANKS = 
 FT_DTYPE_U8, FT_DTYPE_E4M3, FT_DTYPE_F32, FT_DTYPE_BF16 = range(4)
 FT_FORMAT_NVFP4, FT_FORMAT_FP8_BLOCK = range(2)
 STATUS = {0: "FT_OK", 1: "FT_ERR_INVALID_ARG", 2: "FT_ERR_INDIVISIBLE", 3: "FT_ERR_UNSUPPORTED",
-          4: "FT_ERR_WORKSPACE", 5: "FT_ERR_CUDA", 6: "FT_ERR_INVALID_ROUTING", 7: "FT_ERR_TIMEOUT"}
+          4: "FT_ERR_WORKSPACE", 5: "FT_ERR_CUDA", 6: "FT_ERR_INVALID_ROUTING", 7: "FT_ERR_TIMEOUT",
+          8: "FT_ERR_BOUNDS"}
 BANK_NAMES = ("gate_up", "gate_up_scale", "gate_up_global", "down", "down_scale", "down_global")
 
 # Every symbol include/ft_moe.h declares.

@@ -13,6 +13,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libftmoe.so")
 BUILD_DIR = os.path.join(PKG, "_build")
+# the bounds-checking variant (FTMOE_BOUNDS_CHECK: every index derived from the routing tables
+# is checked in the kernels and reported as FT_ERR_BOUNDS), for tests and debugging
+OUT_CHECK = os.path.join(PKG, "libftmoe_check.so")
+BUILD_DIR_CHECK = os.path.join(PKG, "_build_check")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]
@@ -32,15 +36,17 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, check: bool = False) -> str:
+    """Compile (what changed of) the library; check=True builds the bounds-checking variant."""
+    out, build_dir = (OUT_CHECK, BUILD_DIR_CHECK) if check else (OUT, BUILD_DIR)
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(INCLUDE, "*.h"))
-    extra = list(extra or [])
+    extra = list(extra or []) + (["-DFTMOE_BOUNDS_CHECK"] if check else [])
     objs, jobs = [], []
     for src in sources:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             jobs.append([nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj])
@@ -51,13 +57,13 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
             print(r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    if force or jobs or _stale(OUT, objs):
-        tmp = OUT + f".tmp{os.getpid()}"
+    if force or jobs or _stale(out, objs):
+        tmp = out + f".tmp{os.getpid()}"
         r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, OUT)
-    return OUT
+        os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -700,13 +700,14 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         gp.glob = static_cast<const float *>(routed->p[FT_GU_GLOBAL]);
         gp.R = 2 * G.Il; gp.K = G.H; gp.group = G.g; gp.up_off = G.Il; gp.n_mtiles = G.Il / 128;
         gp.n_pos_dev = npad; gp.sorted_slot = sorted; gp.block_expert = bexp; gp.n_slots = n_slots; gp.top_k = G.k;
+        gp.num_experts = G.E;
         gp.h_out = h; gp.h_ld = G.Il; gp.status = status;
         fp8_fields(gp, routed, true, G.Il);
         if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
         auto f16buf = [&](size_t off) { return reinterpret_cast<uint16_t *>(ws + off); };
         auto f32buf = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
         const uint16_t *xb = static_cast<const uint16_t *>(x);
-        e = launch_rows_to_f16(xb, G.H, sorted, npad, 0, n_slots, G.k, L.pmax, f16buf(L.xs), f32buf(L.xs_scale), s);
+        e = launch_rows_to_f16(xb, G.H, sorted, npad, 0, n_slots, G.k, L.pmax, f16buf(L.xs), f32buf(L.xs_scale), s, status);
         if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
         gp.act_scale = f32buf(L.xs_scale);
         // routed and shared expert in one launch (units of the routed experts first)
@@ -720,10 +721,10 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sp.glob = static_cast<const float *>(shared->p[FT_GU_GLOBAL]);
             sp.R = 2 * G.Isl; sp.up_off = G.Isl; sp.n_mtiles = G.Isl / 128;
             sp.n_pos_dev = nullptr; sp.n_pos_static = T; sp.sorted_slot = nullptr; sp.block_expert = nullptr;
-            sp.n_slots = T; sp.top_k = 1; sp.h_out = h_sh; sp.h_ld = G.Isl;
+            sp.n_slots = T; sp.top_k = 1; sp.num_experts = 1; sp.h_out = h_sh; sp.h_ld = G.Isl;
             sp.act_scale = f32buf(L.x16_scale);
             fp8_fields(sp, shared, true, G.Isl);
-            e = launch_rows_to_f16(xb, G.H, nullptr, nullptr, tp, T, 1, tp, f16buf(L.x16), f32buf(L.x16_scale), s);
+            e = launch_rows_to_f16(xb, G.H, nullptr, nullptr, tp, T, 1, tp, f16buf(L.x16), f32buf(L.x16_scale), s, status);
             if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
             gprob[1] = sp;
             gops[1] = {shared->p[FT_GU], 2 * (int64_t)G.Isl, f16buf(L.x16), tp};
@@ -739,11 +740,12 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
         dp.glob = static_cast<const float *>(routed->p[FT_DN_GLOBAL]);
         dp.R = G.H; dp.K = G.Il; dp.group = G.g; dp.up_off = 0; dp.n_mtiles = G.H / 256;
         dp.n_pos_dev = npad; dp.sorted_slot = sorted; dp.block_expert = bexp; dp.n_slots = n_slots; dp.top_k = G.k;
+        dp.num_experts = G.E;
         dp.y_out = y; dp.y_ld = G.H; dp.route_w = topk_w; dp.status = status;
         dp.act_scale = f32buf(L.h16_scale);
         fp8_fields(dp, routed, false, G.Il);
         // h rows are already in sorted-position order: convert them in place of a gather
-        e = launch_rows_to_f16(h, G.Il, nullptr, npad, 0, L.pmax, 1, L.pmax, f16buf(L.h16), f32buf(L.h16_scale), s);
+        e = launch_rows_to_f16(h, G.Il, nullptr, npad, 0, L.pmax, 1, L.pmax, f16buf(L.h16), f32buf(L.h16_scale), s, status);
         if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
         TcParams dprob[2] = {dp, dp};
         TcOperands dops[2] = {{routed->p[FT_DN], (int64_t)G.E * G.H, f16buf(L.h16), L.pmax}, {}};
@@ -753,11 +755,11 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
             sd.scales = static_cast<const uint8_t *>(shared->p[FT_DN_SCALE]);
             sd.glob = static_cast<const float *>(shared->p[FT_DN_GLOBAL]);
             sd.K = G.Isl; sd.n_pos_dev = nullptr; sd.n_pos_static = T; sd.sorted_slot = nullptr;
-            sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.y_out = y_sh; sd.route_w = nullptr;
+            sd.block_expert = nullptr; sd.n_slots = T; sd.top_k = 1; sd.num_experts = 1; sd.y_out = y_sh; sd.route_w = nullptr;
             sd.act_scale = f32buf(L.hsh16_scale);
             fp8_fields(sd, shared, false, G.Isl);
             e = launch_rows_to_f16(h_sh, G.Isl, nullptr, nullptr, tp, T, 1, tp, f16buf(L.hsh16),
-                                   f32buf(L.hsh16_scale), s);
+                                   f32buf(L.hsh16_scale), s, status);
             if (e != cudaSuccess) return cuda_fail(e, "row conversion launch");
             dprob[1] = sd;
             dops[1] = {shared->p[FT_DN], G.H, f16buf(L.hsh16), tp};
@@ -971,10 +973,10 @@ ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *rout
     if ((e = stage_mark(FT_STAGE_GATE_UP, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     // NVFP4 activations: x per expert-sorted position (routed) and per token (shared)
     e = launch_quant_nvfp4(x, false, G.H, sorted, npad, 0, n_slots, G.k, L.pmax, at_u8(L.xq_c), at_u8(L.xq_s),
-                           at_f(L.xq_g), s);
+                           at_f(L.xq_g), s, status);
     if (e == cudaSuccess && G.Is)
         e = launch_quant_nvfp4(x, false, G.H, nullptr, nullptr, tpad, T, 1, tpad, at_u8(L.xs_c), at_u8(L.xs_s),
-                               at_f(L.xs_g), s);
+                               at_f(L.xs_g), s, status);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     auto problem = [&](const ft_moe_banks *b, bool gate_up, bool is_shared) {
         W4Params q = {};
@@ -987,9 +989,10 @@ ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *rout
         q.up_off = gate_up ? il : 0;
         q.n_mtiles = gate_up ? il / 128 : G.H / 256;
         if (is_shared) {
-            q.n_pos_static = T; q.n_slots = T; q.top_k = 1;
+            q.n_pos_static = T; q.n_slots = T; q.top_k = 1; q.num_experts = 1;
         } else {
             q.n_pos_dev = npad; q.sorted_slot = sorted; q.block_expert = bexp; q.n_slots = n_slots; q.top_k = G.k;
+            q.num_experts = G.E;
         }
         q.status = status;
         return q;
@@ -1011,10 +1014,10 @@ ft_status ft_moe_forward_w4a4(const ft_moe_config *cfg, const ft_moe_banks *rout
     if ((e = stage_mark(FT_STAGE_DOWN, s)) != cudaSuccess) return cuda_fail(e, "stage event");
     // h (fp32, position rows) as NVFP4
     e = launch_quant_nvfp4(at_f(L.h), true, G.Il, nullptr, npad, 0, L.pmax, 1, L.pmax, at_u8(L.hq_c), at_u8(L.hq_s),
-                           at_f(L.hq_g), s);
+                           at_f(L.hq_g), s, status);
     if (e == cudaSuccess && G.Is)
         e = launch_quant_nvfp4(at_f(L.hs), true, G.Isl, nullptr, nullptr, tpad, tpad, 1, tpad, at_u8(L.hsq_c),
-                               at_u8(L.hsq_s), at_f(L.hsq_g), s);
+                               at_u8(L.hsq_s), at_f(L.hsq_g), s, status);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     float *y = at_f(L.y), *y_sh = at_f(L.y_sh);
     W4Params dp[2] = {problem(routed, false, false), {}};
@@ -1050,7 +1053,7 @@ ft_status ft_moe_quantize_nvfp4(const void *src, int32_t src_dtype, int32_t rows
     if (!src || !codes || !scales || !glob || !aligned(codes, 8) || !aligned(src, 16) || !aligned(glob, 4))
         return fail(FT_ERR_INVALID_ARG, "pointers must be non-NULL; src 16-byte and codes 8-byte aligned");
     cudaError_t e = launch_quant_nvfp4(src, src_dtype == FT_DTYPE_F32, K, nullptr, nullptr, rows, rows, 1, rows, codes,
-                                       scales, glob, static_cast<cudaStream_t>(stream));
+                                       scales, glob, static_cast<cudaStream_t>(stream), nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     return ok();
 }

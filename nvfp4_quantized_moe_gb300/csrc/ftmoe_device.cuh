@@ -182,6 +182,46 @@ __device__ __forceinline__ uint4 ldg_v4(const void *p)
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+// ---------------------------------------------------------------- routing-derived indices
+
+// In a bounds-checking build (FTMOE_BOUNDS_CHECK defined) every index a kernel derives from
+// the routing tables is checked before it addresses memory; a bad one sets FT_ERR_BOUNDS in
+// the status word (first error wins) and is replaced by a harmless one. In the regular
+// build these return their argument.
+#ifdef FTMOE_BOUNDS_CHECK
+__device__ __forceinline__ void bounds_error(int *status) { raise_status(status, FT_ERR_BOUNDS); }
+// An expert id for addressing an expert's bank: in [0, E), else expert 0.
+__device__ __forceinline__ int chk_expert(int e, int E, int *status)
+{
+    if (e >= 0 && e < E) return e;
+    bounds_error(status);
+    return 0;
+}
+// A slot read from the sorted order: >= n_slots marks padding; negative is an error, read as padding.
+__device__ __forceinline__ int chk_slot(int sl, int n_slots, int *status)
+{
+    if (sl >= 0) return sl;
+    bounds_error(status);
+    return n_slots;
+}
+// A padded position count: a multiple of the block within the buffers' capacity, else 0.
+__device__ __forceinline__ int chk_count(int n, int block, int cap, int *status)
+{
+    if (n >= 0 && n <= cap && n % block == 0) return n;
+    bounds_error(status);
+    return 0;
+}
+#else
+__device__ __forceinline__ int chk_expert(int e, int, int *) { return e; }
+__device__ __forceinline__ int chk_slot(int sl, int, int *) { return sl; }
+__device__ __forceinline__ int chk_count(int n, int, int, int *) { return n; }
+#endif
+// Capacity of the padded positions of n_slots slots over E experts in blocks of B.
+__host__ __device__ __forceinline__ int padded_capacity(int n_slots, int E, int B)
+{
+    return n_slots + (n_slots < E ? n_slots : E) * (B - 1);
+}
+
 // silu(z) = z / (1 + e^-z) with the fast exponential and division: relative error of a
 // few 1e-7 for |z| < 64, far below the bf16 rounding of h that follows. For z < -88
 // the denominator is +inf and the result -0; for large z it is z.

@@ -63,6 +63,7 @@ struct TcParams {
     const int *sorted_slot;  // routed: position -> slot
     const int *block_expert; // routed: block -> expert
     int n_slots, top_k;
+    int num_experts;         // routed: E (block_expert values index the banks); shared: 1
     uint16_t *h_out;         // gate_up: bf16 [positions][h_ld]
     int h_ld;
     float *y_out;            // down: fp32 [slots][y_ld]
@@ -106,7 +107,7 @@ cudaError_t launch_tc_gemm(const TcParams *probs, const TcOperands *ops, int npr
 // padding slots give zero rows). pos < *n_pos_dev, or < n_pos_static when that is null.
 cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
                                int n_pos_static, int n_slots, int top_k, int max_rows, uint16_t *out, float *scale,
-                               cudaStream_t s);
+                               cudaStream_t s, int *status);
 // One W4A4 (native FP4) grouped GEMM problem: NVFP4 weight banks against NVFP4-quantized
 // activation rows (codes, e4m3 scales per 16 elements, fp32 row scale per position).
 struct W4Params {
@@ -120,6 +121,7 @@ struct W4Params {
     const int *sorted_slot;   // routed: position -> slot
     const int *block_expert;  // routed: block -> expert
     int n_slots, top_k;
+    int num_experts;          // routed: E; shared: 1
     float *h_out;             // gate_up: fp32 [positions][h_ld]
     int h_ld;
     float *y_out;             // down: fp32 [slots][y_ld]
@@ -147,7 +149,7 @@ cudaError_t launch_w4a4_gemm(const W4Params *probs, const W4Operands *ops, int n
 // [pos][K/16], fp32 row scales [pos]; padding positions get zeros.
 cudaError_t launch_quant_nvfp4(const void *src, bool f32_src, int K, const int *sorted_slot, const int *n_pos_dev,
                                int n_pos_static, int n_slots, int top_k, int max_rows, uint8_t *codes,
-                               uint8_t *scales, float *glob, cudaStream_t s);
+                               uint8_t *scales, float *glob, cudaStream_t s, int *status);
 
 // 2D tiled tensor map (rows of `row_bytes` bytes, `inner` elements used per row) through
 // the driver's cuTensorMapEncodeTiled; false when the driver refuses the shape.

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_gated_ke
             __syncthreads();
             staged = blk;
         }
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + blk) : 0, p.num_experts, p.status);
         const int i0 = (grp * TPW + tp) * 16;
         const bool tile_ok = i0 < p.up_off;
         const uint8_t *gcodes = p.codes + (size_t)e * p.e_codes + (size_t)(i0 + g) * (p.K / 2);
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_down_ker
             __syncthreads();
             staged = blk;
         }
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + blk) : 0, p.num_experts, p.status);
         const int n0 = (grp * TPW + tw) * 16;
         const bool tile_ok = n0 < p.R;
         const uint8_t *codes = p.codes + (size_t)e * p.e_codes + (size_t)(n0 + g) * (p.K / 2);
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, FTMOE_GEMV_MIN_BLOCKS) gemv_down_ker
                 int dst;
                 float wgt = inv[2 * c + col];
                 if (p.sorted_slot) {
-                    dst = __ldg(p.sorted_slot + pos);
+                    dst = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
                     if (dst >= p.n_slots) continue;
                     if (p.route_w) wgt *= __ldg(p.route_w + dst);
                 } else {

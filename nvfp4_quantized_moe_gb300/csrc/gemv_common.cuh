@@ -14,7 +14,9 @@ constexpr int kStep = 128;     // K elements per warp step (4 lanes x 32)
 
 __device__ __forceinline__ int load_n_pos(const GemvParams &p)
 {
-    return p.n_pos_dev ? *p.n_pos_dev : (p.n_pos_static + kGemvBlock - 1) / kGemvBlock * kGemvBlock;
+    return p.n_pos_dev ? chk_count(*p.n_pos_dev, kGemvBlock, padded_capacity(p.n_slots, p.num_experts, kGemvBlock),
+                                   p.status)
+                       : (p.n_pos_static + kGemvBlock - 1) / kGemvBlock * kGemvBlock;
 }
 
 // Source row of block position `pos` (x row for gate_up, h row for down), or -1 for padding.
@@ -22,7 +24,7 @@ __device__ __forceinline__ int source_row(const GemvParams &p, int pos, int n_po
 {
     if (pos >= n_pos) return -1;
     if (p.sorted_slot) {
-        const int s = __ldg(p.sorted_slot + pos);
+        const int s = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
         if (s >= p.n_slots) return -1;
         return gated ? s / p.top_k : pos;
     }

@@ -297,7 +297,7 @@ __device__ __forceinline__ void fast_unit(const GemvParams &p, const FastLaunch 
                 int dst;
                 float wgt = inv[2 * c + col];
                 if (p.sorted_slot) {
-                    dst = __ldg(p.sorted_slot + pos);
+                    dst = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
                     if (dst >= p.n_slots) continue;
                     if (p.route_w) wgt *= __ldg(p.route_w + dst);
                 } else {
@@ -341,7 +341,8 @@ __device__ __forceinline__ void fast_stage(const GemvParams &p, int blk, int n_p
     __syncthreads();
     if (threadIdx.x < kGemvBlock)
         sm.rows[threadIdx.x] = source_row(p, blk * kGemvBlock + threadIdx.x, n_pos, GATED);
-    if (threadIdx.x == kGemvBlock) sm.s_e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+    if (threadIdx.x == kGemvBlock)
+        sm.s_e = chk_expert(p.block_expert ? __ldg(p.block_expert + blk) : 0, p.num_experts, p.status);
     __syncthreads();
     for (int r = threadIdx.x >> 5; r < kGemvBlock; r += kThreads / 32)
         stage_row_1pass<COHERENT>(p.act, p.K, sm.rows, smem_b, sm.inv, r);
@@ -371,7 +372,7 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
         const int blk = lu / p.n_tiles, grp0 = lu - blk * p.n_tiles;
         const int nu = min(p.n_tiles - grp0, u_hi - u);  // the run: this block's units in range
         u += nu;
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + blk) : 0, p.num_experts, p.status);
         const int r0a = (grp0 * 8 + warp) * 32;  // the warp's first row in the run's first unit
         // units with rows in range form a prefix of the run
         const int nok = r0a < p.R ? min(nu, (p.R - r0a + 255) / 256) : 0;
@@ -419,7 +420,7 @@ __device__ __forceinline__ void down_runs(const FastLaunch &L, int units0, int n
             float w = sm.inv[threadIdx.x];
             if (pos < n_pos) {
                 if (p.sorted_slot) {
-                    const int sl = __ldg(p.sorted_slot + pos);
+                    const int sl = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
                     if (sl < p.n_slots) {
                         dst = sl;
                         if (p.route_w) w *= __ldg(p.route_w + sl);

@@ -135,7 +135,7 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
     const int rows_limit = GATED ? p.up_off : p.R;
     const int r0 = (grp * TPW + tp) * pair_rows;
     const bool ok = r0 < rows_limit;
-    const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+    const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + blk) : 0, p.num_experts, p.status);
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
         const int row_a = r0 + g, row_b = GATED ? p.up_off + r0 + g : r0 + 16 + g;
@@ -248,7 +248,7 @@ __device__ __forceinline__ void fp8_unit(const GemvParams &p, const FastLaunch &
                 int dst;
                 float wgt = inv[2 * c + col];
                 if (p.sorted_slot) {
-                    dst = __ldg(p.sorted_slot + pos);
+                    dst = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
                     if (dst >= p.n_slots) continue;
                     if (p.route_w) wgt *= __ldg(p.route_w + dst);
                 } else {
@@ -293,7 +293,7 @@ __device__ __forceinline__ void fp8_down_runs(const FastLaunch &L, int units0, i
             float w = inv[threadIdx.x];
             if (pos < n_pos) {
                 if (p.sorted_slot) {
-                    const int sl = __ldg(p.sorted_slot + pos);
+                    const int sl = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
                     if (sl < p.n_slots) {
                         dst = sl;
                         if (p.route_w) w *= __ldg(p.route_w + sl);
@@ -311,7 +311,7 @@ __device__ __forceinline__ void fp8_down_runs(const FastLaunch &L, int units0, i
         const int nok = r0a < p.R ? min(nu, (p.R - r0a + 255) / 256) : 0;  // units with rows in range
         const int tot = nok * S;
         if (tot == 0) continue;
-        const int e = p.block_expert ? __ldg(p.block_expert + blk) : 0;
+        const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + blk) : 0, p.num_experts, p.status);
         const uint8_t *ca = p.codes + (size_t)e * p.e_codes + (size_t)(r0a + g) * K + 16 * c;
         const uint8_t *cb = ca + (size_t)16 * K;  // rows r0 + 16 + g
         const size_t row8 = (size_t)8 * K;

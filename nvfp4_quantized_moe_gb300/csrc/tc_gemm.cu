@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
 
     // units: problem 0's (blocks x row tiles), then problem 1's
     auto n_units_of = [&](const TcParams &q) {
-        const int n_pos = q.n_pos_dev ? *q.n_pos_dev : (q.n_pos_static + NT - 1) / NT * NT;
+        const int n_pos = q.n_pos_dev ? chk_count(*q.n_pos_dev, NT, padded_capacity(q.n_slots, q.num_experts, NT), q.status)
+                                      : (q.n_pos_static + NT - 1) / NT * NT;
         return (n_pos / NT) * q.n_mtiles;
     };
     const int units0 = n_units_of(p0);
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 const CUtensorMap *codes_map = u < units0 ? &codes_map0 : &codes_map1;
                 const CUtensorMap *b_map = u < units0 ? &b_map0 : &b_map1;
                 const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
-                const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+                const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + b) : 0, p.num_experts, p.status);
                 const int row_a = e * p.R + m * tile_rows;
                 const int row_b = GATED ? row_a + p.up_off : row_a + MT;
                 const int nk = p.K / KST;
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             const TcParams &p = prob_of(u, lu);
             const int kbn = p.K / 128, nk = p.K / KST;
             const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
-            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+            const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + b) : 0, p.num_experts, p.status);
             const int nb = GATED ? (half ? p.up_off / MT : 0) + m : 2 * m + half;  // the tile's scale block row
             const float *srow = p.sinv + (size_t)e * p.e_sinv + (size_t)nb * kbn;
             float smax = 0.f;
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
             int lu;
             const TcParams &q = prob_of(uu, lu);
             const int bb = lu / q.n_mtiles, mm = lu - bb * q.n_mtiles;
-            const int ee = q.block_expert ? __ldg(q.block_expert + bb) : 0;
+            const int ee = chk_expert(q.block_expert ? __ldg(q.block_expert + bb) : 0, q.num_experts, q.status);
             const int row = ee * q.R + mm * tile_rows + (half ? (GATED ? q.up_off : MT) : 0) + r;
             return q.scales + (size_t)row * (size_t)(q.K / q.group);
         };
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 int dst = pos;
                 if (!GATED) {
                     if (p.sorted_slot) {
-                        dst = __ldg(p.sorted_slot + pos);
+                        dst = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
                         if (dst >= p.n_slots) dst = -1;
                         else if (p.route_w) w *= __ldg(p.route_w + dst);
                     } else if (dst >= p.n_pos_static) {
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
                 tbl_slot[t] = dst;
                 tbl_w[t] = w;
             }
-            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+            const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + b) : 0, p.num_experts, p.status);
             const float *glob_e = p.glob + (size_t)e * p.R;
             const int row0 = GATED ? m * MT + r : m * 2 * MT + r;
             float g0, g1;
@@ -573,16 +574,16 @@ __global__ void __launch_bounds__(tc_threads(GATED), 1)
 // One warp per position.
 __global__ void rows_to_f16_kernel(const uint16_t *__restrict__ src, int K, const int *__restrict__ sorted_slot,
                                    const int *__restrict__ n_pos_dev, int n_pos_static, int n_slots, int top_k,
-                                   uint16_t *__restrict__ out, float *__restrict__ scale)
+                                   uint16_t *__restrict__ out, float *__restrict__ scale, int cap, int *status)
 {
     pdl_enter();
-    const int n_pos = n_pos_dev ? *n_pos_dev : n_pos_static;
+    const int n_pos = n_pos_dev ? chk_count(*n_pos_dev, 1, cap, status) : n_pos_static;
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n_pos; pos += warps) {
         int row = pos;
         if (sorted_slot) {
-            const int sl = __ldg(sorted_slot + pos);
+            const int sl = chk_slot(__ldg(sorted_slot + pos), n_slots, status);
             row = sl < n_slots ? sl / top_k : -1;
         } else if (pos >= n_slots) {
             row = -1;
@@ -675,14 +676,14 @@ static int tc_stages(bool fp8, bool gated)
 
 cudaError_t launch_rows_to_f16(const uint16_t *src, int K, const int *sorted_slot, const int *n_pos_dev,
                                int n_pos_static, int n_slots, int top_k, int max_rows, uint16_t *out, float *scale,
-                               cudaStream_t s)
+                               cudaStream_t s, int *status)
 {
     int blocks = (max_rows + 7) / 8;
     const int cap = sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     FT_LAUNCH(rows_to_f16_kernel, dim3(blocks), dim3(256), 0, s, src, K, sorted_slot, n_pos_dev, n_pos_static,
-              n_slots, top_k, out, scale);
+              n_slots, top_k, out, scale, max_rows, status);
     count_launches(1);
     return cudaGetLastError();
 }

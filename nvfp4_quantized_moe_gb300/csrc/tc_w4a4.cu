@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(kThreads4, 1)
     const uint32_t tmem = *tmem_slot;
 
     auto n_units_of = [&](const W4Params &q) {
-        const int n_pos = q.n_pos_dev ? *q.n_pos_dev : (q.n_pos_static + NT - 1) / NT * NT;
+        const int n_pos = q.n_pos_dev ? chk_count(*q.n_pos_dev, NT, padded_capacity(q.n_slots, q.num_experts, NT), q.status)
+                                      : (q.n_pos_static + NT - 1) / NT * NT;
         return (n_pos / NT) * q.n_mtiles;
     };
     const int units0 = n_units_of(p0);
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
                 const CUtensorMap *wmap = u < units0 ? &wmap0 : &wmap1;
                 const CUtensorMap *amap = u < units0 ? &amap0 : &amap1;
                 const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
-                const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+                const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + b) : 0, p.num_experts, p.status);
                 const int row_a = e * p.R + m * tile_rows;
                 const int row_b = GATED ? row_a + p.up_off : row_a + MT;
                 for (int c = 0; c < p.K / KS4; ++c, ++it) {
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
             int lu;
             const W4Params &p = prob_of(u, lu);
             const int b = lu / p.n_mtiles, m = lu - b * p.n_mtiles;
-            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+            const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + b) : 0, p.num_experts, p.status);
             const int wrow0 = e * p.R + m * tile_rows + r;
             const int wrow1 = GATED ? wrow0 + p.up_off : wrow0 + MT;
             const size_t wstride = (size_t)(p.K / p.group);
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
                 int dst = pos;
                 if (!GATED) {
                     if (p.sorted_slot) {
-                        dst = __ldg(p.sorted_slot + pos);
+                        dst = chk_slot(__ldg(p.sorted_slot + pos), p.n_slots, p.status);
                         if (dst >= p.n_slots) dst = -1;
                         else if (p.route_w) w *= __ldg(p.route_w + dst);
                     } else if (dst >= p.n_pos_static) {
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreads4, 1)
                 tbl_slot[t] = dst;
                 tbl_w[t] = w;
             }
-            const int e = p.block_expert ? __ldg(p.block_expert + b) : 0;
+            const int e = chk_expert(p.block_expert ? __ldg(p.block_expert + b) : 0, p.num_experts, p.status);
             const float *glob_e = p.w_glob + (size_t)e * p.R;
             const int row0 = GATED ? m * MT + r : m * 2 * MT + r;
             const float g0 = __ldg(glob_e + row0);

@@ -79,10 +79,11 @@ __global__ void __launch_bounds__(256) quant_nvfp4_rows_kernel(const void *__res
                                                                  const int *__restrict__ sorted_slot,
                                                                  const int *__restrict__ n_pos_dev, int n_pos_static,
                                                                  int n_slots, int top_k, uint8_t *__restrict__ codes,
-                                                                 uint8_t *__restrict__ scales, float *__restrict__ glob)
+                                                                 uint8_t *__restrict__ scales, float *__restrict__ glob,
+                                                                 int cap, int *status)
 {
     pdl_enter();
-    const int n_pos = n_pos_dev ? *n_pos_dev : n_pos_static;
+    const int n_pos = n_pos_dev ? chk_count(*n_pos_dev, 1, cap, status) : n_pos_static;
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     const int nb = K / 16;
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(256) quant_nvfp4_rows_kernel(const void *__res
     for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n_pos; pos += warps) {
         int row = pos;
         if (sorted_slot) {
-            const int sl = __ldg(sorted_slot + pos);
+            const int sl = chk_slot(__ldg(sorted_slot + pos), n_slots, status);
             row = sl < n_slots ? sl / top_k : -1;
         } else if (pos >= n_slots) {
             row = -1;
@@ -141,18 +142,18 @@ __global__ void __launch_bounds__(256) quant_nvfp4_rows_kernel(const void *__res
 
 cudaError_t launch_quant_nvfp4(const void *src, bool f32_src, int K, const int *sorted_slot, const int *n_pos_dev,
                                int n_pos_static, int n_slots, int top_k, int max_rows, uint8_t *codes,
-                               uint8_t *scales, float *glob, cudaStream_t s)
+                               uint8_t *scales, float *glob, cudaStream_t s, int *status)
 {
     int blocks = (max_rows + 7) / 8;
-    const int cap = sm_count() * 8;
-    if (blocks > cap) blocks = cap;
+    const int bcap = sm_count() * 8;
+    if (blocks > bcap) blocks = bcap;
     if (blocks < 1) blocks = 1;
     if (f32_src)
         FT_LAUNCH(quant_nvfp4_rows_kernel<true>, dim3(blocks), dim3(256), 0, s, src, K, sorted_slot, n_pos_dev,
-                  n_pos_static, n_slots, top_k, codes, scales, glob);
+                  n_pos_static, n_slots, top_k, codes, scales, glob, max_rows, status);
     else
         FT_LAUNCH(quant_nvfp4_rows_kernel<false>, dim3(blocks), dim3(256), 0, s, src, K, sorted_slot, n_pos_dev,
-                  n_pos_static, n_slots, top_k, codes, scales, glob);
+                  n_pos_static, n_slots, top_k, codes, scales, glob, max_rows, status);
     count_launches(1);
     return cudaGetLastError();
 }
