@@ -319,6 +319,19 @@ static int fast_ksplit(int blocks, int units_per_block_ks1, int K0, int K1 = 0)
     return ks;
 }
 
+// K-split of the NVFP4 lean decode kernels: doubled while the doubled unit count still fits
+// twice over the SMs and every warp keeps at least min_kw elements of K (down: at most
+// cap). Measured on qwen36 (T = 1, 8) and the dsv4 shape (T = 1, 16): fewer, longer
+// streams per warp beat more, shorter ones once the units cover the SMs.
+static int decode_ksplit(int blocks, int units_per_block_ks1, int K0, int K1, int min_kw, int cap)
+{
+    int ks = 1;
+    while (ks < cap && blocks * units_per_block_ks1 * ks * 2 <= 2 * sm_count() && (K0 / (2 * ks)) % 128 == 0 &&
+           (K1 / (2 * ks)) % 128 == 0 && K0 / (2 * ks) >= min_kw && K1 / (2 * ks) >= min_kw)
+        ks *= 2;
+    return ks;
+}
+
 // Generic register-fed launch for one problem (shapes the lean kernels do not cover).
 // `rows` = I_l (gated) or H (down); max_blocks bounds the blocks.
 static cudaError_t run_gemv(GemvParams p, bool gated, int max_blocks, int rows, cudaStream_t s)
@@ -833,9 +846,10 @@ ft_status ft_moe_forward(const ft_moe_config *cfg, const ft_moe_banks *routed, c
 
     // Lean register-fed kernels: gate_up (+ shared expert), down (+ shared expert) and the
     // ordered combine, fused into one persistent launch for small batches.
-    const int ks_gu = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H);
-    int ks_dn = fast_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il);
-    if (ks_dn > 4) ks_dn = 4;
+    const int ks_gu = decode_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.Il > G.Isl ? G.Il : G.Isl, 16 * 8), G.H,
+                                    G.H, 512, 8);
+    const int ks_dn = decode_ksplit(max_blocks + (G.Is ? tpad : 0), cdiv(G.H, 32 * 8), G.Il, G.Is ? G.Isl : G.Il,
+                                    256, 2);
     if (gemv_fast_ok(G.H, G.g, ks_gu, 2 * (G.Il > G.Isl ? G.Il : G.Isl)) && gemv_fast_ok(G.Il, G.g, ks_dn, G.H) &&
         (!G.Is || gemv_fast_ok(G.Isl, G.g, ks_dn, G.H))) {
         FusedLaunch FL = {};
