@@ -35,6 +35,16 @@ def test_exports_every_declared_symbol(ft):
         assert hasattr(lib, name), name
 
 
+def test_bounds_checking_build_compiles_and_exports(ft):
+    """The FTMOE_BOUNDS_CHECK variant (libftmoe_check.so) still compiles and exports the same
+    ABI (its kernels run in tests/test_gpu_bounds_check.py)."""
+    from nvfp4_quantized_moe_gb300 import build
+    path = build.build(check=True)
+    lib = ctypes.CDLL(path)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
 def test_layout_matches_pages_bank_shapes(ft):
     with open(os.path.join(ROOT, "tests", "golden", "bank_layout_qwen36.json")) as f:
         g = json.load(f)
